@@ -1,0 +1,217 @@
+/*
+ * qmoe.h -- C ABI of libqmoe.so: the quantized Mixture-of-Experts expert-FFN
+ * grouped GEMM path on one GB300 (sm_103a).
+ *
+ * The problem: tokens A[M, K] are routed to top_k of E experts
+ * (topk_ids[M, top_k], routing weights topk_weights[M, top_k]); slot
+ * s = m*top_k + j of token m goes to expert e = topk_ids[m, j] and produces
+ *     out[m, j, :] = w[m, j] * dequant(Aq[m]) . dequant(Wq[e])^T
+ * in FP8-e4m3 W8A8 (dynamic per-token activation scales, per-output-channel
+ * weight scales) or INT8 W8A16 (per-channel int8 weights against bf16
+ * activations), the two precisions benchmarked in "Tianxing/moe
+ * quantization" (ROCm/triton PR 693, tables "FP8_W8A8 Benchmark" and
+ * "INT8_W8A16 Benchmark", columns M K N E top_k).
+ *
+ * Conventions shared by every entry point
+ *  - Tensor pointers are DEVICE pointers owned by the caller.  The library
+ *    allocates no device memory and keeps no mutable global state except a
+ *    per-device cache of attributes (SM count) and of kernel attributes.
+ *  - Every call is asynchronous on the given stream (a cudaStream_t; NULL is
+ *    the legacy default stream).  Nothing inside synchronises the host.
+ *  - Arguments that can be checked on the host are checked before anything is
+ *    launched; a failed check returns QMOE_ERR_INVALID_ARG or
+ *    QMOE_ERR_UNSUPPORTED and launches nothing.  A failed launch returns
+ *    QMOE_ERR_CUDA (the CUDA error is left for cudaGetLastError()).
+ *  - Errors found on the device are OR-ed into *d_status (an int32 the caller
+ *    zeroes and reads after its own synchronisation; may be NULL):
+ *    QMOE_DEV_INVALID_EXPERT for an expert id outside [0, E),
+ *    QMOE_DEV_TIMEOUT when a bounded wait inside a kernel gave up (the kernel
+ *    then returns early; its outputs are undefined).
+ *  - bf16 tensors are passed as uint16_t bit patterns; e4m3 and E8M0 as bytes.
+ *  - Sizes are int64_t unless they are small counts (E, top_k, BM).  Row
+ *    strides (ld*) are in elements.
+ */
+#ifndef QMOE_H
+#define QMOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* qmoe_stream_t; /* == cudaStream_t */
+
+typedef enum {
+    QMOE_OK = 0,
+    QMOE_ERR_INVALID_ARG = 1,
+    QMOE_ERR_UNSUPPORTED = 2,
+    QMOE_ERR_CUDA = 3
+} qmoe_status_t;
+
+#define QMOE_DEV_INVALID_EXPERT 1
+#define QMOE_DEV_TIMEOUT 2
+
+/* activation scale modes */
+#define QMOE_SCALE_PER_TOKEN 0 /* one fp32 scale per A row */
+#define QMOE_SCALE_MX_1X32 1   /* one E8M0 byte per 32 elements along K */
+/* A row layouts */
+#define QMOE_A_TOKEN_GATHER 0 /* slot s reads A row s / top_k ([M, K])        */
+#define QMOE_A_GROUPED 1      /* slot s reads its compact expert-grouped row ([T, K]) */
+/* output layouts */
+#define QMOE_OUT_SLOT 0      /* out[s, :] of [T, N] == [M, top_k, N]                  */
+#define QMOE_OUT_GROUPED 1   /* out[compact row of s, :] of [T, N] (expert-contiguous) */
+#define QMOE_OUT_TOKEN_SUM 2 /* out[m, :] = sum_j of slot m*top_k+j; [M, N]            */
+
+const char* qmoe_status_string(qmoe_status_t st);
+int qmoe_version(void);
+
+/* ------------------------------------------------------------------------ */
+/* moe_align_block_size                                                     */
+/* ------------------------------------------------------------------------ */
+/* Capacity (entries) that sorted_ids must have for T slots, E experts and
+ * tile size BM: T + E*(BM-1), rounded up to a multiple of BM.  expert_ids
+ * needs capacity/BM entries.  Returns -1 for invalid sizes. */
+int64_t qmoe_align_max_padded(int64_t T, int32_t E, int32_t BM);
+
+/* Sorts the T = M*top_k token-slots by expert and pads every expert's group
+ * to a multiple of the tile size BM (integer work; one kernel launch).
+ * The grouped GEMM needs its rows grouped by expert and each group padded to
+ * its tile: this is the reading of the grouped ("fused") MoE kernel whose
+ * benchmarks "Tianxing/moe quantization" prints, made explicit.
+ *   topk_ids       [T]   int32, row-major [M, top_k], values in [0, E)
+ *   sorted_ids     [cap] int32 out: expert e's slots, ascending s, start at
+ *                  padded_offsets[e]; pad entries hold the sentinel T
+ *   expert_ids     [cap/BM] int32 out: expert of block b, -1 past the end
+ *   num_post_padded[1]  int32 out: sum_e roundup(cnt_e, BM)
+ *   expert_offsets [E+1] int32 out: exclusive prefix sum of cnt_e
+ *   padded_offsets [E+1] int32 out: exclusive prefix sum of roundup(cnt_e, BM)
+ * Slots with an id outside [0, E) are dropped and flag QMOE_DEV_INVALID_EXPERT.
+ * Limits: 1 <= E <= 256, 1 <= BM <= 1024, 0 <= T < 2^31 - E*BM. */
+qmoe_status_t qmoe_moe_align_block_size(const int32_t* topk_ids, int64_t T, int32_t E, int32_t BM,
+                                        int32_t* sorted_ids, int32_t* expert_ids,
+                                        int32_t* num_post_padded, int32_t* expert_offsets,
+                                        int32_t* padded_offsets, int32_t* d_status,
+                                        qmoe_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* quantisers                                                               */
+/* ------------------------------------------------------------------------ */
+/* Dynamic per-token FP8 activation quantisation (the "fp8dq" recipe of
+ * "Enabling MOE Quantization using linear decomposition", pytorch/ao PR 2043,
+ * Summary): for each row r of the bf16 matrix x[rows, cols] (row stride ldx),
+ * amax = max|x|, scale[r] = amax/448 (IEEE fp32 division; 1 if amax == 0),
+ * q[r, c] = e4m3(x/scale) with round-to-nearest-even and saturation to +-448.
+ *   q [rows, cols] bytes (row stride cols), scale [rows] fp32.
+ * cols >= 1.  16-byte aligned rows (ldx % 8 == 0, x 16-B aligned, cols % 8 ==
+ * 0) take the vector path; other shapes are accepted and give identical bytes. */
+qmoe_status_t qmoe_quant_act_fp8(const uint16_t* x, int64_t rows, int64_t cols, int64_t ldx,
+                                 uint8_t* q, float* scale, qmoe_stream_t stream);
+
+/* Per-output-channel weight quantisation, the same rule on fp32 rows: every
+ * (expert, output channel) row of W[E, N, K] is one row (rows = E*N).
+ * fp8: scale = amax/448, e4m3 codes; int8: scale = amax/127,
+ * q = clamp(rint(w/scale), -127, 127) (the "int8wo" recipe of the same page). */
+qmoe_status_t qmoe_quant_weight_fp8(const float* w, int64_t rows, int64_t cols,
+                                    uint8_t* q, float* scale, qmoe_stream_t stream);
+qmoe_status_t qmoe_quant_weight_int8(const float* w, int64_t rows, int64_t cols,
+                                     int8_t* q, float* scale, qmoe_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* grouped GEMM                                                             */
+/* ------------------------------------------------------------------------ */
+typedef struct {
+    size_t struct_size;            /* sizeof(qmoe_gemm_args), for ABI evolution */
+    /* activations */
+    const void* a;                 /* e4m3 bytes (w8a8) or bf16 bits (w8a16)     */
+    int64_t lda;                   /* row stride in elements                      */
+    const float* a_scale;          /* PER_TOKEN: [rows of A] fp32 (w8a8 only)     */
+    int32_t a_scale_mode;          /* QMOE_SCALE_*                                 */
+    const uint8_t* a_sf;           /* MX: E8M0 [sf rows, a_sf_ld]                 */
+    int64_t a_sf_ld;
+    const int32_t* a_sf_padded_offsets; /* MX: [E+1] first sf row of each expert */
+    int32_t a_layout;              /* QMOE_A_*                                     */
+    /* weights W[E, N, K] (K contiguous) */
+    const void* w;                 /* e4m3 bytes (w8a8) or int8 (w8a16)           */
+    const float* w_scale;          /* [E, N] fp32 per output channel              */
+    /* metadata from qmoe_moe_align_block_size with the same BM */
+    const int32_t* sorted_ids;
+    const int32_t* expert_ids;
+    const int32_t* num_post_padded;
+    const int32_t* expert_offsets;
+    const int32_t* padded_offsets;
+    const float* topk_weights;     /* [T] fp32 or NULL (no routing-weight multiply) */
+    /* output, bf16 */
+    uint16_t* out;
+    int32_t out_layout;            /* QMOE_OUT_*                                   */
+    int64_t M, N, K;
+    int32_t E, top_k, BM;
+    int32_t* d_status;
+} qmoe_gemm_args;
+
+/* FP8 W8A8 grouped GEMM (tables "FP8_W8A8 Benchmark" / "Model Results" of
+ * "Tianxing/moe quantization"):
+ *   out = w[s] * a_scale * w_scale[e, n] * sum_k e4m3(A)[k] * e4m3(W[e, n])[k]
+ * with fp32 accumulation on the tensor cores and a bf16 (RNE) result.
+ * Limits: K % 16 == 0, N % 16 == 0, 1 <= E <= 256, 1 <= top_k <= E,
+ * BM in {16, 32, 64, 128, 256}, a and w 16-byte aligned, lda % 16 == 0.
+ * TOKEN_SUM zeroes out[M, N] on the stream first and then adds the top_k slot
+ * rows of each token with bf16x2 atomics (for top_k == 2 the result does not
+ * depend on the order; for larger top_k the rounding order may vary).
+ * QMOE_SCALE_MX_1X32 is not supported yet (QMOE_ERR_UNSUPPORTED). */
+qmoe_status_t qmoe_moe_gemm_w8a8(const qmoe_gemm_args* args, qmoe_stream_t stream);
+
+/* INT8 W8A16 grouped GEMM (table "INT8_W8A16 Benchmark"): int8 weights are
+ * converted exactly to bf16 inside the kernel (offset-binary magic-number
+ * conversion after the int8->fp16 trick of the "INT8 quantization support"
+ * issue, casper-hansen/AutoAWQ 45, moved to fp32/bf16), multiplied with the
+ * bf16 activations on the tensor cores with fp32 accumulation, and the
+ * per-channel scale is applied in the epilogue:
+ *   out = w[s] * w_scale[e, n] * sum_k A[k] * q[e, n, k].
+ * Limits as for w8a8, with lda % 8 == 0 and a_scale unused. */
+qmoe_status_t qmoe_moe_gemm_w8a16(const qmoe_gemm_args* args, qmoe_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* SwiGLU + requantisation                                                  */
+/* ------------------------------------------------------------------------ */
+/* y[rows, 2I] bf16 (row stride ldy) holds gate (first I columns) and up (last
+ * I columns); h = silu(gate) * up in fp32 (silu(g) = g / (1 + exp(-g)),
+ * with exp evaluated by a fixed fp32 Cody-Waite + degree-7 Taylor sequence so
+ * that the result is reproducible bit for bit), then
+ *  mode QMOE_SCALE_PER_TOKEN: scale[r] = amax_r/448, q = e4m3(h/scale);
+ *  mode QMOE_SCALE_MX_1X32:   per 1x32 block along the row, e = smallest
+ *    integer with 448*2^e >= block amax (clamped to [-127, 127], 0 for an
+ *    all-zero block), sf byte e+127, q = e4m3(h*2^-e).
+ * MX rows are the expert-grouped compact rows: expert e owns rows
+ * [expert_offsets[e], expert_offsets[e+1]); its rowwise scale factors are
+ * written at sf rows sf_padded_offsets[e] + (r - expert_offsets[e]), and its
+ * pad rows up to sf_padded_offsets[e+1] and the pad columns past I/32 are
+ * zeroed -- the per-expert scale-factor padding of "[PyTorch] Let
+ * GroupedLinear accept MXFP8 input and gradient" (TransformerEngine PR 2099,
+ * the two-expert [64,128] example), done in the same launch.
+ *   q [rows, I] bytes; scale [rows] fp32 (PER_TOKEN); sf [.., sf_ld] (MX).
+ * Limits: I % 8 == 0 (I % 32 == 0 for MX), ldy % 8 == 0, y 16-B aligned,
+ * sf_ld >= I/32, 1 <= E <= 256 (MX). */
+qmoe_status_t qmoe_silu_mul_quant(const uint16_t* y, int64_t rows, int64_t I, int64_t ldy,
+                                  int32_t mode, uint8_t* q, float* scale, uint8_t* sf,
+                                  int64_t sf_ld, const int32_t* expert_offsets,
+                                  const int32_t* sf_padded_offsets, int32_t E,
+                                  int32_t* d_status, qmoe_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* element-level hooks used by the exhaustive tests                         */
+/* ------------------------------------------------------------------------ */
+/* e4m3 codes of n fp32 values with the same conversion the kernels use. */
+qmoe_status_t qmoe_debug_e4m3_encode(const float* x, uint8_t* q, int64_t n, qmoe_stream_t stream);
+/* bf16 bit patterns of n int8 values through the in-kernel W8A16 operand
+ * conversion (4 values per 32-bit word; n % 4 == 0, 4-byte aligned). */
+qmoe_status_t qmoe_debug_int8_to_bf16(const int8_t* x, uint16_t* y, int64_t n, qmoe_stream_t stream);
+/* h = silu(g) * u through the kernels' fp32 sequence, n values. */
+qmoe_status_t qmoe_debug_silu_mul(const float* g, const float* u, float* h, int64_t n,
+                                  qmoe_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* QMOE_H */

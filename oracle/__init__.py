@@ -87,6 +87,9 @@ def lib():
             L.orc_quant_rows_int8_f32.argtypes = [vp, i64, i64, i64, vp, vp]
             L.orc_silu_mul_quant_token.argtypes = [vp, i64, i64, i64, vp, vp]
             L.orc_silu_mul_quant_mx.argtypes = [vp, i64, i64, i64, vp, vp, i32, vp, vp, i64]
+            L.orc_e4m3_from_f32_array.argtypes = [vp, i64, vp]
+            L.orc_exp_f32_array.argtypes = [vp, i64, vp]
+            L.orc_silu_mul_f32_array.argtypes = [vp, vp, i64, vp]
             L.orc_moe_gemm.argtypes = [ctypes.c_int, vp, i64, vp, vp, i64, vp,
                                        ctypes.c_int, vp, vp, vp, vp, vp, i64, vp, i64, i64, vp]
             _lib = L
@@ -122,6 +125,28 @@ def e4m3_to_f64(b) -> np.ndarray:
 def e4m3_from_f32(x) -> np.ndarray:
     f = lib().orc_e4m3_from_f32
     return np.array([f(float(v)) for v in np.asarray(x, dtype=np.float32).ravel()], dtype=np.uint8)
+
+
+def e4m3_from_f32_array(x: np.ndarray) -> np.ndarray:
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    q = np.empty(x.shape, dtype=np.uint8)
+    lib().orc_e4m3_from_f32_array(_p(x), x.size, _p(q))
+    return q
+
+
+def exp_f32_array(x: np.ndarray) -> np.ndarray:
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    y = np.empty(x.shape, dtype=np.float32)
+    lib().orc_exp_f32_array(_p(x), x.size, _p(y))
+    return y
+
+
+def silu_mul_f32_array(g: np.ndarray, u: np.ndarray) -> np.ndarray:
+    g = np.ascontiguousarray(g, dtype=np.float32)
+    u = np.ascontiguousarray(u, dtype=np.float32)
+    h = np.empty(g.shape, dtype=np.float32)
+    lib().orc_silu_mul_f32_array(_p(g), _p(u), g.size, _p(h))
+    return h
 
 
 def e8m0_to_f64(b) -> np.ndarray:

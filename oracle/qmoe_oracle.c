@@ -392,3 +392,21 @@ void orc_moe_gemm(int a_kind, const void* a, int64_t lda, const float* a_scale,
         free(arow);
     }
 }
+
+/* ------------------------------------------------------------------------- */
+/* Array forms of the element functions above, for exhaustive comparisons.   */
+/* ------------------------------------------------------------------------- */
+void orc_e4m3_from_f32_array(const float* x, int64_t n, uint8_t* q) {
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < n; ++i) q[i] = orc_e4m3_from_f32(x[i]);
+}
+
+void orc_exp_f32_array(const float* x, int64_t n, float* y) {
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < n; ++i) y[i] = orc_exp_f32(x[i]);
+}
+
+void orc_silu_mul_f32_array(const float* g, const float* u, int64_t n, float* h) {
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < n; ++i) h[i] = orc_silu_mul_f32(g[i], u[i]);
+}

@@ -1,0 +1,312 @@
+"""Python binding of libqmoe.so (the quantized MoE grouped GEMM path on GB300).
+
+Argument marshalling only: every function here takes torch CUDA tensors,
+checks dtypes/devices, passes raw device pointers and the current CUDA stream
+to the C ABI declared in include/qmoe.h and raises on a non-OK status.  All
+arithmetic runs in the library's kernels; there is no CPU or PyTorch fallback,
+and a missing library is an ImportError-like failure at first use.
+
+Names follow the C entry points (without the ``qmoe_`` prefix).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libqmoe.so")
+_lib = None
+_lock = threading.Lock()
+
+QMOE_OK, QMOE_ERR_INVALID_ARG, QMOE_ERR_UNSUPPORTED, QMOE_ERR_CUDA = 0, 1, 2, 3
+DEV_INVALID_EXPERT, DEV_TIMEOUT = 1, 2
+SCALE_PER_TOKEN, SCALE_MX_1X32 = 0, 1
+A_TOKEN_GATHER, A_GROUPED = 0, 1
+OUT_SLOT, OUT_GROUPED, OUT_TOKEN_SUM = 0, 1, 2
+
+EXPORTED = (
+    "qmoe_status_string", "qmoe_version", "qmoe_align_max_padded", "qmoe_moe_align_block_size",
+    "qmoe_quant_act_fp8", "qmoe_quant_weight_fp8", "qmoe_quant_weight_int8", "qmoe_moe_gemm_w8a8",
+    "qmoe_moe_gemm_w8a16", "qmoe_silu_mul_quant", "qmoe_debug_e4m3_encode", "qmoe_debug_int8_to_bf16",
+    "qmoe_debug_silu_mul",
+)
+
+
+class QmoeError(RuntimeError):
+    pass
+
+
+class GemmArgs(ctypes.Structure):
+    _fields_ = [
+        ("struct_size", ctypes.c_size_t),
+        ("a", ctypes.c_void_p), ("lda", ctypes.c_int64), ("a_scale", ctypes.c_void_p),
+        ("a_scale_mode", ctypes.c_int32), ("a_sf", ctypes.c_void_p), ("a_sf_ld", ctypes.c_int64),
+        ("a_sf_padded_offsets", ctypes.c_void_p), ("a_layout", ctypes.c_int32),
+        ("w", ctypes.c_void_p), ("w_scale", ctypes.c_void_p),
+        ("sorted_ids", ctypes.c_void_p), ("expert_ids", ctypes.c_void_p), ("num_post_padded", ctypes.c_void_p),
+        ("expert_offsets", ctypes.c_void_p), ("padded_offsets", ctypes.c_void_p),
+        ("topk_weights", ctypes.c_void_p),
+        ("out", ctypes.c_void_p), ("out_layout", ctypes.c_int32),
+        ("M", ctypes.c_int64), ("N", ctypes.c_int64), ("K", ctypes.c_int64),
+        ("E", ctypes.c_int32), ("top_k", ctypes.c_int32), ("BM", ctypes.c_int32),
+        ("d_status", ctypes.c_void_p),
+    ]
+
+
+def load_library(path: str | None = None):
+    """Load libqmoe.so (built in-tree by quantized_moe_grouped_gb300.build)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            p = path or LIB_PATH
+            if not os.path.exists(p):
+                raise QmoeError(f"libqmoe.so not found at {p}; run `python -m quantized_moe_grouped_gb300.build`")
+            L = ctypes.CDLL(p)
+            vp, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32
+            st = ctypes.c_int
+            L.qmoe_status_string.argtypes = [st]
+            L.qmoe_status_string.restype = ctypes.c_char_p
+            L.qmoe_version.restype = ctypes.c_int
+            L.qmoe_align_max_padded.argtypes = [i64, i32, i32]
+            L.qmoe_align_max_padded.restype = i64
+            L.qmoe_moe_align_block_size.argtypes = [vp, i64, i32, i32, vp, vp, vp, vp, vp, vp, vp]
+            L.qmoe_quant_act_fp8.argtypes = [vp, i64, i64, i64, vp, vp, vp]
+            L.qmoe_quant_weight_fp8.argtypes = [vp, i64, i64, vp, vp, vp]
+            L.qmoe_quant_weight_int8.argtypes = [vp, i64, i64, vp, vp, vp]
+            L.qmoe_moe_gemm_w8a8.argtypes = [ctypes.POINTER(GemmArgs), vp]
+            L.qmoe_moe_gemm_w8a16.argtypes = [ctypes.POINTER(GemmArgs), vp]
+            L.qmoe_silu_mul_quant.argtypes = [vp, i64, i64, i64, i32, vp, vp, vp, i64, vp, vp, i32, vp, vp]
+            L.qmoe_debug_e4m3_encode.argtypes = [vp, vp, i64, vp]
+            L.qmoe_debug_int8_to_bf16.argtypes = [vp, vp, i64, vp]
+            L.qmoe_debug_silu_mul.argtypes = [vp, vp, vp, i64, vp]
+            for name in EXPORTED:
+                if name not in ("qmoe_status_string", "qmoe_version", "qmoe_align_max_padded"):
+                    getattr(L, name).restype = st
+            _lib = L
+    return _lib
+
+
+def _check(status: int, what: str) -> None:
+    if status != QMOE_OK:
+        msg = load_library().qmoe_status_string(status).decode()
+        raise QmoeError(f"{what}: {msg} (status {status})")
+
+
+def _ptr(t: torch.Tensor | None):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream: torch.cuda.Stream | None = None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _need(t: torch.Tensor, dtype, name: str):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise QmoeError(f"{name} must be a CUDA tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise QmoeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise QmoeError(f"{name} must be contiguous")
+
+
+# ----------------------------------------------------------------- align ---
+def align_max_padded(T: int, E: int, BM: int) -> int:
+    return int(load_library().qmoe_align_max_padded(int(T), int(E), int(BM)))
+
+
+def alloc_align_outputs(T: int, E: int, BM: int, device="cuda") -> dict:
+    cap = align_max_padded(T, E, BM)
+    i32 = torch.int32
+    return dict(sorted_ids=torch.empty(cap, dtype=i32, device=device),
+                expert_ids=torch.empty(cap // BM, dtype=i32, device=device),
+                num_post_padded=torch.empty(1, dtype=i32, device=device),
+                expert_offsets=torch.empty(E + 1, dtype=i32, device=device),
+                padded_offsets=torch.empty(E + 1, dtype=i32, device=device))
+
+
+def moe_align_block_size(topk_ids: torch.Tensor, E: int, BM: int, out: dict | None = None,
+                         d_status: torch.Tensor | None = None, stream=None) -> dict:
+    _need(topk_ids, torch.int32, "topk_ids")
+    T = topk_ids.numel()
+    o = out if out is not None else alloc_align_outputs(T, E, BM, topk_ids.device)
+    st = load_library().qmoe_moe_align_block_size(
+        _ptr(topk_ids), T, E, BM, _ptr(o["sorted_ids"]), _ptr(o["expert_ids"]), _ptr(o["num_post_padded"]),
+        _ptr(o["expert_offsets"]), _ptr(o["padded_offsets"]), _ptr(d_status), _stream(stream))
+    _check(st, "moe_align_block_size")
+    return o
+
+
+# ------------------------------------------------------------ quantisers ---
+def quant_act_fp8(x: torch.Tensor, q: torch.Tensor | None = None, scale: torch.Tensor | None = None, stream=None):
+    """bf16 [rows, cols] -> (e4m3 bytes uint8 [rows, cols], fp32 scale [rows])."""
+    if not x.is_cuda or x.dtype != torch.bfloat16 or x.dim() != 2 or x.stride(1) != 1:
+        raise QmoeError("x must be a 2-D CUDA bf16 tensor with unit column stride")
+    rows, cols = x.shape
+    q = q if q is not None else torch.empty(rows, cols, dtype=torch.uint8, device=x.device)
+    scale = scale if scale is not None else torch.empty(rows, dtype=torch.float32, device=x.device)
+    st = load_library().qmoe_quant_act_fp8(_ptr(x), rows, cols, x.stride(0), _ptr(q), _ptr(scale), _stream(stream))
+    _check(st, "quant_act_fp8")
+    return q, scale
+
+
+def quant_weight_fp8(w: torch.Tensor, stream=None):
+    """fp32 [..., K] -> (e4m3 uint8 [..., K], fp32 scale [...]) per row (output channel)."""
+    _need(w, torch.float32, "w")
+    K = w.shape[-1]
+    rows = w.numel() // K
+    q = torch.empty(w.shape, dtype=torch.uint8, device=w.device)
+    s = torch.empty(w.shape[:-1], dtype=torch.float32, device=w.device)
+    _check(load_library().qmoe_quant_weight_fp8(_ptr(w), rows, K, _ptr(q), _ptr(s), _stream(stream)),
+           "quant_weight_fp8")
+    return q, s
+
+
+def quant_weight_int8(w: torch.Tensor, stream=None):
+    _need(w, torch.float32, "w")
+    K = w.shape[-1]
+    rows = w.numel() // K
+    q = torch.empty(w.shape, dtype=torch.int8, device=w.device)
+    s = torch.empty(w.shape[:-1], dtype=torch.float32, device=w.device)
+    _check(load_library().qmoe_quant_weight_int8(_ptr(w), rows, K, _ptr(q), _ptr(s), _stream(stream)),
+           "quant_weight_int8")
+    return q, s
+
+
+# ------------------------------------------------------------------ GEMM ---
+def _gemm(fn_name, *, a, a_scale, w, w_scale, align, topk_weights, out, M, top_k, BM, a_layout, out_layout,
+          a_scale_mode=SCALE_PER_TOKEN, a_sf=None, a_sf_padded_offsets=None, d_status=None, stream=None):
+    E, N, K = w.shape
+    args = GemmArgs()
+    args.struct_size = ctypes.sizeof(GemmArgs)
+    args.a = a.data_ptr()
+    args.lda = a.stride(0)
+    args.a_scale = None if a_scale is None else a_scale.data_ptr()
+    args.a_scale_mode = a_scale_mode
+    args.a_sf = None if a_sf is None else a_sf.data_ptr()
+    args.a_sf_ld = 0 if a_sf is None else a_sf.stride(0)
+    args.a_sf_padded_offsets = None if a_sf_padded_offsets is None else a_sf_padded_offsets.data_ptr()
+    args.a_layout = a_layout
+    args.w = w.data_ptr()
+    args.w_scale = w_scale.data_ptr()
+    args.sorted_ids = align["sorted_ids"].data_ptr()
+    args.expert_ids = align["expert_ids"].data_ptr()
+    args.num_post_padded = align["num_post_padded"].data_ptr()
+    args.expert_offsets = align["expert_offsets"].data_ptr()
+    args.padded_offsets = align["padded_offsets"].data_ptr()
+    args.topk_weights = None if topk_weights is None else topk_weights.data_ptr()
+    args.out = out.data_ptr()
+    args.out_layout = out_layout
+    args.M, args.N, args.K = M, N, K
+    args.E, args.top_k, args.BM = E, top_k, BM
+    args.d_status = None if d_status is None else d_status.data_ptr()
+    st = getattr(load_library(), fn_name)(ctypes.byref(args), _stream(stream))
+    _check(st, fn_name)
+    return out
+
+
+def _out_for(out, out_layout, M, top_k, N, device):
+    if out is not None:
+        return out
+    rows = M if out_layout == OUT_TOKEN_SUM else M * top_k
+    return torch.empty(rows, N, dtype=torch.bfloat16, device=device)
+
+
+def moe_gemm_w8a8(a_q: torch.Tensor, a_scale: torch.Tensor, w_q: torch.Tensor, w_scale: torch.Tensor,
+                  align: dict, topk_weights: torch.Tensor | None, *, M: int, top_k: int, BM: int,
+                  a_layout: int = A_TOKEN_GATHER, out_layout: int = OUT_SLOT, out: torch.Tensor | None = None,
+                  d_status: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """FP8 W8A8 grouped GEMM.  a_q uint8 e4m3 [rows, K] (token rows for TOKEN_GATHER,
+    compact grouped rows for GROUPED), a_scale fp32 [rows], w_q uint8 e4m3 [E, N, K],
+    w_scale fp32 [E, N], align = moe_align_block_size(..., BM), topk_weights fp32 [M, top_k]
+    or None.  Returns bf16 [T, N] (SLOT/GROUPED) or [M, N] (TOKEN_SUM)."""
+    _need(a_q, torch.uint8, "a_q")
+    _need(w_q, torch.uint8, "w_q")
+    _need(a_scale, torch.float32, "a_scale")
+    _need(w_scale, torch.float32, "w_scale")
+    if topk_weights is not None:
+        _need(topk_weights, torch.float32, "topk_weights")
+    out = _out_for(out, out_layout, M, top_k, w_q.shape[1], a_q.device)
+    return _gemm("qmoe_moe_gemm_w8a8", a=a_q, a_scale=a_scale, w=w_q, w_scale=w_scale, align=align,
+                 topk_weights=topk_weights, out=out, M=M, top_k=top_k, BM=BM, a_layout=a_layout,
+                 out_layout=out_layout, d_status=d_status, stream=stream)
+
+
+def moe_gemm_w8a16(a: torch.Tensor, w_q: torch.Tensor, w_scale: torch.Tensor, align: dict,
+                   topk_weights: torch.Tensor | None, *, M: int, top_k: int, BM: int,
+                   a_layout: int = A_TOKEN_GATHER, out_layout: int = OUT_SLOT, out: torch.Tensor | None = None,
+                   d_status: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """INT8 W8A16 grouped GEMM: a bf16 [rows, K], w_q int8 [E, N, K], w_scale fp32 [E, N]."""
+    _need(a, torch.bfloat16, "a")
+    _need(w_q, torch.int8, "w_q")
+    _need(w_scale, torch.float32, "w_scale")
+    if topk_weights is not None:
+        _need(topk_weights, torch.float32, "topk_weights")
+    out = _out_for(out, out_layout, M, top_k, w_q.shape[1], a.device)
+    return _gemm("qmoe_moe_gemm_w8a16", a=a, a_scale=None, w=w_q, w_scale=w_scale, align=align,
+                 topk_weights=topk_weights, out=out, M=M, top_k=top_k, BM=BM, a_layout=a_layout,
+                 out_layout=out_layout, d_status=d_status, stream=stream)
+
+
+# ------------------------------------------------------ SwiGLU + quant ---
+def mx_sf_ld(I: int) -> int:
+    return (I // 32 + 3) // 4 * 4
+
+
+def silu_mul_quant(y: torch.Tensor, mode: int = SCALE_PER_TOKEN, *, expert_offsets=None, sf_padded_offsets=None,
+                   sf_rows: int | None = None, q=None, scale=None, sf=None, d_status=None, stream=None):
+    """y bf16 [rows, 2I] (gate | up) -> per-token: (q [rows, I] uint8, scale [rows] fp32);
+    MX: (q, sf [sf_rows, roundup(I/32, 4)] uint8).  For MX, sf_rows must be at
+    least sf_padded_offsets[E] (e.g. align_max_padded(T, E, 128))."""
+    if not y.is_cuda or y.dtype != torch.bfloat16 or y.dim() != 2 or y.stride(1) != 1:
+        raise QmoeError("y must be a 2-D CUDA bf16 tensor with unit column stride")
+    rows, two_i = y.shape
+    I = two_i // 2
+    q = q if q is not None else torch.empty(rows, I, dtype=torch.uint8, device=y.device)
+    L = load_library()
+    if mode == SCALE_PER_TOKEN:
+        scale = scale if scale is not None else torch.empty(rows, dtype=torch.float32, device=y.device)
+        st = L.qmoe_silu_mul_quant(_ptr(y), rows, I, y.stride(0), mode, _ptr(q), _ptr(scale), None, 0, None, None,
+                                   1, _ptr(d_status), _stream(stream))
+        _check(st, "silu_mul_quant")
+        return q, scale
+    _need(expert_offsets, torch.int32, "expert_offsets")
+    _need(sf_padded_offsets, torch.int32, "sf_padded_offsets")
+    E = expert_offsets.numel() - 1
+    ld = mx_sf_ld(I)
+    if sf is None:
+        if sf_rows is None:
+            raise QmoeError("sf_rows (capacity of the scale-factor matrix) is required when sf is not given")
+        sf = torch.empty(sf_rows, ld, dtype=torch.uint8, device=y.device)
+    st = L.qmoe_silu_mul_quant(_ptr(y), rows, I, y.stride(0), mode, _ptr(q), None, _ptr(sf), sf.stride(0),
+                               _ptr(expert_offsets), _ptr(sf_padded_offsets), E, _ptr(d_status), _stream(stream))
+    _check(st, "silu_mul_quant")
+    return q, sf
+
+
+# --------------------------------------------------------- element hooks ---
+def debug_e4m3_encode(x: torch.Tensor, stream=None) -> torch.Tensor:
+    _need(x, torch.float32, "x")
+    q = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+    _check(load_library().qmoe_debug_e4m3_encode(_ptr(x), _ptr(q), x.numel(), _stream(stream)), "debug_e4m3_encode")
+    return q
+
+
+def debug_int8_to_bf16(x: torch.Tensor, stream=None) -> torch.Tensor:
+    _need(x, torch.int8, "x")
+    y = torch.empty(x.shape, dtype=torch.bfloat16, device=x.device)
+    _check(load_library().qmoe_debug_int8_to_bf16(_ptr(x), _ptr(y), x.numel(), _stream(stream)),
+           "debug_int8_to_bf16")
+    return y
+
+
+def debug_silu_mul(g: torch.Tensor, u: torch.Tensor, stream=None) -> torch.Tensor:
+    _need(g, torch.float32, "g")
+    _need(u, torch.float32, "u")
+    h = torch.empty_like(g)
+    _check(load_library().qmoe_debug_silu_mul(_ptr(g), _ptr(u), _ptr(h), g.numel(), _stream(stream)),
+           "debug_silu_mul")
+    return h

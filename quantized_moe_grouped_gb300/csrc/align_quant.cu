@@ -1,0 +1,464 @@
+// align_quant.cu -- moe_align_block_size, the per-row FP8/INT8 quantisers,
+// SwiGLU + per-token / MXFP8 requantisation, and the element-level test hooks.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "common.cuh"
+#include "host_util.h"
+#include "qmoe.h"
+
+namespace qmoe {
+
+// ======================================================================
+// moe_align_block_size: one CTA of 1024 threads.
+//   1. histogram of expert ids in shared memory;
+//   2. exclusive prefix sums (unpadded and padded to BM) by one thread;
+//   3. sentinel fill of sorted_ids and the block -> expert map;
+//   4. stable scatter in chunks of 1024 slots: the rank of a slot among the
+//      slots of its expert in the same warp comes from __match_any_sync, the
+//      offset of the warp from a per-expert scan over the 32 warps, and the
+//      offset of the chunk from a running per-expert cursor.
+// ======================================================================
+constexpr int kAlignThreads = 1024;
+constexpr int kAlignMaxE = 256;
+
+__global__ void __launch_bounds__(kAlignThreads, 1)
+    align_kernel(const int32_t* __restrict__ ids, int64_t T, int E, int BM, int32_t* __restrict__ sorted_ids,
+                 int64_t sorted_cap, int32_t* __restrict__ expert_ids, int64_t blocks_cap,
+                 int32_t* __restrict__ num_post_padded, int32_t* __restrict__ expert_offsets,
+                 int32_t* __restrict__ padded_offsets, int32_t* d_status) {
+    __shared__ int s_cnt[kAlignMaxE];
+    __shared__ int s_poff[kAlignMaxE + 1];
+    __shared__ int s_cursor[kAlignMaxE];
+    __shared__ int s_wcnt[32 * kAlignMaxE];
+    __shared__ int s_bad;
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+
+    for (int e = tid; e < E; e += blockDim.x) {
+        s_cnt[e] = 0;
+        s_cursor[e] = 0;
+    }
+    for (int i = tid; i < 32 * E; i += blockDim.x) s_wcnt[i] = 0;
+    if (tid == 0) s_bad = 0;
+    __syncthreads();
+
+    for (int64_t s = tid; s < T; s += blockDim.x) {
+        const int e = ids[s];
+        if (e >= 0 && e < E) atomicAdd(&s_cnt[e], 1);
+        else s_bad = 1;
+    }
+    __syncthreads();
+
+    if (tid == 0) {
+        int off = 0, poff = 0;
+        for (int e = 0; e < E; ++e) {
+            expert_offsets[e] = off;
+            padded_offsets[e] = poff;
+            s_poff[e] = poff;
+            off += s_cnt[e];
+            poff += (s_cnt[e] + BM - 1) / BM * BM;
+        }
+        expert_offsets[E] = off;
+        padded_offsets[E] = poff;
+        s_poff[E] = poff;
+        *num_post_padded = poff;
+        if (s_bad && d_status) atomicOr(reinterpret_cast<int*>(d_status), QMOE_DEV_INVALID_EXPERT);
+    }
+    __syncthreads();
+
+    const int32_t sentinel = static_cast<int32_t>(T);
+    for (int64_t p = tid; p < sorted_cap; p += blockDim.x) sorted_ids[p] = sentinel;
+    for (int64_t b = tid; b < blocks_cap; b += blockDim.x) {
+        const int64_t p = b * BM;
+        int owner = -1;
+        if (p < s_poff[E]) {
+            int lo = 0, hi = E - 1;  // last e with s_poff[e] <= p
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (s_poff[mid] <= p) lo = mid;
+                else hi = mid - 1;
+            }
+            owner = lo;
+        }
+        expert_ids[b] = owner;
+    }
+    __syncthreads();
+
+    const unsigned lt_mask = (1u << lane) - 1u;
+    for (int64_t base = 0; base < T; base += blockDim.x) {
+        const int64_t s = base + tid;
+        int e = (s < T) ? ids[s] : -1;
+        const bool valid = (e >= 0 && e < E);
+        const int key = valid ? e : E;  // invalid slots only match each other
+        const unsigned peers = __match_any_sync(0xFFFFFFFFu, key);
+        const int rank = __popc(peers & lt_mask);
+        const int leader = __ffs(peers) - 1;
+        if (valid && lane == leader) s_wcnt[warp * E + e] = __popc(peers);
+        __syncthreads();
+        for (int ee = tid; ee < E; ee += blockDim.x) {
+            int run = s_cursor[ee];
+            for (int w = 0; w < 32; ++w) {
+                const int c = s_wcnt[w * E + ee];
+                s_wcnt[w * E + ee] = run;
+                run += c;
+            }
+            s_cursor[ee] = run;
+        }
+        __syncthreads();
+        if (valid) sorted_ids[s_poff[e] + s_wcnt[warp * E + e] + rank] = static_cast<int32_t>(s);
+        __syncthreads();
+        for (int i = tid; i < 32 * E; i += blockDim.x) s_wcnt[i] = 0;
+        __syncthreads();
+    }
+}
+
+// ======================================================================
+// Per-row quantisers: one CTA per row.  Pass 1 takes the row's amax, pass 2
+// re-reads the row (L1/L2) and writes the codes.  The vector path moves 8
+// elements per step (16-byte bf16 or 2x16-byte fp32 loads, 8-byte stores).
+// ======================================================================
+constexpr int kRowThreads = 256;
+
+QMOE_DI float block_max(float v, float* red) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+    const int warp = threadIdx.x >> 5;
+    if ((threadIdx.x & 31) == 0) red[warp] = v;
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        float x = (threadIdx.x < (blockDim.x >> 5)) ? red[threadIdx.x] : 0.0f;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xFFFFFFFFu, x, o));
+        if (threadIdx.x == 0) red[32] = x;
+    }
+    __syncthreads();
+    return red[32];
+}
+
+QMOE_DI void load8(const uint16_t* p, float (&v)[8]) {
+    const uint4 w = *reinterpret_cast<const uint4*>(p);
+    v[0] = bf16_lo(w.x); v[1] = bf16_hi(w.x); v[2] = bf16_lo(w.y); v[3] = bf16_hi(w.y);
+    v[4] = bf16_lo(w.z); v[5] = bf16_hi(w.z); v[6] = bf16_lo(w.w); v[7] = bf16_hi(w.w);
+}
+QMOE_DI void load8(const float* p, float (&v)[8]) {
+    const float4 a = *reinterpret_cast<const float4*>(p);
+    const float4 b = *reinterpret_cast<const float4*>(p + 4);
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+QMOE_DI float load1(const uint16_t* p) { return __uint_as_float(static_cast<uint32_t>(*p) << 16); }
+QMOE_DI float load1(const float* p) { return *p; }
+
+template <typename Tin, bool kVec>
+__global__ void __launch_bounds__(kRowThreads)
+    quant_rows_fp8_kernel(const Tin* __restrict__ x, int64_t cols, int64_t ldx, uint8_t* __restrict__ q,
+                          float* __restrict__ scale) {
+    __shared__ float red[33];
+    const int64_t row = blockIdx.x;
+    const Tin* xr = x + row * ldx;
+    uint8_t* qr = q + row * cols;
+    float amax = 0.0f;
+    if (kVec) {
+        for (int64_t c = static_cast<int64_t>(threadIdx.x) * 8; c < cols; c += kRowThreads * 8) {
+            float v[8];
+            load8(xr + c, v);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
+        }
+    } else {
+        for (int64_t c = threadIdx.x; c < cols; c += kRowThreads) amax = fmaxf(amax, fabsf(load1(xr + c)));
+    }
+    amax = block_max(amax, red);
+    const float s = (amax == 0.0f) ? 1.0f : __fdiv_rn(amax, 448.0f);
+    if (threadIdx.x == 0) scale[row] = s;
+    if (kVec) {
+        for (int64_t c = static_cast<int64_t>(threadIdx.x) * 8; c < cols; c += kRowThreads * 8) {
+            float v[8];
+            load8(xr + c, v);
+            uint2 o;
+            o.x = e4m3x4(__fdiv_rn(v[0], s), __fdiv_rn(v[1], s), __fdiv_rn(v[2], s), __fdiv_rn(v[3], s));
+            o.y = e4m3x4(__fdiv_rn(v[4], s), __fdiv_rn(v[5], s), __fdiv_rn(v[6], s), __fdiv_rn(v[7], s));
+            *reinterpret_cast<uint2*>(qr + c) = o;
+        }
+    } else {
+        for (int64_t c = threadIdx.x; c < cols; c += kRowThreads)
+            qr[c] = static_cast<uint8_t>(e4m3x2(__fdiv_rn(load1(xr + c), s), 0.0f) & 0xFFu);
+    }
+}
+
+__global__ void __launch_bounds__(kRowThreads)
+    quant_rows_int8_kernel(const float* __restrict__ x, int64_t cols, int8_t* __restrict__ q,
+                           float* __restrict__ scale) {
+    __shared__ float red[33];
+    const int64_t row = blockIdx.x;
+    const float* xr = x + row * cols;
+    int8_t* qr = q + row * cols;
+    float amax = 0.0f;
+    for (int64_t c = threadIdx.x; c < cols; c += kRowThreads) amax = fmaxf(amax, fabsf(xr[c]));
+    amax = block_max(amax, red);
+    const float s = (amax == 0.0f) ? 1.0f : __fdiv_rn(amax, 127.0f);
+    if (threadIdx.x == 0) scale[row] = s;
+    for (int64_t c = threadIdx.x; c < cols; c += kRowThreads) {
+        const float v = fminf(fmaxf(rintf(__fdiv_rn(xr[c], s)), -127.0f), 127.0f);
+        qr[c] = static_cast<int8_t>(static_cast<int>(v));
+    }
+}
+
+// ======================================================================
+// SwiGLU + requantisation.
+// Per-token: one CTA per row; h is kept in dynamic shared memory (I floats)
+// between the amax pass and the quantisation pass.
+// MX: one CTA per row, one thread per 1x32 block (h in registers); the CTA
+// also zeroes its row's pad columns and a share of its expert's pad rows.
+// ======================================================================
+QMOE_DI void silu8(const uint16_t* g, const uint16_t* u, float (&h)[8]) {
+    float gv[8], uv[8];
+    load8(g, gv);
+    load8(u, uv);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) h[i] = silu_mul(gv[i], uv[i]);
+}
+
+__global__ void __launch_bounds__(kRowThreads)
+    silu_quant_token_kernel(const uint16_t* __restrict__ y, int64_t I, int64_t ldy, uint8_t* __restrict__ q,
+                            float* __restrict__ scale) {
+    extern __shared__ float s_h[];
+    __shared__ float red[33];
+    const int64_t row = blockIdx.x;
+    const uint16_t* yr = y + row * ldy;
+    float amax = 0.0f;
+    for (int64_t c = static_cast<int64_t>(threadIdx.x) * 8; c < I; c += kRowThreads * 8) {
+        float h[8];
+        silu8(yr + c, yr + I + c, h);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            s_h[c + i] = h[i];
+            amax = fmaxf(amax, fabsf(h[i]));
+        }
+    }
+    amax = block_max(amax, red);  // (contains __syncthreads: s_h is complete)
+    const float s = (amax == 0.0f) ? 1.0f : __fdiv_rn(amax, 448.0f);
+    if (threadIdx.x == 0) scale[row] = s;
+    uint8_t* qr = q + row * I;
+    for (int64_t c = static_cast<int64_t>(threadIdx.x) * 8; c < I; c += kRowThreads * 8) {
+        const float* h = s_h + c;
+        uint2 o;
+        o.x = e4m3x4(__fdiv_rn(h[0], s), __fdiv_rn(h[1], s), __fdiv_rn(h[2], s), __fdiv_rn(h[3], s));
+        o.y = e4m3x4(__fdiv_rn(h[4], s), __fdiv_rn(h[5], s), __fdiv_rn(h[6], s), __fdiv_rn(h[7], s));
+        *reinterpret_cast<uint2*>(qr + c) = o;
+    }
+}
+
+constexpr int kMxThreads = 256;
+
+__global__ void __launch_bounds__(kMxThreads)
+    silu_quant_mx_kernel(const uint16_t* __restrict__ y, int64_t rows, int64_t I, int64_t ldy,
+                         uint8_t* __restrict__ q, uint8_t* __restrict__ sf, int64_t sf_ld,
+                         const int32_t* __restrict__ eoff, const int32_t* __restrict__ soff, int E,
+                         int32_t* d_status) {
+    __shared__ int s_e;
+    const int64_t r = blockIdx.x;
+    if (threadIdx.x == 0) {
+        int lo = 0, hi = E - 1, found = -1;  // last e with eoff[e] <= r, if r < eoff[e+1]
+        if (r < eoff[E]) {
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (eoff[mid] <= r) lo = mid;
+                else hi = mid - 1;
+            }
+            found = lo;
+        }
+        s_e = found;
+    }
+    __syncthreads();
+    const int e = s_e;
+    if (e < 0) return;  // row past the last expert's rows
+    const int64_t local = r - eoff[e];
+    const int64_t cnt = eoff[e + 1] - eoff[e];
+    const int64_t srow = soff[e] + local;
+    const int64_t prow_end = soff[e + 1];
+    const int64_t nblk = I / 32;
+    const uint16_t* yr = y + r * ldy;
+    uint8_t* qr = q + r * I;
+    uint8_t* sfr = sf + srow * sf_ld;
+    for (int64_t b = threadIdx.x; b < nblk; b += kMxThreads) {
+        float h[32];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            float t[8];
+            silu8(yr + b * 32 + c * 8, yr + I + b * 32 + c * 8, t);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) h[c * 8 + i] = t[i];
+        }
+        float a = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) a = fmaxf(a, fabsf(h[i]));
+        const int ex = mx_block_exponent(a);
+        const float mul = pow2_neg(ex);
+        sfr[b] = static_cast<uint8_t>(ex + 127);
+        uint4 o0, o1;
+        o0.x = e4m3x4(__fmul_rn(h[0], mul), __fmul_rn(h[1], mul), __fmul_rn(h[2], mul), __fmul_rn(h[3], mul));
+        o0.y = e4m3x4(__fmul_rn(h[4], mul), __fmul_rn(h[5], mul), __fmul_rn(h[6], mul), __fmul_rn(h[7], mul));
+        o0.z = e4m3x4(__fmul_rn(h[8], mul), __fmul_rn(h[9], mul), __fmul_rn(h[10], mul), __fmul_rn(h[11], mul));
+        o0.w = e4m3x4(__fmul_rn(h[12], mul), __fmul_rn(h[13], mul), __fmul_rn(h[14], mul), __fmul_rn(h[15], mul));
+        o1.x = e4m3x4(__fmul_rn(h[16], mul), __fmul_rn(h[17], mul), __fmul_rn(h[18], mul), __fmul_rn(h[19], mul));
+        o1.y = e4m3x4(__fmul_rn(h[20], mul), __fmul_rn(h[21], mul), __fmul_rn(h[22], mul), __fmul_rn(h[23], mul));
+        o1.z = e4m3x4(__fmul_rn(h[24], mul), __fmul_rn(h[25], mul), __fmul_rn(h[26], mul), __fmul_rn(h[27], mul));
+        o1.w = e4m3x4(__fmul_rn(h[28], mul), __fmul_rn(h[29], mul), __fmul_rn(h[30], mul), __fmul_rn(h[31], mul));
+        *reinterpret_cast<uint4*>(qr + b * 32) = o0;
+        *reinterpret_cast<uint4*>(qr + b * 32 + 16) = o1;
+    }
+    for (int64_t b = nblk + threadIdx.x; b < sf_ld; b += kMxThreads) sfr[b] = 0;  // pad columns
+    // pad rows of expert e: rows soff[e]+cnt .. prow_end-1, shared out over the expert's rows
+    for (int64_t pr = soff[e] + cnt + local; pr < prow_end; pr += cnt) {
+        uint8_t* pp = sf + pr * sf_ld;
+        for (int64_t b = threadIdx.x; b < sf_ld; b += kMxThreads) pp[b] = 0;
+    }
+    (void)rows;
+    (void)d_status;
+}
+
+// ======================================================================
+// element hooks for the exhaustive tests
+// ======================================================================
+__global__ void debug_e4m3_kernel(const float* __restrict__ x, uint8_t* __restrict__ q, int64_t n) {
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+        q[i] = static_cast<uint8_t>(e4m3x2(x[i], 0.0f) & 0xFFu);
+}
+__global__ void debug_i8_kernel(const uint32_t* __restrict__ x, uint2* __restrict__ y, int64_t nw) {
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < nw;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        uint32_t lo, hi;
+        int8x4_to_bf16x4(x[i], lo, hi);
+        y[i] = make_uint2(lo, hi);
+    }
+}
+__global__ void debug_silu_kernel(const float* __restrict__ g, const float* __restrict__ u, float* __restrict__ h,
+                                  int64_t n) {
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+        h[i] = silu_mul(g[i], u[i]);
+}
+
+static int grid_for(int64_t n, int threads) {
+    const int64_t b = (n + threads - 1) / threads;
+    const int64_t cap = static_cast<int64_t>(device_sm_count() > 0 ? device_sm_count() : 132) * 16;
+    return static_cast<int>(b < cap ? (b > 0 ? b : 1) : cap);
+}
+
+}  // namespace qmoe
+
+using namespace qmoe;
+
+extern "C" {
+
+int64_t qmoe_align_max_padded(int64_t T, int32_t E, int32_t BM) {
+    if (T < 0 || E < 1 || BM < 1) return -1;
+    const int64_t cap = T + static_cast<int64_t>(E) * (BM - 1);
+    return (cap + BM - 1) / BM * BM;
+}
+
+qmoe_status_t qmoe_moe_align_block_size(const int32_t* topk_ids, int64_t T, int32_t E, int32_t BM,
+                                        int32_t* sorted_ids, int32_t* expert_ids, int32_t* num_post_padded,
+                                        int32_t* expert_offsets, int32_t* padded_offsets, int32_t* d_status,
+                                        qmoe_stream_t stream) {
+    if (T < 0 || E < 1 || E > kAlignMaxE || BM < 1 || BM > 1024) return QMOE_ERR_INVALID_ARG;
+    const int64_t cap = qmoe_align_max_padded(T, E, BM);
+    if (cap >= (int64_t(1) << 31)) return QMOE_ERR_UNSUPPORTED;
+    if ((T > 0 && !topk_ids) || !sorted_ids || !expert_ids || !num_post_padded || !expert_offsets ||
+        !padded_offsets)
+        return QMOE_ERR_INVALID_ARG;
+    align_kernel<<<1, kAlignThreads, 0, stream>>>(topk_ids, T, E, BM, sorted_ids, cap, expert_ids, cap / BM,
+                                                  num_post_padded, expert_offsets, padded_offsets, d_status);
+    return launch_status();
+}
+
+qmoe_status_t qmoe_quant_act_fp8(const uint16_t* x, int64_t rows, int64_t cols, int64_t ldx, uint8_t* q,
+                                 float* scale, qmoe_stream_t stream) {
+    if (rows < 0 || cols < 1 || ldx < cols) return QMOE_ERR_INVALID_ARG;
+    if (rows == 0) return QMOE_OK;
+    if (!x || !q || !scale || rows > 0x7FFFFFFF) return QMOE_ERR_INVALID_ARG;
+    const bool vec = (cols % 8 == 0) && (ldx % 8 == 0) && aligned16(x) && ((reinterpret_cast<uintptr_t>(q) & 7) == 0);
+    if (vec)
+        quant_rows_fp8_kernel<uint16_t, true><<<static_cast<unsigned>(rows), kRowThreads, 0, stream>>>(x, cols, ldx, q, scale);
+    else
+        quant_rows_fp8_kernel<uint16_t, false><<<static_cast<unsigned>(rows), kRowThreads, 0, stream>>>(x, cols, ldx, q, scale);
+    return launch_status();
+}
+
+qmoe_status_t qmoe_quant_weight_fp8(const float* w, int64_t rows, int64_t cols, uint8_t* q, float* scale,
+                                    qmoe_stream_t stream) {
+    if (rows < 0 || cols < 1) return QMOE_ERR_INVALID_ARG;
+    if (rows == 0) return QMOE_OK;
+    if (!w || !q || !scale || rows > 0x7FFFFFFF) return QMOE_ERR_INVALID_ARG;
+    const bool vec = (cols % 8 == 0) && aligned16(w) && ((reinterpret_cast<uintptr_t>(q) & 7) == 0);
+    if (vec)
+        quant_rows_fp8_kernel<float, true><<<static_cast<unsigned>(rows), kRowThreads, 0, stream>>>(w, cols, cols, q, scale);
+    else
+        quant_rows_fp8_kernel<float, false><<<static_cast<unsigned>(rows), kRowThreads, 0, stream>>>(w, cols, cols, q, scale);
+    return launch_status();
+}
+
+qmoe_status_t qmoe_quant_weight_int8(const float* w, int64_t rows, int64_t cols, int8_t* q, float* scale,
+                                     qmoe_stream_t stream) {
+    if (rows < 0 || cols < 1) return QMOE_ERR_INVALID_ARG;
+    if (rows == 0) return QMOE_OK;
+    if (!w || !q || !scale || rows > 0x7FFFFFFF) return QMOE_ERR_INVALID_ARG;
+    quant_rows_int8_kernel<<<static_cast<unsigned>(rows), kRowThreads, 0, stream>>>(w, cols, q, scale);
+    return launch_status();
+}
+
+qmoe_status_t qmoe_silu_mul_quant(const uint16_t* y, int64_t rows, int64_t I, int64_t ldy, int32_t mode,
+                                  uint8_t* q, float* scale, uint8_t* sf, int64_t sf_ld,
+                                  const int32_t* expert_offsets, const int32_t* sf_padded_offsets, int32_t E,
+                                  int32_t* d_status, qmoe_stream_t stream) {
+    if (rows < 0 || I < 8 || I % 8 != 0 || ldy < 2 * I || ldy % 8 != 0) return QMOE_ERR_INVALID_ARG;
+    if (rows == 0) return QMOE_OK;
+    if (!y || !q || !aligned16(y) || !aligned16(q) || rows > 0x7FFFFFFF) return QMOE_ERR_INVALID_ARG;
+    if (mode == QMOE_SCALE_PER_TOKEN) {
+        if (!scale) return QMOE_ERR_INVALID_ARG;
+        const size_t smem = static_cast<size_t>(I) * sizeof(float);
+        if (smem > 200 * 1024) return QMOE_ERR_UNSUPPORTED;
+        if (smem > 48 * 1024) {
+            if (cudaFuncSetAttribute(silu_quant_token_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     static_cast<int>(smem)) != cudaSuccess)
+                return QMOE_ERR_CUDA;
+        }
+        silu_quant_token_kernel<<<static_cast<unsigned>(rows), kRowThreads, smem, stream>>>(y, I, ldy, q, scale);
+        return launch_status();
+    }
+    if (mode == QMOE_SCALE_MX_1X32) {
+        if (I % 32 != 0 || !sf || sf_ld < I / 32 || !expert_offsets || !sf_padded_offsets || E < 1 || E > 256)
+            return QMOE_ERR_INVALID_ARG;
+        silu_quant_mx_kernel<<<static_cast<unsigned>(rows), kMxThreads, 0, stream>>>(
+            y, rows, I, ldy, q, sf, sf_ld, expert_offsets, sf_padded_offsets, E, d_status);
+        return launch_status();
+    }
+    return QMOE_ERR_INVALID_ARG;
+}
+
+qmoe_status_t qmoe_debug_e4m3_encode(const float* x, uint8_t* q, int64_t n, qmoe_stream_t stream) {
+    if (n < 0 || (n > 0 && (!x || !q))) return QMOE_ERR_INVALID_ARG;
+    if (n == 0) return QMOE_OK;
+    debug_e4m3_kernel<<<grid_for(n, 256), 256, 0, stream>>>(x, q, n);
+    return launch_status();
+}
+
+qmoe_status_t qmoe_debug_int8_to_bf16(const int8_t* x, uint16_t* y, int64_t n, qmoe_stream_t stream) {
+    if (n < 0 || n % 4 != 0 || (n > 0 && (!x || !y || !aligned4(x) || (reinterpret_cast<uintptr_t>(y) & 7))))
+        return QMOE_ERR_INVALID_ARG;
+    if (n == 0) return QMOE_OK;
+    debug_i8_kernel<<<grid_for(n / 4, 256), 256, 0, stream>>>(reinterpret_cast<const uint32_t*>(x),
+                                                              reinterpret_cast<uint2*>(y), n / 4);
+    return launch_status();
+}
+
+qmoe_status_t qmoe_debug_silu_mul(const float* g, const float* u, float* h, int64_t n, qmoe_stream_t stream) {
+    if (n < 0 || (n > 0 && (!g || !u || !h))) return QMOE_ERR_INVALID_ARG;
+    if (n == 0) return QMOE_OK;
+    debug_silu_kernel<<<grid_for(n, 256), 256, 0, stream>>>(g, u, h, n);
+    return launch_status();
+}
+
+}  // extern "C"

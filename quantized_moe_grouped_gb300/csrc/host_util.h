@@ -1,0 +1,35 @@
+// host_util.h -- host-side helpers shared by the qmoe entry points.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "qmoe.h"
+
+namespace qmoe {
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+// Number of SMs of the current device (cached per device ordinal).
+inline int device_sm_count() {
+    static std::mutex mu;
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    std::lock_guard<std::mutex> g(mu);
+    if (cache[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+        cache[dev] = n;
+    }
+    return cache[dev];
+}
+
+inline qmoe_status_t launch_status() {
+    return cudaPeekAtLastError() == cudaSuccess ? QMOE_OK : QMOE_ERR_CUDA;
+}
+
+}  // namespace qmoe

@@ -1,0 +1,166 @@
+"""GPU parity of the integer and quantisation kernels against the CPU oracle:
+bit-exact sorting/padding, e4m3/int8 codes, scales, SwiGLU h and MX scale bytes."""
+import numpy as np
+import pytest
+import torch
+
+from quantized_moe_grouped_gb300 import inputs
+from tests.gpu_util import bf16_to_np_f32, dev, status, to_dev, to_dev_bf16
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def q():
+    import quantized_moe_grouped_gb300 as q
+    q.load_library()
+    return q
+
+
+def test_e4m3_conversion_exhaustive(q, orc):
+    """All 2^32 fp32 bit patterns except NaNs: hardware conversion == oracle encoder."""
+    chunk = 1 << 26
+    for c in range((1 << 32) // chunk):
+        bits = np.arange(chunk, dtype=np.uint32) + np.uint32(c * chunk)
+        x = bits.view(np.float32)
+        keep = ~np.isnan(x)
+        x = x[keep]
+        got = q.debug_e4m3_encode(to_dev(x)).cpu().numpy()
+        ref = orc.e4m3_from_f32_array(x)
+        bad = np.nonzero(got != ref)[0]
+        assert bad.size == 0, (c, x[bad[:4]], got[bad[:4]], ref[bad[:4]])
+
+
+def test_int8_to_bf16_exhaustive(q):
+    x = np.arange(-128, 128, dtype=np.int8)
+    y = q.debug_int8_to_bf16(to_dev(x)).float().cpu().numpy()
+    assert np.array_equal(y, x.astype(np.float32))
+
+
+def test_silu_sequence_bitexact(q, orc):
+    g = np.random.default_rng(1)
+    gs = np.concatenate([
+        (g.random(1 << 22, dtype=np.float32) * 220 - 110),
+        g.standard_normal(1 << 21).astype(np.float32) * 3,
+        np.array([0.0, -0.0, 89.0, -89.0, 104.0, -104.0, 1e-30, -1e-30, 3e38, -3e38], np.float32)])
+    us = g.standard_normal(gs.size).astype(np.float32)
+    got = q.debug_silu_mul(to_dev(gs), to_dev(us)).cpu().numpy()
+    ref = orc.silu_mul_f32_array(gs, us)
+    assert np.array_equal(got.view(np.uint32), ref.view(np.uint32))
+
+
+@pytest.mark.parametrize("M,E,BM", [(64, 8, 16), (64, 8, 32), (200, 8, 64), (4096, 8, 128), (4096, 8, 256),
+                                    (17, 3, 16), (1, 1, 16), (3000, 64, 32), (512, 256, 16)])
+def test_align_bitexact(q, orc, M, E, BM):
+    ids, _ = inputs.routing(M, E, 2 if E > 1 else 1, seed=M + E)
+    st = status()
+    al = q.moe_align_block_size(to_dev(ids), E, BM, d_status=st)
+    ref = orc.moe_align(ids, E, BM)
+    cap = q.align_max_padded(ids.size, E, BM)
+    assert int(st.item()) == 0
+    assert int(al["num_post_padded"].item()) == ref["num_post_padded"]
+    assert np.array_equal(al["sorted_ids"].cpu().numpy(), ref["sorted_ids"][:cap])
+    assert np.array_equal(al["expert_ids"].cpu().numpy(), ref["expert_ids"][: cap // BM])
+    assert np.array_equal(al["expert_offsets"].cpu().numpy(), ref["expert_offsets"])
+    assert np.array_equal(al["padded_offsets"].cpu().numpy(), ref["padded_offsets"])
+
+
+def test_align_skewed_empty_and_invalid(q, orc):
+    ids, _ = inputs.routing(4096, 8, 2, seed=4000, zipf_s=1.2)
+    al = q.moe_align_block_size(to_dev(ids), 8, 128)
+    ref = orc.moe_align(ids, 8, 128)
+    assert np.array_equal(al["sorted_ids"].cpu().numpy(), ref["sorted_ids"])
+    # empty input
+    al0 = q.moe_align_block_size(to_dev(np.zeros(0, np.int32)), 8, 16)
+    assert int(al0["num_post_padded"].item()) == 0
+    assert np.all(al0["sorted_ids"].cpu().numpy() == 0)     # sentinel T == 0
+    assert np.all(al0["expert_ids"].cpu().numpy() == -1)
+    # ids outside [0, E) are dropped and flagged
+    bad = np.array([0, 1, 9, -1, 1, 2], dtype=np.int32)
+    st = status()
+    alb = q.moe_align_block_size(to_dev(bad), 3, 16, d_status=st)
+    refb = orc.moe_align(bad, 3, 16)
+    assert int(st.item()) == q.DEV_INVALID_EXPERT and refb["invalid"]
+    assert np.array_equal(alb["sorted_ids"].cpu().numpy(), refb["sorted_ids"])
+
+
+@pytest.mark.parametrize("rows,cols", [(64, 128), (64, 4096), (333, 6144), (5, 100), (7, 24), (1, 8)])
+def test_quant_act_bitexact(q, orc, rows, cols):
+    x = inputs.activations_bf16(rows, cols, seed=rows + cols)
+    x[0, :] = 0                                   # zero row -> scale 1
+    if rows > 2:
+        x[1, ::3] = 0x8000                        # negative zeros
+        x[2, :] = x[2, 0]                         # constant row
+    qa, sa = q.quant_act_fp8(to_dev_bf16(x))
+    ref_q, ref_s = orc.quant_rows_fp8_bf16(x)
+    assert np.array_equal(qa.cpu().numpy(), ref_q)
+    assert np.array_equal(sa.cpu().numpy().view(np.uint32), ref_s.view(np.uint32))
+
+
+def test_quant_act_strided_rows(q, orc):
+    x = inputs.activations_bf16(40, 256, seed=3)
+    xd = to_dev_bf16(x)[:, :200]                  # ldx = 256, cols = 200
+    qa, sa = q.quant_act_fp8(xd)
+    ref_q, ref_s = orc.quant_rows_fp8_bf16(np.ascontiguousarray(x[:, :200]))
+    assert np.array_equal(qa.cpu().numpy(), ref_q) and np.array_equal(sa.cpu().numpy(), ref_s)
+
+
+@pytest.mark.parametrize("E,N,K", [(8, 256, 128), (3, 40, 100), (2, 64, 4096)])
+def test_quant_weights_bitexact(q, orc, E, N, K):
+    w = inputs.expert_weights_f32(E, N, K, seed=E * N)
+    w[0, 0, :] = 0
+    wq, ws = q.quant_weight_fp8(to_dev(w))
+    rq, rs = orc.quant_rows_fp8_f32(w)
+    assert np.array_equal(wq.cpu().numpy(), rq) and np.array_equal(ws.cpu().numpy(), rs)
+    wq8, ws8 = q.quant_weight_int8(to_dev(w))
+    rq8, rs8 = orc.quant_rows_int8_f32(w)
+    assert np.array_equal(wq8.cpu().numpy(), rq8) and np.array_equal(ws8.cpu().numpy(), rs8)
+
+
+@pytest.mark.parametrize("R,I", [(64, 256), (300, 1024), (8, 14336), (3, 40)])
+def test_silu_quant_token_bitexact(q, orc, R, I):
+    y = inputs.activations_bf16(R, 2 * I, seed=R + I)
+    y[0, :] = 0
+    qq, ss = q.silu_mul_quant(to_dev_bf16(y))
+    rq, rs = orc.silu_mul_quant_token(y)
+    assert np.array_equal(qq.cpu().numpy(), rq)
+    assert np.array_equal(ss.cpu().numpy().view(np.uint32), rs.view(np.uint32))
+
+
+@pytest.mark.parametrize("cnt,I", [([64, 64], 128), ([5, 0, 130, 1, 300, 0, 7, 9], 96),
+                                   ([1000, 40, 0, 513], 1024), ([3], 16384)])
+def test_silu_quant_mx_bitexact(q, orc, cnt, I):
+    R = sum(cnt)
+    E = len(cnt)
+    y = inputs.activations_bf16(R, 2 * I, seed=R + I + E)
+    y[0, :64] = 0                                             # an all-zero 1x32 block
+    eoff = np.array([0] + list(np.cumsum(cnt)), dtype=np.int32)
+    soff = np.array([0] + list(np.cumsum([-(-c // 128) * 128 for c in cnt])), dtype=np.int32)
+    ld = q.mx_sf_ld(I)
+    sf = torch.full((int(soff[-1]) + 5, ld), 0xAB, dtype=torch.uint8, device=dev())   # poison, incl. 5 spare rows
+    qq, sfo = q.silu_mul_quant(to_dev_bf16(y), q.SCALE_MX_1X32, expert_offsets=to_dev(eoff),
+                               sf_padded_offsets=to_dev(soff), sf=sf)
+    rq, rsf = orc.silu_mul_quant_mx(y, eoff, soff)
+    assert np.array_equal(qq.cpu().numpy(), rq)
+    got = sfo.cpu().numpy()
+    assert np.array_equal(got[: soff[-1]], rsf)
+    assert np.all(got[soff[-1]:] == 0xAB)                     # nothing written past the padded rows
+
+
+def test_silu_quant_mx_whole_equals_per_expert(q):
+    """Quantising the concatenated expert rows as a whole equals quantising
+    each expert's rows on its own: identical data, identical padded scale
+    factors (the two-expert example of the TransformerEngine MXFP8 page)."""
+    cnt, I = [64, 64], 128
+    y = inputs.activations_bf16(128, 2 * I, seed=99)
+    yd = to_dev_bf16(y)
+    eoff = to_dev(np.array([0, 64, 128], np.int32))
+    soff = to_dev(np.array([0, 128, 256], np.int32))
+    qw, sfw = q.silu_mul_quant(yd, q.SCALE_MX_1X32, expert_offsets=eoff, sf_padded_offsets=soff, sf_rows=256)
+    for e in range(2):
+        qe, sfe = q.silu_mul_quant(yd[e * 64:(e + 1) * 64], q.SCALE_MX_1X32,
+                                   expert_offsets=to_dev(np.array([0, 64], np.int32)),
+                                   sf_padded_offsets=to_dev(np.array([0, 128], np.int32)), sf_rows=128)
+        assert torch.equal(qe, qw[e * 64:(e + 1) * 64])
+        assert torch.equal(sfe, sfw[e * 128:(e + 1) * 128])
+        assert sfe.shape == (128, 4)

@@ -139,3 +139,12 @@ def test_silu_mul_vs_fp64(orc):
     for a, b, h in zip(gs, us, hs):
         ref = float(a) / (1.0 + math.exp(-float(a))) * float(b) if float(a) > -700 else 0.0
         assert abs(float(h) - ref) <= 6 * f32_ulp(ref) + 2.0 ** -140, (a, b, h, ref)
+
+
+def test_array_forms_match_scalar_forms(orc):
+    g = np.random.default_rng(17)
+    x = (g.standard_normal(5000) * 30).astype(np.float32)
+    u = g.standard_normal(5000).astype(np.float32)
+    assert np.array_equal(orc.e4m3_from_f32_array(x), orc.e4m3_from_f32(x))
+    assert np.array_equal(orc.exp_f32_array(x / 4), orc.exp_f32(x / 4))
+    assert np.array_equal(orc.silu_mul_f32_array(x / 8, u), orc.silu_mul_f32(x / 8, u))
