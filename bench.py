@@ -3,8 +3,9 @@
 Workload: K=4096, N=14336, E=8, top_k=2, M in {64, 128, 256, 512}; A bf16
 N(0,1), W N(0,1/K) quantised per output channel to e4m3, router logits N(0,1)
 -> softmax -> top-2 (renormalised).  One step = one pass of the whole path for
-each M: moe_align_block_size -> quant_act_fp8 -> moe_gemm_w8a8 (SLOT output
-[M, 2, N] bf16 with the routing-weight multiply).  Weights (470 MB of e4m3)
+each M: moe_align_block_size -> quant_act_fp8_sorted (per-token e4m3, rows
+written in padded sorted order) -> moe_gemm_w8a8 (PADDED activation tiles by
+TMA, SLOT output [M, 2, N] bf16 with the routing-weight multiply).  Weights (470 MB of e4m3)
 exceed the 129 MB L2, so every GEMM streams them from HBM.
 
 value  = algorithmic bytes of the four GEMMs / device time of the timed steps
@@ -45,10 +46,10 @@ PAGE_ROWS = ((64, 47.124442, 1480.603863), (128, 93.602312, 1478.376964),
 
 def slot_tile(M: int) -> int:
     """Slot tile (BM) per M: the smallest power of two >= twice the mean slots
-    per expert, in [16, 256], so most experts fit one tile."""
+    per expert, in [16, 128] (BM <= 64 runs the swapped tile, 128 the wide one)."""
     mean = 2 * M * TOP_K // E
     bm = 16
-    while bm < mean and bm < 256:
+    while bm < mean and bm < 128:
         bm *= 2
     return bm
 
@@ -98,7 +99,7 @@ class ClockSampler:
         try:
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
                                          stdout=self.fh, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
@@ -158,8 +159,8 @@ def setup(dev, seed_base=1000):
                   a=torch.from_numpy(a_bits.view(np.int16)).to(dev).view(torch.bfloat16),
                   ids=torch.from_numpy(ids).to(dev), tw=torch.from_numpy(tw).to(dev),
                   align=q.alloc_align_outputs(T, E, BM, dev),
-                  aq=torch.empty(M, K_DIM, dtype=torch.uint8, device=dev),
-                  sa=torch.empty(M, dtype=torch.float32, device=dev),
+                  aq=torch.empty(q.align_max_padded(T, E, BM), K_DIM, dtype=torch.uint8, device=dev),
+                  sa=torch.empty(q.align_max_padded(T, E, BM), dtype=torch.float32, device=dev),
                   out=torch.empty(T, N_DIM, dtype=torch.bfloat16, device=dev),
                   bytes=algorithmic_bytes(M, ids), flops=flops(M))
         # pinned host buffers for the end-to-end leg
@@ -174,52 +175,57 @@ def setup(dev, seed_base=1000):
 def run_path(q, wq, ws, sh, stream, ev=None):
     """One pass of the path for one shape; ev = (before_gemm, after_gemm) events or None."""
     q.moe_align_block_size(sh["ids"], E, sh["BM"], out=sh["align"], stream=stream)
-    q.quant_act_fp8(sh["a"], q=sh["aq"], scale=sh["sa"], stream=stream)
+    q.quant_act_fp8_sorted(sh["a"], sh["align"], TOP_K, q=sh["aq"], scale=sh["sa"], stream=stream)
     if ev is not None:
         ev[0].record(stream)
     q.moe_gemm_w8a8(sh["aq"], sh["sa"], wq, ws, sh["align"], sh["tw"], M=sh["M"], top_k=TOP_K, BM=sh["BM"],
-                    out=sh["out"], stream=stream)
+                    a_layout=q.A_PADDED, out=sh["out"], stream=stream)
     if ev is not None:
         ev[1].record(stream)
 
 
 # ---------------------------------------------------------- CPU oracle ---
-def oracle_sample(seconds: float = 12.0, seed_base=1000, threads: int | None = None):
-    """Time the CPU oracle (dense per-token expert loop in fp64) on a bounded
-    random sample of slots of the sweep; returns (sweep GB/s, cores, sample text)."""
-    import oracle
-    from quantized_moe_grouped_gb300 import inputs
+class OracleBench:
+    """The CPU oracle (dense per-token expert loop in fp64, as it stands) on a
+    bounded random sample of slots of the M=64 shape; the measured per-slot time
+    is extrapolated to every slot of the sweep (the oracle's cost per slot does
+    not depend on M)."""
 
-    if threads:
-        oracle.set_num_threads(threads)
-    cores = oracle.num_threads()
-    rwq = np.empty((E, N_DIM, K_DIM), dtype=np.uint8)
-    rws = np.empty((E, N_DIM), dtype=np.float32)
-    for e in range(E):
-        rwq[e], rws[e] = oracle.quant_rows_fp8_f32(inputs.expert_weight_f32(N_DIM, K_DIM, seed_base, e))
-    M = SWEEP_M[0]
-    a = inputs.activations_bf16(M, K_DIM, seed_base)
-    ids, tw = inputs.routing(M, E, TOP_K, seed_base)
-    raq, rsa = oracle.quant_rows_fp8_bf16(a)
-    T = M * TOP_K
-    rng = np.random.default_rng(0)
-    n, elapsed, done = max(cores, 1), 0.0, 0
-    while elapsed < seconds and done < T:
-        take = min(n, T - done)
-        slots = rng.choice(T, take, replace=False)
-        t0 = time.perf_counter()
-        oracle.moe_gemm(a_kind=oracle.A_FP8_TOKEN, a=raq, a_scale=rsa, w_kind=oracle.W_FP8, w=rwq, w_scale=rws,
-                        topk_ids=ids, topk_w=tw, E=E, slots=slots)
-        elapsed += time.perf_counter() - t0
-        done += take
-    t_slot = elapsed / done
-    tot_bytes = sum(algorithmic_bytes(m, inputs.routing(m, E, TOP_K, seed_base + i)[0])
-                    for i, m in enumerate(SWEEP_M))
-    tot_time = sum(m * TOP_K for m in SWEEP_M) * t_slot
-    sample = (f"{done} random slots of the M=64 shape (K=4096, N=14336, fp64 dense per-slot loop), "
-              f"{elapsed:.1f} s; per-slot time extrapolated to all {sum(m * TOP_K for m in SWEEP_M)} slots "
-              f"of the sweep")
-    return tot_bytes / tot_time / 1e9, tot_bytes, tot_time, cores, sample
+    def __init__(self, seed_base=1000):
+        import oracle
+        from quantized_moe_grouped_gb300 import inputs
+        self.oracle = oracle
+        self.cores = oracle.num_threads()
+        self.rwq = np.empty((E, N_DIM, K_DIM), dtype=np.uint8)
+        self.rws = np.empty((E, N_DIM), dtype=np.float32)
+        for e in range(E):
+            self.rwq[e], self.rws[e] = oracle.quant_rows_fp8_f32(inputs.expert_weight_f32(N_DIM, K_DIM, seed_base, e))
+        M = SWEEP_M[0]
+        a = inputs.activations_bf16(M, K_DIM, seed_base)
+        self.ids, self.tw = inputs.routing(M, E, TOP_K, seed_base)
+        self.raq, self.rsa = oracle.quant_rows_fp8_bf16(a)
+        self.T = M * TOP_K
+        self.sweep_slots = sum(m * TOP_K for m in SWEEP_M)
+        self.sweep_bytes = sum(algorithmic_bytes(m, inputs.routing(m, E, TOP_K, seed_base + i)[0])
+                               for i, m in enumerate(SWEEP_M))
+        self.rng = np.random.default_rng(0)
+
+    def run(self, seconds: float):
+        o = self.oracle
+        n, elapsed, done = max(self.cores, 1), 0.0, 0
+        while elapsed < seconds and done < self.T:
+            take = min(n, self.T - done)
+            slots = self.rng.choice(self.T, take, replace=False)
+            t0 = time.perf_counter()
+            o.moe_gemm(a_kind=o.A_FP8_TOKEN, a=self.raq, a_scale=self.rsa, w_kind=o.W_FP8, w=self.rwq,
+                       w_scale=self.rws, topk_ids=self.ids, topk_w=self.tw, E=E, slots=slots)
+            elapsed += time.perf_counter() - t0
+            done += take
+        t_sweep = self.sweep_slots * elapsed / done
+        sample = (f"{done} random slots of the M=64 shape (K=4096, N=14336; fp64 dense per-slot loop) in "
+                  f"{elapsed:.1f} s on {self.cores} threads; per-slot time extrapolated to the "
+                  f"{self.sweep_slots} slots of the sweep")
+        return self.sweep_bytes / t_sweep / 1e9, t_sweep, sample
 
 
 def run_reference(args) -> None:
@@ -227,20 +233,21 @@ def run_reference(args) -> None:
     if rank != 0:
         return
     steps, warmup = args.steps, args.warmup
-    per_step = max(1.0, min(6.0, 150.0 / max(1, steps + warmup)))
-    vals = []
-    cores, sample = None, None
+    per_step = min(6.0, 120.0 / max(1, steps + warmup))  # one slot batch at least
+    ob = OracleBench()
+    vals, times = [], []
+    sample = None
     for i in range(warmup + steps):
-        v, _, _, cores, sample = oracle_sample(seconds=per_step)
+        v, t_sweep, sample = ob.run(per_step)
         if i >= warmup:
             vals.append(v)
+            times.append(t_sweep)
     value = statistics.median(vals)
-    tot_bytes = sum(algorithmic_bytes(m, np.zeros(1)) for m in SWEEP_M)
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
-            "steps": steps, "warmup": warmup, "ms_per_step": tot_bytes / (value * 1e9) * 1e3,
+            "steps": steps, "warmup": warmup, "ms_per_step": statistics.median(times) * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": {"workload": WORKLOAD, "oracle": "CPU fp64 dense per-token expert loop"},
-            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample},
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": ob.cores, "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
             "gpu_launches": 0}
     print(json.dumps(line), flush=True)
@@ -250,8 +257,8 @@ def run_reference(args) -> None:
 def main() -> None:
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
-    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
@@ -348,8 +355,9 @@ def main() -> None:
     if rank == 0:
         cpu = None
         if world == 1 and not args.no_cpu_baseline:
-            v, _, _, cores, sample = oracle_sample(seconds=12.0)
-            cpu = {"value": v, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample}
+            ob = OracleBench()
+            v, _, sample = ob.run(12.0)
+            cpu = {"value": v, "unit": "GB/s", "cores": ob.cores, "kind": "oracle", "sample": sample}
         sweep = [{"M": sh["M"], "BM": sh["BM"], "gemm_us": g * 1e3, "gemm_GBps": sh["bytes"] / (g * 1e-3) / 1e9,
                   "gemm_TFLOPS": sh["flops"] / (g * 1e-3) / 1e12,
                   "gemm_frac_hbm": sh["bytes"] / (g * 1e-3) / 1e9 / peak, "bytes": sh["bytes"]}

@@ -59,6 +59,9 @@ typedef enum {
 /* A row layouts */
 #define QMOE_A_TOKEN_GATHER 0 /* slot s reads A row s / top_k ([M, K])        */
 #define QMOE_A_GROUPED 1      /* slot s reads its compact expert-grouped row ([T, K]) */
+#define QMOE_A_PADDED 2       /* slot at padded sorted position p reads row p
+                                 ([qmoe_align_max_padded(T,E,BM), K], written by
+                                 qmoe_quant_act_fp8_sorted)                      */
 /* output layouts */
 #define QMOE_OUT_SLOT 0      /* out[s, :] of [T, N] == [M, top_k, N]                  */
 #define QMOE_OUT_GROUPED 1   /* out[compact row of s, :] of [T, N] (expert-contiguous) */
@@ -109,6 +112,20 @@ qmoe_status_t qmoe_moe_align_block_size(const int32_t* topk_ids, int64_t T, int3
 qmoe_status_t qmoe_quant_act_fp8(const uint16_t* x, int64_t rows, int64_t cols, int64_t ldx,
                                  uint8_t* q, float* scale, qmoe_stream_t stream);
 
+/* The same per-token quantisation, with the rows written in the padded sorted
+ * order of the grouped GEMM: for every padded position p < *num_post_padded
+ * with s = sorted_ids[p] < T, row p of q (and scale[p]) is the quantised token
+ * row x[s / top_k]; pad positions get zero codes and scale 0; rows at or past
+ * *num_post_padded are not written.  This fuses the per-slot row gather into
+ * the quantiser, so the GEMM reads its activation tiles as contiguous boxes
+ * (QMOE_A_PADDED).  q holds cap = qmoe_align_max_padded(T, E, BM) rows of
+ * cols bytes; scale cap floats.  Limits: cols % 16 == 0, ldx % 8 == 0,
+ * x and q 16-byte aligned. */
+qmoe_status_t qmoe_quant_act_fp8_sorted(const uint16_t* x, int64_t M, int64_t cols, int64_t ldx,
+                                        const int32_t* sorted_ids, const int32_t* num_post_padded,
+                                        int32_t top_k, int64_t cap, uint8_t* q, float* scale,
+                                        qmoe_stream_t stream);
+
 /* Per-output-channel weight quantisation, the same rule on fp32 rows: every
  * (expert, output channel) row of W[E, N, K] is one row (rows = E*N).
  * fp8: scale = amax/448, e4m3 codes; int8: scale = amax/127,
@@ -148,6 +165,10 @@ typedef struct {
     int64_t M, N, K;
     int32_t E, top_k, BM;
     int32_t* d_status;
+    /* QMOE_OUT_TOKEN_SUM only: fp32 [M, N] scratch owned by the caller (16-byte
+     * aligned).  The library zeroes it, adds every routed slot result into it
+     * in fp32, and writes out = bf16(accum) with a second launch. */
+    float* accum;
 } qmoe_gemm_args;
 
 /* FP8 W8A8 grouped GEMM (tables "FP8_W8A8 Benchmark" / "Model Results" of
@@ -156,9 +177,11 @@ typedef struct {
  * with fp32 accumulation on the tensor cores and a bf16 (RNE) result.
  * Limits: K % 16 == 0, N % 16 == 0, 1 <= E <= 256, 1 <= top_k <= E,
  * BM in {16, 32, 64, 128, 256}, a and w 16-byte aligned, lda % 16 == 0.
- * TOKEN_SUM zeroes out[M, N] on the stream first and then adds the top_k slot
- * rows of each token with bf16x2 atomics (for top_k == 2 the result does not
- * depend on the order; for larger top_k the rounding order may vary).
+ * TOKEN_SUM (the routing-weighted sum over the top_k slots of a token) needs
+ * args->accum: the slot results are added into it with fp32 atomics and a
+ * second launch rounds the sums to bf16 into out[M, N].  For top_k == 2 the
+ * result does not depend on the order of the additions (0 + a + b == 0 + b + a
+ * in IEEE arithmetic); for larger top_k the fp32 rounding order may vary.
  * QMOE_SCALE_MX_1X32 is not supported yet (QMOE_ERR_UNSUPPORTED). */
 qmoe_status_t qmoe_moe_gemm_w8a8(const qmoe_gemm_args* args, qmoe_stream_t stream);
 

@@ -286,12 +286,24 @@ def compact_row_of_slot(topk_ids: np.ndarray, E: int) -> np.ndarray:
     return pos
 
 
+def padded_row_of_slot(topk_ids: np.ndarray, E: int, BM: int) -> np.ndarray:
+    """Padded sorted position of every slot (the oracle's own align with BM)."""
+    ids = np.asarray(topk_ids, dtype=np.int32).ravel()
+    al = moe_align(ids, E, BM)
+    pos = np.empty(ids.size, dtype=np.int64)
+    srt = al["sorted_ids"][: al["num_post_padded"]]
+    valid = srt < ids.size
+    pos[srt[valid]] = np.nonzero(valid)[0]
+    return pos
+
+
 def moe_gemm(*, a_kind, a, a_scale=None, a_sf=None, a_sf_row=None, w_kind, w, w_scale,
-             topk_ids, topk_w, E, a_layout="token", out_layout="slot", slots=None):
+             topk_ids, topk_w, E, a_layout="token", out_layout="slot", slots=None, BM=None):
     """Whole grouped GEMM in fp64 with the requested layouts.
 
     a_layout "token": A row of slot s is s // top_k; "grouped": A row of slot
-    s is its compact grouped position.  out_layout "slot": [T, N] indexed by
+    s is its compact grouped position; "padded": A row of slot s is its padded
+    sorted position for tile size BM.  out_layout "slot": [T, N] indexed by
     s; "grouped": [T, N] indexed by compact position; "token_sum": [M, N], the
     sum over j of slot rows m*top_k + j.  With ``slots`` given, only those
     slots are computed and the per-slot rows [len(slots), N] are returned.
@@ -304,6 +316,8 @@ def moe_gemm(*, a_kind, a, a_scale=None, a_sf=None, a_sf_row=None, w_kind, w, w_
     pos = compact_row_of_slot(ids, E)
     if a_layout == "token":
         a_row = np.arange(T, dtype=np.int64) // top_k
+    elif a_layout == "padded":
+        a_row = padded_row_of_slot(ids, E, BM)
     else:
         a_row = pos
     sl = np.arange(T, dtype=np.int64) if slots is None else np.asarray(slots, dtype=np.int64)

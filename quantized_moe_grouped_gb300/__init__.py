@@ -24,12 +24,12 @@ _lock = threading.Lock()
 QMOE_OK, QMOE_ERR_INVALID_ARG, QMOE_ERR_UNSUPPORTED, QMOE_ERR_CUDA = 0, 1, 2, 3
 DEV_INVALID_EXPERT, DEV_TIMEOUT = 1, 2
 SCALE_PER_TOKEN, SCALE_MX_1X32 = 0, 1
-A_TOKEN_GATHER, A_GROUPED = 0, 1
+A_TOKEN_GATHER, A_GROUPED, A_PADDED = 0, 1, 2
 OUT_SLOT, OUT_GROUPED, OUT_TOKEN_SUM = 0, 1, 2
 
 EXPORTED = (
     "qmoe_status_string", "qmoe_version", "qmoe_align_max_padded", "qmoe_moe_align_block_size",
-    "qmoe_quant_act_fp8", "qmoe_quant_weight_fp8", "qmoe_quant_weight_int8", "qmoe_moe_gemm_w8a8",
+    "qmoe_quant_act_fp8", "qmoe_quant_act_fp8_sorted", "qmoe_quant_weight_fp8", "qmoe_quant_weight_int8", "qmoe_moe_gemm_w8a8",
     "qmoe_moe_gemm_w8a16", "qmoe_silu_mul_quant", "qmoe_debug_e4m3_encode", "qmoe_debug_int8_to_bf16",
     "qmoe_debug_silu_mul",
 )
@@ -53,6 +53,7 @@ class GemmArgs(ctypes.Structure):
         ("M", ctypes.c_int64), ("N", ctypes.c_int64), ("K", ctypes.c_int64),
         ("E", ctypes.c_int32), ("top_k", ctypes.c_int32), ("BM", ctypes.c_int32),
         ("d_status", ctypes.c_void_p),
+        ("accum", ctypes.c_void_p),
     ]
 
 
@@ -74,6 +75,7 @@ def load_library(path: str | None = None):
             L.qmoe_align_max_padded.restype = i64
             L.qmoe_moe_align_block_size.argtypes = [vp, i64, i32, i32, vp, vp, vp, vp, vp, vp, vp]
             L.qmoe_quant_act_fp8.argtypes = [vp, i64, i64, i64, vp, vp, vp]
+            L.qmoe_quant_act_fp8_sorted.argtypes = [vp, i64, i64, i64, vp, vp, i32, i64, vp, vp, vp]
             L.qmoe_quant_weight_fp8.argtypes = [vp, i64, i64, vp, vp, vp]
             L.qmoe_quant_weight_int8.argtypes = [vp, i64, i64, vp, vp, vp]
             L.qmoe_moe_gemm_w8a8.argtypes = [ctypes.POINTER(GemmArgs), vp]
@@ -153,6 +155,23 @@ def quant_act_fp8(x: torch.Tensor, q: torch.Tensor | None = None, scale: torch.T
     return q, scale
 
 
+def quant_act_fp8_sorted(x: torch.Tensor, align: dict, top_k: int, q: torch.Tensor | None = None,
+                         scale: torch.Tensor | None = None, stream=None):
+    """bf16 token rows [M, K] -> e4m3 rows in padded sorted order [cap, K] + fp32 scales [cap]
+    (cap = len(align["sorted_ids"])), the A operand of the QMOE_A_PADDED layout."""
+    if not x.is_cuda or x.dtype != torch.bfloat16 or x.dim() != 2 or x.stride(1) != 1:
+        raise QmoeError("x must be a 2-D CUDA bf16 tensor with unit column stride")
+    M, cols = x.shape
+    cap = align["sorted_ids"].numel()
+    q = q if q is not None else torch.empty(cap, cols, dtype=torch.uint8, device=x.device)
+    scale = scale if scale is not None else torch.empty(cap, dtype=torch.float32, device=x.device)
+    st = load_library().qmoe_quant_act_fp8_sorted(_ptr(x), M, cols, x.stride(0), _ptr(align["sorted_ids"]),
+                                                  _ptr(align["num_post_padded"]), top_k, cap, _ptr(q), _ptr(scale),
+                                                  _stream(stream))
+    _check(st, "quant_act_fp8_sorted")
+    return q, scale
+
+
 def quant_weight_fp8(w: torch.Tensor, stream=None):
     """fp32 [..., K] -> (e4m3 uint8 [..., K], fp32 scale [...]) per row (output channel)."""
     _need(w, torch.float32, "w")
@@ -178,8 +197,11 @@ def quant_weight_int8(w: torch.Tensor, stream=None):
 
 # ------------------------------------------------------------------ GEMM ---
 def _gemm(fn_name, *, a, a_scale, w, w_scale, align, topk_weights, out, M, top_k, BM, a_layout, out_layout,
-          a_scale_mode=SCALE_PER_TOKEN, a_sf=None, a_sf_padded_offsets=None, d_status=None, stream=None):
+          a_scale_mode=SCALE_PER_TOKEN, a_sf=None, a_sf_padded_offsets=None, d_status=None, accum=None,
+          stream=None):
     E, N, K = w.shape
+    if out_layout == OUT_TOKEN_SUM and accum is None:
+        accum = torch.empty(M, N, dtype=torch.float32, device=out.device)
     args = GemmArgs()
     args.struct_size = ctypes.sizeof(GemmArgs)
     args.a = a.data_ptr()
@@ -203,6 +225,7 @@ def _gemm(fn_name, *, a, a_scale, w, w_scale, align, topk_weights, out, M, top_k
     args.M, args.N, args.K = M, N, K
     args.E, args.top_k, args.BM = E, top_k, BM
     args.d_status = None if d_status is None else d_status.data_ptr()
+    args.accum = None if accum is None else accum.data_ptr()
     st = getattr(load_library(), fn_name)(ctypes.byref(args), _stream(stream))
     _check(st, fn_name)
     return out
@@ -218,11 +241,13 @@ def _out_for(out, out_layout, M, top_k, N, device):
 def moe_gemm_w8a8(a_q: torch.Tensor, a_scale: torch.Tensor, w_q: torch.Tensor, w_scale: torch.Tensor,
                   align: dict, topk_weights: torch.Tensor | None, *, M: int, top_k: int, BM: int,
                   a_layout: int = A_TOKEN_GATHER, out_layout: int = OUT_SLOT, out: torch.Tensor | None = None,
-                  d_status: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+                  d_status: torch.Tensor | None = None, accum: torch.Tensor | None = None,
+                  stream=None) -> torch.Tensor:
     """FP8 W8A8 grouped GEMM.  a_q uint8 e4m3 [rows, K] (token rows for TOKEN_GATHER,
     compact grouped rows for GROUPED), a_scale fp32 [rows], w_q uint8 e4m3 [E, N, K],
     w_scale fp32 [E, N], align = moe_align_block_size(..., BM), topk_weights fp32 [M, top_k]
-    or None.  Returns bf16 [T, N] (SLOT/GROUPED) or [M, N] (TOKEN_SUM)."""
+    or None.  Returns bf16 [T, N] (SLOT/GROUPED) or [M, N] (TOKEN_SUM; accum is the
+    fp32 [M, N] scratch the sum needs, allocated here when not given)."""
     _need(a_q, torch.uint8, "a_q")
     _need(w_q, torch.uint8, "w_q")
     _need(a_scale, torch.float32, "a_scale")
@@ -232,13 +257,14 @@ def moe_gemm_w8a8(a_q: torch.Tensor, a_scale: torch.Tensor, w_q: torch.Tensor, w
     out = _out_for(out, out_layout, M, top_k, w_q.shape[1], a_q.device)
     return _gemm("qmoe_moe_gemm_w8a8", a=a_q, a_scale=a_scale, w=w_q, w_scale=w_scale, align=align,
                  topk_weights=topk_weights, out=out, M=M, top_k=top_k, BM=BM, a_layout=a_layout,
-                 out_layout=out_layout, d_status=d_status, stream=stream)
+                 out_layout=out_layout, d_status=d_status, accum=accum, stream=stream)
 
 
 def moe_gemm_w8a16(a: torch.Tensor, w_q: torch.Tensor, w_scale: torch.Tensor, align: dict,
                    topk_weights: torch.Tensor | None, *, M: int, top_k: int, BM: int,
                    a_layout: int = A_TOKEN_GATHER, out_layout: int = OUT_SLOT, out: torch.Tensor | None = None,
-                   d_status: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+                   d_status: torch.Tensor | None = None, accum: torch.Tensor | None = None,
+                   stream=None) -> torch.Tensor:
     """INT8 W8A16 grouped GEMM: a bf16 [rows, K], w_q int8 [E, N, K], w_scale fp32 [E, N]."""
     _need(a, torch.bfloat16, "a")
     _need(w_q, torch.int8, "w_q")
@@ -248,7 +274,7 @@ def moe_gemm_w8a16(a: torch.Tensor, w_q: torch.Tensor, w_scale: torch.Tensor, al
     out = _out_for(out, out_layout, M, top_k, w_q.shape[1], a.device)
     return _gemm("qmoe_moe_gemm_w8a16", a=a, a_scale=None, w=w_q, w_scale=w_scale, align=align,
                  topk_weights=topk_weights, out=out, M=M, top_k=top_k, BM=BM, a_layout=a_layout,
-                 out_layout=out_layout, d_status=d_status, stream=stream)
+                 out_layout=out_layout, d_status=d_status, accum=accum, stream=stream)
 
 
 # ------------------------------------------------------ SwiGLU + quant ---

@@ -186,6 +186,44 @@ __global__ void __launch_bounds__(kRowThreads)
     }
 }
 
+// Per-token FP8 quantisation written in padded sorted order (one CTA per
+// padded position; the token row is re-quantised for each of its slots).
+__global__ void __launch_bounds__(kRowThreads)
+    quant_rows_fp8_sorted_kernel(const uint16_t* __restrict__ x, int64_t cols, int64_t ldx,
+                                 const int32_t* __restrict__ sorted_ids, const int32_t* __restrict__ npp,
+                                 int64_t T, int top_k, uint8_t* __restrict__ q, float* __restrict__ scale) {
+    __shared__ float red[33];
+    const int64_t p = blockIdx.x;
+    if (p >= *npp) return;
+    const int s = sorted_ids[p];
+    uint8_t* qr = q + p * cols;
+    if (s < 0 || s >= T) {  // pad position
+        for (int64_t c = static_cast<int64_t>(threadIdx.x) * 16; c < cols; c += kRowThreads * 16)
+            *reinterpret_cast<uint4*>(qr + c) = make_uint4(0u, 0u, 0u, 0u);
+        if (threadIdx.x == 0) scale[p] = 0.0f;
+        return;
+    }
+    const uint16_t* xr = x + static_cast<int64_t>(s / top_k) * ldx;
+    float amax = 0.0f;
+    for (int64_t c = static_cast<int64_t>(threadIdx.x) * 8; c < cols; c += kRowThreads * 8) {
+        float v[8];
+        load8(xr + c, v);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
+    }
+    amax = block_max(amax, red);
+    const float sc = (amax == 0.0f) ? 1.0f : __fdiv_rn(amax, 448.0f);
+    if (threadIdx.x == 0) scale[p] = sc;
+    for (int64_t c = static_cast<int64_t>(threadIdx.x) * 8; c < cols; c += kRowThreads * 8) {
+        float v[8];
+        load8(xr + c, v);
+        uint2 o;
+        o.x = e4m3x4(__fdiv_rn(v[0], sc), __fdiv_rn(v[1], sc), __fdiv_rn(v[2], sc), __fdiv_rn(v[3], sc));
+        o.y = e4m3x4(__fdiv_rn(v[4], sc), __fdiv_rn(v[5], sc), __fdiv_rn(v[6], sc), __fdiv_rn(v[7], sc));
+        *reinterpret_cast<uint2*>(qr + c) = o;
+    }
+}
+
 __global__ void __launch_bounds__(kRowThreads)
     quant_rows_int8_kernel(const float* __restrict__ x, int64_t cols, int8_t* __restrict__ q,
                            float* __restrict__ scale) {
@@ -384,6 +422,20 @@ qmoe_status_t qmoe_quant_act_fp8(const uint16_t* x, int64_t rows, int64_t cols, 
         quant_rows_fp8_kernel<uint16_t, true><<<static_cast<unsigned>(rows), kRowThreads, 0, stream>>>(x, cols, ldx, q, scale);
     else
         quant_rows_fp8_kernel<uint16_t, false><<<static_cast<unsigned>(rows), kRowThreads, 0, stream>>>(x, cols, ldx, q, scale);
+    return launch_status();
+}
+
+qmoe_status_t qmoe_quant_act_fp8_sorted(const uint16_t* x, int64_t M, int64_t cols, int64_t ldx,
+                                        const int32_t* sorted_ids, const int32_t* num_post_padded, int32_t top_k,
+                                        int64_t cap, uint8_t* q, float* scale, qmoe_stream_t stream) {
+    if (M < 0 || cols < 16 || cols % 16 != 0 || ldx < cols || ldx % 8 != 0 || top_k < 1 || cap < 0)
+        return QMOE_ERR_INVALID_ARG;
+    if (cap == 0) return QMOE_OK;
+    if (!x || !sorted_ids || !num_post_padded || !q || !scale || !aligned16(x) || !aligned16(q) ||
+        cap > 0x7FFFFFFF)
+        return QMOE_ERR_INVALID_ARG;
+    quant_rows_fp8_sorted_kernel<<<static_cast<unsigned>(cap), kRowThreads, 0, stream>>>(
+        x, cols, ldx, sorted_ids, num_post_padded, M * top_k, top_k, q, scale);
     return launch_status();
 }
 

@@ -1,30 +1,40 @@
 // gemm_kernel.cuh -- persistent grouped GEMM for the MoE expert FFN on sm_103a.
 //
-// One tile = 128 output channels n of one expert e  x  BN sorted slots (one
-// BM-block of the align output, BN == BM).  The expert weight rows are the
-// MMA "A" operand (M = 128) and the slot activations the "B" operand
-// (N = BN), so small slot counts (decode) keep the tensor-core M dimension
-// full while the kernel streams W at HBM rate.  D = W_tile . A_slots^T
-// lives in TMEM (fp32), double-buffered so the epilogue of one tile overlaps
+// Two tile shapes share one warp-specialised kernel template:
+//
+//  * swapped (BM <= 64, the decode regime): one tile = 128 output channels n
+//    of one expert x BN sorted slots (one BM block, BN == BM).  The weight rows
+//    are the MMA "A" operand (M = 128) and the slot activations the "B"
+//    operand (N = BN), so a handful of slots per expert still fills the
+//    tensor-core M dimension while the kernel streams W at HBM rate.
+//  * wide (BM >= 128): one tile = 128 sorted slots (MMA M) x 256 output
+//    channels (MMA N).  Per byte of weights it gathers a quarter of the
+//    activation bytes the swapped shape would need at BN = 256.
+//
+// D lives in TMEM (fp32), double-buffered so the epilogue of one tile overlaps
 // the main loop of the next.
 //
 // Warp roles (one CTA per SM, persistent over tiles, static round robin):
-//   warp 0      TMA producer: W[e, n0:n0+128, k0:k0+BK] -> smem ring
+//   warp 0      TMA producer: weight tile W[e, n0:n0+WR, k0:k0+BK] -> smem ring,
+//               and the activation tile when its rows are contiguous (GROUPED
+//               compact rows or PADDED sorted rows)
 //   warp 1      TMEM owner + single-thread tcgen05.mma issuer
-//   warps 2-3   activation producers: gather the BN slot rows (token rows
-//               for TOKEN_GATHER, compact rows for GROUPED) with 16-byte
-//               cp.async into the 128-byte-swizzled K-major layout
+//   warps 2-3   activation gather for TOKEN_GATHER: the tile's token rows with
+//               16-byte cp.async into the 128-byte-swizzled K-major layout
 //   warps 4-7   epilogue: TMEM -> registers, x w_scale[e,n] x a_scale x w[s],
-//               bf16, store (or bf16x2 atomic add for TOKEN_SUM)
+//               bf16 store (TOKEN_SUM: fp32 vector atomic add into the
+//               caller's accumulation buffer, rounded to bf16 by a second launch)
 //   warps 8-11  (W8A16 only) int8 -> bf16 converters, smem -> smem
 //
-// Every wait is bounded (common.cuh: mbar_wait); on a timeout the CTA raises
-// an abort flag, all roles leave their loops, copies in flight are drained
-// and TMEM is released before the kernel returns with QMOE_DEV_TIMEOUT set.
+// Every wait is bounded (mbar_wait); on a timeout the CTA raises an abort
+// flag, all roles leave their loops, copies in flight are drained and TMEM is
+// released before the kernel returns with QMOE_DEV_TIMEOUT set.
 #pragma once
 
 #include "common.cuh"
 #include "host_util.h"
+
+#include <string.h>
 
 #include <mutex>
 
@@ -43,34 +53,42 @@ struct GemmParams {
     const float* topk_w;
     const float* w_scale;
     uint16_t* out;
+    float* accum;                // TOKEN_SUM: fp32 [M, N] accumulation buffer
     int64_t N;
     int64_t T;
-    int32_t E, top_k, a_layout, out_layout;
+    int32_t E, top_k, a_layout, out_layout, BM;
+    int32_t a_tma;               // 1: activation tiles by TMA (GROUPED / PADDED rows), 0: cp.async gather
     int32_t num_k_blocks;
     int32_t* d_status;
 };
 
-template <bool kBF16, int BN>
+template <bool kBF16, bool kWide, int BN>
 struct GemmCfg {
+    static constexpr int kSlotRows = kWide ? 128 : BN;      // slots per tile
+    static constexpr int kWRows = kWide ? 256 : 128;        // weight rows (output channels) per tile
+    static constexpr int kMmaN = kWide ? 256 : BN;
     static constexpr int kBK = kBF16 ? 64 : 128;            // K elements per stage (128 bytes of MMA operand)
-    static constexpr int kWBytes = 128 * 128;                // MMA-A tile: 128 rows x 128 bytes
-    static constexpr int kBBytes = BN * 128;                 // MMA-B tile: BN rows x 128 bytes
-    static constexpr int kRawBytes = kBF16 ? 128 * 64 : 0;   // int8 weight tile before conversion
+    static constexpr int kWBytes = kWRows * 128;
+    static constexpr int kActBytes = kSlotRows * 128;
+    static constexpr int kRawBytes = kBF16 ? kWRows * 64 : 0;  // int8 weight tile before conversion
     static constexpr int kWLoadBytes = kBF16 ? kRawBytes : kWBytes;
-    static constexpr int kStageBytes = kWBytes + kBBytes + kRawBytes;
+    static constexpr int kStageBytes = kWBytes + kActBytes + kRawBytes;
     static constexpr int kStagesRaw = (200 * 1024) / kStageBytes;
     static constexpr int kStages = kStagesRaw > 8 ? 8 : kStagesRaw;
-    static constexpr int kLag = kStages - 1 < 3 ? kStages - 1 : 3;  // cp.async completion lag (stages)
+    // cp.async completion lag (stages): the MMA can run kStages - kLag - 1 stages
+    // ahead of the gather warps, so the lag shrinks when the ring is short.
+    static constexpr int kLag = kStages >= 6 ? 3 : (kStages >= 5 ? 2 : 1);
     static constexpr int kBProdThreads = 64;
     static constexpr int kEpiThreads = 128;
     static constexpr int kConvThreads = 128;
     static constexpr int kThreads = kBF16 ? 384 : 256;
-    static constexpr int kTmemCols = 2 * BN < 32 ? 32 : 2 * BN;
-    static constexpr uint32_t kIdesc = make_idesc(kBF16 ? kFmtBF16 : kFmtE4M3, 128, BN);
+    static constexpr int kAccCols = kMmaN;                  // TMEM columns per accumulator
+    static constexpr int kTmemCols = 2 * kAccCols < 32 ? 32 : 2 * kAccCols;
+    static constexpr uint32_t kIdesc = make_idesc(kBF16 ? kFmtBF16 : kFmtE4M3, 128, kMmaN);
     static constexpr int kDynSmem = kStages * kStageBytes + 1024;
     static_assert(kStages >= 2, "need at least two pipeline stages");
-    static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N must be a multiple of 16 in [16, 256]");
-    static_assert(kBBytes % 1024 == 0 && kWBytes % 1024 == 0 && kRawBytes % 1024 == 0, "1 KB tile alignment");
+    static_assert(kMmaN % 16 == 0 && kMmaN >= 16 && kMmaN <= 256, "MMA N must be a multiple of 16 in [16, 256]");
+    static_assert(kActBytes % 1024 == 0 && kWBytes % 1024 == 0 && kRawBytes % 1024 == 0, "1 KB tile alignment");
 };
 
 // Waits with a time limit but without honouring the abort flag (used for the
@@ -85,23 +103,47 @@ QMOE_DI uint32_t pack_bf16x2(float lo, float hi) {
     return *reinterpret_cast<const uint32_t*>(&v);
 }
 
-QMOE_DI void red_add_bf16x2(uint16_t* dst, uint32_t v) {
-    asm volatile("red.global.add.noftz.bf16x2 [%0], %1;" ::"l"(dst), "r"(v) : "memory");
+QMOE_DI void red_add_f32x2(float* dst, float a, float b) {
+    asm volatile("red.global.add.v2.f32 [%0], {%1, %2};" ::"l"(dst), "f"(a), "f"(b) : "memory");
+}
+QMOE_DI void red_add_f32x4(float* dst, float a, float b, float c, float d) {
+    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "f"(a), "f"(b), "f"(c), "f"(d)
+                 : "memory");
 }
 
-template <bool kBF16, int BN>
-__global__ void __launch_bounds__(GemmCfg<kBF16, BN>::kThreads, 1)
-    moe_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const GemmParams p) {
-    using C = GemmCfg<kBF16, BN>;
+// 32 TMEM lanes x 32 consecutive 32-bit columns per warp.
+QMOE_DI void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+template <bool kBF16, bool kWide, int BN>
+__global__ void __launch_bounds__(GemmCfg<kBF16, kWide, BN>::kThreads, 1)
+    moe_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_a,
+                    const GemmParams p) {
+    using C = GemmCfg<kBF16, kWide, BN>;
     constexpr int S = C::kStages;
+    constexpr int SR = C::kSlotRows;
+    constexpr int WR = C::kWRows;
     extern __shared__ uint8_t smem_raw[];
     __shared__ uint64_t bar_full[S], bar_empty[S], bar_conv[S];
     __shared__ uint64_t bar_tfull[2], bar_tempty[2], bar_drain;
     __shared__ uint32_t s_tmem_base;
     __shared__ int s_abort;
-    __shared__ int32_t s_brow[BN];   // activation producers: source row of each B row (-1: zero)
-    __shared__ float s_cscale[BN];   // epilogue: a_scale * routing weight of each column
-    __shared__ int32_t s_crow[BN];   // epilogue: output row of each column (-1: padding)
+    __shared__ int32_t s_brow[SR];                 // activation producers: source row of each slot row (-1: zero)
+    __shared__ float s_cscale[kWide ? 1 : SR];     // swapped epilogue: a_scale * routing weight per column
+    __shared__ int32_t s_crow[kWide ? 1 : SR];     // swapped epilogue: output row per column (-1: padding)
+    __shared__ float s_wsc[kWide ? WR : 1];        // wide epilogue: w_scale per column
 
     const uint32_t raw_addr = smem_u32(smem_raw);
     uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
@@ -110,7 +152,7 @@ __global__ void __launch_bounds__(GemmCfg<kBF16, BN>::kThreads, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
-            mbar_init(&bar_full[s], 1 + C::kBProdThreads);
+            mbar_init(&bar_full[s], p.a_tma ? 1 : 1 + C::kBProdThreads);
             mbar_init(&bar_empty[s], 1);
             mbar_init(&bar_conv[s], C::kConvThreads);
         }
@@ -129,16 +171,23 @@ __global__ void __launch_bounds__(GemmCfg<kBF16, BN>::kThreads, 1)
     const uint32_t tmem_base = s_tmem_base;
     volatile int* abort = &s_abort;
 
-    const int num_sb = *p.num_post_padded / BN;
-    const int n_blocks = static_cast<int>((p.N + 127) / 128);
+    const int num_sb = *p.num_post_padded / SR;
+    const int n_blocks = static_cast<int>((p.N + WR - 1) / WR);
     const int num_tiles = num_sb * n_blocks;
     const int nkb = p.num_k_blocks;
     auto w_tile = [&](int s) { return smem + s * C::kStageBytes; };
-    auto b_tile = [&](int s) { return smem + s * C::kStageBytes + C::kWBytes; };
-    auto raw_tile = [&](int s) { return smem + s * C::kStageBytes + C::kWBytes + C::kBBytes; };
+    auto act_tile = [&](int s) { return smem + s * C::kStageBytes + C::kWBytes; };
+    auto raw_tile = [&](int s) { return smem + s * C::kStageBytes + C::kWBytes + C::kActBytes; };
+    // Expert of a tile, or -1 when the tile is to be skipped: an invalid expert
+    // id, or (tiles narrower than BM) a tile whose first slot is padding --
+    // valid slots precede the padding inside an expert's region, so the whole
+    // tile is padding then.
     auto tile_expert = [&](int tile) {
-        const int e = p.expert_ids[tile % num_sb];
-        return (e >= 0 && e < p.E) ? e : -1;
+        const int sb = tile % num_sb;
+        const int e = p.expert_ids[sb * SR / p.BM];
+        if (e < 0 || e >= p.E) return -1;
+        if (SR < p.BM && p.sorted_ids[sb * SR] >= p.T) return -1;
+        return e;
     };
 
     if (warp == 0) {
@@ -146,16 +195,23 @@ __global__ void __launch_bounds__(GemmCfg<kBF16, BN>::kThreads, 1)
         if (lane == 0) {
             int it = 0;
             bool ok = true;
+            const uint32_t tx = C::kWLoadBytes + (p.a_tma ? C::kActBytes : 0);
             for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
                 const int e = tile_expert(tile);
                 if (e < 0) continue;
                 const int nb = tile / num_sb;
+                const int sb = tile % num_sb;
+                // first activation row of the tile: padded position, or compact grouped row
+                const int arow0 = (p.a_layout == QMOE_A_PADDED)
+                                      ? sb * SR
+                                      : p.expert_offsets[e] + (sb * SR - p.padded_offsets[e]);
                 for (int kb = 0; kb < nkb; ++kb, ++it) {
                     const int s = it % S;
                     const uint32_t ph = (it / S) & 1;
                     if (!mbar_wait(&bar_empty[s], ph ^ 1, abort, p.d_status)) { ok = false; break; }
-                    mbar_arrive_expect_tx(&bar_full[s], C::kWLoadBytes);
-                    tma_load_3d(&tmap_w, &bar_full[s], kBF16 ? raw_tile(s) : w_tile(s), kb * C::kBK, nb * 128, e);
+                    mbar_arrive_expect_tx(&bar_full[s], tx);
+                    tma_load_3d(&tmap_w, &bar_full[s], kBF16 ? raw_tile(s) : w_tile(s), kb * C::kBK, nb * WR, e);
+                    if (p.a_tma) tma_load_2d(&tmap_a, &bar_full[s], act_tile(s), kb * C::kBK, arow0);
                 }
             }
             if (!ok) {  // let copies already issued land before the CTA can exit
@@ -174,15 +230,17 @@ __global__ void __launch_bounds__(GemmCfg<kBF16, BN>::kThreads, 1)
                 const uint32_t aph = (tcount >> 1) & 1;
                 if (!mbar_wait(&bar_tempty[acc], aph ^ 1, abort, p.d_status)) break;
                 tc_fence_after();
-                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * C::kAccCols);
                 for (int kb = 0; kb < nkb; ++kb, ++it) {
                     const int s = it % S;
                     const uint32_t ph = (it / S) & 1;
                     if (!mbar_wait(&bar_full[s], ph, abort, p.d_status)) { ok = false; break; }
                     if (kBF16 && !mbar_wait(&bar_conv[s], ph, abort, p.d_status)) { ok = false; break; }
                     tc_fence_after();
-                    const uint64_t da = desc_kmajor_sw128(smem_u32(w_tile(s)));
-                    const uint64_t db = desc_kmajor_sw128(smem_u32(b_tile(s)));
+                    const uint64_t dw = desc_kmajor_sw128(smem_u32(w_tile(s)));
+                    const uint64_t dx = desc_kmajor_sw128(smem_u32(act_tile(s)));
+                    const uint64_t da = kWide ? dx : dw;
+                    const uint64_t db = kWide ? dw : dx;
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
                         if (kBF16) mma_f16(d_tmem, da + 2 * k, db + 2 * k, C::kIdesc, (kb | k) != 0);
@@ -198,18 +256,18 @@ __global__ void __launch_bounds__(GemmCfg<kBF16, BN>::kThreads, 1)
             mbar_wait_drain(&bar_drain, 0, p.d_status);
         }
     } else if (warp < 4) {
-        // ------------------------------------- activation producers ---
+        // ------------------------------- activation gather (TOKEN_GATHER) ---
         const int pt = threadIdx.x - 64;
         int it = 0;
-        bool ok = true;
+        bool ok = !p.a_tma;
         for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
             if (*abort) break;
             const int e = tile_expert(tile);
             if (e < 0) continue;
             const int sb = tile % num_sb;
             named_bar_sync(1, C::kBProdThreads);
-            for (int j = pt; j < BN; j += C::kBProdThreads) {
-                const int pos = sb * BN + j;
+            for (int j = pt; j < SR; j += C::kBProdThreads) {
+                const int pos = sb * SR + j;
                 const int s = p.sorted_ids[pos];
                 int row = -1;
                 if (s >= 0 && s < p.T)
@@ -222,9 +280,9 @@ __global__ void __launch_bounds__(GemmCfg<kBF16, BN>::kThreads, 1)
                 const int s = it % S;
                 const uint32_t ph = (it / S) & 1;
                 if (!mbar_wait(&bar_empty[s], ph ^ 1, abort, p.d_status)) { ok = false; break; }
-                uint8_t* dst_tile = b_tile(s);
+                uint8_t* dst_tile = act_tile(s);
                 const int64_t k0 = static_cast<int64_t>(kb) * 128;
-                for (int idx = pt; idx < BN * 8; idx += C::kBProdThreads) {
+                for (int idx = pt; idx < SR * 8; idx += C::kBProdThreads) {
                     const int r = idx >> 3, c = idx & 7;
                     const int row = s_brow[r];
                     const int64_t kbyte = k0 + c * 16;
@@ -247,7 +305,6 @@ __global__ void __launch_bounds__(GemmCfg<kBF16, BN>::kThreads, 1)
         // ------------------------------------------------- epilogue ---
         const int et = threadIdx.x - 128;
         const int q = warp & 3;  // TMEM lane quadrant of this warp
-        const bool even = (lane & 1) == 0;
         int tcount = 0;
         for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
             if (*abort) break;
@@ -257,48 +314,105 @@ __global__ void __launch_bounds__(GemmCfg<kBF16, BN>::kThreads, 1)
             const int nb = tile / num_sb;
             const int acc = tcount & 1;
             const uint32_t aph = (tcount >> 1) & 1;
-            named_bar_sync(2, C::kEpiThreads);
-            for (int j = et; j < BN; j += C::kEpiThreads) {
-                const int pos = sb * BN + j;
+            const uint32_t t_base =
+                tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * C::kAccCols);
+            if constexpr (kWide) {
+                // lane = slot row, columns = 256 output channels
+                named_bar_sync(2, C::kEpiThreads);
+                for (int c = et; c < WR; c += C::kEpiThreads) {
+                    const int64_t n = static_cast<int64_t>(nb) * WR + c;
+                    s_wsc[c] = (n < p.N) ? p.w_scale[static_cast<int64_t>(e) * p.N + n] : 0.0f;
+                }
+                named_bar_sync(2, C::kEpiThreads);
+                const int pos = sb * SR + q * 32 + lane;
                 const int s = p.sorted_ids[pos];
-                if (s < 0 || s >= p.T) {
-                    s_crow[j] = -1;
-                    s_cscale[j] = 0.0f;
-                } else {
+                const bool valid = s >= 0 && s < p.T;
+                float rs = 0.0f;
+                int64_t orow = 0;
+                if (valid) {
                     const int m = s / p.top_k;
                     const int compact = p.expert_offsets[e] + (pos - p.padded_offsets[e]);
-                    const int arow = (p.a_layout == QMOE_A_TOKEN_GATHER) ? m : compact;
-                    const float sa = p.a_scale ? p.a_scale[arow] : 1.0f;
-                    const float wr = p.topk_w ? p.topk_w[s] : 1.0f;
-                    s_cscale[j] = sa * wr;
-                    s_crow[j] = (p.out_layout == QMOE_OUT_SLOT) ? s : (p.out_layout == QMOE_OUT_GROUPED ? compact : m);
+                    const int arow = (p.a_layout == QMOE_A_TOKEN_GATHER) ? m
+                                     : (p.a_layout == QMOE_A_GROUPED ? compact : pos);
+                    rs = (p.a_scale ? p.a_scale[arow] : 1.0f) * (p.topk_w ? p.topk_w[s] : 1.0f);
+                    orow = (p.out_layout == QMOE_OUT_SLOT) ? s : (p.out_layout == QMOE_OUT_GROUPED ? compact : m);
                 }
-            }
-            named_bar_sync(2, C::kEpiThreads);
-            if (!mbar_wait(&bar_tfull[acc], aph, abort, p.d_status)) break;
-            tc_fence_after();
-            const int64_t n = static_cast<int64_t>(nb) * 128 + q * 32 + lane;
-            const float sw = (n < p.N) ? p.w_scale[static_cast<int64_t>(e) * p.N + n] : 0.0f;
-            const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
-            const int64_t nn = even ? n : n - 1;
-            for (int c0 = 0; c0 < BN; c0 += 16) {
-                float v[16];
-                tmem_ld16(t_row + c0, v);
+                if (!mbar_wait(&bar_tfull[acc], aph, abort, p.d_status)) break;
+                tc_fence_after();
+                const int64_t col0 = orow * p.N + static_cast<int64_t>(nb) * WR;
+                const int64_t n_left = p.N - static_cast<int64_t>(nb) * WR;
+                const bool tsum = p.out_layout == QMOE_OUT_TOKEN_SUM;
+                for (int c0 = 0; c0 < WR; c0 += 32) {
+                    float v[32];
+                    tmem_ld32(t_base + c0, v);
+                    if (!valid) continue;
 #pragma unroll
-                for (int i = 0; i < 16; i += 2) {
-                    const int j = c0 + i;
-                    const float v0 = v[i] * sw * s_cscale[j];
-                    const float v1 = v[i + 1] * sw * s_cscale[j + 1];
-                    const float o0 = __shfl_xor_sync(0xFFFFFFFFu, v0, 1);
-                    const float o1 = __shfl_xor_sync(0xFFFFFFFFu, v1, 1);
-                    // even lane: column j at (n, n+1); odd lane: column j+1 at (n-1, n)
-                    const int col = even ? j : j + 1;
-                    const int row = s_crow[col];
-                    if (row >= 0 && nn < p.N) {
-                        const uint32_t packed = even ? pack_bf16x2(v0, o0) : pack_bf16x2(o1, v1);
-                        uint16_t* dst = p.out + static_cast<int64_t>(row) * p.N + nn;
-                        if (p.out_layout == QMOE_OUT_TOKEN_SUM) red_add_bf16x2(dst, packed);
-                        else *reinterpret_cast<uint32_t*>(dst) = packed;
+                    for (int g = 0; g < 4; ++g) {
+                        const int cc = c0 + g * 8;
+                        if (cc >= n_left) break;
+                        float x[8];
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) x[i] = v[g * 8 + i] * s_wsc[cc + i] * rs;
+                        if (tsum) {
+                            red_add_f32x4(p.accum + col0 + cc, x[0], x[1], x[2], x[3]);
+                            red_add_f32x4(p.accum + col0 + cc + 4, x[4], x[5], x[6], x[7]);
+                        } else {
+                            uint4 o;
+                            o.x = pack_bf16x2(x[0], x[1]);
+                            o.y = pack_bf16x2(x[2], x[3]);
+                            o.z = pack_bf16x2(x[4], x[5]);
+                            o.w = pack_bf16x2(x[6], x[7]);
+                            *reinterpret_cast<uint4*>(p.out + col0 + cc) = o;
+                        }
+                    }
+                }
+            } else {
+                // lane = output channel, columns = BN slots
+                const bool even = (lane & 1) == 0;
+                named_bar_sync(2, C::kEpiThreads);
+                for (int j = et; j < SR; j += C::kEpiThreads) {
+                    const int pos = sb * SR + j;
+                    const int s = p.sorted_ids[pos];
+                    if (s < 0 || s >= p.T) {
+                        s_crow[j] = -1;
+                        s_cscale[j] = 0.0f;
+                    } else {
+                        const int m = s / p.top_k;
+                        const int compact = p.expert_offsets[e] + (pos - p.padded_offsets[e]);
+                        const int arow = (p.a_layout == QMOE_A_TOKEN_GATHER) ? m
+                                         : (p.a_layout == QMOE_A_GROUPED ? compact : pos);
+                        const float sa = p.a_scale ? p.a_scale[arow] : 1.0f;
+                        const float wr = p.topk_w ? p.topk_w[s] : 1.0f;
+                        s_cscale[j] = sa * wr;
+                        s_crow[j] = (p.out_layout == QMOE_OUT_SLOT) ? s
+                                                                    : (p.out_layout == QMOE_OUT_GROUPED ? compact : m);
+                    }
+                }
+                named_bar_sync(2, C::kEpiThreads);
+                if (!mbar_wait(&bar_tfull[acc], aph, abort, p.d_status)) break;
+                tc_fence_after();
+                const int64_t n = static_cast<int64_t>(nb) * WR + q * 32 + lane;
+                const float sw = (n < p.N) ? p.w_scale[static_cast<int64_t>(e) * p.N + n] : 0.0f;
+                const int64_t nn = even ? n : n - 1;
+                for (int c0 = 0; c0 < SR; c0 += 16) {
+                    float v[16];
+                    tmem_ld16(t_base + c0, v);
+#pragma unroll
+                    for (int i = 0; i < 16; i += 2) {
+                        const int j = c0 + i;
+                        const float v0 = v[i] * sw * s_cscale[j];
+                        const float v1 = v[i + 1] * sw * s_cscale[j + 1];
+                        const float o0 = __shfl_xor_sync(0xFFFFFFFFu, v0, 1);
+                        const float o1 = __shfl_xor_sync(0xFFFFFFFFu, v1, 1);
+                        // even lane: column j at (n, n+1); odd lane: column j+1 at (n-1, n)
+                        const int col = even ? j : j + 1;
+                        const int row = s_crow[col];
+                        if (row >= 0 && nn < p.N) {
+                            const float lo = even ? v0 : o1, hi = even ? o0 : v1;
+                            const int64_t off = static_cast<int64_t>(row) * p.N + nn;
+                            if (p.out_layout == QMOE_OUT_TOKEN_SUM) red_add_f32x2(p.accum + off, lo, hi);
+                            else *reinterpret_cast<uint32_t*>(p.out + off) = pack_bf16x2(lo, hi);
+                        }
                     }
                 }
             }
@@ -322,7 +436,7 @@ __global__ void __launch_bounds__(GemmCfg<kBF16, BN>::kThreads, 1)
                     uint8_t* dst = w_tile(s);
                     const int c = ct & 3;
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
+                    for (int i = 0; i < WR / 32; ++i) {
                         const int r = (ct >> 2) + 32 * i;
                         const uint4 w = *reinterpret_cast<const uint4*>(raw + r * 64 + c * 16);
                         uint4 o0, o1;
@@ -368,23 +482,39 @@ inline EncodeTiledFn encode_tiled_fn() {
     return fn;
 }
 
-// Weight map over W[E][N][K] bytes: box {box_k, 128, 1}.
-inline bool make_weight_map(CUtensorMap* map, const void* w, int64_t E, int64_t N, int64_t K, int box_k,
+// Weight map over W[E][N][K] bytes: box {box_k, box_rows, 1}.
+inline bool make_weight_map(CUtensorMap* map, const void* w, int64_t E, int64_t N, int64_t K, int box_k, int box_rows,
                             bool swizzle128) {
     EncodeTiledFn enc = encode_tiled_fn();
     if (!enc) return false;
     cuuint64_t dims[3] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(E)};
     cuuint64_t strides[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(N * K)};
-    cuuint32_t box[3] = {static_cast<cuuint32_t>(box_k), 128u, 1u};
+    cuuint32_t box[3] = {static_cast<cuuint32_t>(box_k), static_cast<cuuint32_t>(box_rows), 1u};
     cuuint32_t estr[3] = {1u, 1u, 1u};
     return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(w), dims, strides, box, estr,
                CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <bool kBF16, int BN>
-inline qmoe_status_t launch_gemm(const CUtensorMap& map, const GemmParams& p, int64_t max_tiles, cudaStream_t st) {
-    using C = GemmCfg<kBF16, BN>;
+// Activation map over A[rows][K] (1- or 2-byte elements): box {128 bytes, box_rows}, 128-byte swizzle.
+inline bool make_act_map(CUtensorMap* map, const void* a, int64_t rows, int64_t K, int64_t lda, int elem,
+                         int box_rows) {
+    EncodeTiledFn enc = encode_tiled_fn();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(lda * elem)};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / elem), static_cast<cuuint32_t>(box_rows)};
+    cuuint32_t estr[2] = {1u, 1u};
+    return enc(map, elem == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_UINT16, 2,
+               const_cast<void*>(a), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <bool kBF16, bool kWide, int BN>
+inline qmoe_status_t launch_gemm(const void* w, int64_t E, int64_t N, int64_t K, const GemmParams& p,
+                                 int64_t max_padded, int64_t a_rows, int64_t lda, cudaStream_t st) {
+    using C = GemmCfg<kBF16, kWide, BN>;
     static std::mutex mu;
     static bool attr_set[64] = {false};
     int dev = 0;
@@ -392,19 +522,27 @@ inline qmoe_status_t launch_gemm(const CUtensorMap& map, const GemmParams& p, in
     {
         std::lock_guard<std::mutex> g(mu);
         if (!attr_set[dev]) {
-            if (cudaFuncSetAttribute(moe_gemm_kernel<kBF16, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+            if (cudaFuncSetAttribute(moe_gemm_kernel<kBF16, kWide, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      C::kDynSmem) != cudaSuccess)
                 return QMOE_ERR_CUDA;
             attr_set[dev] = true;
         }
     }
+    CUtensorMap map, amap;
+    if (!make_weight_map(&map, w, E, N, K, C::kBK, C::kWRows, !kBF16)) return QMOE_ERR_CUDA;
+    memset(&amap, 0, sizeof(amap));
+    if (p.a_tma && !make_act_map(&amap, p.a, a_rows, K, lda, kBF16 ? 2 : 1, C::kSlotRows)) return QMOE_ERR_CUDA;
     const int sms = device_sm_count();
     if (sms <= 0) return QMOE_ERR_CUDA;
+    const int64_t max_tiles = ((max_padded + C::kSlotRows - 1) / C::kSlotRows) * ((N + C::kWRows - 1) / C::kWRows);
     const int64_t grid = max_tiles < sms ? max_tiles : sms;
     if (grid <= 0) return QMOE_OK;
-    moe_gemm_kernel<kBF16, BN><<<static_cast<unsigned>(grid), C::kThreads, C::kDynSmem, st>>>(map, p);
+    moe_gemm_kernel<kBF16, kWide, BN><<<static_cast<unsigned>(grid), C::kThreads, C::kDynSmem, st>>>(map, amap, p);
     return launch_status();
 }
+
+// out[i] = bf16(accum[i]) for the TOKEN_SUM layout (defined in gemm_w8a8.cu).
+qmoe_status_t launch_token_sum_finalize(const float* accum, uint16_t* out, int64_t n, cudaStream_t st);
 
 // Shared argument checks and dispatch for both precisions.
 template <bool kBF16>
@@ -413,7 +551,8 @@ inline qmoe_status_t run_moe_gemm(const qmoe_gemm_args* a, cudaStream_t st) {
     if (a->M < 0 || a->N < 16 || a->N % 16 != 0 || a->K < 16 || a->K % 16 != 0) return QMOE_ERR_INVALID_ARG;
     if (a->E < 1 || a->E > 256 || a->top_k < 1 || a->top_k > a->E) return QMOE_ERR_INVALID_ARG;
     if (a->BM != 16 && a->BM != 32 && a->BM != 64 && a->BM != 128 && a->BM != 256) return QMOE_ERR_UNSUPPORTED;
-    if (a->a_layout != QMOE_A_TOKEN_GATHER && a->a_layout != QMOE_A_GROUPED) return QMOE_ERR_INVALID_ARG;
+    if (a->a_layout != QMOE_A_TOKEN_GATHER && a->a_layout != QMOE_A_GROUPED && a->a_layout != QMOE_A_PADDED)
+        return QMOE_ERR_INVALID_ARG;
     if (a->out_layout < QMOE_OUT_SLOT || a->out_layout > QMOE_OUT_TOKEN_SUM) return QMOE_ERR_INVALID_ARG;
     const int64_t elem = kBF16 ? 2 : 1;
     if (a->lda < a->K || (a->lda * elem) % 16 != 0) return QMOE_ERR_INVALID_ARG;
@@ -431,11 +570,11 @@ inline qmoe_status_t run_moe_gemm(const qmoe_gemm_args* a, cudaStream_t st) {
         return QMOE_ERR_INVALID_ARG;
     if (!aligned16(a->a) || !aligned16(a->w) || !aligned16(a->out)) return QMOE_ERR_INVALID_ARG;
 
-    CUtensorMap map;
-    if (!make_weight_map(&map, a->w, a->E, a->N, a->K, kBF16 ? 64 : 128, !kBF16)) return QMOE_ERR_CUDA;
-
-    if (a->out_layout == QMOE_OUT_TOKEN_SUM) {
-        if (cudaMemsetAsync(a->out, 0, static_cast<size_t>(a->M * a->N) * 2, st) != cudaSuccess) return QMOE_ERR_CUDA;
+    const bool tsum = a->out_layout == QMOE_OUT_TOKEN_SUM;
+    if (tsum) {
+        if (!a->accum || !aligned16(a->accum)) return QMOE_ERR_INVALID_ARG;
+        if (cudaMemsetAsync(a->accum, 0, static_cast<size_t>(a->M * a->N) * sizeof(float), st) != cudaSuccess)
+            return QMOE_ERR_CUDA;
     }
     GemmParams p;
     p.a = static_cast<const uint8_t*>(a->a);
@@ -450,23 +589,28 @@ inline qmoe_status_t run_moe_gemm(const qmoe_gemm_args* a, cudaStream_t st) {
     p.topk_w = a->topk_weights;
     p.w_scale = a->w_scale;
     p.out = a->out;
+    p.accum = a->accum;
     p.N = a->N;
     p.T = T;
     p.E = a->E;
     p.top_k = a->top_k;
     p.a_layout = a->a_layout;
     p.out_layout = a->out_layout;
+    p.BM = a->BM;
+    p.a_tma = a->a_layout != QMOE_A_TOKEN_GATHER;
     p.num_k_blocks = static_cast<int32_t>((a->K + (kBF16 ? 63 : 127)) / (kBF16 ? 64 : 128));
     p.d_status = a->d_status;
-    const int64_t cap_padded = T + static_cast<int64_t>(a->E) * (a->BM - 1);
-    const int64_t max_tiles = ((cap_padded + a->BM - 1) / a->BM) * ((a->N + 127) / 128);
+    const int64_t max_padded = (T + static_cast<int64_t>(a->E) * (a->BM - 1) + a->BM - 1) / a->BM * a->BM;
+    const int64_t a_rows = a->a_layout == QMOE_A_PADDED ? max_padded : (a->a_layout == QMOE_A_GROUPED ? T : a->M);
+    qmoe_status_t r;
     switch (a->BM) {
-        case 16: return launch_gemm<kBF16, 16>(map, p, max_tiles, st);
-        case 32: return launch_gemm<kBF16, 32>(map, p, max_tiles, st);
-        case 64: return launch_gemm<kBF16, 64>(map, p, max_tiles, st);
-        case 128: return launch_gemm<kBF16, 128>(map, p, max_tiles, st);
-        default: return launch_gemm<kBF16, 256>(map, p, max_tiles, st);
+        case 16: r = launch_gemm<kBF16, false, 16>(a->w, a->E, a->N, a->K, p, max_padded, a_rows, a->lda, st); break;
+        case 32: r = launch_gemm<kBF16, false, 32>(a->w, a->E, a->N, a->K, p, max_padded, a_rows, a->lda, st); break;
+        case 64: r = launch_gemm<kBF16, false, 64>(a->w, a->E, a->N, a->K, p, max_padded, a_rows, a->lda, st); break;
+        default: r = launch_gemm<kBF16, true, 128>(a->w, a->E, a->N, a->K, p, max_padded, a_rows, a->lda, st); break;
     }
+    if (r != QMOE_OK || !tsum) return r;
+    return launch_token_sum_finalize(a->accum, a->out, a->M * a->N, st);
 }
 
 }  // namespace qmoe

@@ -1,5 +1,41 @@
-// gemm_w8a8.cu -- FP8 e4m3 W8A8 grouped GEMM entry point (tcgen05 kind::f8f6f4).
+// gemm_w8a8.cu -- FP8 e4m3 W8A8 grouped GEMM entry point (tcgen05 kind::f8f6f4),
+// and the bf16 rounding pass of the TOKEN_SUM layout shared by both precisions.
 #include "gemm_kernel.cuh"
+
+namespace qmoe {
+
+// out = bf16(accum), 8 elements per step (n % 8 == 0, 16-byte aligned), else 1.
+__global__ void token_sum_finalize_kernel(const float* __restrict__ accum, uint16_t* __restrict__ out, int64_t n) {
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    const int64_t i0 = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
+    if ((n & 7) == 0) {
+        for (int64_t i = i0; i < n / 8; i += stride) {
+            const float4 a = reinterpret_cast<const float4*>(accum)[2 * i];
+            const float4 b = reinterpret_cast<const float4*>(accum)[2 * i + 1];
+            uint4 o;
+            o.x = pack_bf16x2(a.x, a.y);
+            o.y = pack_bf16x2(a.z, a.w);
+            o.z = pack_bf16x2(b.x, b.y);
+            o.w = pack_bf16x2(b.z, b.w);
+            reinterpret_cast<uint4*>(out)[i] = o;
+        }
+    } else {
+        for (int64_t i = i0; i < n; i += stride) out[i] = static_cast<uint16_t>(pack_bf16x2(accum[i], 0.0f) & 0xFFFFu);
+    }
+}
+
+qmoe_status_t launch_token_sum_finalize(const float* accum, uint16_t* out, int64_t n, cudaStream_t st) {
+    if (n <= 0) return QMOE_OK;
+    const int sms = device_sm_count();
+    const int64_t work = (n & 7) == 0 ? n / 8 : n;
+    int64_t blocks = (work + 255) / 256;
+    const int64_t cap = static_cast<int64_t>(sms > 0 ? sms : 132) * 8;
+    if (blocks > cap) blocks = cap;
+    token_sum_finalize_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(accum, out, n);
+    return launch_status();
+}
+
+}  // namespace qmoe
 
 extern "C" qmoe_status_t qmoe_moe_gemm_w8a8(const qmoe_gemm_args* args, qmoe_stream_t stream) {
     return qmoe::run_moe_gemm<false>(args, stream);

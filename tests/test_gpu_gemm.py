@@ -64,7 +64,8 @@ def test_w8a8_tiny_all_tile_sizes(q, orc, BM):
 
 @pytest.mark.parametrize("a_layout,out_layout", LAYOUTS)
 @pytest.mark.parametrize("M,K,N,E,top_k,BM", [(200, 272, 208, 8, 2, 32), (37, 512, 384, 5, 3, 16),
-                                              (300, 96, 128, 4, 1, 64)])
+                                              (300, 96, 128, 4, 1, 64), (150, 272, 400, 8, 2, 128),
+                                              (90, 160, 272, 5, 3, 256), (700, 128, 528, 8, 2, 128)])
 def test_w8a8_layouts_ragged(q, orc, a_layout, out_layout, M, K, N, E, top_k, BM):
     p = fp8_problem(q, orc, M, K, N, E, top_k, seed=M + K + N)
     T = M * top_k
@@ -157,12 +158,13 @@ def test_w8a16_parity(q, orc, a_layout, out_layout, M, K, N, E, top_k, BM):
     check(bf16_to_np_f32(out), ref)
 
 
-def test_fp8_layer_stagewise(q, orc):
+@pytest.mark.parametrize("BM", [64, 128])
+def test_fp8_layer_stagewise(q, orc, BM):
     """One FFN layer (reduced Mixtral shape): up GEMM (token gather -> grouped
     rows) -> SwiGLU + per-token FP8 -> down GEMM (grouped rows -> sum over
     top_k with routing weights).  Each stage's oracle takes the GPU's
     previous-stage output, so quantised bytes must match exactly."""
-    M, K, I, Nd, E, top_k, BM = 256, 256, 384, 256, 8, 2, 64
+    M, K, I, Nd, E, top_k = 256, 256, 384, 256, 8, 2
     a = inputs.activations_bf16(M, K, 31)
     w1 = inputs.expert_weights_f32(E, 2 * I, K, 31, weight_set=0)
     w2 = inputs.expert_weights_f32(E, Nd, I, 31, weight_set=1)
@@ -220,3 +222,33 @@ def test_w8a8_decode_full_size_sampled(q, orc):
     ok, ratio = oracle.gemm_tolerance_ok(full[slots], ref, rms=rms)
     assert ok, ratio
     assert np.all(np.isfinite(full))
+
+
+@pytest.mark.parametrize("M,K,N,E,top_k,BM,out_layout", [(64, 128, 256, 8, 2, 32, 0), (200, 272, 208, 8, 2, 64, 2),
+                                                         (333, 512, 400, 8, 2, 128, 0), (90, 160, 272, 5, 3, 256, 2)])
+def test_w8a8_padded_sorted_activations(q, orc, M, K, N, E, top_k, BM, out_layout):
+    """quant_act_fp8_sorted (bit-exact against the oracle's per-token codes placed
+    at the padded sorted positions) feeding the GEMM's PADDED activation layout."""
+    p = fp8_problem(q, orc, M, K, N, E, top_k, seed=M * 3 + BM)
+    al = q.moe_align_block_size(to_dev(p["ids"]), E, BM)
+    aq_p, sa_p = q.quant_act_fp8_sorted(to_dev_bf16(p["a"]), al, top_k)
+    ref_al = orc.moe_align(p["ids"], E, BM)
+    n = ref_al["num_post_padded"]
+    srt = ref_al["sorted_ids"][:n]
+    valid = srt < M * top_k
+    exp_q = np.zeros((n, K), dtype=np.uint8)
+    exp_s = np.zeros(n, dtype=np.float32)
+    exp_q[valid] = p["raq"][srt[valid] // top_k]
+    exp_s[valid] = p["rsa"][srt[valid] // top_k]
+    assert np.array_equal(aq_p.cpu().numpy()[:n], exp_q)
+    assert np.array_equal(sa_p.cpu().numpy()[:n], exp_s)
+    out = q.moe_gemm_w8a8(aq_p, sa_p, p["wq"], p["ws"], al, to_dev(p["tw"]), M=M, top_k=top_k, BM=BM,
+                          a_layout=q.A_PADDED, out_layout=out_layout)
+    cap = aq_p.shape[0]
+    a_full = np.zeros((cap, K), dtype=np.uint8)
+    s_full = np.zeros(cap, dtype=np.float32)
+    a_full[:n], s_full[:n] = exp_q, exp_s
+    ref = orc.moe_gemm(a_kind=orc.A_FP8_TOKEN, a=a_full, a_scale=s_full, w_kind=orc.W_FP8, w=p["rwq"],
+                       w_scale=p["rws"], topk_ids=p["ids"], topk_w=p["tw"], E=E, a_layout="padded", BM=BM,
+                       out_layout={0: "slot", 2: "token_sum"}[out_layout])
+    check(bf16_to_np_f32(out), ref)
