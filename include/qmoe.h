@@ -185,6 +185,28 @@ typedef struct {
  * QMOE_SCALE_MX_1X32 is not supported yet (QMOE_ERR_UNSUPPORTED). */
 qmoe_status_t qmoe_moe_gemm_w8a8(const qmoe_gemm_args* args, qmoe_stream_t stream);
 
+/* FP8 W8A8 grouped GEMM with the TOKEN_SUM layout that allocates nothing.
+ * The pages have no counterpart to this entry point; it exists for callers
+ * that cannot call cudaMalloc (allocator-managed runtimes that forbid it on
+ * their hot path, plugins that only receive input and output buffers), which
+ * therefore cannot provide args->accum.  It computes exactly what
+ * qmoe_moe_gemm_w8a8 computes for QMOE_OUT_TOKEN_SUM, but the fp32
+ * accumulation buffer is a fixed array of QMOE_NOALLOC_ACCUM_MAX_ELEMS floats
+ * (16 MiB) compiled into the library: every GPU that loads the library holds
+ * it until the process exits.  args->accum is ignored.
+ *  - args->out_layout must be QMOE_OUT_TOKEN_SUM (else QMOE_ERR_INVALID_ARG);
+ *    M*N above QMOE_NOALLOC_ACCUM_MAX_ELEMS returns QMOE_ERR_UNSUPPORTED and
+ *    launches nothing.
+ *  - The first call on a device looks up the array's device address (with
+ *    that device current); make that first call before any stream capture.
+ *  - All calls share the one array: the first M*N floats are zeroed on the
+ *    stream at every call, but calls whose work overlaps on the GPU (other
+ *    streams, other host threads) race on it and must be serialised by the
+ *    caller.
+ *  - No cudaMalloc, cudaFree or allocating library call is made. */
+#define QMOE_NOALLOC_ACCUM_MAX_ELEMS (4u << 20)
+qmoe_status_t qmoe_moe_gemm_w8a8_token_sum_noalloc(const qmoe_gemm_args* args, qmoe_stream_t stream);
+
 /* INT8 W8A16 grouped GEMM (table "INT8_W8A16 Benchmark"): int8 weights are
  * converted exactly to bf16 inside the kernel (offset-binary magic-number
  * conversion after the int8->fp16 trick of the "INT8 quantization support"

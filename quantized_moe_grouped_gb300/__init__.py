@@ -31,8 +31,9 @@ EXPORTED = (
     "qmoe_status_string", "qmoe_version", "qmoe_align_max_padded", "qmoe_moe_align_block_size",
     "qmoe_quant_act_fp8", "qmoe_quant_act_fp8_sorted", "qmoe_quant_weight_fp8", "qmoe_quant_weight_int8", "qmoe_moe_gemm_w8a8",
     "qmoe_moe_gemm_w8a16", "qmoe_silu_mul_quant", "qmoe_debug_e4m3_encode", "qmoe_debug_int8_to_bf16",
-    "qmoe_debug_silu_mul",
+    "qmoe_debug_silu_mul", "qmoe_moe_gemm_w8a8_token_sum_noalloc",
 )
+NOALLOC_ACCUM_MAX_ELEMS = 4 << 20
 
 
 class QmoeError(RuntimeError):
@@ -80,6 +81,7 @@ def load_library(path: str | None = None):
             L.qmoe_quant_weight_int8.argtypes = [vp, i64, i64, vp, vp, vp]
             L.qmoe_moe_gemm_w8a8.argtypes = [ctypes.POINTER(GemmArgs), vp]
             L.qmoe_moe_gemm_w8a16.argtypes = [ctypes.POINTER(GemmArgs), vp]
+            L.qmoe_moe_gemm_w8a8_token_sum_noalloc.argtypes = [ctypes.POINTER(GemmArgs), vp]
             L.qmoe_silu_mul_quant.argtypes = [vp, i64, i64, i64, i32, vp, vp, vp, i64, vp, vp, i32, vp, vp]
             L.qmoe_debug_e4m3_encode.argtypes = [vp, vp, i64, vp]
             L.qmoe_debug_int8_to_bf16.argtypes = [vp, vp, i64, vp]
@@ -258,6 +260,40 @@ def moe_gemm_w8a8(a_q: torch.Tensor, a_scale: torch.Tensor, w_q: torch.Tensor, w
     return _gemm("qmoe_moe_gemm_w8a8", a=a_q, a_scale=a_scale, w=w_q, w_scale=w_scale, align=align,
                  topk_weights=topk_weights, out=out, M=M, top_k=top_k, BM=BM, a_layout=a_layout,
                  out_layout=out_layout, d_status=d_status, accum=accum, stream=stream)
+
+
+def moe_gemm_w8a8_token_sum_noalloc(a_q: torch.Tensor, a_scale: torch.Tensor, w_q: torch.Tensor,
+                                    w_scale: torch.Tensor, align: dict, topk_weights: torch.Tensor | None, *,
+                                    M: int, top_k: int, BM: int, a_layout: int = A_TOKEN_GATHER,
+                                    out: torch.Tensor | None = None, d_status: torch.Tensor | None = None,
+                                    stream=None) -> torch.Tensor:
+    """Sum over top_k of the FP8 grouped GEMM (bf16 [M, N]) using the library's
+    built-in fp32 scratch instead of a caller buffer, for callers that cannot
+    allocate device memory (M*N <= NOALLOC_ACCUM_MAX_ELEMS; calls that overlap
+    on the GPU share the scratch and must not run concurrently)."""
+    _need(a_q, torch.uint8, "a_q")
+    _need(w_q, torch.uint8, "w_q")
+    _need(a_scale, torch.float32, "a_scale")
+    _need(w_scale, torch.float32, "w_scale")
+    if M * w_q.shape[1] > NOALLOC_ACCUM_MAX_ELEMS:
+        raise QmoeError(f"M*N = {M * w_q.shape[1]} exceeds the built-in scratch ({NOALLOC_ACCUM_MAX_ELEMS} floats)")
+    out = _out_for(out, OUT_TOKEN_SUM, M, top_k, w_q.shape[1], a_q.device)
+    E, N, K = w_q.shape
+    args = GemmArgs()
+    args.struct_size = ctypes.sizeof(GemmArgs)
+    args.a, args.lda, args.a_scale = a_q.data_ptr(), a_q.stride(0), a_scale.data_ptr()
+    args.a_scale_mode, args.a_layout = SCALE_PER_TOKEN, a_layout
+    args.w, args.w_scale = w_q.data_ptr(), w_scale.data_ptr()
+    args.sorted_ids, args.expert_ids = align["sorted_ids"].data_ptr(), align["expert_ids"].data_ptr()
+    args.num_post_padded = align["num_post_padded"].data_ptr()
+    args.expert_offsets, args.padded_offsets = align["expert_offsets"].data_ptr(), align["padded_offsets"].data_ptr()
+    args.topk_weights = None if topk_weights is None else topk_weights.data_ptr()
+    args.out, args.out_layout = out.data_ptr(), OUT_TOKEN_SUM
+    args.M, args.N, args.K, args.E, args.top_k, args.BM = M, N, K, E, top_k, BM
+    args.d_status = None if d_status is None else d_status.data_ptr()
+    st = load_library().qmoe_moe_gemm_w8a8_token_sum_noalloc(ctypes.byref(args), _stream(stream))
+    _check(st, "moe_gemm_w8a8_token_sum_noalloc")
+    return out
 
 
 def moe_gemm_w8a16(a: torch.Tensor, w_q: torch.Tensor, w_scale: torch.Tensor, align: dict,
