@@ -74,6 +74,23 @@ def page_aggregate():
     return sum(b) / sum(t) / 1e9, sum(flops(m) for m in SWEEP_M) / sum(t) / 1e12
 
 
+def recorded_traffic():
+    """DRAM bytes per step of the GEMM launches from the committed ncu record,
+    or None when the kernel sources changed since it was taken."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "gemm_fp8_decode_sweep_traffic.json")
+    try:
+        rec = json.load(open(path))
+        h = hashlib.sha256()
+        for src in rec["sources"]:
+            h.update(open(os.path.join(ROOT, src), "rb").read())
+        if h.hexdigest() != rec["sources_sha256"]:
+            return None
+        return int(rec["traffic_bytes_per_step"])
+    except Exception:
+        return None
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -253,6 +270,129 @@ def run_reference(args) -> None:
     print(json.dumps(line), flush=True)
 
 
+# ----------------------------------------------------------------- suite ---
+def _timed(fn, reps, flush=None):
+    """Median device time (ms) of fn() over reps runs, each after an L2 flush."""
+    import torch
+    ts = []
+    for _ in range(reps):
+        if flush is not None:
+            flush.zero_()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        fn()
+        b.record()
+        torch.cuda.synchronize()
+        ts.append(a.elapsed_time(b))
+    return statistics.median(ts)
+
+
+def run_suite(reps: int = 20) -> None:
+    """Per-entry-point timings of the other workloads (not the bench line):
+    INT8 W8A16 sweep, Mixtral-8x7B- and 8x22B-shaped FP8 layers.  Weights are
+    N(0, 1/K) drawn with torch's seeded device generator (timing only); every
+    kernel is timed after a 512 MB L2 flush."""
+    import torch
+
+    import quantized_moe_grouped_gb300 as q
+    from quantized_moe_grouped_gb300 import inputs
+
+    q.load_library()
+    dev = torch.device("cuda", 0)
+    torch.manual_seed(0)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    hbm, _ = measured_peaks()
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            bf16_peak = float(json.load(f)["bf16_tflops"])
+    except Exception:
+        bf16_peak = 1900.0
+    fp8_peak = 2.0 * bf16_peak          # nominal fp8:bf16 dense ratio 2
+
+    def line(workload, kernel, ms, nbytes, nflops, bound):
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        tfl = nflops / (ms * 1e-3) / 1e12
+        roof_ms = max(nbytes / (hbm * 1e9), nflops / ((fp8_peak if bound == "fp8" else bf16_peak) * 1e12)) * 1e3
+        print(json.dumps({"suite": workload, "kernel": kernel, "us": ms * 1e3, "GBps": gbs, "TFLOPS": tfl,
+                          "roofline_us": roof_ms * 1e3, "frac_of_roofline": roof_ms / ms}), flush=True)
+
+    def weights_fp8(E_, N_, K_):
+        wq = torch.empty(E_, N_, K_, dtype=torch.uint8, device=dev)
+        ws = torch.empty(E_, N_, dtype=torch.float32, device=dev)
+        for e in range(E_):
+            w = torch.randn(N_, K_, device=dev) * (1.0 / np.sqrt(K_))
+            wq[e], ws[e] = q.quant_weight_fp8(w)
+        return wq, ws
+
+    def weights_int8(E_, N_, K_):
+        wq = torch.empty(E_, N_, K_, dtype=torch.int8, device=dev)
+        ws = torch.empty(E_, N_, dtype=torch.float32, device=dev)
+        for e in range(E_):
+            w = torch.randn(N_, K_, device=dev) * (1.0 / np.sqrt(K_))
+            wq[e], ws[e] = q.quant_weight_int8(w)
+        return wq, ws
+
+    # INT8 W8A16 sweep
+    for wl in inputs.int8_w8a16_sweep():
+        wq, ws = weights_int8(E, wl.N, wl.K)
+        a = torch.from_numpy(inputs.activations_bf16(wl.M, wl.K, wl.seed).view(np.int16)).to(dev).view(torch.bfloat16)
+        ids, tw = inputs.routing(wl.M, E, TOP_K, wl.seed)
+        BM = 32 if wl.M <= 64 else 128
+        al = q.moe_align_block_size(torch.from_numpy(ids).to(dev), E, BM)
+        twd = torch.from_numpy(tw).to(dev)
+        out = torch.empty(wl.M * TOP_K, wl.N, dtype=torch.bfloat16, device=dev)
+        ms = _timed(lambda: q.moe_gemm_w8a16(a, wq, ws, al, twd, M=wl.M, top_k=TOP_K, BM=BM, out=out), reps, flush)
+        hit = len(np.unique(ids))
+        nbytes = hit * wl.N * wl.K + hit * wl.N * 4 + wl.M * wl.K * 2 + wl.M * TOP_K * (8 + 2 * wl.N)
+        line(wl.name, f"moe_gemm_w8a16 BM={BM}", ms, nbytes, 2.0 * wl.M * TOP_K * wl.K * wl.N, "bf16")
+        del wq, ws
+
+    # FP8 layers
+    for wl in (inputs.mixtral_8x7b_layer(), inputs.mixtral_8x22b_layer()):
+        M, K, I, Nd = wl.M, wl.K, wl.inter, wl.N
+        T = M * TOP_K
+        BM = 128
+        ids, tw = inputs.routing(M, E, TOP_K, wl.seed, wl.zipf_s)
+        hit = len(np.unique(ids))
+        idsd, twd = torch.from_numpy(ids).to(dev), torch.from_numpy(tw).to(dev)
+        a = torch.from_numpy(inputs.activations_bf16(M, K, wl.seed).view(np.int16)).to(dev).view(torch.bfloat16)
+        w1q, w1s = weights_fp8(E, 2 * I, K)
+        al = q.moe_align_block_size(idsd, E, BM)
+        ms = _timed(lambda: q.moe_align_block_size(idsd, E, BM, out=al), reps)
+        line(wl.name, "moe_align_block_size", ms, T * 4 + al["sorted_ids"].numel() * 4, 0, "fp8")
+        aq, sa = q.quant_act_fp8_sorted(a, al, TOP_K)
+        ms = _timed(lambda: q.quant_act_fp8_sorted(a, al, TOP_K, q=aq, scale=sa), reps, flush)
+        line(wl.name, "quant_act_fp8_sorted", ms, M * K * 2 + T * (K + 4), 0, "fp8")
+        up = torch.empty(T, 2 * I, dtype=torch.bfloat16, device=dev)
+        ms = _timed(lambda: q.moe_gemm_w8a8(aq, sa, w1q, w1s, al, None, M=M, top_k=TOP_K, BM=BM,
+                                            a_layout=q.A_PADDED, out_layout=q.OUT_GROUPED, out=up), reps, flush)
+        line(wl.name, "moe_gemm_w8a8 up (padded A -> grouped out)", ms,
+             hit * 2 * I * K + hit * 2 * I * 4 + T * (K + 4) + T * 2 * I * 2, 2.0 * T * K * 2 * I, "fp8")
+        del w1q, w1s
+        if wl.act_scale == "token":
+            hq, hs = q.silu_mul_quant(up)
+            ms = _timed(lambda: q.silu_mul_quant(up, q=hq, scale=hs), reps, flush)
+            line(wl.name, "silu_mul_quant per-token", ms, T * 2 * I * 2 + T * (I + 4), 0, "fp8")
+            w2q, w2s = weights_fp8(E, Nd, I)
+            out = torch.empty(M, Nd, dtype=torch.bfloat16, device=dev)
+            acc = torch.empty(M, Nd, dtype=torch.float32, device=dev)
+            ms = _timed(lambda: q.moe_gemm_w8a8(hq, hs, w2q, w2s, al, twd, M=M, top_k=TOP_K, BM=BM,
+                                                a_layout=q.A_GROUPED, out_layout=q.OUT_TOKEN_SUM, out=out,
+                                                accum=acc), reps, flush)
+            line(wl.name, "moe_gemm_w8a8 down (grouped A -> token sum)", ms,
+                 hit * Nd * I + hit * Nd * 4 + T * (I + 4) + T * 8 + M * Nd * 2, 2.0 * T * I * Nd, "fp8")
+            del w2q, w2s
+        else:
+            sf_rows = q.align_max_padded(T, E, 128)
+            hq, sf = q.silu_mul_quant(up, q.SCALE_MX_1X32, expert_offsets=al["expert_offsets"],
+                                      sf_padded_offsets=al["padded_offsets"], sf_rows=sf_rows)
+            ms = _timed(lambda: q.silu_mul_quant(up, q.SCALE_MX_1X32, expert_offsets=al["expert_offsets"],
+                                                 sf_padded_offsets=al["padded_offsets"], q=hq, sf=sf), reps, flush)
+            line(wl.name, "silu_mul_quant mxfp8", ms, T * 2 * I * 2 + T * I + T * (I // 32), 0, "fp8")
+        del up
+
+
 # ------------------------------------------------------------------ main ---
 def main() -> None:
     ap = argparse.ArgumentParser()
@@ -261,7 +401,11 @@ def main() -> None:
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--suite", action="store_true", help="per-kernel timings of the other workloads instead")
     args = ap.parse_args()
+    if args.suite:
+        run_suite()
+        return
     args.warmup = max(args.warmup, 3)
     if args.impl == "reference":
         run_reference(args)
@@ -371,7 +515,8 @@ def main() -> None:
                        "(470 MB of e4m3 weights streamed by every GEMM)", "parallelism": f"replicas x{world}"},
             "roofline": {"bound": "hbm", "kernel": "moe_gemm_kernel<fp8>", "achieved": achieved, "peak": peak,
                          "peak_kind": f"{peak_kind} (hbm_gbs, burst)", "unit": "GB/s", "frac": achieved / peak,
-                         "traffic": None},
+                         "traffic": recorded_traffic(), "algorithmic_bytes": step_bytes,
+                         "per": "one step = the four GEMM launches of the sweep"},
             "sweep": sweep,
             "vs_baseline_note": f"page aggregate over the same sweep: {page_gbs:.0f} GB/s, {page_tflops:.0f} TFLOPS "
                                 "(ROCm GPU, unnamed)",
