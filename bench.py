@@ -390,6 +390,16 @@ def run_suite(reps: int = 20) -> None:
             ms = _timed(lambda: q.silu_mul_quant(up, q.SCALE_MX_1X32, expert_offsets=al["expert_offsets"],
                                                  sf_padded_offsets=al["padded_offsets"], q=hq, sf=sf), reps, flush)
             line(wl.name, "silu_mul_quant mxfp8", ms, T * 2 * I * 2 + T * I + T * (I // 32), 0, "fp8")
+            w2q, w2s = weights_fp8(E, Nd, I)
+            out = torch.empty(M, Nd, dtype=torch.bfloat16, device=dev)
+            acc = torch.empty(M, Nd, dtype=torch.float32, device=dev)
+            ms = _timed(lambda: q.moe_gemm_w8a8(hq, None, w2q, w2s, al, twd, M=M, top_k=TOP_K, BM=BM,
+                                                a_layout=q.A_GROUPED, out_layout=q.OUT_TOKEN_SUM, out=out,
+                                                accum=acc, a_scale_mode=q.SCALE_MX_1X32, a_sf=sf,
+                                                a_sf_padded_offsets=al["padded_offsets"]), reps, flush)
+            line(wl.name, "moe_gemm_w8a8 down mxfp8 (grouped A -> token sum)", ms,
+                 hit * Nd * I + hit * Nd * 4 + T * (I + I // 32) + T * 8 + M * Nd * 2, 2.0 * T * I * Nd, "fp8")
+            del w2q, w2s
         del up
 
 

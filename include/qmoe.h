@@ -182,7 +182,13 @@ typedef struct {
  * second launch rounds the sums to bf16 into out[M, N].  For top_k == 2 the
  * result does not depend on the order of the additions (0 + a + b == 0 + b + a
  * in IEEE arithmetic); for larger top_k the fp32 rounding order may vary.
- * QMOE_SCALE_MX_1X32 is not supported yet (QMOE_ERR_UNSUPPORTED). */
+ * QMOE_SCALE_MX_1X32 (the MXFP8 intermediate of qmoe_silu_mul_quant): A holds
+ * e4m3 codes in compact grouped rows (QMOE_A_GROUPED) and a_sf their E8M0
+ * scales, row r of expert e at sf row a_sf_padded_offsets[e] + (r -
+ * expert_offsets[e]), one byte per 32 elements along K (row stride a_sf_ld, a
+ * multiple of 4 and >= roundup(K/32, 4)); a_scale is unused.  The scales are
+ * applied inside the tensor-core MMA (block-scaled kind::mxf8f6f4).  Needs
+ * K % 32 == 0 and BM >= 128 (else QMOE_ERR_UNSUPPORTED). */
 qmoe_status_t qmoe_moe_gemm_w8a8(const qmoe_gemm_args* args, qmoe_stream_t stream);
 
 /* FP8 W8A8 grouped GEMM with the TOKEN_SUM layout that allocates nothing.

@@ -240,11 +240,12 @@ def _out_for(out, out_layout, M, top_k, N, device):
     return torch.empty(rows, N, dtype=torch.bfloat16, device=device)
 
 
-def moe_gemm_w8a8(a_q: torch.Tensor, a_scale: torch.Tensor, w_q: torch.Tensor, w_scale: torch.Tensor,
+def moe_gemm_w8a8(a_q: torch.Tensor, a_scale: torch.Tensor | None, w_q: torch.Tensor, w_scale: torch.Tensor,
                   align: dict, topk_weights: torch.Tensor | None, *, M: int, top_k: int, BM: int,
                   a_layout: int = A_TOKEN_GATHER, out_layout: int = OUT_SLOT, out: torch.Tensor | None = None,
                   d_status: torch.Tensor | None = None, accum: torch.Tensor | None = None,
-                  stream=None) -> torch.Tensor:
+                  a_scale_mode: int = SCALE_PER_TOKEN, a_sf: torch.Tensor | None = None,
+                  a_sf_padded_offsets: torch.Tensor | None = None, stream=None) -> torch.Tensor:
     """FP8 W8A8 grouped GEMM.  a_q uint8 e4m3 [rows, K] (token rows for TOKEN_GATHER,
     compact grouped rows for GROUPED), a_scale fp32 [rows], w_q uint8 e4m3 [E, N, K],
     w_scale fp32 [E, N], align = moe_align_block_size(..., BM), topk_weights fp32 [M, top_k]
@@ -252,14 +253,19 @@ def moe_gemm_w8a8(a_q: torch.Tensor, a_scale: torch.Tensor, w_q: torch.Tensor, w
     fp32 [M, N] scratch the sum needs, allocated here when not given)."""
     _need(a_q, torch.uint8, "a_q")
     _need(w_q, torch.uint8, "w_q")
-    _need(a_scale, torch.float32, "a_scale")
+    if a_scale_mode == SCALE_PER_TOKEN:
+        _need(a_scale, torch.float32, "a_scale")
+    else:
+        _need(a_sf, torch.uint8, "a_sf")
+        _need(a_sf_padded_offsets, torch.int32, "a_sf_padded_offsets")
     _need(w_scale, torch.float32, "w_scale")
     if topk_weights is not None:
         _need(topk_weights, torch.float32, "topk_weights")
     out = _out_for(out, out_layout, M, top_k, w_q.shape[1], a_q.device)
     return _gemm("qmoe_moe_gemm_w8a8", a=a_q, a_scale=a_scale, w=w_q, w_scale=w_scale, align=align,
                  topk_weights=topk_weights, out=out, M=M, top_k=top_k, BM=BM, a_layout=a_layout,
-                 out_layout=out_layout, d_status=d_status, accum=accum, stream=stream)
+                 out_layout=out_layout, d_status=d_status, accum=accum, a_scale_mode=a_scale_mode, a_sf=a_sf,
+                 a_sf_padded_offsets=a_sf_padded_offsets, stream=stream)
 
 
 def moe_gemm_w8a8_token_sum_noalloc(a_q: torch.Tensor, a_scale: torch.Tensor, w_q: torch.Tensor,

@@ -58,11 +58,14 @@ struct GemmParams {
     int64_t T;
     int32_t E, top_k, a_layout, out_layout, BM;
     int32_t a_tma;               // 1: activation tiles by TMA (GROUPED / PADDED rows), 0: cp.async gather
+    const uint8_t* a_sf;         // MX: E8M0 scale rows of the grouped activations
+    int64_t a_sf_ld;
+    const int32_t* a_sf_poff;    // MX: first scale row of each expert
     int32_t num_k_blocks;
     int32_t* d_status;
 };
 
-template <bool kBF16, bool kWide, int BN>
+template <bool kBF16, bool kWide, int BN, bool kMX = false>
 struct GemmCfg {
     static constexpr int kSlotRows = kWide ? 128 : BN;      // slots per tile
     static constexpr int kWRows = kWide ? 256 : 128;        // weight rows (output channels) per tile
@@ -81,10 +84,19 @@ struct GemmCfg {
     static constexpr int kBProdThreads = 64;
     static constexpr int kEpiThreads = 128;
     static constexpr int kConvThreads = 128;
-    static constexpr int kThreads = kBF16 ? 384 : 256;
+    static constexpr int kThreads = (kBF16 || kMX) ? 384 : 256;
     static constexpr int kAccCols = kMmaN;                  // TMEM columns per accumulator
-    static constexpr int kTmemCols = 2 * kAccCols < 32 ? 32 : 2 * kAccCols;
-    static constexpr uint32_t kIdesc = make_idesc(kBF16 ? kFmtBF16 : kFmtE4M3, 128, kMmaN);
+    // MX: one accumulator (256 columns), then four scale columns per stage for
+    // the 128 activation rows (4-column aligned) and 8 columns of constant
+    // weight scales 2^0 (8-column aligned).
+    static constexpr int kAccBufs = kMX ? 1 : 2;
+    static constexpr int kSfaCol = kAccCols;
+    static constexpr int kSfbCol = (kAccCols + 4 * kStages + 7) / 8 * 8;
+    static constexpr int kTmemCols = kMX ? 512 : (2 * kAccCols < 32 ? 32 : 2 * kAccCols);
+    static constexpr uint32_t kIdesc =
+        kMX ? make_idesc_mx(128, kMmaN) : make_idesc(kBF16 ? kFmtBF16 : kFmtE4M3, 128, kMmaN);
+    static_assert(!kMX || (kWide && !kBF16), "MX scales: FP8 wide tile only");
+    static_assert(!kMX || kSfbCol + 8 <= 512, "TMEM columns");
     static constexpr int kDynSmem = kStages * kStageBytes + 1024;
     static_assert(kStages >= 2, "need at least two pipeline stages");
     static_assert(kMmaN % 16 == 0 && kMmaN >= 16 && kMmaN <= 256, "MMA N must be a multiple of 16 in [16, 256]");
@@ -127,17 +139,17 @@ QMOE_DI void tmem_ld32(uint32_t taddr, float (&v)[32]) {
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-template <bool kBF16, bool kWide, int BN>
-__global__ void __launch_bounds__(GemmCfg<kBF16, kWide, BN>::kThreads, 1)
+template <bool kBF16, bool kWide, int BN, bool kMX>
+__global__ void __launch_bounds__(GemmCfg<kBF16, kWide, BN, kMX>::kThreads, 1)
     moe_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_a,
                     const GemmParams p) {
-    using C = GemmCfg<kBF16, kWide, BN>;
+    using C = GemmCfg<kBF16, kWide, BN, kMX>;
     constexpr int S = C::kStages;
     constexpr int SR = C::kSlotRows;
     constexpr int WR = C::kWRows;
     extern __shared__ uint8_t smem_raw[];
     __shared__ uint64_t bar_full[S], bar_empty[S], bar_conv[S];
-    __shared__ uint64_t bar_tfull[2], bar_tempty[2], bar_drain;
+    __shared__ uint64_t bar_tfull[2], bar_tempty[2], bar_drain, bar_sfb;
     __shared__ uint32_t s_tmem_base;
     __shared__ int s_abort;
     __shared__ int32_t s_brow[SR];                 // activation producers: source row of each slot row (-1: zero)
@@ -161,6 +173,7 @@ __global__ void __launch_bounds__(GemmCfg<kBF16, kWide, BN>::kThreads, 1)
             mbar_init(&bar_tempty[i], C::kEpiThreads);
         }
         mbar_init(&bar_drain, 1);
+        mbar_init(&bar_sfb, C::kConvThreads);
         s_abort = 0;
         fence_mbar_init();
     }
@@ -224,10 +237,14 @@ __global__ void __launch_bounds__(GemmCfg<kBF16, kWide, BN>::kThreads, 1)
         if (lane == 0) {
             int it = 0, tcount = 0;
             bool ok = true;
+            if (kMX) {  // constant weight scales written once by the scale warps
+                ok = mbar_wait(&bar_sfb, 0, abort, p.d_status);
+                tc_fence_after();
+            }
             for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
                 if (tile_expert(tile) < 0) continue;
-                const int acc = tcount & 1;
-                const uint32_t aph = (tcount >> 1) & 1;
+                const int acc = tcount % C::kAccBufs;
+                const uint32_t aph = (tcount / C::kAccBufs) & 1;
                 if (!mbar_wait(&bar_tempty[acc], aph ^ 1, abort, p.d_status)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * C::kAccCols);
@@ -235,7 +252,7 @@ __global__ void __launch_bounds__(GemmCfg<kBF16, kWide, BN>::kThreads, 1)
                     const int s = it % S;
                     const uint32_t ph = (it / S) & 1;
                     if (!mbar_wait(&bar_full[s], ph, abort, p.d_status)) { ok = false; break; }
-                    if (kBF16 && !mbar_wait(&bar_conv[s], ph, abort, p.d_status)) { ok = false; break; }
+                    if ((kBF16 || kMX) && !mbar_wait(&bar_conv[s], ph, abort, p.d_status)) { ok = false; break; }
                     tc_fence_after();
                     const uint64_t dw = desc_kmajor_sw128(smem_u32(w_tile(s)));
                     const uint64_t dx = desc_kmajor_sw128(smem_u32(act_tile(s)));
@@ -243,7 +260,10 @@ __global__ void __launch_bounds__(GemmCfg<kBF16, kWide, BN>::kThreads, 1)
                     const uint64_t db = kWide ? dw : dx;
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
-                        if (kBF16) mma_f16(d_tmem, da + 2 * k, db + 2 * k, C::kIdesc, (kb | k) != 0);
+                        if (kMX)
+                            mma_mxf8(d_tmem, da + 2 * k, db + 2 * k, C::kIdesc | (static_cast<uint32_t>(k) << 29),
+                                     tmem_base + C::kSfaCol + 4 * s, tmem_base + C::kSfbCol, (kb | k) != 0);
+                        else if (kBF16) mma_f16(d_tmem, da + 2 * k, db + 2 * k, C::kIdesc, (kb | k) != 0);
                         else mma_f8f6f4(d_tmem, da + 2 * k, db + 2 * k, C::kIdesc, (kb | k) != 0);
                     }
                     tc_commit(&bar_empty[s]);
@@ -312,8 +332,8 @@ __global__ void __launch_bounds__(GemmCfg<kBF16, kWide, BN>::kThreads, 1)
             if (e < 0) continue;
             const int sb = tile % num_sb;
             const int nb = tile / num_sb;
-            const int acc = tcount & 1;
-            const uint32_t aph = (tcount >> 1) & 1;
+            const int acc = tcount % C::kAccBufs;
+            const uint32_t aph = (tcount / C::kAccBufs) & 1;
             const uint32_t t_base =
                 tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * C::kAccCols);
             if constexpr (kWide) {
@@ -420,6 +440,48 @@ __global__ void __launch_bounds__(GemmCfg<kBF16, kWide, BN>::kThreads, 1)
             mbar_arrive(&bar_tempty[acc]);
             ++tcount;
         }
+    } else if (kMX) {
+        // ----------------------------- activation scales -> TMEM (MX) ---
+        // A stage's scales for the 128 tile rows occupy four 32-bit columns in
+        // the 32 x 4 x 4 arrangement: row r at lane r % 32, column r / 32, byte
+        // k = the 32-wide K block of the stage's k-th MMA; every lane quadrant
+        // holds the same copy, so each of the four warps writes all 128 rows.
+        const int q = warp & 3;
+        const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+        tmem_st4(lane_base + C::kSfbCol, 0x7F7F7F7Fu);
+        tmem_st4(lane_base + C::kSfbCol + 4, 0x7F7F7F7Fu);
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(&bar_sfb);
+        int it = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+            const int e = tile_expert(tile);
+            if (e < 0) continue;
+            const int sb = tile % num_sb;
+            const int cnt = p.expert_offsets[e + 1] - p.expert_offsets[e];
+            const uint8_t* sfrow[4];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const int i = sb * SR + c * 32 + lane - p.padded_offsets[e];  // local row of tile row 32c + lane
+                sfrow[c] = (i < cnt) ? p.a_sf + (static_cast<int64_t>(p.a_sf_poff[e]) + i) * p.a_sf_ld : nullptr;
+            }
+            for (int kb = 0; kb < nkb; ++kb, ++it) {
+                const int s = it % S;
+                const uint32_t ph = (it / S) & 1;
+                if (!mbar_wait(&bar_empty[s], ph ^ 1, abort, p.d_status)) ok = false;
+                ok = __all_sync(0xFFFFFFFFu, ok);
+                if (!ok) break;
+                uint32_t v[4];
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    v[c] = sfrow[c] ? *reinterpret_cast<const uint32_t*>(sfrow[c] + kb * 4) : 0x7F7F7F7Fu;
+                tmem_st4v(lane_base + C::kSfaCol + 4 * s, v[0], v[1], v[2], v[3]);
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(&bar_conv[s]);
+            }
+        }
     } else {
         // ---------------------------------- int8 -> bf16 converters ---
         if (kBF16) {
@@ -511,10 +573,10 @@ inline bool make_act_map(CUtensorMap* map, const void* a, int64_t rows, int64_t 
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <bool kBF16, bool kWide, int BN>
+template <bool kBF16, bool kWide, int BN, bool kMX = false>
 inline qmoe_status_t launch_gemm(const void* w, int64_t E, int64_t N, int64_t K, const GemmParams& p,
                                  int64_t max_padded, int64_t a_rows, int64_t lda, cudaStream_t st) {
-    using C = GemmCfg<kBF16, kWide, BN>;
+    using C = GemmCfg<kBF16, kWide, BN, kMX>;
     static std::mutex mu;
     static bool attr_set[64] = {false};
     int dev = 0;
@@ -522,7 +584,7 @@ inline qmoe_status_t launch_gemm(const void* w, int64_t E, int64_t N, int64_t K,
     {
         std::lock_guard<std::mutex> g(mu);
         if (!attr_set[dev]) {
-            if (cudaFuncSetAttribute(moe_gemm_kernel<kBF16, kWide, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+            if (cudaFuncSetAttribute(moe_gemm_kernel<kBF16, kWide, BN, kMX>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      C::kDynSmem) != cudaSuccess)
                 return QMOE_ERR_CUDA;
             attr_set[dev] = true;
@@ -537,7 +599,7 @@ inline qmoe_status_t launch_gemm(const void* w, int64_t E, int64_t N, int64_t K,
     const int64_t max_tiles = ((max_padded + C::kSlotRows - 1) / C::kSlotRows) * ((N + C::kWRows - 1) / C::kWRows);
     const int64_t grid = max_tiles < sms ? max_tiles : sms;
     if (grid <= 0) return QMOE_OK;
-    moe_gemm_kernel<kBF16, kWide, BN><<<static_cast<unsigned>(grid), C::kThreads, C::kDynSmem, st>>>(map, amap, p);
+    moe_gemm_kernel<kBF16, kWide, BN, kMX><<<static_cast<unsigned>(grid), C::kThreads, C::kDynSmem, st>>>(map, amap, p);
     return launch_status();
 }
 
@@ -556,10 +618,16 @@ inline qmoe_status_t run_moe_gemm(const qmoe_gemm_args* a, cudaStream_t st) {
     if (a->out_layout < QMOE_OUT_SLOT || a->out_layout > QMOE_OUT_TOKEN_SUM) return QMOE_ERR_INVALID_ARG;
     const int64_t elem = kBF16 ? 2 : 1;
     if (a->lda < a->K || (a->lda * elem) % 16 != 0) return QMOE_ERR_INVALID_ARG;
+    const bool mx = !kBF16 && a->a_scale_mode == QMOE_SCALE_MX_1X32;
     if (kBF16) {
         if (a->a_scale_mode != QMOE_SCALE_PER_TOKEN) return QMOE_ERR_UNSUPPORTED;
+    } else if (mx) {
+        // MX activations: grouped rows (as written by qmoe_silu_mul_quant), wide tile only
+        if (a->a_layout != QMOE_A_GROUPED || a->BM < 128) return QMOE_ERR_UNSUPPORTED;
+        if (a->K % 32 != 0 || !a->a_sf || !a->a_sf_padded_offsets || a->a_sf_ld < (a->K / 32 + 3) / 4 * 4 ||
+            a->a_sf_ld % 4 != 0 || !aligned4(a->a_sf))
+            return QMOE_ERR_INVALID_ARG;
     } else {
-        if (a->a_scale_mode == QMOE_SCALE_MX_1X32) return QMOE_ERR_UNSUPPORTED;
         if (a->a_scale_mode != QMOE_SCALE_PER_TOKEN || !a->a_scale) return QMOE_ERR_INVALID_ARG;
     }
     const int64_t T = a->M * a->top_k;
@@ -580,7 +648,10 @@ inline qmoe_status_t run_moe_gemm(const qmoe_gemm_args* a, cudaStream_t st) {
     p.a = static_cast<const uint8_t*>(a->a);
     p.lda_bytes = a->lda * elem;
     p.a_row_bytes = a->K * elem;
-    p.a_scale = kBF16 ? nullptr : a->a_scale;
+    p.a_scale = (kBF16 || mx) ? nullptr : a->a_scale;
+    p.a_sf = mx ? a->a_sf : nullptr;
+    p.a_sf_ld = mx ? a->a_sf_ld : 0;
+    p.a_sf_poff = mx ? a->a_sf_padded_offsets : nullptr;
     p.sorted_ids = a->sorted_ids;
     p.expert_ids = a->expert_ids;
     p.num_post_padded = a->num_post_padded;
@@ -603,6 +674,13 @@ inline qmoe_status_t run_moe_gemm(const qmoe_gemm_args* a, cudaStream_t st) {
     const int64_t max_padded = (T + static_cast<int64_t>(a->E) * (a->BM - 1) + a->BM - 1) / a->BM * a->BM;
     const int64_t a_rows = a->a_layout == QMOE_A_PADDED ? max_padded : (a->a_layout == QMOE_A_GROUPED ? T : a->M);
     qmoe_status_t r;
+    if constexpr (!kBF16) {
+        if (mx) {
+            r = launch_gemm<false, true, 128, true>(a->w, a->E, a->N, a->K, p, max_padded, a_rows, a->lda, st);
+            if (r != QMOE_OK || !tsum) return r;
+            return launch_token_sum_finalize(a->accum, a->out, a->M * a->N, st);
+        }
+    }
     switch (a->BM) {
         case 16: r = launch_gemm<kBF16, false, 16>(a->w, a->E, a->N, a->K, p, max_padded, a_rows, a->lda, st); break;
         case 32: r = launch_gemm<kBF16, false, 32>(a->w, a->E, a->N, a->K, p, max_padded, a_rows, a->lda, st); break;

@@ -252,3 +252,41 @@ def test_w8a8_padded_sorted_activations(q, orc, M, K, N, E, top_k, BM, out_layou
                        w_scale=p["rws"], topk_ids=p["ids"], topk_w=p["tw"], E=E, a_layout="padded", BM=BM,
                        out_layout={0: "slot", 2: "token_sum"}[out_layout])
     check(bf16_to_np_f32(out), ref)
+
+
+@pytest.mark.parametrize("M,I,N,E,BM,zipf,out_layout", [(256, 256, 256, 8, 128, None, 2), (300, 384, 272, 8, 256, 1.2, 2),
+                                                        (150, 160, 384, 5, 128, None, 1)])
+def test_w8a8_mx_activations(q, orc, M, I, N, E, BM, zipf, out_layout):
+    """Down GEMM on MXFP8 activations: SwiGLU + MX 1x32 requantisation (bit-exact
+    against the oracle), then the block-scaled FP8 GEMM over the grouped rows,
+    against the oracle's fp64 dequantisation with the E8M0 block scales."""
+    top_k = 2
+    T = M * top_k
+    ids, tw = inputs.routing(M, E, top_k, seed=M + I, zipf_s=zipf)
+    y = inputs.activations_bf16(T, 2 * I, seed=M + I)
+    al = q.moe_align_block_size(to_dev(ids), E, BM)
+    al128 = q.moe_align_block_size(to_dev(ids), E, 128)
+    hq, sf = q.silu_mul_quant(to_dev_bf16(y), q.SCALE_MX_1X32, expert_offsets=al128["expert_offsets"],
+                              sf_padded_offsets=al128["padded_offsets"], sf_rows=q.align_max_padded(T, E, 128))
+    ref_al = orc.moe_align(ids, E, 128)
+    rq, rsf = orc.silu_mul_quant_mx(y, ref_al["expert_offsets"], ref_al["padded_offsets"])
+    assert np.array_equal(hq.cpu().numpy(), rq)
+    nsf = ref_al["padded_offsets"][-1]
+    assert np.array_equal(sf.cpu().numpy()[:nsf], rsf)
+    w = inputs.expert_weights_f32(E, N, I, seed=M + I, weight_set=1)
+    wq, ws = q.quant_weight_fp8(to_dev(w))
+    rwq, rws = orc.quant_rows_fp8_f32(w)
+    st = status()
+    out = q.moe_gemm_w8a8(hq, None, wq, ws, al, to_dev(tw), M=M, top_k=top_k, BM=BM, a_layout=q.A_GROUPED,
+                          out_layout=out_layout, a_scale_mode=q.SCALE_MX_1X32, a_sf=sf,
+                          a_sf_padded_offsets=al128["padded_offsets"], d_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    eoff, poff = ref_al["expert_offsets"], ref_al["padded_offsets"]
+    sf_row = np.empty(T, dtype=np.int64)
+    for e in range(E):
+        sf_row[eoff[e]:eoff[e + 1]] = poff[e] + np.arange(eoff[e + 1] - eoff[e])
+    ref = orc.moe_gemm(a_kind=orc.A_FP8_MX, a=rq, a_sf=rsf, a_sf_row=sf_row, w_kind=orc.W_FP8, w=rwq, w_scale=rws,
+                       topk_ids=ids, topk_w=tw, E=E, a_layout="grouped",
+                       out_layout={1: "grouped", 2: "token_sum"}[out_layout])
+    check(bf16_to_np_f32(out), ref)
