@@ -126,6 +126,19 @@ qmoe_status_t qmoe_quant_act_fp8_sorted(const uint16_t* x, int64_t M, int64_t co
                                         int32_t top_k, int64_t cap, uint8_t* q, float* scale,
                                         qmoe_stream_t stream);
 
+/* moe_align_block_size and qmoe_quant_act_fp8_sorted in one launch (for
+ * T = M*top_k <= 4096; larger T issues the two launches).  Outputs are those
+ * of the two calls -- identical align outputs, identical codes and scales at
+ * every valid padded position -- except that pad rows of q and scale are not
+ * written (the grouped GEMM never stores results of pad rows).  Each token row
+ * is quantised once and copied to its top_k positions.  Limits as for the two
+ * calls, with top_k <= 8. */
+qmoe_status_t qmoe_moe_align_quant_fp8(const uint16_t* x, int64_t M, int64_t cols, int64_t ldx,
+                                       const int32_t* topk_ids, int32_t top_k, int32_t E, int32_t BM,
+                                       int32_t* sorted_ids, int32_t* expert_ids, int32_t* num_post_padded,
+                                       int32_t* expert_offsets, int32_t* padded_offsets, uint8_t* q, float* scale,
+                                       int32_t* d_status, qmoe_stream_t stream);
+
 /* Per-output-channel weight quantisation, the same rule on fp32 rows: every
  * (expert, output channel) row of W[E, N, K] is one row (rows = E*N).
  * fp8: scale = amax/448, e4m3 codes; int8: scale = amax/127,

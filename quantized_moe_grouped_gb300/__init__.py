@@ -29,7 +29,7 @@ OUT_SLOT, OUT_GROUPED, OUT_TOKEN_SUM = 0, 1, 2
 
 EXPORTED = (
     "qmoe_status_string", "qmoe_version", "qmoe_align_max_padded", "qmoe_moe_align_block_size",
-    "qmoe_quant_act_fp8", "qmoe_quant_act_fp8_sorted", "qmoe_quant_weight_fp8", "qmoe_quant_weight_int8", "qmoe_moe_gemm_w8a8",
+    "qmoe_quant_act_fp8", "qmoe_quant_act_fp8_sorted", "qmoe_moe_align_quant_fp8", "qmoe_quant_weight_fp8", "qmoe_quant_weight_int8", "qmoe_moe_gemm_w8a8",
     "qmoe_moe_gemm_w8a16", "qmoe_silu_mul_quant", "qmoe_debug_e4m3_encode", "qmoe_debug_int8_to_bf16",
     "qmoe_debug_silu_mul", "qmoe_moe_gemm_w8a8_token_sum_noalloc",
 )
@@ -77,6 +77,8 @@ def load_library(path: str | None = None):
             L.qmoe_moe_align_block_size.argtypes = [vp, i64, i32, i32, vp, vp, vp, vp, vp, vp, vp]
             L.qmoe_quant_act_fp8.argtypes = [vp, i64, i64, i64, vp, vp, vp]
             L.qmoe_quant_act_fp8_sorted.argtypes = [vp, i64, i64, i64, vp, vp, i32, i64, vp, vp, vp]
+            L.qmoe_moe_align_quant_fp8.argtypes = [vp, i64, i64, i64, vp, i32, i32, i32, vp, vp, vp, vp, vp, vp,
+                                                   vp, vp, vp]
             L.qmoe_quant_weight_fp8.argtypes = [vp, i64, i64, vp, vp, vp]
             L.qmoe_quant_weight_int8.argtypes = [vp, i64, i64, vp, vp, vp]
             L.qmoe_moe_gemm_w8a8.argtypes = [ctypes.POINTER(GemmArgs), vp]
@@ -172,6 +174,29 @@ def quant_act_fp8_sorted(x: torch.Tensor, align: dict, top_k: int, q: torch.Tens
                                                   _stream(stream))
     _check(st, "quant_act_fp8_sorted")
     return q, scale
+
+
+def moe_align_quant_fp8(x: torch.Tensor, topk_ids: torch.Tensor, E: int, BM: int, align: dict | None = None,
+                        q: torch.Tensor | None = None, scale: torch.Tensor | None = None,
+                        d_status: torch.Tensor | None = None, stream=None):
+    """moe_align_block_size + quant_act_fp8_sorted in one launch (small batches).
+    Returns (align dict, q [cap, K] uint8, scale [cap] fp32); pad rows unwritten."""
+    if not x.is_cuda or x.dtype != torch.bfloat16 or x.dim() != 2 or x.stride(1) != 1:
+        raise QmoeError("x must be a 2-D CUDA bf16 tensor with unit column stride")
+    _need(topk_ids, torch.int32, "topk_ids")
+    M, cols = x.shape
+    top_k = topk_ids.numel() // max(M, 1) if M > 0 else 1
+    T = topk_ids.numel()
+    o = align if align is not None else alloc_align_outputs(T, E, BM, x.device)
+    cap = o["sorted_ids"].numel()
+    q = q if q is not None else torch.empty(cap, cols, dtype=torch.uint8, device=x.device)
+    scale = scale if scale is not None else torch.empty(cap, dtype=torch.float32, device=x.device)
+    st = load_library().qmoe_moe_align_quant_fp8(
+        _ptr(x), M, cols, x.stride(0), _ptr(topk_ids), top_k, E, BM, _ptr(o["sorted_ids"]), _ptr(o["expert_ids"]),
+        _ptr(o["num_post_padded"]), _ptr(o["expert_offsets"]), _ptr(o["padded_offsets"]), _ptr(q), _ptr(scale),
+        _ptr(d_status), _stream(stream))
+    _check(st, "moe_align_quant_fp8")
+    return o, q, scale
 
 
 def quant_weight_fp8(w: torch.Tensor, stream=None):

@@ -224,6 +224,136 @@ __global__ void __launch_bounds__(kRowThreads)
     }
 }
 
+// ======================================================================
+// Fused align + sorted per-token quantisation for small slot counts (one
+// launch).  CTAs 0..M-1: one token each -- histogram of all ids in shared
+// memory, padded offsets, the padded position of each of the token's slots
+// (its rank among the earlier slots of the same expert), one quantisation of
+// the token row written to every such position, and sorted_ids at those
+// positions.  CTA M: expert/padded offsets, num_post_padded, the block ->
+// expert map and the sentinel at every pad position.  Pad rows of q are left
+// unwritten (the grouped GEMM never stores their results).
+// ======================================================================
+constexpr int kFusedMaxT = 4096;
+
+__global__ void __launch_bounds__(kRowThreads)
+    align_quant_fused_kernel(const uint16_t* __restrict__ x, int64_t M, int64_t cols, int64_t ldx,
+                             const int32_t* __restrict__ ids, int top_k, int E, int BM,
+                             int32_t* __restrict__ sorted_ids, int64_t cap, int32_t* __restrict__ expert_ids,
+                             int32_t* __restrict__ num_post_padded, int32_t* __restrict__ expert_offsets,
+                             int32_t* __restrict__ padded_offsets, uint8_t* __restrict__ q,
+                             float* __restrict__ scale, int32_t* d_status) {
+    __shared__ int s_ids[kFusedMaxT];
+    __shared__ int s_cnt[kAlignMaxE];
+    __shared__ int s_poff[kAlignMaxE + 1];
+    __shared__ int s_rank[8];
+    __shared__ float red[33];
+    const int T = static_cast<int>(M) * top_k;
+    const int tid = threadIdx.x;
+    for (int e = tid; e < E; e += blockDim.x) s_cnt[e] = 0;
+    __syncthreads();
+    for (int i = tid; i < T; i += blockDim.x) {
+        const int e = ids[i];
+        s_ids[i] = e;
+        if (e >= 0 && e < E) atomicAdd(&s_cnt[e], 1);
+    }
+    __syncthreads();
+    if (tid == 0) {
+        int poff = 0;
+        for (int e = 0; e < E; ++e) {
+            s_poff[e] = poff;
+            poff += (s_cnt[e] + BM - 1) / BM * BM;
+        }
+        s_poff[E] = poff;
+    }
+    __syncthreads();
+    const int64_t b = blockIdx.x;
+    if (b == M) {
+        // offsets, block map and pad sentinels
+        if (tid == 0) {
+            int off = 0;
+            bool bad = false;
+            for (int e = 0; e < E; ++e) {
+                expert_offsets[e] = off;
+                padded_offsets[e] = s_poff[e];
+                off += s_cnt[e];
+            }
+            expert_offsets[E] = off;
+            padded_offsets[E] = s_poff[E];
+            *num_post_padded = s_poff[E];
+            bad = off != T;
+            if (bad && d_status) atomicOr(reinterpret_cast<int*>(d_status), QMOE_DEV_INVALID_EXPERT);
+        }
+        for (int64_t blk = tid; blk < cap / BM; blk += blockDim.x) {
+            const int64_t p = blk * BM;
+            int owner = -1;
+            if (p < s_poff[E]) {
+                int lo = 0, hi = E - 1;
+                while (lo < hi) {
+                    const int mid = (lo + hi + 1) >> 1;
+                    if (s_poff[mid] <= p) lo = mid;
+                    else hi = mid - 1;
+                }
+                owner = lo;
+            }
+            expert_ids[blk] = owner;
+        }
+        for (int64_t p = tid; p < cap; p += blockDim.x) {
+            bool pad = p >= s_poff[E];
+            if (!pad) {
+                int lo = 0, hi = E - 1;
+                while (lo < hi) {
+                    const int mid = (lo + hi + 1) >> 1;
+                    if (s_poff[mid] <= p) lo = mid;
+                    else hi = mid - 1;
+                }
+                pad = p - s_poff[lo] >= s_cnt[lo];
+            }
+            if (pad) sorted_ids[p] = T;
+        }
+        return;
+    }
+    // token b: padded positions of its slots
+    for (int j = 0; j < top_k; ++j) {
+        const int s = static_cast<int>(b) * top_k + j;
+        const int e = s_ids[s];
+        int c = 0;
+        if (e >= 0 && e < E)
+            for (int i = tid; i < s; i += blockDim.x) c += (s_ids[i] == e);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xFFFFFFFFu, c, o);
+        if ((tid & 31) == 0) red[tid >> 5] = __int_as_float(c);
+        __syncthreads();
+        if (tid == 0) {
+            int tot = 0;
+            for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) tot += __float_as_int(red[w]);
+            s_rank[j] = (e >= 0 && e < E) ? s_poff[e] + tot : -1;
+            if (e >= 0 && e < E) sorted_ids[s_poff[e] + tot] = s;
+        }
+        __syncthreads();
+    }
+    const uint16_t* xr = x + b * ldx;
+    float amax = 0.0f;
+    for (int64_t c = static_cast<int64_t>(tid) * 8; c < cols; c += kRowThreads * 8) {
+        float v[8];
+        load8(xr + c, v);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
+    }
+    amax = block_max(amax, red);
+    const float sc = (amax == 0.0f) ? 1.0f : __fdiv_rn(amax, 448.0f);
+    if (tid < top_k && s_rank[tid] >= 0) scale[s_rank[tid]] = sc;
+    for (int64_t c = static_cast<int64_t>(tid) * 8; c < cols; c += kRowThreads * 8) {
+        float v[8];
+        load8(xr + c, v);
+        uint2 o;
+        o.x = e4m3x4(__fdiv_rn(v[0], sc), __fdiv_rn(v[1], sc), __fdiv_rn(v[2], sc), __fdiv_rn(v[3], sc));
+        o.y = e4m3x4(__fdiv_rn(v[4], sc), __fdiv_rn(v[5], sc), __fdiv_rn(v[6], sc), __fdiv_rn(v[7], sc));
+        for (int j = 0; j < top_k; ++j)
+            if (s_rank[j] >= 0) *reinterpret_cast<uint2*>(q + static_cast<int64_t>(s_rank[j]) * cols + c) = o;
+    }
+}
+
 __global__ void __launch_bounds__(kRowThreads)
     quant_rows_int8_kernel(const float* __restrict__ x, int64_t cols, int8_t* __restrict__ q,
                            float* __restrict__ scale) {
@@ -436,6 +566,31 @@ qmoe_status_t qmoe_quant_act_fp8_sorted(const uint16_t* x, int64_t M, int64_t co
         return QMOE_ERR_INVALID_ARG;
     quant_rows_fp8_sorted_kernel<<<static_cast<unsigned>(cap), kRowThreads, 0, stream>>>(
         x, cols, ldx, sorted_ids, num_post_padded, M * top_k, top_k, q, scale);
+    return launch_status();
+}
+
+qmoe_status_t qmoe_moe_align_quant_fp8(const uint16_t* x, int64_t M, int64_t cols, int64_t ldx,
+                                       const int32_t* topk_ids, int32_t top_k, int32_t E, int32_t BM,
+                                       int32_t* sorted_ids, int32_t* expert_ids, int32_t* num_post_padded,
+                                       int32_t* expert_offsets, int32_t* padded_offsets, uint8_t* q, float* scale,
+                                       int32_t* d_status, qmoe_stream_t stream) {
+    if (M < 0 || top_k < 1 || top_k > 8 || E < 1 || E > kAlignMaxE || BM < 1 || BM > 1024) return QMOE_ERR_INVALID_ARG;
+    if (cols < 16 || cols % 16 != 0 || ldx < cols || ldx % 8 != 0) return QMOE_ERR_INVALID_ARG;
+    const int64_t T = M * top_k;
+    const int64_t cap = qmoe_align_max_padded(T, E, BM);
+    if (cap >= (int64_t(1) << 31)) return QMOE_ERR_UNSUPPORTED;
+    if ((M > 0 && (!x || !topk_ids)) || !sorted_ids || !expert_ids || !num_post_padded || !expert_offsets ||
+        !padded_offsets || !q || !scale || (M > 0 && !aligned16(x)) || !aligned16(q))
+        return QMOE_ERR_INVALID_ARG;
+    if (T > kFusedMaxT) {  // large batches: the two separate launches
+        qmoe_status_t st = qmoe_moe_align_block_size(topk_ids, T, E, BM, sorted_ids, expert_ids, num_post_padded,
+                                                     expert_offsets, padded_offsets, d_status, stream);
+        if (st != QMOE_OK) return st;
+        return qmoe_quant_act_fp8_sorted(x, M, cols, ldx, sorted_ids, num_post_padded, top_k, cap, q, scale, stream);
+    }
+    align_quant_fused_kernel<<<static_cast<unsigned>(M + 1), kRowThreads, 0, stream>>>(
+        x, M, cols, ldx, topk_ids, top_k, E, BM, sorted_ids, cap, expert_ids, num_post_padded, expert_offsets,
+        padded_offsets, q, scale, d_status);
     return launch_status();
 }
 

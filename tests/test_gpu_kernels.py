@@ -164,3 +164,29 @@ def test_silu_quant_mx_whole_equals_per_expert(q):
         assert torch.equal(qe, qw[e * 64:(e + 1) * 64])
         assert torch.equal(sfe, sfw[e * 128:(e + 1) * 128])
         assert sfe.shape == (128, 4)
+
+
+@pytest.mark.parametrize("M,K,E,top_k,BM", [(64, 4096, 8, 2, 32), (1, 128, 8, 2, 16), (333, 256, 8, 2, 64),
+                                            (512, 4096, 8, 2, 128), (100, 64, 5, 3, 16), (2100, 128, 8, 2, 128)])
+def test_fused_align_quant_bitexact(q, orc, M, K, E, top_k, BM):
+    """One-launch align + sorted quantisation == the oracle's align and per-token
+    codes placed at every valid padded position (the last case exceeds the
+    one-launch limit and takes the two-launch path)."""
+    x = inputs.activations_bf16(M, K, seed=M + K)
+    ids, _ = inputs.routing(M, E, top_k, seed=M + K)
+    st = status()
+    al, qq, ss = q.moe_align_quant_fp8(to_dev_bf16(x), to_dev(ids), E, BM, d_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    ref = orc.moe_align(ids, E, BM)
+    cap = al["sorted_ids"].numel()
+    assert np.array_equal(al["sorted_ids"].cpu().numpy(), ref["sorted_ids"][:cap])
+    assert np.array_equal(al["expert_ids"].cpu().numpy(), ref["expert_ids"][: cap // BM])
+    assert np.array_equal(al["expert_offsets"].cpu().numpy(), ref["expert_offsets"])
+    assert np.array_equal(al["padded_offsets"].cpu().numpy(), ref["padded_offsets"])
+    assert int(al["num_post_padded"].item()) == ref["num_post_padded"]
+    rq, rs = orc.quant_rows_fp8_bf16(x)
+    srt = ref["sorted_ids"][: ref["num_post_padded"]]
+    valid = np.nonzero(srt < M * top_k)[0]
+    assert np.array_equal(qq.cpu().numpy()[valid], rq[srt[valid] // top_k])
+    assert np.array_equal(ss.cpu().numpy()[valid], rs[srt[valid] // top_k])
