@@ -289,7 +289,7 @@ def _timed(fn, reps, flush=None):
     return statistics.median(ts)
 
 
-def run_suite(reps: int = 20) -> None:
+def run_suite(reps: int = 20, only: str | None = None) -> None:
     """Per-entry-point timings of the other workloads (not the bench line):
     INT8 W8A16 sweep, Mixtral-8x7B- and 8x22B-shaped FP8 layers.  Weights are
     N(0, 1/K) drawn with torch's seeded device generator (timing only); every
@@ -336,6 +336,8 @@ def run_suite(reps: int = 20) -> None:
 
     # INT8 W8A16 sweep
     for wl in inputs.int8_w8a16_sweep():
+        if only and only not in wl.name:
+            continue
         wq, ws = weights_int8(E, wl.N, wl.K)
         a = torch.from_numpy(inputs.activations_bf16(wl.M, wl.K, wl.seed).view(np.int16)).to(dev).view(torch.bfloat16)
         ids, tw = inputs.routing(wl.M, E, TOP_K, wl.seed)
@@ -343,14 +345,22 @@ def run_suite(reps: int = 20) -> None:
         al = q.moe_align_block_size(torch.from_numpy(ids).to(dev), E, BM)
         twd = torch.from_numpy(tw).to(dev)
         out = torch.empty(wl.M * TOP_K, wl.N, dtype=torch.bfloat16, device=dev)
-        ms = _timed(lambda: q.moe_gemm_w8a16(a, wq, ws, al, twd, M=wl.M, top_k=TOP_K, BM=BM, out=out), reps, flush)
         hit = len(np.unique(ids))
         nbytes = hit * wl.N * wl.K + hit * wl.N * 4 + wl.M * wl.K * 2 + wl.M * TOP_K * (8 + 2 * wl.N)
-        line(wl.name, f"moe_gemm_w8a16 BM={BM}", ms, nbytes, 2.0 * wl.M * TOP_K * wl.K * wl.N, "bf16")
+        ms = _timed(lambda: q.moe_gemm_w8a16(a, wq, ws, al, twd, M=wl.M, top_k=TOP_K, BM=BM, out=out), reps, flush)
+        line(wl.name, f"moe_gemm_w8a16 BM={BM} token-gather A", ms, nbytes, 2.0 * wl.M * TOP_K * wl.K * wl.N, "bf16")
+        ap = q.gather_sorted_bf16(a, al, TOP_K)
+        ms = _timed(lambda: q.gather_sorted_bf16(a, al, TOP_K, out=ap), reps, flush)
+        line(wl.name, "gather_sorted_bf16", ms, wl.M * wl.K * 2 + wl.M * TOP_K * wl.K * 2, 0, "bf16")
+        ms = _timed(lambda: q.moe_gemm_w8a16(ap, wq, ws, al, twd, M=wl.M, top_k=TOP_K, BM=BM, a_layout=q.A_PADDED,
+                                             out=out), reps, flush)
+        line(wl.name, f"moe_gemm_w8a16 BM={BM} padded A", ms, nbytes, 2.0 * wl.M * TOP_K * wl.K * wl.N, "bf16")
         del wq, ws
 
     # FP8 layers
     for wl in (inputs.mixtral_8x7b_layer(), inputs.mixtral_8x22b_layer()):
+        if only and only not in wl.name:
+            continue
         M, K, I, Nd = wl.M, wl.K, wl.inter, wl.N
         T = M * TOP_K
         BM = 128
@@ -413,9 +423,11 @@ def main() -> None:
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--suite", action="store_true", help="per-kernel timings of the other workloads instead")
+    ap.add_argument("--only", default=None, help="--suite: workloads whose name contains this text")
+    ap.add_argument("--reps", type=int, default=20, help="--suite: timed repetitions per kernel")
     args = ap.parse_args()
     if args.suite:
-        run_suite()
+        run_suite(args.reps, args.only)
         return
     args.warmup = max(args.warmup, 3)
     if args.impl == "reference":

@@ -139,6 +139,16 @@ qmoe_status_t qmoe_moe_align_quant_fp8(const uint16_t* x, int64_t M, int64_t col
                                        int32_t* expert_offsets, int32_t* padded_offsets, uint8_t* q, float* scale,
                                        int32_t* d_status, qmoe_stream_t stream);
 
+/* bf16 token rows copied into the padded sorted order of the grouped GEMM
+ * (the activation operand of qmoe_moe_gemm_w8a16 with QMOE_A_PADDED): row p <
+ * *num_post_padded of out is x[sorted_ids[p] / top_k], or zeros for a pad
+ * position; rows at or past *num_post_padded are not written.  out holds
+ * cap = qmoe_align_max_padded(T, E, BM) rows of cols bf16.  Limits: cols % 8
+ * == 0, ldx % 8 == 0, x and out 16-byte aligned. */
+qmoe_status_t qmoe_gather_sorted_bf16(const uint16_t* x, int64_t M, int64_t cols, int64_t ldx,
+                                      const int32_t* sorted_ids, const int32_t* num_post_padded, int32_t top_k,
+                                      int64_t cap, uint16_t* out, qmoe_stream_t stream);
+
 /* Per-output-channel weight quantisation, the same rule on fp32 rows: every
  * (expert, output channel) row of W[E, N, K] is one row (rows = E*N).
  * fp8: scale = amax/448, e4m3 codes; int8: scale = amax/127,

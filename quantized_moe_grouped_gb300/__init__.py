@@ -29,7 +29,7 @@ OUT_SLOT, OUT_GROUPED, OUT_TOKEN_SUM = 0, 1, 2
 
 EXPORTED = (
     "qmoe_status_string", "qmoe_version", "qmoe_align_max_padded", "qmoe_moe_align_block_size",
-    "qmoe_quant_act_fp8", "qmoe_quant_act_fp8_sorted", "qmoe_moe_align_quant_fp8", "qmoe_quant_weight_fp8", "qmoe_quant_weight_int8", "qmoe_moe_gemm_w8a8",
+    "qmoe_quant_act_fp8", "qmoe_quant_act_fp8_sorted", "qmoe_moe_align_quant_fp8", "qmoe_gather_sorted_bf16", "qmoe_quant_weight_fp8", "qmoe_quant_weight_int8", "qmoe_moe_gemm_w8a8",
     "qmoe_moe_gemm_w8a16", "qmoe_silu_mul_quant", "qmoe_debug_e4m3_encode", "qmoe_debug_int8_to_bf16",
     "qmoe_debug_silu_mul", "qmoe_moe_gemm_w8a8_token_sum_noalloc",
 )
@@ -79,6 +79,7 @@ def load_library(path: str | None = None):
             L.qmoe_quant_act_fp8_sorted.argtypes = [vp, i64, i64, i64, vp, vp, i32, i64, vp, vp, vp]
             L.qmoe_moe_align_quant_fp8.argtypes = [vp, i64, i64, i64, vp, i32, i32, i32, vp, vp, vp, vp, vp, vp,
                                                    vp, vp, vp]
+            L.qmoe_gather_sorted_bf16.argtypes = [vp, i64, i64, i64, vp, vp, i32, i64, vp, vp]
             L.qmoe_quant_weight_fp8.argtypes = [vp, i64, i64, vp, vp, vp]
             L.qmoe_quant_weight_int8.argtypes = [vp, i64, i64, vp, vp, vp]
             L.qmoe_moe_gemm_w8a8.argtypes = [ctypes.POINTER(GemmArgs), vp]
@@ -197,6 +198,21 @@ def moe_align_quant_fp8(x: torch.Tensor, topk_ids: torch.Tensor, E: int, BM: int
         _ptr(d_status), _stream(stream))
     _check(st, "moe_align_quant_fp8")
     return o, q, scale
+
+
+def gather_sorted_bf16(x: torch.Tensor, align: dict, top_k: int, out: torch.Tensor | None = None, stream=None):
+    """bf16 token rows [M, K] -> rows in padded sorted order [cap, K] (the PADDED
+    activation operand of moe_gemm_w8a16); pad rows zero."""
+    if not x.is_cuda or x.dtype != torch.bfloat16 or x.dim() != 2 or x.stride(1) != 1:
+        raise QmoeError("x must be a 2-D CUDA bf16 tensor with unit column stride")
+    M, cols = x.shape
+    cap = align["sorted_ids"].numel()
+    out = out if out is not None else torch.empty(cap, cols, dtype=torch.bfloat16, device=x.device)
+    st = load_library().qmoe_gather_sorted_bf16(_ptr(x), M, cols, x.stride(0), _ptr(align["sorted_ids"]),
+                                                _ptr(align["num_post_padded"]), top_k, cap, _ptr(out),
+                                                _stream(stream))
+    _check(st, "gather_sorted_bf16")
+    return out
 
 
 def quant_weight_fp8(w: torch.Tensor, stream=None):

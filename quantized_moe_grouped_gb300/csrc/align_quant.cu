@@ -354,6 +354,24 @@ __global__ void __launch_bounds__(kRowThreads)
     }
 }
 
+// bf16 token rows copied into padded sorted order (one CTA per padded
+// position; pad rows zeroed, rows at or past num_post_padded untouched).
+__global__ void __launch_bounds__(kRowThreads)
+    gather_sorted_bf16_kernel(const uint16_t* __restrict__ x, int64_t cols, int64_t ldx,
+                              const int32_t* __restrict__ sorted_ids, const int32_t* __restrict__ npp, int64_t T,
+                              int top_k, uint16_t* __restrict__ out) {
+    const int64_t p = blockIdx.x;
+    if (p >= *npp) return;
+    const int s = sorted_ids[p];
+    uint4* dst = reinterpret_cast<uint4*>(out + p * cols);
+    if (s < 0 || s >= T) {
+        for (int64_t c = threadIdx.x; c < cols / 8; c += kRowThreads) dst[c] = make_uint4(0u, 0u, 0u, 0u);
+        return;
+    }
+    const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<int64_t>(s / top_k) * ldx);
+    for (int64_t c = threadIdx.x; c < cols / 8; c += kRowThreads) dst[c] = src[c];
+}
+
 __global__ void __launch_bounds__(kRowThreads)
     quant_rows_int8_kernel(const float* __restrict__ x, int64_t cols, int8_t* __restrict__ q,
                            float* __restrict__ scale) {
@@ -591,6 +609,19 @@ qmoe_status_t qmoe_moe_align_quant_fp8(const uint16_t* x, int64_t M, int64_t col
     align_quant_fused_kernel<<<static_cast<unsigned>(M + 1), kRowThreads, 0, stream>>>(
         x, M, cols, ldx, topk_ids, top_k, E, BM, sorted_ids, cap, expert_ids, num_post_padded, expert_offsets,
         padded_offsets, q, scale, d_status);
+    return launch_status();
+}
+
+qmoe_status_t qmoe_gather_sorted_bf16(const uint16_t* x, int64_t M, int64_t cols, int64_t ldx,
+                                      const int32_t* sorted_ids, const int32_t* num_post_padded, int32_t top_k,
+                                      int64_t cap, uint16_t* out, qmoe_stream_t stream) {
+    if (M < 0 || cols < 8 || cols % 8 != 0 || ldx < cols || ldx % 8 != 0 || top_k < 1 || cap < 0)
+        return QMOE_ERR_INVALID_ARG;
+    if (cap == 0) return QMOE_OK;
+    if (!x || !sorted_ids || !num_post_padded || !out || !aligned16(x) || !aligned16(out) || cap > 0x7FFFFFFF)
+        return QMOE_ERR_INVALID_ARG;
+    gather_sorted_bf16_kernel<<<static_cast<unsigned>(cap), kRowThreads, 0, stream>>>(
+        x, cols, ldx, sorted_ids, num_post_padded, M * top_k, top_k, out);
     return launch_status();
 }
 

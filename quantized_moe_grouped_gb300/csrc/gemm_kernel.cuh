@@ -24,7 +24,9 @@
 //   warps 4-7   epilogue: TMEM -> registers, x w_scale[e,n] x a_scale x w[s],
 //               bf16 store (TOKEN_SUM: fp32 vector atomic add into the
 //               caller's accumulation buffer, rounded to bf16 by a second launch)
-//   warps 8-11  (W8A16 only) int8 -> bf16 converters, smem -> smem
+//   warps 8-15  W8A16: int8 -> bf16 converters (raw ring -> main ring), two
+//               groups of four warps taking alternate stages
+//   warps 8-11  MX: the activation scale writers (global -> TMEM)
 //
 // Every wait is bounded (mbar_wait); on a timeout the CTA raises an abort
 // flag, all roles leave their loops, copies in flight are drained and TMEM is
@@ -74,17 +76,23 @@ struct GemmCfg {
     static constexpr int kWBytes = kWRows * 128;
     static constexpr int kActBytes = kSlotRows * 128;
     static constexpr int kRawBytes = kBF16 ? kWRows * 64 : 0;  // int8 weight tile before conversion
-    static constexpr int kWLoadBytes = kBF16 ? kRawBytes : kWBytes;
-    static constexpr int kStageBytes = kWBytes + kActBytes + kRawBytes;
-    static constexpr int kStagesRaw = (200 * 1024) / kStageBytes;
-    static constexpr int kStages = kStagesRaw > 8 ? 8 : kStagesRaw;
+    // Main ring: MMA operand tiles (weights -- converted to bf16 for W8A16 --
+    // and activations).  W8A16 adds a separate, deeper ring of raw int8 weight
+    // tiles so that the weight stream keeps many bytes in flight while the
+    // converted tiles need only a few stages.
+    static constexpr int kStageBytes = kWBytes + kActBytes;
+    static constexpr int kStagesFit = (200 * 1024) / kStageBytes;
+    static constexpr int kStages = kBF16 ? (kWide ? 3 : 4) : (kStagesFit > 8 ? 8 : kStagesFit);
+    static constexpr int kRawFit = kBF16 ? (200 * 1024 - kStages * kStageBytes) / (kRawBytes > 0 ? kRawBytes : 1) : 0;
+    static constexpr int kRawStages = kBF16 ? (kRawFit > 16 ? 16 : kRawFit) : 0;
     // cp.async completion lag (stages): the MMA can run kStages - kLag - 1 stages
     // ahead of the gather warps, so the lag shrinks when the ring is short.
     static constexpr int kLag = kStages >= 6 ? 3 : (kStages >= 5 ? 2 : 1);
     static constexpr int kBProdThreads = 64;
     static constexpr int kEpiThreads = 128;
     static constexpr int kConvThreads = 128;
-    static constexpr int kThreads = (kBF16 || kMX) ? 384 : 256;
+    static constexpr int kConvGroups = kBF16 ? 2 : 1;       // converter groups alternate stages
+    static constexpr int kThreads = kBF16 ? 512 : (kMX ? 384 : 256);
     static constexpr int kAccCols = kMmaN;                  // TMEM columns per accumulator
     // MX: one accumulator (256 columns), then four scale columns per stage for
     // the 128 activation rows (4-column aligned) and 8 columns of constant
@@ -97,8 +105,9 @@ struct GemmCfg {
         kMX ? make_idesc_mx(128, kMmaN) : make_idesc(kBF16 ? kFmtBF16 : kFmtE4M3, 128, kMmaN);
     static_assert(!kMX || (kWide && !kBF16), "MX scales: FP8 wide tile only");
     static_assert(!kMX || kSfbCol + 8 <= 512, "TMEM columns");
-    static constexpr int kDynSmem = kStages * kStageBytes + 1024;
+    static constexpr int kDynSmem = kStages * kStageBytes + kRawStages * kRawBytes + 1024;
     static_assert(kStages >= 2, "need at least two pipeline stages");
+    static_assert(!kBF16 || kRawStages >= 2, "need at least two raw weight stages");
     static_assert(kMmaN % 16 == 0 && kMmaN >= 16 && kMmaN <= 256, "MMA N must be a multiple of 16 in [16, 256]");
     static_assert(kActBytes % 1024 == 0 && kWBytes % 1024 == 0 && kRawBytes % 1024 == 0, "1 KB tile alignment");
 };
@@ -148,7 +157,8 @@ __global__ void __launch_bounds__(GemmCfg<kBF16, kWide, BN, kMX>::kThreads, 1)
     constexpr int SR = C::kSlotRows;
     constexpr int WR = C::kWRows;
     extern __shared__ uint8_t smem_raw[];
-    __shared__ uint64_t bar_full[S], bar_empty[S], bar_conv[S];
+    constexpr int R = C::kRawStages > 0 ? C::kRawStages : 1;
+    __shared__ uint64_t bar_full[S], bar_empty[S], bar_conv[S], bar_raw_full[R], bar_raw_empty[R];
     __shared__ uint64_t bar_tfull[2], bar_tempty[2], bar_drain, bar_sfb;
     __shared__ uint32_t s_tmem_base;
     __shared__ int s_abort;
@@ -164,13 +174,18 @@ __global__ void __launch_bounds__(GemmCfg<kBF16, kWide, BN, kMX>::kThreads, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
-            mbar_init(&bar_full[s], p.a_tma ? 1 : 1 + C::kBProdThreads);
+            // arrivals: the TMA thread (weights and/or activation tile), or the 64 gather threads
+            mbar_init(&bar_full[s], p.a_tma ? 1 : (kBF16 ? 0 : 1) + C::kBProdThreads);
             mbar_init(&bar_empty[s], 1);
             mbar_init(&bar_conv[s], C::kConvThreads);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&bar_tfull[i], 1);
             mbar_init(&bar_tempty[i], C::kEpiThreads);
+        }
+        for (int r = 0; r < R; ++r) {
+            mbar_init(&bar_raw_full[r], 1);
+            mbar_init(&bar_raw_empty[r], C::kConvThreads);
         }
         mbar_init(&bar_drain, 1);
         mbar_init(&bar_sfb, C::kConvThreads);
@@ -190,7 +205,7 @@ __global__ void __launch_bounds__(GemmCfg<kBF16, kWide, BN, kMX>::kThreads, 1)
     const int nkb = p.num_k_blocks;
     auto w_tile = [&](int s) { return smem + s * C::kStageBytes; };
     auto act_tile = [&](int s) { return smem + s * C::kStageBytes + C::kWBytes; };
-    auto raw_tile = [&](int s) { return smem + s * C::kStageBytes + C::kWBytes + C::kActBytes; };
+    auto raw_tile = [&](int r) { return smem + S * C::kStageBytes + r * C::kRawBytes; };
     // Expert of a tile, or -1 when the tile is to be skipped: an invalid expert
     // id, or (tiles narrower than BM) a tile whose first slot is padding --
     // valid slots precede the padding inside an expert's region, so the whole
@@ -208,7 +223,7 @@ __global__ void __launch_bounds__(GemmCfg<kBF16, kWide, BN, kMX>::kThreads, 1)
         if (lane == 0) {
             int it = 0;
             bool ok = true;
-            const uint32_t tx = C::kWLoadBytes + (p.a_tma ? C::kActBytes : 0);
+            const uint32_t tx = C::kWBytes + (p.a_tma ? C::kActBytes : 0);
             for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
                 const int e = tile_expert(tile);
                 if (e < 0) continue;
@@ -219,12 +234,20 @@ __global__ void __launch_bounds__(GemmCfg<kBF16, kWide, BN, kMX>::kThreads, 1)
                                       ? sb * SR
                                       : p.expert_offsets[e] + (sb * SR - p.padded_offsets[e]);
                 for (int kb = 0; kb < nkb; ++kb, ++it) {
-                    const int s = it % S;
-                    const uint32_t ph = (it / S) & 1;
-                    if (!mbar_wait(&bar_empty[s], ph ^ 1, abort, p.d_status)) { ok = false; break; }
-                    mbar_arrive_expect_tx(&bar_full[s], tx);
-                    tma_load_3d(&tmap_w, &bar_full[s], kBF16 ? raw_tile(s) : w_tile(s), kb * C::kBK, nb * WR, e);
-                    if (p.a_tma) tma_load_2d(&tmap_a, &bar_full[s], act_tile(s), kb * C::kBK, arow0);
+                    if constexpr (kBF16) {  // raw int8 weights into their own ring
+                        const int r = it % R;
+                        const uint32_t rph = (it / R) & 1;
+                        if (!mbar_wait(&bar_raw_empty[r], rph ^ 1, abort, p.d_status)) { ok = false; break; }
+                        mbar_arrive_expect_tx(&bar_raw_full[r], C::kRawBytes);
+                        tma_load_3d(&tmap_w, &bar_raw_full[r], raw_tile(r), kb * C::kBK, nb * WR, e);
+                    } else {
+                        const int s = it % S;
+                        const uint32_t ph = (it / S) & 1;
+                        if (!mbar_wait(&bar_empty[s], ph ^ 1, abort, p.d_status)) { ok = false; break; }
+                        mbar_arrive_expect_tx(&bar_full[s], tx);
+                        tma_load_3d(&tmap_w, &bar_full[s], w_tile(s), kb * C::kBK, nb * WR, e);
+                        if (p.a_tma) tma_load_2d(&tmap_a, &bar_full[s], act_tile(s), kb * C::kBK, arow0);
+                    }
                 }
             }
             if (!ok) {  // let copies already issued land before the CTA can exit
@@ -274,6 +297,31 @@ __global__ void __launch_bounds__(GemmCfg<kBF16, kWide, BN, kMX>::kThreads, 1)
             }
             tc_commit(&bar_drain);  // every MMA issued above has completed once this fires
             mbar_wait_drain(&bar_drain, 0, p.d_status);
+        }
+    } else if (warp < 4 && kBF16 && p.a_tma) {
+        // ------------------- W8A16: activation tiles by TMA (own thread) ---
+        if (warp == 2 && lane == 0) {
+            int it = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+                const int e = tile_expert(tile);
+                if (e < 0) continue;
+                const int sb = tile % num_sb;
+                const int arow0 = (p.a_layout == QMOE_A_PADDED)
+                                      ? sb * SR
+                                      : p.expert_offsets[e] + (sb * SR - p.padded_offsets[e]);
+                for (int kb = 0; kb < nkb; ++kb, ++it) {
+                    const int s = it % S;
+                    const uint32_t ph = (it / S) & 1;
+                    if (!mbar_wait(&bar_empty[s], ph ^ 1, abort, p.d_status)) { ok = false; break; }
+                    mbar_arrive_expect_tx(&bar_full[s], C::kActBytes);
+                    tma_load_2d(&tmap_a, &bar_full[s], act_tile(s), kb * C::kBK, arow0);
+                }
+            }
+            if (!ok) {
+                const uint64_t t0 = global_timer_ns();
+                while (global_timer_ns() - t0 < 2000000ull) {}
+            }
         }
     } else if (warp < 4) {
         // ------------------------------- activation gather (TOKEN_GATHER) ---
@@ -485,16 +533,22 @@ __global__ void __launch_bounds__(GemmCfg<kBF16, kWide, BN, kMX>::kThreads, 1)
     } else {
         // ---------------------------------- int8 -> bf16 converters ---
         if (kBF16) {
-            const int ct = threadIdx.x - 256;
+            const int group = (warp - 8) >> 2;
+            const int ct = threadIdx.x - 256 - group * C::kConvThreads;
             int it = 0;
             bool ok = true;
             for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
                 if (tile_expert(tile) < 0) continue;
                 for (int kb = 0; kb < nkb; ++kb, ++it) {
+                    if ((it & 1) != group) continue;
                     const int s = it % S;
                     const uint32_t ph = (it / S) & 1;
-                    if (!mbar_wait(&bar_full[s], ph, abort, p.d_status)) { ok = false; break; }
-                    const uint8_t* raw = raw_tile(s);
+                    const int r = it % R;
+                    const uint32_t rph = (it / R) & 1;
+                    // raw tile landed, and the MMA is done with the previous use of slot s
+                    if (!mbar_wait(&bar_raw_full[r], rph, abort, p.d_status)) { ok = false; break; }
+                    if (!mbar_wait(&bar_empty[s], ph ^ 1, abort, p.d_status)) { ok = false; break; }
+                    const uint8_t* raw = raw_tile(r);
                     uint8_t* dst = w_tile(s);
                     const int c = ct & 3;
 #pragma unroll
@@ -511,6 +565,7 @@ __global__ void __launch_bounds__(GemmCfg<kBF16, kWide, BN, kMX>::kThreads, 1)
                     }
                     fence_proxy_async_smem();
                     mbar_arrive(&bar_conv[s]);
+                    mbar_arrive(&bar_raw_empty[r]);
                 }
             }
         }

@@ -290,3 +290,33 @@ def test_w8a8_mx_activations(q, orc, M, I, N, E, BM, zipf, out_layout):
                        topk_ids=ids, topk_w=tw, E=E, a_layout="grouped",
                        out_layout={1: "grouped", 2: "token_sum"}[out_layout])
     check(bf16_to_np_f32(out), ref)
+
+
+@pytest.mark.parametrize("M,K,N,E,top_k,BM,out_layout", [(64, 4096, 256, 8, 2, 32, 0), (200, 272, 208, 8, 2, 64, 2),
+                                                         (520, 256, 400, 8, 2, 128, 0), (90, 160, 272, 5, 3, 256, 2),
+                                                         (33, 512, 128, 4, 2, 16, 0)])
+def test_w8a16_padded_sorted_activations(q, orc, M, K, N, E, top_k, BM, out_layout):
+    """gather_sorted_bf16 (exact copy of token rows to padded sorted positions)
+    feeding the W8A16 GEMM's PADDED layout, with the decoupled int8 ring."""
+    a = inputs.activations_bf16(M, K, seed=M + N + 7)
+    w = inputs.expert_weights_f32(E, N, K, seed=M + N + 7)
+    ids, tw = inputs.routing(M, E, top_k, seed=M + N + 7)
+    wq, ws = q.quant_weight_int8(to_dev(w))
+    rwq, rws = orc.quant_rows_int8_f32(w)
+    al = q.moe_align_block_size(to_dev(ids), E, BM)
+    ap = q.gather_sorted_bf16(to_dev_bf16(a), al, top_k)
+    ref_al = orc.moe_align(ids, E, BM)
+    n = ref_al["num_post_padded"]
+    srt = ref_al["sorted_ids"][:n]
+    valid = srt < M * top_k
+    exp = np.zeros((n, K), dtype=np.uint16)
+    exp[valid] = a[srt[valid] // top_k]
+    got = ap.view(torch.int16).cpu().numpy().view(np.uint16)[:n]
+    assert np.array_equal(got, exp)
+    out = q.moe_gemm_w8a16(ap, wq, ws, al, to_dev(tw), M=M, top_k=top_k, BM=BM, a_layout=q.A_PADDED,
+                           out_layout=out_layout)
+    a_full = np.zeros((ap.shape[0], K), dtype=np.uint16)
+    a_full[:n] = exp
+    ref = orc.moe_gemm(a_kind=orc.A_BF16, a=a_full, w_kind=orc.W_INT8, w=rwq, w_scale=rws, topk_ids=ids, topk_w=tw,
+                       E=E, a_layout="padded", BM=BM, out_layout={0: "slot", 2: "token_sum"}[out_layout])
+    check(bf16_to_np_f32(out), ref)
