@@ -31,7 +31,7 @@ EXPORTED = (
     "qmoe_status_string", "qmoe_version", "qmoe_align_max_padded", "qmoe_moe_align_block_size",
     "qmoe_quant_act_fp8", "qmoe_quant_act_fp8_sorted", "qmoe_moe_align_quant_fp8", "qmoe_gather_sorted_bf16", "qmoe_quant_weight_fp8", "qmoe_quant_weight_int8", "qmoe_moe_gemm_w8a8",
     "qmoe_moe_gemm_w8a16", "qmoe_silu_mul_quant", "qmoe_debug_e4m3_encode", "qmoe_debug_int8_to_bf16",
-    "qmoe_debug_silu_mul", "qmoe_moe_gemm_w8a8_token_sum_noalloc",
+    "qmoe_debug_silu_mul", "qmoe_debug_div_by_scale", "qmoe_moe_gemm_w8a8_token_sum_noalloc",
 )
 NOALLOC_ACCUM_MAX_ELEMS = 4 << 20
 
@@ -89,6 +89,7 @@ def load_library(path: str | None = None):
             L.qmoe_debug_e4m3_encode.argtypes = [vp, vp, i64, vp]
             L.qmoe_debug_int8_to_bf16.argtypes = [vp, vp, i64, vp]
             L.qmoe_debug_silu_mul.argtypes = [vp, vp, vp, i64, vp]
+            L.qmoe_debug_div_by_scale.argtypes = [vp, ctypes.c_float, vp, i64, vp]
             for name in EXPORTED:
                 if name not in ("qmoe_status_string", "qmoe_version", "qmoe_align_max_padded"):
                     getattr(L, name).restype = st
@@ -419,3 +420,11 @@ def debug_silu_mul(g: torch.Tensor, u: torch.Tensor, stream=None) -> torch.Tenso
     _check(load_library().qmoe_debug_silu_mul(_ptr(g), _ptr(u), _ptr(h), g.numel(), _stream(stream)),
            "debug_silu_mul")
     return h
+
+
+def debug_div_by_scale(x: torch.Tensor, s: float, stream=None) -> torch.Tensor:
+    _need(x, torch.float32, "x")
+    q = torch.empty_like(x)
+    _check(load_library().qmoe_debug_div_by_scale(_ptr(x), float(s), _ptr(q), x.numel(), _stream(stream)),
+           "debug_div_by_scale")
+    return q

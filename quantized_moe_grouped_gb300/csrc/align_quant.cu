@@ -149,6 +149,17 @@ QMOE_DI void load8(const float* p, float (&v)[8]) {
 QMOE_DI float load1(const uint16_t* p) { return __uint_as_float(static_cast<uint32_t>(*p) << 16); }
 QMOE_DI float load1(const float* p) { return *p; }
 
+// e4m3 codes of v[0..7] / s (correctly rounded quotients, see div_rn_by), 8 bytes.
+QMOE_DI uint2 quant8(const float (&v)[8], float s, float rinv) {
+    float q[8];
+#pragma unroll
+    for (int i = 0; i < 8; i += 2) div2_rn_by(v[i], v[i + 1], s, rinv, q[i], q[i + 1]);
+    uint2 o;
+    o.x = e4m3x4(q[0], q[1], q[2], q[3]);
+    o.y = e4m3x4(q[4], q[5], q[6], q[7]);
+    return o;
+}
+
 template <typename Tin, bool kVec>
 __global__ void __launch_bounds__(kRowThreads)
     quant_rows_fp8_kernel(const Tin* __restrict__ x, int64_t cols, int64_t ldx, uint8_t* __restrict__ q,
@@ -170,19 +181,17 @@ __global__ void __launch_bounds__(kRowThreads)
     }
     amax = block_max(amax, red);
     const float s = (amax == 0.0f) ? 1.0f : __fdiv_rn(amax, 448.0f);
+    const float rinv = __frcp_rn(s);
     if (threadIdx.x == 0) scale[row] = s;
     if (kVec) {
         for (int64_t c = static_cast<int64_t>(threadIdx.x) * 8; c < cols; c += kRowThreads * 8) {
             float v[8];
             load8(xr + c, v);
-            uint2 o;
-            o.x = e4m3x4(__fdiv_rn(v[0], s), __fdiv_rn(v[1], s), __fdiv_rn(v[2], s), __fdiv_rn(v[3], s));
-            o.y = e4m3x4(__fdiv_rn(v[4], s), __fdiv_rn(v[5], s), __fdiv_rn(v[6], s), __fdiv_rn(v[7], s));
-            *reinterpret_cast<uint2*>(qr + c) = o;
+            *reinterpret_cast<uint2*>(qr + c) = quant8(v, s, rinv);
         }
     } else {
         for (int64_t c = threadIdx.x; c < cols; c += kRowThreads)
-            qr[c] = static_cast<uint8_t>(e4m3x2(__fdiv_rn(load1(xr + c), s), 0.0f) & 0xFFu);
+            qr[c] = static_cast<uint8_t>(e4m3x2(div_rn_by(load1(xr + c), s, rinv), 0.0f) & 0xFFu);
     }
 }
 
@@ -213,14 +222,12 @@ __global__ void __launch_bounds__(kRowThreads)
     }
     amax = block_max(amax, red);
     const float sc = (amax == 0.0f) ? 1.0f : __fdiv_rn(amax, 448.0f);
+    const float rinv = __frcp_rn(sc);
     if (threadIdx.x == 0) scale[p] = sc;
     for (int64_t c = static_cast<int64_t>(threadIdx.x) * 8; c < cols; c += kRowThreads * 8) {
         float v[8];
         load8(xr + c, v);
-        uint2 o;
-        o.x = e4m3x4(__fdiv_rn(v[0], sc), __fdiv_rn(v[1], sc), __fdiv_rn(v[2], sc), __fdiv_rn(v[3], sc));
-        o.y = e4m3x4(__fdiv_rn(v[4], sc), __fdiv_rn(v[5], sc), __fdiv_rn(v[6], sc), __fdiv_rn(v[7], sc));
-        *reinterpret_cast<uint2*>(qr + c) = o;
+        *reinterpret_cast<uint2*>(qr + c) = quant8(v, sc, rinv);
     }
 }
 
@@ -342,13 +349,12 @@ __global__ void __launch_bounds__(kRowThreads)
     }
     amax = block_max(amax, red);
     const float sc = (amax == 0.0f) ? 1.0f : __fdiv_rn(amax, 448.0f);
+    const float rinv = __frcp_rn(sc);
     if (tid < top_k && s_rank[tid] >= 0) scale[s_rank[tid]] = sc;
     for (int64_t c = static_cast<int64_t>(tid) * 8; c < cols; c += kRowThreads * 8) {
         float v[8];
         load8(xr + c, v);
-        uint2 o;
-        o.x = e4m3x4(__fdiv_rn(v[0], sc), __fdiv_rn(v[1], sc), __fdiv_rn(v[2], sc), __fdiv_rn(v[3], sc));
-        o.y = e4m3x4(__fdiv_rn(v[4], sc), __fdiv_rn(v[5], sc), __fdiv_rn(v[6], sc), __fdiv_rn(v[7], sc));
+        const uint2 o = quant8(v, sc, rinv);
         for (int j = 0; j < top_k; ++j)
             if (s_rank[j] >= 0) *reinterpret_cast<uint2*>(q + static_cast<int64_t>(s_rank[j]) * cols + c) = o;
     }
@@ -383,9 +389,10 @@ __global__ void __launch_bounds__(kRowThreads)
     for (int64_t c = threadIdx.x; c < cols; c += kRowThreads) amax = fmaxf(amax, fabsf(xr[c]));
     amax = block_max(amax, red);
     const float s = (amax == 0.0f) ? 1.0f : __fdiv_rn(amax, 127.0f);
+    const float rinv = __frcp_rn(s);
     if (threadIdx.x == 0) scale[row] = s;
     for (int64_t c = threadIdx.x; c < cols; c += kRowThreads) {
-        const float v = fminf(fmaxf(rintf(__fdiv_rn(xr[c], s)), -127.0f), 127.0f);
+        const float v = fminf(fmaxf(rintf(div_rn_by(xr[c], s, rinv)), -127.0f), 127.0f);
         qr[c] = static_cast<int8_t>(static_cast<int>(v));
     }
 }
@@ -402,7 +409,7 @@ QMOE_DI void silu8(const uint16_t* g, const uint16_t* u, float (&h)[8]) {
     load8(g, gv);
     load8(u, uv);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) h[i] = silu_mul(gv[i], uv[i]);
+    for (int i = 0; i < 8; i += 2) silu_mul2(gv[i], gv[i + 1], uv[i], uv[i + 1], h[i], h[i + 1]);
 }
 
 __global__ void __launch_bounds__(kRowThreads)
@@ -424,14 +431,14 @@ __global__ void __launch_bounds__(kRowThreads)
     }
     amax = block_max(amax, red);  // (contains __syncthreads: s_h is complete)
     const float s = (amax == 0.0f) ? 1.0f : __fdiv_rn(amax, 448.0f);
+    const float rinv = __frcp_rn(s);
     if (threadIdx.x == 0) scale[row] = s;
     uint8_t* qr = q + row * I;
     for (int64_t c = static_cast<int64_t>(threadIdx.x) * 8; c < I; c += kRowThreads * 8) {
-        const float* h = s_h + c;
-        uint2 o;
-        o.x = e4m3x4(__fdiv_rn(h[0], s), __fdiv_rn(h[1], s), __fdiv_rn(h[2], s), __fdiv_rn(h[3], s));
-        o.y = e4m3x4(__fdiv_rn(h[4], s), __fdiv_rn(h[5], s), __fdiv_rn(h[6], s), __fdiv_rn(h[7], s));
-        *reinterpret_cast<uint2*>(qr + c) = o;
+        const float4 a = *reinterpret_cast<const float4*>(s_h + c);
+        const float4 b = *reinterpret_cast<const float4*>(s_h + c + 4);
+        const float h[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+        *reinterpret_cast<uint2*>(qr + c) = quant8(h, s, rinv);
     }
 }
 
@@ -520,11 +527,23 @@ __global__ void debug_i8_kernel(const uint32_t* __restrict__ x, uint2* __restric
         y[i] = make_uint2(lo, hi);
     }
 }
+// Pairs go through the packed sequence the kernels use, an odd last element
+// through the scalar one.
 __global__ void debug_silu_kernel(const float* __restrict__ g, const float* __restrict__ u, float* __restrict__ h,
                                   int64_t n) {
-    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
-         i += static_cast<int64_t>(gridDim.x) * blockDim.x)
-        h[i] = silu_mul(g[i], u[i]);
+    for (int64_t i = 2 * (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x); i < n;
+         i += 2 * static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        if (i + 1 < n) silu_mul2(g[i], g[i + 1], u[i], u[i + 1], h[i], h[i + 1]);
+        else h[i] = silu_mul(g[i], u[i]);
+    }
+}
+__global__ void debug_div_kernel(const float* __restrict__ x, float s, float* __restrict__ q, int64_t n) {
+    const float rinv = __frcp_rn(s);
+    for (int64_t i = 2 * (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x); i < n;
+         i += 2 * static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        if (i + 1 < n) div2_rn_by(x[i], x[i + 1], s, rinv, q[i], q[i + 1]);
+        else q[i] = div_rn_by(x[i], s, rinv);
+    }
 }
 
 static int grid_for(int64_t n, int threads) {
@@ -695,7 +714,14 @@ qmoe_status_t qmoe_debug_int8_to_bf16(const int8_t* x, uint16_t* y, int64_t n, q
 qmoe_status_t qmoe_debug_silu_mul(const float* g, const float* u, float* h, int64_t n, qmoe_stream_t stream) {
     if (n < 0 || (n > 0 && (!g || !u || !h))) return QMOE_ERR_INVALID_ARG;
     if (n == 0) return QMOE_OK;
-    debug_silu_kernel<<<grid_for(n, 256), 256, 0, stream>>>(g, u, h, n);
+    debug_silu_kernel<<<grid_for((n + 1) / 2, 256), 256, 0, stream>>>(g, u, h, n);
+    return launch_status();
+}
+
+qmoe_status_t qmoe_debug_div_by_scale(const float* x, float s, float* q, int64_t n, qmoe_stream_t stream) {
+    if (n < 0 || (n > 0 && (!x || !q))) return QMOE_ERR_INVALID_ARG;
+    if (n == 0) return QMOE_OK;
+    debug_div_kernel<<<grid_for((n + 1) / 2, 256), 256, 0, stream>>>(x, s, q, n);
     return launch_status();
 }
 

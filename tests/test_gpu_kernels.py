@@ -190,3 +190,24 @@ def test_fused_align_quant_bitexact(q, orc, M, K, E, top_k, BM):
     valid = np.nonzero(srt < M * top_k)[0]
     assert np.array_equal(qq.cpu().numpy()[valid], rq[srt[valid] // top_k])
     assert np.array_equal(ss.cpu().numpy()[valid], rs[srt[valid] // top_k])
+
+
+@pytest.mark.parametrize("s", [np.float32(1.0), np.float32(1.0 / 448.0), np.float32(3.0), np.float32(0.0123456),
+                               np.nextafter(np.float32(2.0), np.float32(0)), np.float32(7.0e-3) / np.float32(448.0)])
+def test_division_by_row_scale_exhaustive(q, s):
+    """The kernels' division by a row scale s equals IEEE fp32 division (numpy)
+    bit for bit for every fp32 dividend the kernels can pass, |x| <= 512 s
+    (they divide values bounded by amax = 448 s)."""
+    chunk = 1 << 26
+    sd = np.float32(s)
+    lim = np.float32(512.0) * sd
+    for c in range((1 << 32) // chunk):
+        bits = np.arange(chunk, dtype=np.uint32) + np.uint32(c * chunk)
+        x = bits.view(np.float32)
+        x = x[np.isfinite(x) & (np.abs(x) <= lim)]
+        if x.size == 0:
+            continue
+        got = q.debug_div_by_scale(to_dev(x), float(sd)).cpu().numpy()
+        ref = (x / sd).astype(np.float32)
+        bad = np.nonzero(got.view(np.uint32) != ref.view(np.uint32))[0]
+        assert bad.size == 0, (float(sd), x[bad[:4]], got[bad[:4]], ref[bad[:4]])
