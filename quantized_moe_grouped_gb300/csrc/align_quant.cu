@@ -404,13 +404,19 @@ __global__ void __launch_bounds__(kRowThreads)
 // MX: one CTA per row, one thread per 1x32 block (h in registers); the CTA
 // also zeroes its row's pad columns and a share of its expert's pad rows.
 // ======================================================================
-QMOE_DI void silu8(const uint16_t* g, const uint16_t* u, float (&h)[8]) {
+QMOE_DI void unpack8(const uint4 w, float (&v)[8]) {
+    v[0] = bf16_lo(w.x); v[1] = bf16_hi(w.x); v[2] = bf16_lo(w.y); v[3] = bf16_hi(w.y);
+    v[4] = bf16_lo(w.z); v[5] = bf16_hi(w.z); v[6] = bf16_lo(w.w); v[7] = bf16_hi(w.w);
+}
+// h for 8 elements from raw gate / up words (already loaded).
+QMOE_DI void silu8w(const uint4 gw, const uint4 uw, float (&h)[8]) {
     float gv[8], uv[8];
-    load8(g, gv);
-    load8(u, uv);
+    unpack8(gw, gv);
+    unpack8(uw, uv);
 #pragma unroll
     for (int i = 0; i < 8; i += 2) silu_mul2(gv[i], gv[i + 1], uv[i], uv[i + 1], h[i], h[i + 1]);
 }
+constexpr int kSiluBatch = 4;  // 8-element chunks whose loads are issued before any arithmetic
 
 __global__ void __launch_bounds__(kRowThreads)
     silu_quant_token_kernel(const uint16_t* __restrict__ y, int64_t I, int64_t ldy, uint8_t* __restrict__ q,
@@ -420,13 +426,27 @@ __global__ void __launch_bounds__(kRowThreads)
     const int64_t row = blockIdx.x;
     const uint16_t* yr = y + row * ldy;
     float amax = 0.0f;
-    for (int64_t c = static_cast<int64_t>(threadIdx.x) * 8; c < I; c += kRowThreads * 8) {
-        float h[8];
-        silu8(yr + c, yr + I + c, h);
+    for (int64_t c0 = static_cast<int64_t>(threadIdx.x) * 8; c0 < I; c0 += kRowThreads * 8 * kSiluBatch) {
+        uint4 gw[kSiluBatch], uw[kSiluBatch];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            s_h[c + i] = h[i];
-            amax = fmaxf(amax, fabsf(h[i]));
+        for (int j = 0; j < kSiluBatch; ++j) {
+            const int64_t c = c0 + static_cast<int64_t>(j) * kRowThreads * 8;
+            if (c < I) {
+                gw[j] = *reinterpret_cast<const uint4*>(yr + c);
+                uw[j] = *reinterpret_cast<const uint4*>(yr + I + c);
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < kSiluBatch; ++j) {
+            const int64_t c = c0 + static_cast<int64_t>(j) * kRowThreads * 8;
+            if (c < I) {
+                float h[8];
+                silu8w(gw[j], uw[j], h);
+                *reinterpret_cast<float4*>(s_h + c) = make_float4(h[0], h[1], h[2], h[3]);
+                *reinterpret_cast<float4*>(s_h + c + 4) = make_float4(h[4], h[5], h[6], h[7]);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(h[i]));
+            }
         }
     }
     amax = block_max(amax, red);  // (contains __syncthreads: s_h is complete)
@@ -476,10 +496,16 @@ __global__ void __launch_bounds__(kMxThreads)
     uint8_t* sfr = sf + srow * sf_ld;
     for (int64_t b = threadIdx.x; b < nblk; b += kMxThreads) {
         float h[32];
+        uint4 gw[4], uw[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            gw[c] = *reinterpret_cast<const uint4*>(yr + b * 32 + c * 8);
+            uw[c] = *reinterpret_cast<const uint4*>(yr + I + b * 32 + c * 8);
+        }
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
             float t[8];
-            silu8(yr + b * 32 + c * 8, yr + I + b * 32 + c * 8, t);
+            silu8w(gw[c], uw[c], t);
 #pragma unroll
             for (int i = 0; i < 8; ++i) h[c * 8 + i] = t[i];
         }
