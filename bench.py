@@ -14,7 +14,8 @@ value  = algorithmic bytes of the four GEMMs / device time of the timed steps
          + routing + bf16 output), in GB/s; the line also carries TFLOPS.
 e2e    = the same metric through the public API with pinned host buffers: per
          step the activations and routing go host -> device and the outputs
-         device -> host inside the timed region.
+         device -> host inside the timed region (copies on their own streams,
+         overlapping the kernels of other shapes).
 roofline = the grouped GEMM kernel alone (CUDA events around each launch).
 cpu_baseline / --impl reference = the CPU oracle on a bounded sample of slots.
 
@@ -489,18 +490,44 @@ def main() -> None:
     h2d = sum(sh["a_h"].numel() * 2 + sh["ids_h"].numel() * 4 + sh["tw_h"].numel() * 4 for sh in shapes)
     d2h = sum(sh["out_h"].numel() * 2 for sh in shapes)
     e2e_steps = max(3, min(args.steps, 200))
+    # Copies run on their own streams and overlap the kernels: a shape's inputs
+    # go host -> device once the previous step's kernels of that shape are done
+    # with them, its kernels wait for that copy and for the previous copy-out
+    # of its output buffer, and outputs go device -> host on two alternating
+    # streams (two copy engines).
+    h2d_stream = torch.cuda.Stream(dev)
+    d2h_streams = [torch.cuda.Stream(dev), torch.cuda.Stream(dev)]
+    ev_in = [torch.cuda.Event() for _ in shapes]
+    ev_gemm = [torch.cuda.Event() for _ in shapes]
+    ev_done = [torch.cuda.Event() for _ in shapes]
+    for i in range(n_sh):
+        ev_gemm[i].record(stream)
+        ev_done[i].record(d2h_streams[i % 2])
     barrier()
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
+    h2d_stream.wait_event(e0)
     for _ in range(e2e_steps):
-        for sh in shapes:
-            sh["a"].copy_(sh["a_h"], non_blocking=True)
-            sh["ids"].copy_(sh["ids_h"], non_blocking=True)
-            sh["tw"].copy_(sh["tw_h"], non_blocking=True)
+        for i, sh in enumerate(shapes):
+            h2d_stream.wait_event(ev_gemm[i])
+            with torch.cuda.stream(h2d_stream):
+                sh["a"].copy_(sh["a_h"], non_blocking=True)
+                sh["ids"].copy_(sh["ids_h"], non_blocking=True)
+                sh["tw"].copy_(sh["tw_h"], non_blocking=True)
+            ev_in[i].record(h2d_stream)
+            stream.wait_event(ev_in[i])
+            stream.wait_event(ev_done[i])
             run_path(q, wq, ws, sh, stream)
-            sh["out_h"].copy_(sh["out"], non_blocking=True)
+            ev_gemm[i].record(stream)
+            out_stream = d2h_streams[i % 2]
+            out_stream.wait_event(ev_gemm[i])
+            with torch.cuda.stream(out_stream):
+                sh["out_h"].copy_(sh["out"], non_blocking=True)
+            ev_done[i].record(out_stream)
+    for ev in ev_done:
+        stream.wait_event(ev)
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
