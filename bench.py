@@ -342,7 +342,7 @@ def run_suite(reps: int = 20, only: str | None = None) -> None:
         wq, ws = weights_int8(E, wl.N, wl.K)
         a = torch.from_numpy(inputs.activations_bf16(wl.M, wl.K, wl.seed).view(np.int16)).to(dev).view(torch.bfloat16)
         ids, tw = inputs.routing(wl.M, E, TOP_K, wl.seed)
-        BM = 32 if wl.M <= 64 else 128
+        BM = 128  # the wide tile: more weight bytes per bf16 MMA than the swapped one, also at decode
         al = q.moe_align_block_size(torch.from_numpy(ids).to(dev), E, BM)
         twd = torch.from_numpy(tw).to(dev)
         out = torch.empty(wl.M * TOP_K, wl.N, dtype=torch.bfloat16, device=dev)
