@@ -284,6 +284,11 @@ qmoe_status_t qmoe_debug_int8_to_bf16(const int8_t* x, uint16_t* y, int64_t n, q
 /* h = silu(g) * u through the kernels' fp32 sequence, n values. */
 qmoe_status_t qmoe_debug_silu_mul(const float* g, const float* u, float* h, int64_t n,
                                   qmoe_stream_t stream);
+/* Failure-detection check: one thread waits, through the bounded wait every
+ * GEMM pipeline wait uses, on an mbarrier nothing arrives at; after limit_ns
+ * (at most 1 s) it gives up and ORs QMOE_DEV_TIMEOUT into *d_status.  The
+ * kernel returns normally and the context stays usable. */
+qmoe_status_t qmoe_debug_wait_timeout(int32_t* d_status, int64_t limit_ns, qmoe_stream_t stream);
 /* q = x / s through the kernels' division by a row scale (correctly rounded,
  * like IEEE fp32 division), n values. */
 qmoe_status_t qmoe_debug_div_by_scale(const float* x, float s, float* q, int64_t n, qmoe_stream_t stream);

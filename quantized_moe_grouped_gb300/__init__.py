@@ -31,7 +31,8 @@ EXPORTED = (
     "qmoe_status_string", "qmoe_version", "qmoe_align_max_padded", "qmoe_moe_align_block_size",
     "qmoe_quant_act_fp8", "qmoe_quant_act_fp8_sorted", "qmoe_moe_align_quant_fp8", "qmoe_gather_sorted_bf16", "qmoe_quant_weight_fp8", "qmoe_quant_weight_int8", "qmoe_moe_gemm_w8a8",
     "qmoe_moe_gemm_w8a16", "qmoe_silu_mul_quant", "qmoe_debug_e4m3_encode", "qmoe_debug_int8_to_bf16",
-    "qmoe_debug_silu_mul", "qmoe_debug_div_by_scale", "qmoe_moe_gemm_w8a8_token_sum_noalloc",
+    "qmoe_debug_silu_mul", "qmoe_debug_div_by_scale", "qmoe_debug_wait_timeout",
+    "qmoe_moe_gemm_w8a8_token_sum_noalloc",
 )
 NOALLOC_ACCUM_MAX_ELEMS = 4 << 20
 
@@ -90,6 +91,7 @@ def load_library(path: str | None = None):
             L.qmoe_debug_int8_to_bf16.argtypes = [vp, vp, i64, vp]
             L.qmoe_debug_silu_mul.argtypes = [vp, vp, vp, i64, vp]
             L.qmoe_debug_div_by_scale.argtypes = [vp, ctypes.c_float, vp, i64, vp]
+            L.qmoe_debug_wait_timeout.argtypes = [vp, i64, vp]
             for name in EXPORTED:
                 if name not in ("qmoe_status_string", "qmoe_version", "qmoe_align_max_padded"):
                     getattr(L, name).restype = st
@@ -428,3 +430,9 @@ def debug_div_by_scale(x: torch.Tensor, s: float, stream=None) -> torch.Tensor:
     _check(load_library().qmoe_debug_div_by_scale(_ptr(x), float(s), _ptr(q), x.numel(), _stream(stream)),
            "debug_div_by_scale")
     return q
+
+
+def debug_wait_timeout(d_status: torch.Tensor, limit_ns: int, stream=None) -> None:
+    _need(d_status, torch.int32, "d_status")
+    _check(load_library().qmoe_debug_wait_timeout(_ptr(d_status), int(limit_ns), _stream(stream)),
+           "debug_wait_timeout")

@@ -572,6 +572,20 @@ __global__ void debug_div_kernel(const float* __restrict__ x, float s, float* __
     }
 }
 
+// One thread waits on an mbarrier that nothing arrives at, through the same
+// bounded wait the GEMM uses, with a short limit: it must give up, record
+// QMOE_DEV_TIMEOUT and return.
+__global__ void debug_wait_timeout_kernel(int32_t* d_status, uint64_t limit_ns) {
+    __shared__ uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        abort_flag = 0;
+        fence_mbar_init();
+        mbar_wait(&bar, 0, &abort_flag, d_status, limit_ns);
+    }
+}
+
 static int grid_for(int64_t n, int threads) {
     const int64_t b = (n + threads - 1) / threads;
     const int64_t cap = static_cast<int64_t>(device_sm_count() > 0 ? device_sm_count() : 132) * 16;
@@ -741,6 +755,12 @@ qmoe_status_t qmoe_debug_silu_mul(const float* g, const float* u, float* h, int6
     if (n < 0 || (n > 0 && (!g || !u || !h))) return QMOE_ERR_INVALID_ARG;
     if (n == 0) return QMOE_OK;
     debug_silu_kernel<<<grid_for((n + 1) / 2, 256), 256, 0, stream>>>(g, u, h, n);
+    return launch_status();
+}
+
+qmoe_status_t qmoe_debug_wait_timeout(int32_t* d_status, int64_t limit_ns, qmoe_stream_t stream) {
+    if (!d_status || limit_ns < 0 || limit_ns > 1000000000) return QMOE_ERR_INVALID_ARG;
+    debug_wait_timeout_kernel<<<1, 32, 0, stream>>>(d_status, static_cast<uint64_t>(limit_ns));
     return launch_status();
 }
 

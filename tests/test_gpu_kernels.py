@@ -211,3 +211,21 @@ def test_division_by_row_scale_exhaustive(q, s):
         ref = (x / sd).astype(np.float32)
         bad = np.nonzero(got.view(np.uint32) != ref.view(np.uint32))[0]
         assert bad.size == 0, (float(sd), x[bad[:4]], got[bad[:4]], ref[bad[:4]])
+
+
+def test_bounded_wait_reports_timeout_and_context_survives(q, orc):
+    """A wait on an mbarrier that nothing arrives at gives up after its limit,
+    records QMOE_DEV_TIMEOUT in d_status and returns; the context keeps
+    working (a quantisation launched afterwards is still bit-exact)."""
+    import time
+    st = status()
+    t0 = time.perf_counter()
+    q.debug_wait_timeout(st, 20_000_000)          # 20 ms
+    torch.cuda.synchronize()
+    dt = time.perf_counter() - t0
+    assert int(st.item()) == q.DEV_TIMEOUT
+    assert 0.015 < dt < 5.0
+    x = inputs.activations_bf16(8, 64, seed=1)
+    qa, sa = q.quant_act_fp8(to_dev_bf16(x))
+    rq, rs = orc.quant_rows_fp8_bf16(x)
+    assert np.array_equal(qa.cpu().numpy(), rq)
