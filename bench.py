@@ -358,6 +358,25 @@ def run_suite(reps: int = 20, only: str | None = None) -> None:
         line(wl.name, f"moe_gemm_w8a16 BM={BM} padded A", ms, nbytes, 2.0 * wl.M * TOP_K * wl.K * wl.N, "bf16")
         del wq, ws
 
+    # Fused activation + MXFP8 on the TransformerEngine GroupedLinear page's input
+    # (8 experts x 4000 rows, width 4096): SReLU on [32000, 4096]; SwiGLU on the
+    # same input read as gate|up, [32000, 2 x 2048].  Page: ~142 us (SReLU) and
+    # ~343 us (SwiGLU) fused, plus 75 / 84 us of scale-factor padding kernels,
+    # on unnamed hardware -- context only.
+    if not only or "activation" in only:
+        rows, width = 8 * 4000, 4096
+        y = (torch.randn(rows, width, device=dev)).to(torch.bfloat16)
+        eoff = torch.arange(0, rows + 1, 4000, dtype=torch.int32, device=dev)
+        soff = torch.arange(0, 8 * 4096 + 1, 4096, dtype=torch.int32, device=dev)
+        for name, fn, I in (("srelu_quant mxfp8 [32000, 4096]", q.srelu_quant, width),
+                            ("silu_mul_quant mxfp8 [32000, 2x2048]", q.silu_mul_quant, width // 2)):
+            hq, sf = fn(y, q.SCALE_MX_1X32, expert_offsets=eoff, sf_padded_offsets=soff, sf_rows=8 * 4096)
+            ms = _timed(lambda: fn(y, q.SCALE_MX_1X32, expert_offsets=eoff, sf_padded_offsets=soff, q=hq, sf=sf),
+                        reps, flush)
+            line("activation + MXFP8 8x4000x4096", name, ms, rows * width * 2 + rows * I + 8 * 4096 * (I // 32), 0,
+                 "fp8")
+        del y
+
     # FP8 layers
     for wl in (inputs.mixtral_8x7b_layer(), inputs.mixtral_8x22b_layer()):
         if only and only not in wl.name:

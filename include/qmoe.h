@@ -273,6 +273,17 @@ qmoe_status_t qmoe_silu_mul_quant(const uint16_t* y, int64_t rows, int64_t I, in
                                   const int32_t* sf_padded_offsets, int32_t E,
                                   int32_t* d_status, qmoe_stream_t stream);
 
+/* SReLU + requantisation, the second fused activation of "[PyTorch] Let
+ * GroupedLinear accept MXFP8 input and gradient" (Description: "SReLU + MXFP8
+ * Quantization"): y[rows, I] bf16 (not gated), h = relu(y)^2 in fp32 (exact
+ * for bf16 inputs), then the same per-token or MX 1x32 requantisation, scale
+ * layout and per-expert scale-factor padding as qmoe_silu_mul_quant.  Limits
+ * as there, with ldy >= I. */
+qmoe_status_t qmoe_srelu_quant(const uint16_t* y, int64_t rows, int64_t I, int64_t ldy, int32_t mode, uint8_t* q,
+                               float* scale, uint8_t* sf, int64_t sf_ld, const int32_t* expert_offsets,
+                               const int32_t* sf_padded_offsets, int32_t E, int32_t* d_status,
+                               qmoe_stream_t stream);
+
 /* ------------------------------------------------------------------------ */
 /* element-level hooks used by the exhaustive tests                         */
 /* ------------------------------------------------------------------------ */

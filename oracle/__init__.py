@@ -87,6 +87,10 @@ def lib():
             L.orc_quant_rows_int8_f32.argtypes = [vp, i64, i64, i64, vp, vp]
             L.orc_silu_mul_quant_token.argtypes = [vp, i64, i64, i64, vp, vp]
             L.orc_silu_mul_quant_mx.argtypes = [vp, i64, i64, i64, vp, vp, i32, vp, vp, i64]
+            L.orc_srelu_quant_token.argtypes = [vp, i64, i64, i64, vp, vp]
+            L.orc_srelu_quant_mx.argtypes = [vp, i64, i64, i64, vp, vp, i32, vp, vp, i64]
+            L.orc_srelu_f32.argtypes = [ctypes.c_float]
+            L.orc_srelu_f32.restype = ctypes.c_float
             L.orc_e4m3_from_f32_array.argtypes = [vp, i64, vp]
             L.orc_exp_f32_array.argtypes = [vp, i64, vp]
             L.orc_silu_mul_f32_array.argtypes = [vp, vp, i64, vp]
@@ -249,6 +253,33 @@ def silu_mul_quant_mx(y_bits: np.ndarray, expert_offsets: np.ndarray, sf_padded_
     q = np.zeros((R, I), dtype=np.uint8)
     sf = np.zeros((int(soff[E]), ld), dtype=np.uint8)
     lib().orc_silu_mul_quant_mx(_p(y), R, I, C2, _p(eoff), _p(soff), E, _p(q), _p(sf), ld)
+    return q, sf
+
+
+def srelu_f32(x) -> np.ndarray:
+    f = lib().orc_srelu_f32
+    return np.array([f(float(v)) for v in np.asarray(x, dtype=np.float32).ravel()], dtype=np.float32)
+
+
+def srelu_quant_token(y_bits: np.ndarray):
+    y = np.ascontiguousarray(y_bits, dtype=np.uint16)
+    R, I = y.shape
+    q = np.empty((R, I), dtype=np.uint8)
+    s = np.empty(R, dtype=np.float32)
+    lib().orc_srelu_quant_token(_p(y), R, I, I, _p(q), _p(s))
+    return q, s
+
+
+def srelu_quant_mx(y_bits: np.ndarray, expert_offsets: np.ndarray, sf_padded_offsets: np.ndarray):
+    y = np.ascontiguousarray(y_bits, dtype=np.uint16)
+    R, I = y.shape
+    E = len(expert_offsets) - 1
+    eoff = np.ascontiguousarray(expert_offsets, dtype=np.int32)
+    soff = np.ascontiguousarray(sf_padded_offsets, dtype=np.int32)
+    ld = mx_sf_ld(I)
+    q = np.zeros((R, I), dtype=np.uint8)
+    sf = np.zeros((int(soff[E]), ld), dtype=np.uint8)
+    lib().orc_srelu_quant_mx(_p(y), R, I, I, _p(eoff), _p(soff), E, _p(q), _p(sf), ld)
     return q, sf
 
 

@@ -282,22 +282,38 @@ float orc_silu_mul_f32(float g, float u) {
     return gs * u;
 }
 
-/* h for one row of a fused gate|up matrix y[R, 2I] (gate = first I columns). */
-static void swiglu_row(const uint16_t* yr, int64_t I, float* h) {
+/* Squared ReLU (the SReLU of "[PyTorch] Let GroupedLinear accept MXFP8 input
+ * and gradient", Description): relu(x)^2 = x*x for x > 0, else 0.  For a bf16
+ * x the fp32 product is exact. */
+float orc_srelu_f32(float x) { return (x > 0.0f) ? x * x : 0.0f; }
+
+/* h for one row.  act 0: SwiGLU of a fused gate|up row y[2I] (gate = first I
+ * columns); act 1: SReLU of a plain row y[I]. */
+static void act_row(int act, const uint16_t* yr, int64_t I, float* h) {
     for (int64_t i = 0; i < I; ++i)
-        h[i] = orc_silu_mul_f32(orc_bf16_to_f32(yr[i]), orc_bf16_to_f32(yr[I + i]));
+        h[i] = (act == 0) ? orc_silu_mul_f32(orc_bf16_to_f32(yr[i]), orc_bf16_to_f32(yr[I + i]))
+                          : orc_srelu_f32(orc_bf16_to_f32(yr[i]));
 }
 
-/* silu_mul_quant, per-token mode: h -> row amax -> scale -> e4m3(h/scale). */
-void orc_silu_mul_quant_token(const uint16_t* y, int64_t R, int64_t I, int64_t ldy,
-                              uint8_t* q, float* scale) {
+/* activation + per-token requantisation: h -> row amax -> scale -> e4m3(h/scale). */
+static void act_quant_token(int act, const uint16_t* y, int64_t R, int64_t I, int64_t ldy,
+                            uint8_t* q, float* scale) {
 #pragma omp parallel for schedule(dynamic, 16)
     for (int64_t r = 0; r < R; ++r) {
         float* h = (float*)malloc((size_t)I * sizeof(float));
-        swiglu_row(y + r * ldy, I, h);
+        act_row(act, y + r * ldy, I, h);
         quant_row_fp8(h, I, q + r * I, scale + r);
         free(h);
     }
+}
+
+void orc_silu_mul_quant_token(const uint16_t* y, int64_t R, int64_t I, int64_t ldy,
+                              uint8_t* q, float* scale) {
+    act_quant_token(0, y, R, I, ldy, q, scale);
+}
+
+void orc_srelu_quant_token(const uint16_t* y, int64_t R, int64_t I, int64_t ldy, uint8_t* q, float* scale) {
+    act_quant_token(1, y, R, I, ldy, q, scale);
 }
 
 /* silu_mul_quant, MX mode: for each 1x32 block of h along the row, exponent
@@ -308,9 +324,9 @@ void orc_silu_mul_quant_token(const uint16_t* y, int64_t R, int64_t I, int64_t l
  * sf_padded_offsets[e] + (r - expert_offsets[e]); every other byte (pad rows
  * of each expert, pad columns past I/32) is 0.  sf must hold
  * sf_padded_offsets[E] * sf_ld bytes. */
-void orc_silu_mul_quant_mx(const uint16_t* y, int64_t R, int64_t I, int64_t ldy,
-                           const int32_t* expert_offsets, const int32_t* sf_padded_offsets, int32_t E,
-                           uint8_t* q, uint8_t* sf, int64_t sf_ld) {
+static void act_quant_mx(int act, const uint16_t* y, int64_t R, int64_t I, int64_t ldy,
+                         const int32_t* expert_offsets, const int32_t* sf_padded_offsets, int32_t E,
+                         uint8_t* q, uint8_t* sf, int64_t sf_ld) {
     memset(sf, 0, (size_t)sf_padded_offsets[E] * (size_t)sf_ld);
     int64_t nblk = I / 32;
 #pragma omp parallel for schedule(dynamic, 16)
@@ -320,7 +336,7 @@ void orc_silu_mul_quant_mx(const uint16_t* y, int64_t R, int64_t I, int64_t ldy,
         if (e >= E) continue;                          /* row not owned by any expert */
         int64_t srow = (int64_t)sf_padded_offsets[e] + (r - expert_offsets[e]);
         float* h = (float*)malloc((size_t)I * sizeof(float));
-        swiglu_row(y + r * ldy, I, h);
+        act_row(act, y + r * ldy, I, h);
         for (int64_t b = 0; b < nblk; ++b) {
             float amax = 0.0f;
             for (int64_t k = 0; k < 32; ++k) {
@@ -334,6 +350,18 @@ void orc_silu_mul_quant_mx(const uint16_t* y, int64_t R, int64_t I, int64_t ldy,
         }
         free(h);
     }
+}
+
+void orc_silu_mul_quant_mx(const uint16_t* y, int64_t R, int64_t I, int64_t ldy,
+                           const int32_t* expert_offsets, const int32_t* sf_padded_offsets, int32_t E,
+                           uint8_t* q, uint8_t* sf, int64_t sf_ld) {
+    act_quant_mx(0, y, R, I, ldy, expert_offsets, sf_padded_offsets, E, q, sf, sf_ld);
+}
+
+void orc_srelu_quant_mx(const uint16_t* y, int64_t R, int64_t I, int64_t ldy,
+                        const int32_t* expert_offsets, const int32_t* sf_padded_offsets, int32_t E,
+                        uint8_t* q, uint8_t* sf, int64_t sf_ld) {
+    act_quant_mx(1, y, R, I, ldy, expert_offsets, sf_padded_offsets, E, q, sf, sf_ld);
 }
 
 /* ------------------------------------------------------------------------- */

@@ -30,7 +30,7 @@ OUT_SLOT, OUT_GROUPED, OUT_TOKEN_SUM = 0, 1, 2
 EXPORTED = (
     "qmoe_status_string", "qmoe_version", "qmoe_align_max_padded", "qmoe_moe_align_block_size",
     "qmoe_quant_act_fp8", "qmoe_quant_act_fp8_sorted", "qmoe_moe_align_quant_fp8", "qmoe_gather_sorted_bf16", "qmoe_quant_weight_fp8", "qmoe_quant_weight_int8", "qmoe_moe_gemm_w8a8",
-    "qmoe_moe_gemm_w8a16", "qmoe_silu_mul_quant", "qmoe_debug_e4m3_encode", "qmoe_debug_int8_to_bf16",
+    "qmoe_moe_gemm_w8a16", "qmoe_silu_mul_quant", "qmoe_srelu_quant", "qmoe_debug_e4m3_encode", "qmoe_debug_int8_to_bf16",
     "qmoe_debug_silu_mul", "qmoe_debug_div_by_scale", "qmoe_debug_wait_timeout",
     "qmoe_moe_gemm_w8a8_token_sum_noalloc",
 )
@@ -87,6 +87,7 @@ def load_library(path: str | None = None):
             L.qmoe_moe_gemm_w8a16.argtypes = [ctypes.POINTER(GemmArgs), vp]
             L.qmoe_moe_gemm_w8a8_token_sum_noalloc.argtypes = [ctypes.POINTER(GemmArgs), vp]
             L.qmoe_silu_mul_quant.argtypes = [vp, i64, i64, i64, i32, vp, vp, vp, i64, vp, vp, i32, vp, vp]
+            L.qmoe_srelu_quant.argtypes = [vp, i64, i64, i64, i32, vp, vp, vp, i64, vp, vp, i32, vp, vp]
             L.qmoe_debug_e4m3_encode.argtypes = [vp, vp, i64, vp]
             L.qmoe_debug_int8_to_bf16.argtypes = [vp, vp, i64, vp]
             L.qmoe_debug_silu_mul.argtypes = [vp, vp, vp, i64, vp]
@@ -368,22 +369,34 @@ def mx_sf_ld(I: int) -> int:
     return (I // 32 + 3) // 4 * 4
 
 
+def srelu_quant(y: torch.Tensor, mode: int = SCALE_PER_TOKEN, *, expert_offsets=None, sf_padded_offsets=None,
+                sf_rows: int | None = None, q=None, scale=None, sf=None, d_status=None, stream=None):
+    """y bf16 [rows, I] -> relu(y)^2 requantised like silu_mul_quant (per-token or MX)."""
+    return _act_quant("qmoe_srelu_quant", False, y, mode, expert_offsets, sf_padded_offsets, sf_rows, q, scale, sf,
+                      d_status, stream)
+
+
 def silu_mul_quant(y: torch.Tensor, mode: int = SCALE_PER_TOKEN, *, expert_offsets=None, sf_padded_offsets=None,
                    sf_rows: int | None = None, q=None, scale=None, sf=None, d_status=None, stream=None):
     """y bf16 [rows, 2I] (gate | up) -> per-token: (q [rows, I] uint8, scale [rows] fp32);
     MX: (q, sf [sf_rows, roundup(I/32, 4)] uint8).  For MX, sf_rows must be at
     least sf_padded_offsets[E] (e.g. align_max_padded(T, E, 128))."""
+    return _act_quant("qmoe_silu_mul_quant", True, y, mode, expert_offsets, sf_padded_offsets, sf_rows, q, scale, sf,
+                      d_status, stream)
+
+
+def _act_quant(fn_name, gated, y, mode, expert_offsets, sf_padded_offsets, sf_rows, q, scale, sf, d_status, stream):
     if not y.is_cuda or y.dtype != torch.bfloat16 or y.dim() != 2 or y.stride(1) != 1:
         raise QmoeError("y must be a 2-D CUDA bf16 tensor with unit column stride")
-    rows, two_i = y.shape
-    I = two_i // 2
+    rows, width = y.shape
+    I = width // 2 if gated else width
     q = q if q is not None else torch.empty(rows, I, dtype=torch.uint8, device=y.device)
-    L = load_library()
+    fn = getattr(load_library(), fn_name)
     if mode == SCALE_PER_TOKEN:
         scale = scale if scale is not None else torch.empty(rows, dtype=torch.float32, device=y.device)
-        st = L.qmoe_silu_mul_quant(_ptr(y), rows, I, y.stride(0), mode, _ptr(q), _ptr(scale), None, 0, None, None,
-                                   1, _ptr(d_status), _stream(stream))
-        _check(st, "silu_mul_quant")
+        st = fn(_ptr(y), rows, I, y.stride(0), mode, _ptr(q), _ptr(scale), None, 0, None, None, 1, _ptr(d_status),
+                _stream(stream))
+        _check(st, fn_name)
         return q, scale
     _need(expert_offsets, torch.int32, "expert_offsets")
     _need(sf_padded_offsets, torch.int32, "sf_padded_offsets")
@@ -393,9 +406,9 @@ def silu_mul_quant(y: torch.Tensor, mode: int = SCALE_PER_TOKEN, *, expert_offse
         if sf_rows is None:
             raise QmoeError("sf_rows (capacity of the scale-factor matrix) is required when sf is not given")
         sf = torch.empty(sf_rows, ld, dtype=torch.uint8, device=y.device)
-    st = L.qmoe_silu_mul_quant(_ptr(y), rows, I, y.stride(0), mode, _ptr(q), None, _ptr(sf), sf.stride(0),
-                               _ptr(expert_offsets), _ptr(sf_padded_offsets), E, _ptr(d_status), _stream(stream))
-    _check(st, "silu_mul_quant")
+    st = fn(_ptr(y), rows, I, y.stride(0), mode, _ptr(q), None, _ptr(sf), sf.stride(0), _ptr(expert_offsets),
+            _ptr(sf_padded_offsets), E, _ptr(d_status), _stream(stream))
+    _check(st, fn_name)
     return q, sf
 
 

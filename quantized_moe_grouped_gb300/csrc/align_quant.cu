@@ -418,9 +418,27 @@ QMOE_DI void silu8w(const uint4 gw, const uint4 uw, float (&h)[8]) {
 }
 constexpr int kSiluBatch = 4;  // 8-element chunks whose loads are issued before any arithmetic
 
+// Activations of the requantisation kernels.  Gated: h = silu(gate) * up from
+// a fused gate|up row; not gated: h = relu(x)^2 (SReLU; the fp32 square of a
+// bf16 value is exact).
+struct ActSwiGLU {
+    static constexpr bool kGated = true;
+    QMOE_DI static void apply8(const uint4 gw, const uint4 uw, float (&h)[8]) { silu8w(gw, uw, h); }
+};
+struct ActSReLU {
+    static constexpr bool kGated = false;
+    QMOE_DI static void apply8(const uint4 xw, const uint4, float (&h)[8]) {
+        float v[8];
+        unpack8(xw, v);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) h[i] = (v[i] > 0.0f) ? __fmul_rn(v[i], v[i]) : 0.0f;
+    }
+};
+
+template <class Act>
 __global__ void __launch_bounds__(kRowThreads)
-    silu_quant_token_kernel(const uint16_t* __restrict__ y, int64_t I, int64_t ldy, uint8_t* __restrict__ q,
-                            float* __restrict__ scale) {
+    act_quant_token_kernel(const uint16_t* __restrict__ y, int64_t I, int64_t ldy, uint8_t* __restrict__ q,
+                           float* __restrict__ scale) {
     extern __shared__ float s_h[];
     __shared__ float red[33];
     const int64_t row = blockIdx.x;
@@ -433,7 +451,7 @@ __global__ void __launch_bounds__(kRowThreads)
             const int64_t c = c0 + static_cast<int64_t>(j) * kRowThreads * 8;
             if (c < I) {
                 gw[j] = *reinterpret_cast<const uint4*>(yr + c);
-                uw[j] = *reinterpret_cast<const uint4*>(yr + I + c);
+                uw[j] = Act::kGated ? *reinterpret_cast<const uint4*>(yr + I + c) : make_uint4(0u, 0u, 0u, 0u);
             }
         }
 #pragma unroll
@@ -441,7 +459,7 @@ __global__ void __launch_bounds__(kRowThreads)
             const int64_t c = c0 + static_cast<int64_t>(j) * kRowThreads * 8;
             if (c < I) {
                 float h[8];
-                silu8w(gw[j], uw[j], h);
+                Act::apply8(gw[j], uw[j], h);
                 *reinterpret_cast<float4*>(s_h + c) = make_float4(h[0], h[1], h[2], h[3]);
                 *reinterpret_cast<float4*>(s_h + c + 4) = make_float4(h[4], h[5], h[6], h[7]);
 #pragma unroll
@@ -464,76 +482,69 @@ __global__ void __launch_bounds__(kRowThreads)
 
 constexpr int kMxThreads = 256;
 
+// One thread per (row, 1x32 block) item over a flat grid, so short rows keep
+// every thread busy.  The thread with b == 0 of a row also zeroes the row's pad
+// columns and its share of the expert's pad rows.
+template <class Act>
 __global__ void __launch_bounds__(kMxThreads)
-    silu_quant_mx_kernel(const uint16_t* __restrict__ y, int64_t rows, int64_t I, int64_t ldy,
-                         uint8_t* __restrict__ q, uint8_t* __restrict__ sf, int64_t sf_ld,
-                         const int32_t* __restrict__ eoff, const int32_t* __restrict__ soff, int E,
-                         int32_t* d_status) {
-    __shared__ int s_e;
-    const int64_t r = blockIdx.x;
-    if (threadIdx.x == 0) {
-        int lo = 0, hi = E - 1, found = -1;  // last e with eoff[e] <= r, if r < eoff[e+1]
-        if (r < eoff[E]) {
-            while (lo < hi) {
-                const int mid = (lo + hi + 1) >> 1;
-                if (eoff[mid] <= r) lo = mid;
-                else hi = mid - 1;
-            }
-            found = lo;
-        }
-        s_e = found;
+    act_quant_mx_kernel(const uint16_t* __restrict__ y, int64_t rows, int64_t I, int64_t ldy,
+                        uint8_t* __restrict__ q, uint8_t* __restrict__ sf, int64_t sf_ld,
+                        const int32_t* __restrict__ eoff, const int32_t* __restrict__ soff, int E,
+                        int32_t* d_status) {
+    const int64_t nblk = I / 32;
+    const int64_t g = blockIdx.x * static_cast<int64_t>(kMxThreads) + threadIdx.x;
+    if (g >= rows * nblk) return;
+    const int64_t r = g / nblk;
+    const int64_t b = g - r * nblk;
+    if (r >= eoff[E]) return;  // row past the last expert's rows
+    int lo = 0, hi = E - 1;    // last e with eoff[e] <= r
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (eoff[mid] <= r) lo = mid;
+        else hi = mid - 1;
     }
-    __syncthreads();
-    const int e = s_e;
-    if (e < 0) return;  // row past the last expert's rows
+    const int e = lo;
     const int64_t local = r - eoff[e];
     const int64_t cnt = eoff[e + 1] - eoff[e];
     const int64_t srow = soff[e] + local;
-    const int64_t prow_end = soff[e + 1];
-    const int64_t nblk = I / 32;
     const uint16_t* yr = y + r * ldy;
     uint8_t* qr = q + r * I;
     uint8_t* sfr = sf + srow * sf_ld;
-    for (int64_t b = threadIdx.x; b < nblk; b += kMxThreads) {
-        float h[32];
-        uint4 gw[4], uw[4];
+    float h[32];
+    uint4 gw[4], uw[4];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            gw[c] = *reinterpret_cast<const uint4*>(yr + b * 32 + c * 8);
-            uw[c] = *reinterpret_cast<const uint4*>(yr + I + b * 32 + c * 8);
-        }
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            float t[8];
-            silu8w(gw[c], uw[c], t);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) h[c * 8 + i] = t[i];
-        }
-        float a = 0.0f;
-#pragma unroll
-        for (int i = 0; i < 32; ++i) a = fmaxf(a, fabsf(h[i]));
-        const int ex = mx_block_exponent(a);
-        const float mul = pow2_neg(ex);
-        sfr[b] = static_cast<uint8_t>(ex + 127);
-        uint4 o0, o1;
-        o0.x = e4m3x4(__fmul_rn(h[0], mul), __fmul_rn(h[1], mul), __fmul_rn(h[2], mul), __fmul_rn(h[3], mul));
-        o0.y = e4m3x4(__fmul_rn(h[4], mul), __fmul_rn(h[5], mul), __fmul_rn(h[6], mul), __fmul_rn(h[7], mul));
-        o0.z = e4m3x4(__fmul_rn(h[8], mul), __fmul_rn(h[9], mul), __fmul_rn(h[10], mul), __fmul_rn(h[11], mul));
-        o0.w = e4m3x4(__fmul_rn(h[12], mul), __fmul_rn(h[13], mul), __fmul_rn(h[14], mul), __fmul_rn(h[15], mul));
-        o1.x = e4m3x4(__fmul_rn(h[16], mul), __fmul_rn(h[17], mul), __fmul_rn(h[18], mul), __fmul_rn(h[19], mul));
-        o1.y = e4m3x4(__fmul_rn(h[20], mul), __fmul_rn(h[21], mul), __fmul_rn(h[22], mul), __fmul_rn(h[23], mul));
-        o1.z = e4m3x4(__fmul_rn(h[24], mul), __fmul_rn(h[25], mul), __fmul_rn(h[26], mul), __fmul_rn(h[27], mul));
-        o1.w = e4m3x4(__fmul_rn(h[28], mul), __fmul_rn(h[29], mul), __fmul_rn(h[30], mul), __fmul_rn(h[31], mul));
-        *reinterpret_cast<uint4*>(qr + b * 32) = o0;
-        *reinterpret_cast<uint4*>(qr + b * 32 + 16) = o1;
+    for (int c = 0; c < 4; ++c) {
+        gw[c] = *reinterpret_cast<const uint4*>(yr + b * 32 + c * 8);
+        uw[c] = Act::kGated ? *reinterpret_cast<const uint4*>(yr + I + b * 32 + c * 8) : make_uint4(0u, 0u, 0u, 0u);
     }
-    for (int64_t b = nblk + threadIdx.x; b < sf_ld; b += kMxThreads) sfr[b] = 0;  // pad columns
-    // pad rows of expert e: rows soff[e]+cnt .. prow_end-1, shared out over the expert's rows
-    for (int64_t pr = soff[e] + cnt + local; pr < prow_end; pr += cnt) {
-        uint8_t* pp = sf + pr * sf_ld;
-        for (int64_t b = threadIdx.x; b < sf_ld; b += kMxThreads) pp[b] = 0;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        float t[8];
+        Act::apply8(gw[c], uw[c], t);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) h[c * 8 + i] = t[i];
     }
-    (void)rows;
+    float a = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) a = fmaxf(a, fabsf(h[i]));
+    const int ex = mx_block_exponent(a);
+    const float mul = pow2_neg(ex);
+    sfr[b] = static_cast<uint8_t>(ex + 127);
+    uint32_t o[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        o[i] = e4m3x4(__fmul_rn(h[4 * i], mul), __fmul_rn(h[4 * i + 1], mul), __fmul_rn(h[4 * i + 2], mul),
+                      __fmul_rn(h[4 * i + 3], mul));
+    *reinterpret_cast<uint4*>(qr + b * 32) = make_uint4(o[0], o[1], o[2], o[3]);
+    *reinterpret_cast<uint4*>(qr + b * 32 + 16) = make_uint4(o[4], o[5], o[6], o[7]);
+    if (b == 0) {
+        for (int64_t c = nblk; c < sf_ld; ++c) sfr[c] = 0;  // pad columns
+        // pad rows of expert e (soff[e]+cnt .. soff[e+1]-1), shared out over the expert's rows
+        for (int64_t pr = soff[e] + cnt + local; pr < soff[e + 1]; pr += cnt) {
+            uint8_t* pp = sf + pr * sf_ld;
+            for (int64_t c = 0; c < sf_ld; ++c) pp[c] = 0;
+        }
+    }
     (void)d_status;
 }
 
@@ -590,6 +601,40 @@ static int grid_for(int64_t n, int threads) {
     const int64_t b = (n + threads - 1) / threads;
     const int64_t cap = static_cast<int64_t>(device_sm_count() > 0 ? device_sm_count() : 132) * 16;
     return static_cast<int>(b < cap ? (b > 0 ? b : 1) : cap);
+}
+
+template <class Act>
+static qmoe_status_t run_act_quant(const uint16_t* y, int64_t rows, int64_t I, int64_t ldy, int32_t mode,
+                                   uint8_t* q, float* scale, uint8_t* sf, int64_t sf_ld,
+                                   const int32_t* expert_offsets, const int32_t* sf_padded_offsets, int32_t E,
+                                   int32_t* d_status, qmoe_stream_t stream) {
+    const int64_t width = Act::kGated ? 2 * I : I;
+    if (rows < 0 || I < 8 || I % 8 != 0 || ldy < width || ldy % 8 != 0) return QMOE_ERR_INVALID_ARG;
+    if (rows == 0) return QMOE_OK;
+    if (!y || !q || !aligned16(y) || !aligned16(q) || rows > 0x7FFFFFFF) return QMOE_ERR_INVALID_ARG;
+    if (mode == QMOE_SCALE_PER_TOKEN) {
+        if (!scale) return QMOE_ERR_INVALID_ARG;
+        const size_t smem = static_cast<size_t>(I) * sizeof(float);
+        if (smem > 200 * 1024) return QMOE_ERR_UNSUPPORTED;
+        if (smem > 48 * 1024) {
+            if (cudaFuncSetAttribute(act_quant_token_kernel<Act>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     static_cast<int>(smem)) != cudaSuccess)
+                return QMOE_ERR_CUDA;
+        }
+        act_quant_token_kernel<Act><<<static_cast<unsigned>(rows), kRowThreads, smem, stream>>>(y, I, ldy, q, scale);
+        return launch_status();
+    }
+    if (mode == QMOE_SCALE_MX_1X32) {
+        if (I % 32 != 0 || !sf || sf_ld < I / 32 || !expert_offsets || !sf_padded_offsets || E < 1 || E > 256)
+            return QMOE_ERR_INVALID_ARG;
+        const int64_t items = rows * (I / 32);
+        const int64_t blocks = (items + kMxThreads - 1) / kMxThreads;
+        if (blocks > 0x7FFFFFFF) return QMOE_ERR_UNSUPPORTED;
+        act_quant_mx_kernel<Act><<<static_cast<unsigned>(blocks), kMxThreads, 0, stream>>>(
+            y, rows, I, ldy, q, sf, sf_ld, expert_offsets, sf_padded_offsets, E, d_status);
+        return launch_status();
+    }
+    return QMOE_ERR_INVALID_ARG;
 }
 
 }  // namespace qmoe
@@ -710,29 +755,16 @@ qmoe_status_t qmoe_silu_mul_quant(const uint16_t* y, int64_t rows, int64_t I, in
                                   uint8_t* q, float* scale, uint8_t* sf, int64_t sf_ld,
                                   const int32_t* expert_offsets, const int32_t* sf_padded_offsets, int32_t E,
                                   int32_t* d_status, qmoe_stream_t stream) {
-    if (rows < 0 || I < 8 || I % 8 != 0 || ldy < 2 * I || ldy % 8 != 0) return QMOE_ERR_INVALID_ARG;
-    if (rows == 0) return QMOE_OK;
-    if (!y || !q || !aligned16(y) || !aligned16(q) || rows > 0x7FFFFFFF) return QMOE_ERR_INVALID_ARG;
-    if (mode == QMOE_SCALE_PER_TOKEN) {
-        if (!scale) return QMOE_ERR_INVALID_ARG;
-        const size_t smem = static_cast<size_t>(I) * sizeof(float);
-        if (smem > 200 * 1024) return QMOE_ERR_UNSUPPORTED;
-        if (smem > 48 * 1024) {
-            if (cudaFuncSetAttribute(silu_quant_token_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     static_cast<int>(smem)) != cudaSuccess)
-                return QMOE_ERR_CUDA;
-        }
-        silu_quant_token_kernel<<<static_cast<unsigned>(rows), kRowThreads, smem, stream>>>(y, I, ldy, q, scale);
-        return launch_status();
-    }
-    if (mode == QMOE_SCALE_MX_1X32) {
-        if (I % 32 != 0 || !sf || sf_ld < I / 32 || !expert_offsets || !sf_padded_offsets || E < 1 || E > 256)
-            return QMOE_ERR_INVALID_ARG;
-        silu_quant_mx_kernel<<<static_cast<unsigned>(rows), kMxThreads, 0, stream>>>(
-            y, rows, I, ldy, q, sf, sf_ld, expert_offsets, sf_padded_offsets, E, d_status);
-        return launch_status();
-    }
-    return QMOE_ERR_INVALID_ARG;
+    return run_act_quant<ActSwiGLU>(y, rows, I, ldy, mode, q, scale, sf, sf_ld, expert_offsets, sf_padded_offsets,
+                                    E, d_status, stream);
+}
+
+qmoe_status_t qmoe_srelu_quant(const uint16_t* y, int64_t rows, int64_t I, int64_t ldy, int32_t mode, uint8_t* q,
+                               float* scale, uint8_t* sf, int64_t sf_ld, const int32_t* expert_offsets,
+                               const int32_t* sf_padded_offsets, int32_t E, int32_t* d_status,
+                               qmoe_stream_t stream) {
+    return run_act_quant<ActSReLU>(y, rows, I, ldy, mode, q, scale, sf, sf_ld, expert_offsets, sf_padded_offsets,
+                                   E, d_status, stream);
 }
 
 qmoe_status_t qmoe_debug_e4m3_encode(const float* x, uint8_t* q, int64_t n, qmoe_stream_t stream) {

@@ -229,3 +229,28 @@ def test_bounded_wait_reports_timeout_and_context_survives(q, orc):
     qa, sa = q.quant_act_fp8(to_dev_bf16(x))
     rq, rs = orc.quant_rows_fp8_bf16(x)
     assert np.array_equal(qa.cpu().numpy(), rq)
+
+
+@pytest.mark.parametrize("R,I", [(64, 256), (300, 1024), (3, 40), (8, 16384)])
+def test_srelu_quant_token_bitexact(q, orc, R, I):
+    y = inputs.activations_bf16(R, I, seed=R + I + 5)
+    y[0, :] = 0
+    qq, ss = q.srelu_quant(to_dev_bf16(y))
+    rq, rs = orc.srelu_quant_token(y)
+    assert np.array_equal(qq.cpu().numpy(), rq)
+    assert np.array_equal(ss.cpu().numpy().view(np.uint32), rs.view(np.uint32))
+
+
+@pytest.mark.parametrize("cnt,I", [([64, 64], 128), ([5, 0, 130, 1, 300, 0, 7, 9], 96), ([4000, 4000], 256)])
+def test_srelu_quant_mx_bitexact(q, orc, cnt, I):
+    R = sum(cnt)
+    y = inputs.activations_bf16(R, I, seed=R + I + 6)
+    eoff = np.array([0] + list(np.cumsum(cnt)), dtype=np.int32)
+    soff = np.array([0] + list(np.cumsum([-(-c // 128) * 128 for c in cnt])), dtype=np.int32)
+    ld = q.mx_sf_ld(I)
+    sf = torch.full((int(soff[-1]), ld), 0xAB, dtype=torch.uint8, device=dev())
+    qq, sfo = q.srelu_quant(to_dev_bf16(y), q.SCALE_MX_1X32, expert_offsets=to_dev(eoff),
+                            sf_padded_offsets=to_dev(soff), sf=sf)
+    rq, rsf = orc.srelu_quant_mx(y, eoff, soff)
+    assert np.array_equal(qq.cpu().numpy(), rq)
+    assert np.array_equal(sfo.cpu().numpy(), rsf)

@@ -154,3 +154,36 @@ def test_silu_quant_mx_ragged_experts_and_pad_columns(orc):
         blk = sf[soff[e]:soff[e + 1]]
         assert np.array_equal(blk[: cnt[e], :3], sfr[eoff[e]:eoff[e + 1]])
         assert np.all(blk[cnt[e]:] == 0)
+
+
+def test_srelu_exact_square(orc):
+    x = inputs.f32_to_bf16_bits(np.concatenate([np.random.default_rng(4).standard_normal(2000) * 30,
+                                               [0.0, -0.0, 1e-30, -1e-30, 3e38]]).astype(np.float32))
+    xf = inputs.bf16_bits_to_f32(x)
+    h = orc.srelu_f32(xf)
+    with np.errstate(over="ignore"):
+        ref = np.where(xf > 0, xf.astype(np.float64) ** 2, 0.0).astype(np.float32)   # exact, or overflow to inf
+    assert np.array_equal(h, ref)
+    assert np.all(h[xf <= 0] == 0) and not np.any(np.signbit(h))
+
+
+def test_srelu_quant_token_and_mx(orc):
+    y = inputs.activations_bf16(10, 96, seed=31)
+    yf = inputs.bf16_bits_to_f32(y)
+    h = np.where(yf > 0, yf * yf, np.float32(0)).astype(np.float32)
+    q, s = orc.srelu_quant_token(y)
+    assert np.array_equal(s, (np.abs(h).max(axis=1) / np.float32(448)).astype(np.float32))
+    ref = torch.from_numpy((h / s[:, None]).astype(np.float32)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(q, ref)
+    cnt = [3, 0, 7]
+    y2 = inputs.activations_bf16(sum(cnt), 64, seed=32)
+    eoff = np.array([0] + list(np.cumsum(cnt)), np.int32)
+    soff = np.array([0] + list(np.cumsum([-(-c // 128) * 128 for c in cnt])), np.int32)
+    q2, sf2 = orc.srelu_quant_mx(y2, eoff, soff)
+    y2f = inputs.bf16_bits_to_f32(y2)
+    h2 = np.where(y2f > 0, y2f * y2f, np.float32(0)).astype(np.float32)
+    qr, sfr = _mx_reference(h2)
+    assert np.array_equal(q2, qr)
+    for e in range(3):
+        assert np.array_equal(sf2[soff[e]:soff[e] + cnt[e], :2], sfr[eoff[e]:eoff[e + 1]])
+        assert np.all(sf2[soff[e] + cnt[e]:soff[e + 1]] == 0)
