@@ -274,12 +274,16 @@ def run_reference(args) -> None:
 
 # ----------------------------------------------------------------- suite ---
 def _timed(fn, reps, flush=None):
-    """Median device time (ms) of fn() over reps runs, each after an L2 flush."""
+    """Median device time (ms) of fn() over reps runs, each after an L2 flush.
+    A 30 us device sleep before the start event keeps the GPU busy while the
+    host enqueues fn's launches, so short kernels are timed without the host's
+    launch latency."""
     import torch
     ts = []
     for _ in range(reps):
         if flush is not None:
             flush.zero_()
+        torch.cuda._sleep(60000)
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
         a.record()
@@ -376,6 +380,30 @@ def run_suite(reps: int = 20, only: str | None = None) -> None:
             line("activation + MXFP8 8x4000x4096", name, ms, rows * width * 2 + rows * I + 8 * 4096 * (I // 32), 0,
                  "fp8")
         del y
+
+    # Router front: fp32 logits [M, 8] -> top-2 -> align -> sorted e4m3 rows,
+    # fused into one launch at decode sizes, against the separate launches.
+    if not only or "router" in only:
+        for M in (64, 512, 4096):
+            K = 4096
+            lg = torch.randn(M, E, device=dev)
+            a = torch.randn(M, K, device=dev).to(torch.bfloat16)
+            ids, tw = q.moe_router_topk(lg, TOP_K)
+            ms = _timed(lambda: q.moe_router_topk(lg, TOP_K, topk_ids=ids, topk_weights=tw), reps)
+            line(f"router M={M} E={E} top_k={TOP_K}", "moe_router_topk", ms, M * E * 4 + M * TOP_K * 8, 0, "fp8")
+            BM = 32 if M <= 64 else 128
+            ids2, tw2, al, aq, sa = q.moe_route_align_quant_fp8(lg, a, TOP_K, BM)
+            ms = _timed(lambda: q.moe_route_align_quant_fp8(lg, a, TOP_K, BM, align=al, topk_ids=ids2,
+                                                            topk_weights=tw2, q=aq, scale=sa), reps, flush)
+            line(f"router M={M} E={E} top_k={TOP_K}", f"moe_route_align_quant_fp8 BM={BM}", ms,
+                 M * E * 4 + M * TOP_K * 8 + M * K * 2 + M * TOP_K * (K + 8), 0, "fp8")
+
+            def separate():
+                q.moe_router_topk(lg, TOP_K, topk_ids=ids, topk_weights=tw)
+                q.moe_align_quant_fp8(a, ids, E, BM, align=al, q=aq, scale=sa)
+            ms = _timed(separate, reps, flush)
+            line(f"router M={M} E={E} top_k={TOP_K}", f"moe_router_topk + moe_align_quant_fp8 BM={BM}", ms,
+                 M * E * 4 + M * TOP_K * 8 + M * K * 2 + M * TOP_K * (K + 8), 0, "fp8")
 
     # FP8 layers
     for wl in (inputs.mixtral_8x7b_layer(), inputs.mixtral_8x22b_layer()):

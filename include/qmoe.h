@@ -149,6 +149,33 @@ qmoe_status_t qmoe_gather_sorted_bf16(const uint16_t* x, int64_t M, int64_t cols
                                       const int32_t* sorted_ids, const int32_t* num_post_padded, int32_t top_k,
                                       int64_t cap, uint16_t* out, qmoe_stream_t stream);
 
+/* Router (the step in front of the grouped GEMM; the "top_k" column of the
+ * "Tianxing/moe quantization" tables): fp32 logits [M, E] -> softmax -> the
+ * top_k experts -> weights renormalised to sum to one.  Softmax is strictly
+ * increasing, so the selected experts are the top_k logits and their
+ * renormalised weights are the softmax over the selected logits alone; per
+ * token, in fp32: e_1..e_k = the top_k logits in descending order, ties to
+ * the lower expert id; p_j = exp(l_{e_j} - l_{e_1}) (the same fixed exp as
+ * qmoe_silu_mul_quant); S = sum of p_j in that order; w_j = p_j / S (IEEE).
+ *   logits [M, E] fp32, finite, row-major; topk_ids [M, top_k] int32;
+ *   topk_weights [M, top_k] fp32 (device memory, caller-owned).
+ * Limits: 1 <= E <= 256, 1 <= top_k <= min(E, 8); else
+ * QMOE_ERR_INVALID_ARG before any launch. */
+qmoe_status_t qmoe_moe_router_topk(const float* logits, int64_t M, int32_t E, int32_t top_k, int32_t* topk_ids,
+                                   float* topk_weights, qmoe_stream_t stream);
+
+/* Router + moe_align_block_size + per-token quantisation in padded sorted
+ * order in one launch for T = M*top_k <= 4096 (larger T: three launches), the
+ * decode-sized front of the grouped GEMM.  Outputs are those of
+ * qmoe_moe_router_topk followed by qmoe_moe_align_quant_fp8 (pad rows of q and
+ * scale not written).  Limits as there. */
+qmoe_status_t qmoe_moe_route_align_quant_fp8(const float* logits, const uint16_t* x, int64_t M, int64_t cols,
+                                             int64_t ldx, int32_t E, int32_t top_k, int32_t BM, int32_t* topk_ids,
+                                             float* topk_weights, int32_t* sorted_ids, int32_t* expert_ids,
+                                             int32_t* num_post_padded, int32_t* expert_offsets,
+                                             int32_t* padded_offsets, uint8_t* q, float* scale, int32_t* d_status,
+                                             qmoe_stream_t stream);
+
 /* Per-output-channel weight quantisation, the same rule on fp32 rows: every
  * (expert, output channel) row of W[E, N, K] is one row (rows = E*N).
  * fp8: scale = amax/448, e4m3 codes; int8: scale = amax/127,

@@ -89,6 +89,7 @@ def lib():
             L.orc_silu_mul_quant_mx.argtypes = [vp, i64, i64, i64, vp, vp, i32, vp, vp, i64]
             L.orc_srelu_quant_token.argtypes = [vp, i64, i64, i64, vp, vp]
             L.orc_srelu_quant_mx.argtypes = [vp, i64, i64, i64, vp, vp, i32, vp, vp, i64]
+            L.orc_router_topk.argtypes = [vp, i64, i32, i32, vp, vp]
             L.orc_srelu_f32.argtypes = [ctypes.c_float]
             L.orc_srelu_f32.restype = ctypes.c_float
             L.orc_e4m3_from_f32_array.argtypes = [vp, i64, vp]
@@ -281,6 +282,16 @@ def srelu_quant_mx(y_bits: np.ndarray, expert_offsets: np.ndarray, sf_padded_off
     sf = np.zeros((int(soff[E]), ld), dtype=np.uint8)
     lib().orc_srelu_quant_mx(_p(y), R, I, I, _p(eoff), _p(soff), E, _p(q), _p(sf), ld)
     return q, sf
+
+
+def router_topk(logits: np.ndarray, k: int):
+    """fp32 logits [M, E] -> (topk_ids int32 [M, k], topk_weights fp32 [M, k])."""
+    l = np.ascontiguousarray(logits, dtype=np.float32)
+    M, E = l.shape
+    ids = np.empty((M, k), dtype=np.int32)
+    w = np.empty((M, k), dtype=np.float32)
+    lib().orc_router_topk(_p(l), M, E, k, _p(ids), _p(w))
+    return ids, w
 
 
 # ------------------------------------------------------------------- GEMM ---

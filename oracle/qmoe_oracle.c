@@ -365,6 +365,40 @@ void orc_srelu_quant_mx(const uint16_t* y, int64_t R, int64_t I, int64_t ldy,
 }
 
 /* ------------------------------------------------------------------------- */
+/* Router: softmax over the E logits of a token -> top-k -> renormalise (the  */
+/* router sits in front of the grouped GEMM; the "top_k" column of the        */
+/* "Tianxing/moe quantization" tables).  Softmax is strictly increasing, so   */
+/* its top-k are the top-k logits, and the renormalised weights of the        */
+/* selected experts are the softmax over the selected logits alone:           */
+/*   e_1..e_k = the k largest logits in descending order, ties to the lower   */
+/*   expert id (exact comparisons);  p_j = exp(l_{e_j} - l_{e_1}) with the    */
+/*   fixed exp;  S = sum of p_j in selection order;  w_j = p_j / S  (fp32).   */
+/* ------------------------------------------------------------------------- */
+void orc_router_topk(const float* logits, int64_t M, int32_t E, int32_t k, int32_t* ids, float* w) {
+#pragma omp parallel for schedule(static)
+    for (int64_t m = 0; m < M; ++m) {
+        const float* l = logits + m * E;
+        int* taken = (int*)calloc((size_t)E, sizeof(int));
+        float p[8];
+        for (int j = 0; j < k; ++j) {
+            int best = -1;
+            for (int e = 0; e < E; ++e)
+                if (!taken[e] && (best < 0 || l[e] > l[best])) best = e;
+            taken[best] = 1;
+            ids[m * k + j] = best;
+        }
+        const float top = l[ids[m * k]];
+        float S = 0.0f;
+        for (int j = 0; j < k; ++j) {
+            p[j] = orc_exp_f32(l[ids[m * k + j]] - top);
+            S = S + p[j];
+        }
+        for (int j = 0; j < k; ++j) w[m * k + j] = p[j] / S;
+        free(taken);
+    }
+}
+
+/* ------------------------------------------------------------------------- */
 /* Grouped GEMM, dense per-token expert loop in fp64.                         */
 /* For each listed slot s (slots[i]):                                          */
 /*   e   = topk_ids[s]                                                         */

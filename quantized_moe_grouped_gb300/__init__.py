@@ -29,7 +29,7 @@ OUT_SLOT, OUT_GROUPED, OUT_TOKEN_SUM = 0, 1, 2
 
 EXPORTED = (
     "qmoe_status_string", "qmoe_version", "qmoe_align_max_padded", "qmoe_moe_align_block_size",
-    "qmoe_quant_act_fp8", "qmoe_quant_act_fp8_sorted", "qmoe_moe_align_quant_fp8", "qmoe_gather_sorted_bf16", "qmoe_quant_weight_fp8", "qmoe_quant_weight_int8", "qmoe_moe_gemm_w8a8",
+    "qmoe_quant_act_fp8", "qmoe_quant_act_fp8_sorted", "qmoe_moe_align_quant_fp8", "qmoe_moe_router_topk", "qmoe_moe_route_align_quant_fp8", "qmoe_gather_sorted_bf16", "qmoe_quant_weight_fp8", "qmoe_quant_weight_int8", "qmoe_moe_gemm_w8a8",
     "qmoe_moe_gemm_w8a16", "qmoe_silu_mul_quant", "qmoe_srelu_quant", "qmoe_debug_e4m3_encode", "qmoe_debug_int8_to_bf16",
     "qmoe_debug_silu_mul", "qmoe_debug_div_by_scale", "qmoe_debug_wait_timeout",
     "qmoe_moe_gemm_w8a8_token_sum_noalloc",
@@ -80,6 +80,9 @@ def load_library(path: str | None = None):
             L.qmoe_quant_act_fp8_sorted.argtypes = [vp, i64, i64, i64, vp, vp, i32, i64, vp, vp, vp]
             L.qmoe_moe_align_quant_fp8.argtypes = [vp, i64, i64, i64, vp, i32, i32, i32, vp, vp, vp, vp, vp, vp,
                                                    vp, vp, vp]
+            L.qmoe_moe_router_topk.argtypes = [vp, i64, i32, i32, vp, vp, vp]
+            L.qmoe_moe_route_align_quant_fp8.argtypes = [vp, vp, i64, i64, i64, i32, i32, i32, vp, vp, vp, vp, vp,
+                                                         vp, vp, vp, vp, vp, vp]
             L.qmoe_gather_sorted_bf16.argtypes = [vp, i64, i64, i64, vp, vp, i32, i64, vp, vp]
             L.qmoe_quant_weight_fp8.argtypes = [vp, i64, i64, vp, vp, vp]
             L.qmoe_quant_weight_int8.argtypes = [vp, i64, i64, vp, vp, vp]
@@ -202,6 +205,41 @@ def moe_align_quant_fp8(x: torch.Tensor, topk_ids: torch.Tensor, E: int, BM: int
         _ptr(d_status), _stream(stream))
     _check(st, "moe_align_quant_fp8")
     return o, q, scale
+
+
+def moe_router_topk(logits: torch.Tensor, top_k: int, topk_ids=None, topk_weights=None, stream=None):
+    """fp32 logits [M, E] -> (topk_ids int32 [M, top_k], topk_weights fp32 [M, top_k])."""
+    _need(logits, torch.float32, "logits")
+    M, E = logits.shape
+    ids = topk_ids if topk_ids is not None else torch.empty(M, top_k, dtype=torch.int32, device=logits.device)
+    w = topk_weights if topk_weights is not None else torch.empty(M, top_k, dtype=torch.float32, device=logits.device)
+    _check(load_library().qmoe_moe_router_topk(_ptr(logits), M, E, top_k, _ptr(ids), _ptr(w), _stream(stream)),
+           "moe_router_topk")
+    return ids, w
+
+
+def moe_route_align_quant_fp8(logits: torch.Tensor, x: torch.Tensor, top_k: int, BM: int, align: dict | None = None,
+                              topk_ids=None, topk_weights=None, q=None, scale=None, d_status=None, stream=None):
+    """Router + align + per-token e4m3 rows in padded sorted order (one launch for small batches).
+    Returns (topk_ids, topk_weights, align dict, q [cap, K], scale [cap])."""
+    _need(logits, torch.float32, "logits")
+    if not x.is_cuda or x.dtype != torch.bfloat16 or x.dim() != 2 or x.stride(1) != 1:
+        raise QmoeError("x must be a 2-D CUDA bf16 tensor with unit column stride")
+    M, E = logits.shape
+    cols = x.shape[1]
+    T = M * top_k
+    o = align if align is not None else alloc_align_outputs(T, E, BM, x.device)
+    ids = topk_ids if topk_ids is not None else torch.empty(M, top_k, dtype=torch.int32, device=x.device)
+    w = topk_weights if topk_weights is not None else torch.empty(M, top_k, dtype=torch.float32, device=x.device)
+    cap = o["sorted_ids"].numel()
+    q = q if q is not None else torch.empty(cap, cols, dtype=torch.uint8, device=x.device)
+    scale = scale if scale is not None else torch.empty(cap, dtype=torch.float32, device=x.device)
+    st = load_library().qmoe_moe_route_align_quant_fp8(
+        _ptr(logits), _ptr(x), M, cols, x.stride(0), E, top_k, BM, _ptr(ids), _ptr(w), _ptr(o["sorted_ids"]),
+        _ptr(o["expert_ids"]), _ptr(o["num_post_padded"]), _ptr(o["expert_offsets"]), _ptr(o["padded_offsets"]),
+        _ptr(q), _ptr(scale), _ptr(d_status), _stream(stream))
+    _check(st, "moe_route_align_quant_fp8")
+    return ids, w, o, q, scale
 
 
 def gather_sorted_bf16(x: torch.Tensor, align: dict, top_k: int, out: torch.Tensor | None = None, stream=None):

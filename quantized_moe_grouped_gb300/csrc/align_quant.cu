@@ -232,6 +232,75 @@ __global__ void __launch_bounds__(kRowThreads)
 }
 
 // ======================================================================
+// Router: softmax -> top-k -> renormalise.  The top-k of the softmax are the
+// top-k logits and the renormalised weights are the softmax over the selected
+// logits, so per token: the k largest logits, descending, ties to the lower
+// id (one pass over the E logits, an insertion into a k-long register list
+// ordered by (value desc, id asc)); p_j = exp_seq(l_j - l_1); S = sum of p_j
+// in order; w_j = p_j / S.
+// ======================================================================
+constexpr int kRouterMaxE = 256;
+constexpr int kRouterMaxK = 8;
+
+QMOE_DI void route_token(const float* __restrict__ l, int E, int k, int* ids, float* w) {
+    float tv[kRouterMaxK];
+    int ti[kRouterMaxK];
+#pragma unroll
+    for (int j = 0; j < kRouterMaxK; ++j) {
+        tv[j] = 0.0f;
+        ti[j] = -1;
+    }
+    for (int e = 0; e < E; ++e) {
+        float v = l[e];
+        int id = e;
+#pragma unroll
+        for (int j = 0; j < kRouterMaxK; ++j) {
+            if (j < k && (ti[j] < 0 || v > tv[j] || (v == tv[j] && id < ti[j]))) {
+                const float t = tv[j];
+                const int u = ti[j];
+                tv[j] = v;
+                ti[j] = id;
+                v = t;
+                id = u;
+                if (id < 0) break;
+            }
+        }
+    }
+    float p[kRouterMaxK];
+    float S = 0.0f;
+#pragma unroll
+    for (int j = 0; j < kRouterMaxK; ++j) {
+        if (j < k) {
+            p[j] = exp_seq(__fsub_rn(tv[j], tv[0]));
+            S = __fadd_rn(S, p[j]);
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < kRouterMaxK; ++j) {
+        if (j < k) {
+            ids[j] = ti[j];
+            w[j] = __fdiv_rn(p[j], S);
+        }
+    }
+}
+
+__global__ void router_topk_kernel(const float* __restrict__ logits, int64_t M, int E, int k,
+                                   int32_t* __restrict__ topk_ids, float* __restrict__ topk_w) {
+    for (int64_t m = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; m < M;
+         m += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        int ids[kRouterMaxK];
+        float w[kRouterMaxK];
+        route_token(logits + m * E, E, k, ids, w);
+#pragma unroll
+        for (int j = 0; j < kRouterMaxK; ++j) {
+            if (j >= k) break;
+            topk_ids[m * k + j] = ids[j];
+            topk_w[m * k + j] = w[j];
+        }
+    }
+}
+
+// ======================================================================
 // Fused align + sorted per-token quantisation for small slot counts (one
 // launch).  CTAs 0..M-1: one token each -- histogram of all ids in shared
 // memory, padded offsets, the padded position of each of the token's slots
@@ -243,9 +312,14 @@ __global__ void __launch_bounds__(kRowThreads)
 // ======================================================================
 constexpr int kFusedMaxT = 4096;
 
+// kRoute: the ids come from routing fp32 logits [M, E] in the same launch --
+// every CTA routes all tokens (its histogram needs them) and CTA m writes
+// token m's ids and weights.
+template <bool kRoute>
 __global__ void __launch_bounds__(kRowThreads)
     align_quant_fused_kernel(const uint16_t* __restrict__ x, int64_t M, int64_t cols, int64_t ldx,
-                             const int32_t* __restrict__ ids, int top_k, int E, int BM,
+                             const int32_t* __restrict__ ids, const float* __restrict__ logits,
+                             int32_t* __restrict__ ids_out, float* __restrict__ w_out, int top_k, int E, int BM,
                              int32_t* __restrict__ sorted_ids, int64_t cap, int32_t* __restrict__ expert_ids,
                              int32_t* __restrict__ num_post_padded, int32_t* __restrict__ expert_offsets,
                              int32_t* __restrict__ padded_offsets, uint8_t* __restrict__ q,
@@ -259,10 +333,28 @@ __global__ void __launch_bounds__(kRowThreads)
     const int tid = threadIdx.x;
     for (int e = tid; e < E; e += blockDim.x) s_cnt[e] = 0;
     __syncthreads();
-    for (int i = tid; i < T; i += blockDim.x) {
-        const int e = ids[i];
-        s_ids[i] = e;
-        if (e >= 0 && e < E) atomicAdd(&s_cnt[e], 1);
+    if constexpr (kRoute) {
+        for (int m = tid; m < static_cast<int>(M); m += blockDim.x) {
+            int rid[kRouterMaxK];
+            float rw[kRouterMaxK];
+            route_token(logits + static_cast<int64_t>(m) * E, E, top_k, rid, rw);
+#pragma unroll
+            for (int j = 0; j < kRouterMaxK; ++j) {
+                if (j >= top_k) break;
+                s_ids[m * top_k + j] = rid[j];
+                atomicAdd(&s_cnt[rid[j]], 1);
+                if (m == static_cast<int>(blockIdx.x)) {
+                    ids_out[m * top_k + j] = rid[j];
+                    w_out[m * top_k + j] = rw[j];
+                }
+            }
+        }
+    } else {
+        for (int i = tid; i < T; i += blockDim.x) {
+            const int e = ids[i];
+            s_ids[i] = e;
+            if (e >= 0 && e < E) atomicAdd(&s_cnt[e], 1);
+        }
     }
     __syncthreads();
     if (tid == 0) {
@@ -710,9 +802,48 @@ qmoe_status_t qmoe_moe_align_quant_fp8(const uint16_t* x, int64_t M, int64_t col
         if (st != QMOE_OK) return st;
         return qmoe_quant_act_fp8_sorted(x, M, cols, ldx, sorted_ids, num_post_padded, top_k, cap, q, scale, stream);
     }
-    align_quant_fused_kernel<<<static_cast<unsigned>(M + 1), kRowThreads, 0, stream>>>(
-        x, M, cols, ldx, topk_ids, top_k, E, BM, sorted_ids, cap, expert_ids, num_post_padded, expert_offsets,
-        padded_offsets, q, scale, d_status);
+    align_quant_fused_kernel<false><<<static_cast<unsigned>(M + 1), kRowThreads, 0, stream>>>(
+        x, M, cols, ldx, topk_ids, nullptr, nullptr, nullptr, top_k, E, BM, sorted_ids, cap, expert_ids,
+        num_post_padded, expert_offsets, padded_offsets, q, scale, d_status);
+    return launch_status();
+}
+
+qmoe_status_t qmoe_moe_router_topk(const float* logits, int64_t M, int32_t E, int32_t top_k, int32_t* topk_ids,
+                                   float* topk_weights, qmoe_stream_t stream) {
+    if (M < 0 || E < 1 || E > kRouterMaxE || top_k < 1 || top_k > 8 || top_k > E) return QMOE_ERR_INVALID_ARG;
+    if (M == 0) return QMOE_OK;
+    if (!logits || !topk_ids || !topk_weights) return QMOE_ERR_INVALID_ARG;
+    router_topk_kernel<<<grid_for(M, 128), 128, 0, stream>>>(logits, M, E, top_k, topk_ids, topk_weights);
+    return launch_status();
+}
+
+qmoe_status_t qmoe_moe_route_align_quant_fp8(const float* logits, const uint16_t* x, int64_t M, int64_t cols,
+                                             int64_t ldx, int32_t E, int32_t top_k, int32_t BM, int32_t* topk_ids,
+                                             float* topk_weights, int32_t* sorted_ids, int32_t* expert_ids,
+                                             int32_t* num_post_padded, int32_t* expert_offsets,
+                                             int32_t* padded_offsets, uint8_t* q, float* scale, int32_t* d_status,
+                                             qmoe_stream_t stream) {
+    if (M < 0 || top_k < 1 || top_k > 8 || top_k > E || E < 1 || E > kAlignMaxE || BM < 1 || BM > 1024)
+        return QMOE_ERR_INVALID_ARG;
+    if (cols < 16 || cols % 16 != 0 || ldx < cols || ldx % 8 != 0) return QMOE_ERR_INVALID_ARG;
+    const int64_t T = M * top_k;
+    const int64_t cap = qmoe_align_max_padded(T, E, BM);
+    if (cap >= (int64_t(1) << 31)) return QMOE_ERR_UNSUPPORTED;
+    if ((M > 0 && (!x || !logits)) || !topk_ids || !topk_weights || !sorted_ids || !expert_ids ||
+        !num_post_padded || !expert_offsets || !padded_offsets || !q || !scale || (M > 0 && !aligned16(x)) ||
+        !aligned16(q))
+        return QMOE_ERR_INVALID_ARG;
+    if (T > kFusedMaxT) {  // large batches: router, align and quantisation as three launches
+        qmoe_status_t st = qmoe_moe_router_topk(logits, M, E, top_k, topk_ids, topk_weights, stream);
+        if (st != QMOE_OK) return st;
+        st = qmoe_moe_align_block_size(topk_ids, T, E, BM, sorted_ids, expert_ids, num_post_padded, expert_offsets,
+                                       padded_offsets, d_status, stream);
+        if (st != QMOE_OK) return st;
+        return qmoe_quant_act_fp8_sorted(x, M, cols, ldx, sorted_ids, num_post_padded, top_k, cap, q, scale, stream);
+    }
+    align_quant_fused_kernel<true><<<static_cast<unsigned>(M + 1), kRowThreads, 0, stream>>>(
+        x, M, cols, ldx, nullptr, logits, topk_ids, topk_weights, top_k, E, BM, sorted_ids, cap, expert_ids,
+        num_post_padded, expert_offsets, padded_offsets, q, scale, d_status);
     return launch_status();
 }
 

@@ -254,3 +254,43 @@ def test_srelu_quant_mx_bitexact(q, orc, cnt, I):
     rq, rsf = orc.srelu_quant_mx(y, eoff, soff)
     assert np.array_equal(qq.cpu().numpy(), rq)
     assert np.array_equal(sfo.cpu().numpy(), rsf)
+
+
+@pytest.mark.parametrize("M,E,k", [(1, 8, 2), (777, 8, 2), (300, 64, 6), (129, 256, 8), (64, 5, 5), (5000, 16, 1)])
+def test_router_topk_bitexact(q, orc, M, E, k):
+    """Router kernel == the oracle's fixed fp32 sequence: ids and weight bits."""
+    l = inputs.router_logits(M, E, seed=M + E, zipf_s=1.0).astype(np.float32)
+    l[0, :] = 0.0  # an all-tie row
+    ids, w = q.moe_router_topk(to_dev(l), k)
+    torch.cuda.synchronize()
+    rid, rw = orc.router_topk(l, k)
+    assert np.array_equal(ids.cpu().numpy(), rid)
+    assert np.array_equal(w.cpu().numpy().view(np.uint32), rw.view(np.uint32))
+
+
+@pytest.mark.parametrize("M,K,E,top_k,BM", [(64, 4096, 8, 2, 32), (1, 128, 8, 2, 16), (333, 256, 64, 6, 64),
+                                            (512, 4096, 8, 2, 128), (2100, 128, 8, 2, 128)])
+def test_fused_route_align_quant_bitexact(q, orc, M, K, E, top_k, BM):
+    """Router + align + sorted quantisation in one launch == the oracle's router,
+    align and per-token codes (the last case exceeds the one-launch limit)."""
+    x = inputs.activations_bf16(M, K, seed=M + K + 1)
+    l = inputs.router_logits(M, E, seed=M + 3, zipf_s=1.1).astype(np.float32)
+    st = status()
+    ids, w, al, qq, ss = q.moe_route_align_quant_fp8(to_dev(l), to_dev_bf16(x), top_k, BM, d_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    rid, rw = orc.router_topk(l, top_k)
+    assert np.array_equal(ids.cpu().numpy(), rid)
+    assert np.array_equal(w.cpu().numpy().view(np.uint32), rw.view(np.uint32))
+    ref = orc.moe_align(rid, E, BM)
+    cap = al["sorted_ids"].numel()
+    assert np.array_equal(al["sorted_ids"].cpu().numpy(), ref["sorted_ids"][:cap])
+    assert np.array_equal(al["expert_ids"].cpu().numpy(), ref["expert_ids"][: cap // BM])
+    assert np.array_equal(al["expert_offsets"].cpu().numpy(), ref["expert_offsets"])
+    assert np.array_equal(al["padded_offsets"].cpu().numpy(), ref["padded_offsets"])
+    assert int(al["num_post_padded"].item()) == ref["num_post_padded"]
+    rq, rs = orc.quant_rows_fp8_bf16(x)
+    srt = ref["sorted_ids"][: ref["num_post_padded"]]
+    valid = np.nonzero(srt < M * top_k)[0]
+    assert np.array_equal(qq.cpu().numpy()[valid], rq[srt[valid] // top_k])
+    assert np.array_equal(ss.cpu().numpy()[valid], rs[srt[valid] // top_k])
