@@ -67,6 +67,8 @@ struct GemmParams {
     int32_t* d_status;
 };
 
+constexpr int kGemmMaxE = 256;  // experts per call (the align's limit)
+
 template <bool kBF16, bool kWide, int BN, bool kMX = false>
 struct GemmCfg {
     static constexpr int kSlotRows = kWide ? 128 : BN;      // slots per tile
@@ -166,6 +168,7 @@ __global__ void __launch_bounds__(GemmCfg<kBF16, kWide, BN, kMX>::kThreads, 1)
     __shared__ float s_cscale[kWide ? 1 : SR];     // swapped epilogue: a_scale * routing weight per column
     __shared__ int32_t s_crow[kWide ? 1 : SR];     // swapped epilogue: output row per column (-1: padding)
     __shared__ float s_wsc[kWide ? WR : 1];        // wide epilogue: w_scale per column
+    __shared__ int32_t s_poff[kGemmMaxE + 1];      // padded_offsets: first padded position of each expert
 
     const uint32_t raw_addr = smem_u32(smem_raw);
     uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
@@ -192,6 +195,7 @@ __global__ void __launch_bounds__(GemmCfg<kBF16, kWide, BN, kMX>::kThreads, 1)
         s_abort = 0;
         fence_mbar_init();
     }
+    for (int i = threadIdx.x; i <= p.E; i += blockDim.x) s_poff[i] = p.padded_offsets[i];
     if (warp == 1) tmem_alloc(&s_tmem_base, C::kTmemCols);
     tc_fence_before();
     __syncthreads();
@@ -199,23 +203,34 @@ __global__ void __launch_bounds__(GemmCfg<kBF16, kWide, BN, kMX>::kThreads, 1)
     const uint32_t tmem_base = s_tmem_base;
     volatile int* abort = &s_abort;
 
-    const int num_sb = *p.num_post_padded / SR;
     const int n_blocks = static_cast<int>((p.N + WR - 1) / WR);
-    const int num_tiles = num_sb * n_blocks;
+    const int num_tiles = s_poff[p.E] / SR * n_blocks;
     const int nkb = p.num_k_blocks;
     auto w_tile = [&](int s) { return smem + s * C::kStageBytes; };
     auto act_tile = [&](int s) { return smem + s * C::kStageBytes + C::kWBytes; };
     auto raw_tile = [&](int r) { return smem + S * C::kStageBytes + r * C::kRawBytes; };
-    // Expert of a tile, or -1 when the tile is to be skipped: an invalid expert
-    // id, or (tiles narrower than BM) a tile whose first slot is padding --
-    // valid slots precede the padding inside an expert's region, so the whole
-    // tile is padding then.
-    auto tile_expert = [&](int tile) {
-        const int sb = tile % num_sb;
-        const int e = p.expert_ids[sb * SR / p.BM];
-        if (e < 0 || e >= p.E) return -1;
+    // Tile order: expert by expert (expert e owns the slot blocks
+    // [s_poff[e], s_poff[e+1]) / SR); inside an expert, weight block major and
+    // slot block fastest.  The slot blocks that share a weight tile run at the
+    // same time (one HBM read of the tile), and while an expert's weight tiles
+    // stream its activation rows stay in L2.  Returns the expert, or -1 when
+    // the tile is to be skipped: (tiles narrower than BM) a tile whose first
+    // slot is padding -- valid slots precede the padding inside an expert's
+    // region, so the whole tile is padding then.
+    auto tile_expert = [&](int tile, int& sb, int& nb) {
+        int lo = 0, hi = p.E - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (s_poff[mid] / SR * n_blocks <= tile) lo = mid;
+            else hi = mid - 1;
+        }
+        const int sb0 = s_poff[lo] / SR;
+        const int nsb = s_poff[lo + 1] / SR - sb0;
+        const int local = tile - sb0 * n_blocks;
+        nb = local / nsb;
+        sb = sb0 + local % nsb;
         if (SR < p.BM && p.sorted_ids[sb * SR] >= p.T) return -1;
-        return e;
+        return lo;
     };
 
     if (warp == 0) {
@@ -225,10 +240,9 @@ __global__ void __launch_bounds__(GemmCfg<kBF16, kWide, BN, kMX>::kThreads, 1)
             bool ok = true;
             const uint32_t tx = C::kWBytes + (p.a_tma ? C::kActBytes : 0);
             for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
-                const int e = tile_expert(tile);
+                int sb, nb;
+                const int e = tile_expert(tile, sb, nb);
                 if (e < 0) continue;
-                const int nb = tile / num_sb;
-                const int sb = tile % num_sb;
                 // first activation row of the tile: padded position, or compact grouped row
                 const int arow0 = (p.a_layout == QMOE_A_PADDED)
                                       ? sb * SR
@@ -265,7 +279,8 @@ __global__ void __launch_bounds__(GemmCfg<kBF16, kWide, BN, kMX>::kThreads, 1)
                 tc_fence_after();
             }
             for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
-                if (tile_expert(tile) < 0) continue;
+                int sb, nb;
+                if (tile_expert(tile, sb, nb) < 0) continue;
                 const int acc = tcount % C::kAccBufs;
                 const uint32_t aph = (tcount / C::kAccBufs) & 1;
                 if (!mbar_wait(&bar_tempty[acc], aph ^ 1, abort, p.d_status)) break;
@@ -304,9 +319,9 @@ __global__ void __launch_bounds__(GemmCfg<kBF16, kWide, BN, kMX>::kThreads, 1)
             int it = 0;
             bool ok = true;
             for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
-                const int e = tile_expert(tile);
+                int sb, nb;
+                const int e = tile_expert(tile, sb, nb);
                 if (e < 0) continue;
-                const int sb = tile % num_sb;
                 const int arow0 = (p.a_layout == QMOE_A_PADDED)
                                       ? sb * SR
                                       : p.expert_offsets[e] + (sb * SR - p.padded_offsets[e]);
@@ -330,9 +345,9 @@ __global__ void __launch_bounds__(GemmCfg<kBF16, kWide, BN, kMX>::kThreads, 1)
         bool ok = !p.a_tma;
         for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
             if (*abort) break;
-            const int e = tile_expert(tile);
+            int sb, nb;
+            const int e = tile_expert(tile, sb, nb);
             if (e < 0) continue;
-            const int sb = tile % num_sb;
             named_bar_sync(1, C::kBProdThreads);
             for (int j = pt; j < SR; j += C::kBProdThreads) {
                 const int pos = sb * SR + j;
@@ -376,10 +391,9 @@ __global__ void __launch_bounds__(GemmCfg<kBF16, kWide, BN, kMX>::kThreads, 1)
         int tcount = 0;
         for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
             if (*abort) break;
-            const int e = tile_expert(tile);
+            int sb, nb;
+            const int e = tile_expert(tile, sb, nb);
             if (e < 0) continue;
-            const int sb = tile % num_sb;
-            const int nb = tile / num_sb;
             const int acc = tcount % C::kAccBufs;
             const uint32_t aph = (tcount / C::kAccBufs) & 1;
             const uint32_t t_base =
@@ -504,9 +518,9 @@ __global__ void __launch_bounds__(GemmCfg<kBF16, kWide, BN, kMX>::kThreads, 1)
         int it = 0;
         bool ok = true;
         for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
-            const int e = tile_expert(tile);
+            int sb, nb;
+            const int e = tile_expert(tile, sb, nb);
             if (e < 0) continue;
-            const int sb = tile % num_sb;
             const int cnt = p.expert_offsets[e + 1] - p.expert_offsets[e];
             const uint8_t* sfrow[4];
 #pragma unroll
@@ -538,7 +552,8 @@ __global__ void __launch_bounds__(GemmCfg<kBF16, kWide, BN, kMX>::kThreads, 1)
             int it = 0;
             bool ok = true;
             for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
-                if (tile_expert(tile) < 0) continue;
+                int sb, nb;
+                if (tile_expert(tile, sb, nb) < 0) continue;
                 for (int kb = 0; kb < nkb; ++kb, ++it) {
                     if ((it & 1) != group) continue;
                     const int s = it % S;
@@ -666,7 +681,7 @@ template <bool kBF16>
 inline qmoe_status_t run_moe_gemm(const qmoe_gemm_args* a, cudaStream_t st) {
     if (!a || a->struct_size < sizeof(qmoe_gemm_args)) return QMOE_ERR_INVALID_ARG;
     if (a->M < 0 || a->N < 16 || a->N % 16 != 0 || a->K < 16 || a->K % 16 != 0) return QMOE_ERR_INVALID_ARG;
-    if (a->E < 1 || a->E > 256 || a->top_k < 1 || a->top_k > a->E) return QMOE_ERR_INVALID_ARG;
+    if (a->E < 1 || a->E > kGemmMaxE || a->top_k < 1 || a->top_k > a->E) return QMOE_ERR_INVALID_ARG;
     if (a->BM != 16 && a->BM != 32 && a->BM != 64 && a->BM != 128 && a->BM != 256) return QMOE_ERR_UNSUPPORTED;
     if (a->a_layout != QMOE_A_TOKEN_GATHER && a->a_layout != QMOE_A_GROUPED && a->a_layout != QMOE_A_PADDED)
         return QMOE_ERR_INVALID_ARG;
@@ -728,6 +743,8 @@ inline qmoe_status_t run_moe_gemm(const qmoe_gemm_args* a, cudaStream_t st) {
     p.d_status = a->d_status;
     const int64_t max_padded = (T + static_cast<int64_t>(a->E) * (a->BM - 1) + a->BM - 1) / a->BM * a->BM;
     const int64_t a_rows = a->a_layout == QMOE_A_PADDED ? max_padded : (a->a_layout == QMOE_A_GROUPED ? T : a->M);
+    // the kernel numbers its tiles (slot blocks x weight blocks) with 32-bit ints
+    if (max_padded / 16 * ((a->N + 127) / 128) >= (int64_t(1) << 31)) return QMOE_ERR_UNSUPPORTED;
     qmoe_status_t r;
     if constexpr (!kBF16) {
         if (mx) {
