@@ -91,14 +91,16 @@ struct GemmCfg {
     // ahead of the gather warps, so the lag shrinks when the ring is short.
     static constexpr int kLag = kStages >= 6 ? 3 : (kStages >= 5 ? 2 : 1);
     static constexpr int kBProdThreads = 64;
-    static constexpr int kEpiThreads = 128;
+    static constexpr int kEpiThreads = kMX ? 256 : 128;   // MX: two groups of four warps, one per column half
+    static constexpr int kSfBytes = 512;                   // MX: one stage's activation scales in shared memory
     static constexpr int kConvThreads = 128;
     static constexpr int kConvGroups = kBF16 ? 2 : 1;       // converter groups alternate stages
     static constexpr int kThreads = kBF16 ? 512 : (kMX ? 384 : 256);
     static constexpr int kAccCols = kMmaN;                  // TMEM columns per accumulator
     // MX: one accumulator (256 columns), then four scale columns per stage for
     // the 128 activation rows (4-column aligned) and 8 columns of constant
-    // weight scales 2^0 (8-column aligned).
+    // weight scales 2^0 (8-column aligned), all copied in from shared memory
+    // by the MMA thread.
     static constexpr int kAccBufs = kMX ? 1 : 2;
     static constexpr int kSfaCol = kAccCols;
     static constexpr int kSfbCol = (kAccCols + 4 * kStages + 7) / 8 * 8;
@@ -107,7 +109,8 @@ struct GemmCfg {
         kMX ? make_idesc_mx(128, kMmaN) : make_idesc(kBF16 ? kFmtBF16 : kFmtE4M3, 128, kMmaN);
     static_assert(!kMX || (kWide && !kBF16), "MX scales: FP8 wide tile only");
     static_assert(!kMX || kSfbCol + 8 <= 512, "TMEM columns");
-    static constexpr int kDynSmem = kStages * kStageBytes + kRawStages * kRawBytes + 1024;
+    static constexpr int kDynSmem =
+        kStages * kStageBytes + kRawStages * kRawBytes + (kMX ? (kStages + 1) * kSfBytes : 0) + 1024;
     static_assert(kStages >= 2, "need at least two pipeline stages");
     static_assert(!kBF16 || kRawStages >= 2, "need at least two raw weight stages");
     static_assert(kMmaN % 16 == 0 && kMmaN >= 16 && kMmaN <= 256, "MMA N must be a multiple of 16 in [16, 256]");
@@ -150,6 +153,30 @@ QMOE_DI void tmem_ld32(uint32_t taddr, float (&v)[32]) {
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// 32 columns of this warp's 32 TMEM lanes, without the wait: the caller issues
+// several, then tmem_wait_ld_regs on each set before using the values.
+QMOE_DI void tmem_ld32_nowait(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+}
+QMOE_DI void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+// Ties the registers of an earlier tmem_ld32_nowait to a point after
+// tmem_wait_ld, so that no use of them is scheduled before the wait.
+QMOE_DI void tmem_wait_ld_regs(uint32_t (&r)[32]) {
+    asm volatile(""
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                   "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
+                   "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]),
+                   "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]),
+                   "+r"(r[29]), "+r"(r[30]), "+r"(r[31]));
+}
+
 template <bool kBF16, bool kWide, int BN, bool kMX>
 __global__ void __launch_bounds__(GemmCfg<kBF16, kWide, BN, kMX>::kThreads, 1)
     moe_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_a,
@@ -161,7 +188,7 @@ __global__ void __launch_bounds__(GemmCfg<kBF16, kWide, BN, kMX>::kThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     constexpr int R = C::kRawStages > 0 ? C::kRawStages : 1;
     __shared__ uint64_t bar_full[S], bar_empty[S], bar_conv[S], bar_raw_full[R], bar_raw_empty[R];
-    __shared__ uint64_t bar_tfull[2], bar_tempty[2], bar_drain, bar_sfb;
+    __shared__ uint64_t bar_tfull[2], bar_tempty[2], bar_drain;
     __shared__ uint32_t s_tmem_base;
     __shared__ int s_abort;
     __shared__ int32_t s_brow[SR];                 // activation producers: source row of each slot row (-1: zero)
@@ -174,11 +201,16 @@ __global__ void __launch_bounds__(GemmCfg<kBF16, kWide, BN, kMX>::kThreads, 1)
     uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    // MX scale staging: S stage buffers, then the constant weight-scale block
+    auto sf_smem = [&](int s) {
+        return smem + S * C::kStageBytes + C::kRawStages * C::kRawBytes + s * C::kSfBytes;
+    };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
-            // arrivals: the TMA thread (weights and/or activation tile), or the 64 gather threads
-            mbar_init(&bar_full[s], p.a_tma ? 1 : (kBF16 ? 0 : 1) + C::kBProdThreads);
+            // arrivals: the TMA thread (weights and/or activation tile), or the 64 gather threads;
+            // MX adds the 32 lanes of the scale warp
+            mbar_init(&bar_full[s], (p.a_tma ? 1 : (kBF16 ? 0 : 1) + C::kBProdThreads) + (kMX ? 32 : 0));
             mbar_init(&bar_empty[s], 1);
             mbar_init(&bar_conv[s], C::kConvThreads);
         }
@@ -191,11 +223,14 @@ __global__ void __launch_bounds__(GemmCfg<kBF16, kWide, BN, kMX>::kThreads, 1)
             mbar_init(&bar_raw_empty[r], C::kConvThreads);
         }
         mbar_init(&bar_drain, 1);
-        mbar_init(&bar_sfb, C::kConvThreads);
         s_abort = 0;
         fence_mbar_init();
     }
     for (int i = threadIdx.x; i <= p.E; i += blockDim.x) s_poff[i] = p.padded_offsets[i];
+    if constexpr (kMX) {  // weight scales 2^0: E8M0 byte 127 everywhere
+        if (threadIdx.x < C::kSfBytes / 4) reinterpret_cast<uint32_t*>(sf_smem(S))[threadIdx.x] = 0x7F7F7F7Fu;
+        fence_proxy_async_smem();
+    }
     if (warp == 1) tmem_alloc(&s_tmem_base, C::kTmemCols);
     tc_fence_before();
     __syncthreads();
@@ -274,9 +309,10 @@ __global__ void __launch_bounds__(GemmCfg<kBF16, kWide, BN, kMX>::kThreads, 1)
         if (lane == 0) {
             int it = 0, tcount = 0;
             bool ok = true;
-            if (kMX) {  // constant weight scales written once by the scale warps
-                ok = mbar_wait(&bar_sfb, 0, abort, p.d_status);
-                tc_fence_after();
+            if (kMX) {  // constant weight scales: two 4-column copies of the 2^0 block
+                const uint64_t sd = desc_rows16_noswizzle(smem_u32(sf_smem(S)));
+                tmem_cp_32x128b_x4(tmem_base + C::kSfbCol, sd);
+                tmem_cp_32x128b_x4(tmem_base + C::kSfbCol + 4, sd);
             }
             for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
                 int sb, nb;
@@ -290,8 +326,10 @@ __global__ void __launch_bounds__(GemmCfg<kBF16, kWide, BN, kMX>::kThreads, 1)
                     const int s = it % S;
                     const uint32_t ph = (it / S) & 1;
                     if (!mbar_wait(&bar_full[s], ph, abort, p.d_status)) { ok = false; break; }
-                    if ((kBF16 || kMX) && !mbar_wait(&bar_conv[s], ph, abort, p.d_status)) { ok = false; break; }
+                    if (kBF16 && !mbar_wait(&bar_conv[s], ph, abort, p.d_status)) { ok = false; break; }
                     tc_fence_after();
+                    if constexpr (kMX)  // this stage's activation scales, ahead of its MMAs in the same pipe
+                        tmem_cp_32x128b_x4(tmem_base + C::kSfaCol + 4 * s, desc_rows16_noswizzle(smem_u32(sf_smem(s))));
                     const uint64_t dw = desc_kmajor_sw128(smem_u32(w_tile(s)));
                     const uint64_t dx = desc_kmajor_sw128(smem_u32(act_tile(s)));
                     const uint64_t da = kWide ? dx : dw;
@@ -312,6 +350,54 @@ __global__ void __launch_bounds__(GemmCfg<kBF16, kWide, BN, kMX>::kThreads, 1)
             }
             tc_commit(&bar_drain);  // every MMA issued above has completed once this fires
             mbar_wait_drain(&bar_drain, 0, p.d_status);
+        }
+    } else if (kMX && warp == 2) {
+        // ------------------------- activation scales -> shared memory (MX) ---
+        // A stage's scales for the 128 tile rows as the 32 rows of 16 bytes the
+        // TMEM copy takes: row i holds, for c = 0..3, the four bytes of tile
+        // row 32c + i, one per 32-wide K block of the stage (TMEM lane i, column
+        // c, byte k for the stage's k-th MMA); the copy replicates the 32 rows
+        // into every lane quadrant.  Scale words are loaded kPf stages before
+        // their slot frees, so their latency stays off the MMA's path.
+        int it = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+            int sb, nb;
+            const int e = tile_expert(tile, sb, nb);
+            if (e < 0) continue;
+            const int cnt = p.expert_offsets[e + 1] - p.expert_offsets[e];
+            const uint8_t* sfrow[4];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const int i = sb * SR + c * 32 + lane - s_poff[e];  // local row of tile row 32c + lane
+                sfrow[c] = (i < cnt) ? p.a_sf + (static_cast<int64_t>(p.a_sf_poff[e]) + i) * p.a_sf_ld : nullptr;
+            }
+            constexpr int kPf = 4;
+            uint32_t pf[kPf][4];
+            auto load_stage = [&](int kb, uint32_t* v) {
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    v[c] = (sfrow[c] && kb < nkb) ? __ldg(reinterpret_cast<const uint32_t*>(sfrow[c] + kb * 4))
+                                                  : 0x7F7F7F7Fu;
+            };
+#pragma unroll
+            for (int j = 0; j < kPf; ++j) load_stage(j, pf[j]);
+            for (int kb0 = 0; ok && kb0 < nkb; kb0 += kPf) {
+#pragma unroll
+                for (int j = 0; j < kPf; ++j) {
+                    if (kb0 + j >= nkb) break;
+                    const int s = it % S;
+                    const uint32_t ph = (it / S) & 1;
+                    if (!mbar_wait(&bar_empty[s], ph ^ 1, abort, p.d_status)) ok = false;
+                    ok = __all_sync(0xFFFFFFFFu, ok);
+                    if (!ok) break;
+                    *reinterpret_cast<uint4*>(sf_smem(s) + 16 * lane) = make_uint4(pf[j][0], pf[j][1], pf[j][2], pf[j][3]);
+                    fence_proxy_async_smem();
+                    mbar_arrive(&bar_full[s]);
+                    load_stage(kb0 + j + kPf, pf[j]);
+                    ++it;
+                }
+            }
         }
     } else if (warp < 4 && kBF16 && p.a_tma) {
         // ------------------- W8A16: activation tiles by TMA (own thread) ---
@@ -384,7 +470,7 @@ __global__ void __launch_bounds__(GemmCfg<kBF16, kWide, BN, kMX>::kThreads, 1)
         cp_async_wait<0>();
         fence_proxy_async_smem();
         for (int j = (it > C::kLag ? it - C::kLag : 0); j < it; ++j) mbar_arrive(&bar_full[j % S]);
-    } else if (warp < 8) {
+    } else if (warp < 8 || kMX) {
         // ------------------------------------------------- epilogue ---
         const int et = threadIdx.x - 128;
         const int q = warp & 3;  // TMEM lane quadrant of this warp
@@ -424,27 +510,64 @@ __global__ void __launch_bounds__(GemmCfg<kBF16, kWide, BN, kMX>::kThreads, 1)
                 const int64_t col0 = orow * p.N + static_cast<int64_t>(nb) * WR;
                 const int64_t n_left = p.N - static_cast<int64_t>(nb) * WR;
                 const bool tsum = p.out_layout == QMOE_OUT_TOKEN_SUM;
-                for (int c0 = 0; c0 < WR; c0 += 32) {
-                    float v[32];
-                    tmem_ld32(t_base + c0, v);
-                    if (!valid) continue;
+                // scale and write 8 consecutive output channels starting at column cc
+                auto emit8 = [&](int cc, const float* v) {
+                    float x[8];
 #pragma unroll
-                    for (int g = 0; g < 4; ++g) {
-                        const int cc = c0 + g * 8;
-                        if (cc >= n_left) break;
-                        float x[8];
+                    for (int i = 0; i < 8; ++i) x[i] = v[i] * s_wsc[cc + i] * rs;
+                    if (tsum) {
+                        red_add_f32x4(p.accum + col0 + cc, x[0], x[1], x[2], x[3]);
+                        red_add_f32x4(p.accum + col0 + cc + 4, x[4], x[5], x[6], x[7]);
+                    } else {
+                        uint4 o;
+                        o.x = pack_bf16x2(x[0], x[1]);
+                        o.y = pack_bf16x2(x[2], x[3]);
+                        o.z = pack_bf16x2(x[4], x[5]);
+                        o.w = pack_bf16x2(x[6], x[7]);
+                        *reinterpret_cast<uint4*>(p.out + col0 + cc) = o;
+                    }
+                };
+                if constexpr (kMX) {
+                    // One accumulator: read this warp's 128 columns out in one go
+                    // and hand the accumulator back to the MMA before the stores.
+                    const int h = (warp - 4) >> 2;  // column half of this group
+                    uint32_t r[4][32];
 #pragma unroll
-                        for (int i = 0; i < 8; ++i) x[i] = v[g * 8 + i] * s_wsc[cc + i] * rs;
-                        if (tsum) {
-                            red_add_f32x4(p.accum + col0 + cc, x[0], x[1], x[2], x[3]);
-                            red_add_f32x4(p.accum + col0 + cc + 4, x[4], x[5], x[6], x[7]);
-                        } else {
-                            uint4 o;
-                            o.x = pack_bf16x2(x[0], x[1]);
-                            o.y = pack_bf16x2(x[2], x[3]);
-                            o.z = pack_bf16x2(x[4], x[5]);
-                            o.w = pack_bf16x2(x[6], x[7]);
-                            *reinterpret_cast<uint4*>(p.out + col0 + cc) = o;
+                    for (int j = 0; j < 4; ++j) tmem_ld32_nowait(t_base + h * 128 + 32 * j, r[j]);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) tmem_wait_ld_regs(r[j]);
+                    tc_fence_before();
+                    mbar_arrive(&bar_tempty[acc]);
+                    if (valid) {
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+#pragma unroll
+                            for (int g = 0; g < 4; ++g) {
+                                const int cc = h * 128 + 32 * j + g * 8;
+                                if (cc < n_left) {
+                                    float v[8];
+#pragma unroll
+                                    for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[j][g * 8 + i]);
+                                    emit8(cc, v);
+                                }
+                            }
+                        }
+                    }
+                } else {
+                    for (int c0 = 0; c0 < WR; c0 += 32) {
+                        float v[32];
+                        tmem_ld32(t_base + c0, v);
+                        if (c0 + 32 == WR) {  // accumulator read out: the MMA may reuse it while the stores finish
+                            tc_fence_before();
+                            mbar_arrive(&bar_tempty[acc]);
+                        }
+                        if (!valid) continue;
+#pragma unroll
+                        for (int g = 0; g < 4; ++g) {
+                            const int cc = c0 + g * 8;
+                            if (cc >= n_left) break;
+                            emit8(cc, v + g * 8);
                         }
                     }
                 }
@@ -498,51 +621,11 @@ __global__ void __launch_bounds__(GemmCfg<kBF16, kWide, BN, kMX>::kThreads, 1)
                     }
                 }
             }
-            tc_fence_before();
-            mbar_arrive(&bar_tempty[acc]);
-            ++tcount;
-        }
-    } else if (kMX) {
-        // ----------------------------- activation scales -> TMEM (MX) ---
-        // A stage's scales for the 128 tile rows occupy four 32-bit columns in
-        // the 32 x 4 x 4 arrangement: row r at lane r % 32, column r / 32, byte
-        // k = the 32-wide K block of the stage's k-th MMA; every lane quadrant
-        // holds the same copy, so each of the four warps writes all 128 rows.
-        const int q = warp & 3;
-        const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
-        tmem_st4(lane_base + C::kSfbCol, 0x7F7F7F7Fu);
-        tmem_st4(lane_base + C::kSfbCol + 4, 0x7F7F7F7Fu);
-        tmem_wait_st();
-        tc_fence_before();
-        mbar_arrive(&bar_sfb);
-        int it = 0;
-        bool ok = true;
-        for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
-            int sb, nb;
-            const int e = tile_expert(tile, sb, nb);
-            if (e < 0) continue;
-            const int cnt = p.expert_offsets[e + 1] - p.expert_offsets[e];
-            const uint8_t* sfrow[4];
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                const int i = sb * SR + c * 32 + lane - p.padded_offsets[e];  // local row of tile row 32c + lane
-                sfrow[c] = (i < cnt) ? p.a_sf + (static_cast<int64_t>(p.a_sf_poff[e]) + i) * p.a_sf_ld : nullptr;
-            }
-            for (int kb = 0; kb < nkb; ++kb, ++it) {
-                const int s = it % S;
-                const uint32_t ph = (it / S) & 1;
-                if (!mbar_wait(&bar_empty[s], ph ^ 1, abort, p.d_status)) ok = false;
-                ok = __all_sync(0xFFFFFFFFu, ok);
-                if (!ok) break;
-                uint32_t v[4];
-#pragma unroll
-                for (int c = 0; c < 4; ++c)
-                    v[c] = sfrow[c] ? *reinterpret_cast<const uint32_t*>(sfrow[c] + kb * 4) : 0x7F7F7F7Fu;
-                tmem_st4v(lane_base + C::kSfaCol + 4 * s, v[0], v[1], v[2], v[3]);
-                tmem_wait_st();
+            if constexpr (!kWide) {
                 tc_fence_before();
-                mbar_arrive(&bar_conv[s]);
+                mbar_arrive(&bar_tempty[acc]);
             }
+            ++tcount;
         }
     } else {
         // ---------------------------------- int8 -> bf16 converters ---

@@ -255,11 +255,14 @@ def test_w8a8_padded_sorted_activations(q, orc, M, K, N, E, top_k, BM, out_layou
 
 
 @pytest.mark.parametrize("M,I,N,E,BM,zipf,out_layout", [(256, 256, 256, 8, 128, None, 2), (300, 384, 272, 8, 256, 1.2, 2),
-                                                        (150, 160, 384, 5, 128, None, 1)])
+                                                        (150, 160, 384, 5, 128, None, 1),
+                                                        (1024, 256, 2560, 8, 128, 1.2, 2)])
 def test_w8a8_mx_activations(q, orc, M, I, N, E, BM, zipf, out_layout):
     """Down GEMM on MXFP8 activations: SwiGLU + MX 1x32 requantisation (bit-exact
     against the oracle), then the block-scaled FP8 GEMM over the grouped rows,
-    against the oracle's fp64 dequantisation with the E8M0 block scales."""
+    against the oracle's fp64 dequantisation with the E8M0 block scales.  The
+    last case has more tiles than the GPU has SMs, so CTAs reuse their single
+    accumulator."""
     top_k = 2
     T = M * top_k
     ids, tw = inputs.routing(M, E, top_k, seed=M + I, zipf_s=zipf)
