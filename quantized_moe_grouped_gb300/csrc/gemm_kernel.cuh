@@ -24,8 +24,9 @@
 //   warps 4-7   epilogue: TMEM -> registers, x w_scale[e,n] x a_scale x w[s],
 //               bf16 store (TOKEN_SUM: fp32 vector atomic add into the
 //               caller's accumulation buffer, rounded to bf16 by a second launch)
-//   warps 8-15  W8A16: int8 -> bf16 converters (raw ring -> main ring), two
-//               groups of four warps taking alternate stages
+//   warps 8+    W8A16: int8 -> bf16 converters (raw ring -> main ring), two
+//               groups (eight warps each for the wide tile, four for the
+//               swapped one) taking alternate stages
 //   warps 8-11  MX: the activation scale writers (global -> TMEM)
 //
 // Every wait is bounded (mbar_wait); on a timeout the CTA raises an abort
@@ -93,9 +94,11 @@ struct GemmCfg {
     static constexpr int kBProdThreads = 64;
     static constexpr int kEpiThreads = kMX ? 256 : 128;   // MX: two groups of four warps, one per column half
     static constexpr int kSfBytes = 512;                   // MX: one stage's activation scales in shared memory
-    static constexpr int kConvThreads = 128;
+    // W8A16 converter group: 8 warps for the wide tile (256 weight rows per
+    // stage), 4 for the swapped one; groups alternate stages
+    static constexpr int kConvThreads = (kBF16 && kWide) ? 256 : 128;
     static constexpr int kConvGroups = kBF16 ? 2 : 1;       // converter groups alternate stages
-    static constexpr int kThreads = kBF16 ? 512 : (kMX ? 384 : 256);
+    static constexpr int kThreads = kBF16 ? 256 + 2 * kConvThreads : (kMX ? 384 : 256);
     static constexpr int kAccCols = kMmaN;                  // TMEM columns per accumulator
     // MX: one accumulator (256 columns), then four scale columns per stage for
     // the 128 activation rows (4-column aligned) and 8 columns of constant
@@ -630,7 +633,7 @@ __global__ void __launch_bounds__(GemmCfg<kBF16, kWide, BN, kMX>::kThreads, 1)
     } else {
         // ---------------------------------- int8 -> bf16 converters ---
         if (kBF16) {
-            const int group = (warp - 8) >> 2;
+            const int group = (warp - 8) / (C::kConvThreads / 32);
             const int ct = threadIdx.x - 256 - group * C::kConvThreads;
             int it = 0;
             bool ok = true;
@@ -649,9 +652,10 @@ __global__ void __launch_bounds__(GemmCfg<kBF16, kWide, BN, kMX>::kThreads, 1)
                     const uint8_t* raw = raw_tile(r);
                     uint8_t* dst = w_tile(s);
                     const int c = ct & 3;
+                    constexpr int kRowsPerPass = C::kConvThreads / 4;  // four threads per 64-byte row
 #pragma unroll
-                    for (int i = 0; i < WR / 32; ++i) {
-                        const int r = (ct >> 2) + 32 * i;
+                    for (int i = 0; i < WR / kRowsPerPass; ++i) {
+                        const int r = (ct >> 2) + kRowsPerPass * i;
                         const uint4 w = *reinterpret_cast<const uint4*>(raw + r * 64 + c * 16);
                         uint4 o0, o1;
                         int8x4_to_bf16x4(w.x, o0.x, o0.y);
