@@ -34,7 +34,7 @@ _lock = threading.Lock()
 _lib = None
 
 A_FP8_TOKEN, A_FP8_MX, A_BF16 = 0, 1, 2
-W_FP8, W_INT8 = 0, 1
+W_FP8, W_INT8, W_MX = 0, 1, 2
 
 
 def build(force: bool = False) -> str:
@@ -89,6 +89,9 @@ def lib():
             L.orc_silu_mul_quant_mx.argtypes = [vp, i64, i64, i64, vp, vp, i32, vp, vp, i64]
             L.orc_srelu_quant_token.argtypes = [vp, i64, i64, i64, vp, vp]
             L.orc_srelu_quant_mx.argtypes = [vp, i64, i64, i64, vp, vp, i32, vp, vp, i64]
+            L.orc_quant_mxfp8_rows.argtypes = [vp, i64, i64, i64, vp, vp, i32, vp, vp, i64]
+            L.orc_quant_mxfp8_cols_bf16.argtypes = [vp, i64, i64, i64, vp, vp, i64, i64]
+            L.orc_quant_rows_mxfp8_f32.argtypes = [vp, i64, i64, vp, vp, i64]
             L.orc_router_topk.argtypes = [vp, i64, i32, i32, vp, vp]
             L.orc_srelu_f32.argtypes = [ctypes.c_float]
             L.orc_srelu_f32.restype = ctypes.c_float
@@ -96,7 +99,7 @@ def lib():
             L.orc_exp_f32_array.argtypes = [vp, i64, vp]
             L.orc_silu_mul_f32_array.argtypes = [vp, vp, i64, vp]
             L.orc_moe_gemm.argtypes = [ctypes.c_int, vp, i64, vp, vp, i64, vp,
-                                       ctypes.c_int, vp, vp, vp, vp, vp, i64, vp, i64, i64, vp]
+                                       ctypes.c_int, vp, vp, vp, i64, vp, vp, vp, i64, vp, i64, i64, vp]
             _lib = L
     return _lib
 
@@ -284,6 +287,48 @@ def srelu_quant_mx(y_bits: np.ndarray, expert_offsets: np.ndarray, sf_padded_off
     return q, sf
 
 
+def quant_mxfp8_rows(y_bits: np.ndarray, expert_offsets: np.ndarray, sf_padded_offsets: np.ndarray):
+    """bf16 rows [R, I] -> e4m3 [R, I] + E8M0 rowwise factors padded per expert (no activation)."""
+    y = np.ascontiguousarray(y_bits, dtype=np.uint16)
+    R, I = y.shape
+    E = len(expert_offsets) - 1
+    eoff = np.ascontiguousarray(expert_offsets, dtype=np.int32)
+    soff = np.ascontiguousarray(sf_padded_offsets, dtype=np.int32)
+    ld = mx_sf_ld(I)
+    q = np.zeros((R, I), dtype=np.uint8)
+    sf = np.zeros((int(soff[E]), ld), dtype=np.uint8)
+    lib().orc_quant_mxfp8_rows(_p(y), R, I, I, _p(eoff), _p(soff), E, _p(q), _p(sf), ld)
+    return q, sf
+
+
+def mx_colwise_sf_shape(R: int, C: int):
+    """Columnwise factor shape: ceil(R/32) blocks padded to a multiple of 4, C padded to 128."""
+    return ((R + 31) // 32 + 3) // 4 * 4, (C + 127) // 128 * 128
+
+
+def quant_mxfp8_cols(x_bits: np.ndarray):
+    """bf16 [R, C] -> e4m3 [R, C] quantised in 32x1 column blocks + E8M0 factors."""
+    x = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    R, C = x.shape
+    sr, sc = mx_colwise_sf_shape(R, C)
+    q = np.zeros((R, C), dtype=np.uint8)
+    sf = np.zeros((sr, sc), dtype=np.uint8)
+    lib().orc_quant_mxfp8_cols_bf16(_p(x), R, C, C, _p(q), _p(sf), sr, sc)
+    return q, sf
+
+
+def quant_rows_mxfp8_f32(w: np.ndarray):
+    """fp32 [..., C] rows -> e4m3 codes (same shape) + E8M0 [rows, mx_sf_ld(C)]."""
+    w = np.ascontiguousarray(w, dtype=np.float32)
+    C = w.shape[-1]
+    R = w.size // C
+    ld = mx_sf_ld(C)
+    q = np.zeros(w.shape, dtype=np.uint8)
+    sf = np.zeros((R, ld), dtype=np.uint8)
+    lib().orc_quant_rows_mxfp8_f32(_p(w), R, C, _p(q), _p(sf), ld)
+    return q, sf
+
+
 def router_topk(logits: np.ndarray, k: int):
     """fp32 logits [M, E] -> (topk_ids int32 [M, k], topk_weights fp32 [M, k])."""
     l = np.ascontiguousarray(logits, dtype=np.float32)
@@ -296,7 +341,7 @@ def router_topk(logits: np.ndarray, k: int):
 
 # ------------------------------------------------------------------- GEMM ---
 def moe_gemm_slots(*, a_kind, a, a_scale=None, a_sf=None, a_sf_row=None, w_kind, w, w_scale,
-                   topk_ids, topk_w, a_row, slots, N, K):
+                   topk_ids, topk_w, a_row, slots, N, K, w_sf=None):
     """Per-slot result [len(slots), N] in fp64 (see orc_moe_gemm)."""
     a = np.ascontiguousarray(a)
     lda = a.shape[-1]
@@ -309,10 +354,12 @@ def moe_gemm_slots(*, a_kind, a, a_scale=None, a_sf=None, a_sf_row=None, w_kind,
     a_sf_ld = 0 if a_sf is None else a_sf.shape[-1]
     a_sf_row = None if a_sf_row is None else np.ascontiguousarray(a_sf_row, dtype=np.int64)
     w = np.ascontiguousarray(w)
-    w_scale = np.ascontiguousarray(w_scale, dtype=np.float32)
+    w_scale = None if w_scale is None else np.ascontiguousarray(w_scale, dtype=np.float32)
+    w_sf = None if w_sf is None else np.ascontiguousarray(w_sf, dtype=np.uint8)
+    w_sf_ld = 0 if w_sf is None else w_sf.shape[-1]
     out = np.empty((slots.size, N), dtype=np.float64)
     lib().orc_moe_gemm(int(a_kind), _p(a), lda, _p(a_scale), _p(a_sf), a_sf_ld, _p(a_sf_row),
-                       int(w_kind), _p(w), _p(w_scale), _p(ids), _p(tw),
+                       int(w_kind), _p(w), _p(w_scale), _p(w_sf), w_sf_ld, _p(ids), _p(tw),
                        _p(slots), slots.size, _p(a_row), int(N), int(K), _p(out))
     return out
 
@@ -340,7 +387,7 @@ def padded_row_of_slot(topk_ids: np.ndarray, E: int, BM: int) -> np.ndarray:
 
 
 def moe_gemm(*, a_kind, a, a_scale=None, a_sf=None, a_sf_row=None, w_kind, w, w_scale,
-             topk_ids, topk_w, E, a_layout="token", out_layout="slot", slots=None, BM=None):
+             topk_ids, topk_w, E, a_layout="token", out_layout="slot", slots=None, BM=None, w_sf=None):
     """Whole grouped GEMM in fp64 with the requested layouts.
 
     a_layout "token": A row of slot s is s // top_k; "grouped": A row of slot
@@ -365,7 +412,7 @@ def moe_gemm(*, a_kind, a, a_scale=None, a_sf=None, a_sf_row=None, w_kind, w, w_
     sl = np.arange(T, dtype=np.int64) if slots is None else np.asarray(slots, dtype=np.int64)
     res = moe_gemm_slots(a_kind=a_kind, a=a, a_scale=a_scale, a_sf=a_sf, a_sf_row=a_sf_row,
                          w_kind=w_kind, w=w, w_scale=w_scale, topk_ids=ids, topk_w=topk_w,
-                         a_row=a_row, slots=sl, N=N, K=K)
+                         a_row=a_row, slots=sl, N=N, K=K, w_sf=w_sf)
     if slots is not None:
         return res
     if out_layout == "slot":

@@ -291,8 +291,9 @@ float orc_srelu_f32(float x) { return (x > 0.0f) ? x * x : 0.0f; }
  * columns); act 1: SReLU of a plain row y[I]. */
 static void act_row(int act, const uint16_t* yr, int64_t I, float* h) {
     for (int64_t i = 0; i < I; ++i)
-        h[i] = (act == 0) ? orc_silu_mul_f32(orc_bf16_to_f32(yr[i]), orc_bf16_to_f32(yr[I + i]))
-                          : orc_srelu_f32(orc_bf16_to_f32(yr[i]));
+        h[i] = (act == 0)   ? orc_silu_mul_f32(orc_bf16_to_f32(yr[i]), orc_bf16_to_f32(yr[I + i]))
+               : (act == 1) ? orc_srelu_f32(orc_bf16_to_f32(yr[i]))
+                            : orc_bf16_to_f32(yr[i]);  /* act 2: no activation (plain MXFP8 input) */
 }
 
 /* activation + per-token requantisation: h -> row amax -> scale -> e4m3(h/scale). */
@@ -364,6 +365,65 @@ void orc_srelu_quant_mx(const uint16_t* y, int64_t R, int64_t I, int64_t ldy,
     act_quant_mx(1, y, R, I, ldy, expert_offsets, sf_padded_offsets, E, q, sf, sf_ld);
 }
 
+/* Plain MXFP8 quantisation of bf16 rows ("MXFP8 input" of "[PyTorch] Let
+ * GroupedLinear accept MXFP8 input and gradient"): the MX rows above with no
+ * activation, rowwise factors padded per expert to 128 rows. */
+void orc_quant_mxfp8_rows(const uint16_t* y, int64_t R, int64_t I, int64_t ldy,
+                          const int32_t* expert_offsets, const int32_t* sf_padded_offsets, int32_t E,
+                          uint8_t* q, uint8_t* sf, int64_t sf_ld) {
+    act_quant_mx(2, y, R, I, ldy, expert_offsets, sf_padded_offsets, E, q, sf, sf_ld);
+}
+
+/* Columnwise MXFP8 (the colwise scaling factors of the same page, Description:
+ * a [128, 128] tensor has colwise factors [4, 128]; a [64, 128] one [4, 128],
+ * its two blocks of rows padded to 4): in each column, blocks of 32
+ * consecutive rows (the last block holds the rows that are left); per block
+ * the MX rule on its amax gives e, the byte e + 127 goes to sf[rb * sf_ld + c]
+ * and every element of the block becomes e4m3(x * 2^-e) in place.  sf has
+ * sf_rows >= ceil(R/32) rows of sf_ld >= C bytes; entries outside the blocks
+ * are zero. */
+void orc_quant_mxfp8_cols_bf16(const uint16_t* x, int64_t R, int64_t C, int64_t ldx, uint8_t* q,
+                               uint8_t* sf, int64_t sf_rows, int64_t sf_ld) {
+    memset(sf, 0, (size_t)sf_rows * (size_t)sf_ld);
+    int64_t nrb = (R + 31) / 32;
+#pragma omp parallel for schedule(static)
+    for (int64_t c = 0; c < C; ++c) {
+        for (int64_t rb = 0; rb < nrb; ++rb) {
+            int64_t r1 = (rb + 1) * 32 < R ? (rb + 1) * 32 : R;
+            float amax = 0.0f;
+            for (int64_t r = rb * 32; r < r1; ++r) {
+                float a = fabsf(orc_bf16_to_f32(x[r * ldx + c]));
+                if (a > amax) amax = a;
+            }
+            int ex = orc_mx_scale_exponent(amax);
+            sf[rb * sf_ld + c] = (uint8_t)(ex + 127);
+            float mul = ldexpf(1.0f, -ex);
+            for (int64_t r = rb * 32; r < r1; ++r) q[r * C + c] = orc_e4m3_from_f32(orc_bf16_to_f32(x[r * ldx + c]) * mul);
+        }
+    }
+}
+
+/* MXFP8 weights: each of the R rows of C values (R = E*N weight rows, C = K)
+ * in 1x32 blocks along the row with the same rule; sf[row * sf_ld + c/32],
+ * columns past C/32 zero.  C is a multiple of 32. */
+void orc_quant_rows_mxfp8_f32(const float* w, int64_t R, int64_t C, uint8_t* q, uint8_t* sf, int64_t sf_ld) {
+    memset(sf, 0, (size_t)R * (size_t)sf_ld);
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < R; ++r) {
+        for (int64_t b = 0; b < C / 32; ++b) {
+            float amax = 0.0f;
+            for (int64_t k = 0; k < 32; ++k) {
+                float a = fabsf(w[r * C + b * 32 + k]);
+                if (a > amax) amax = a;
+            }
+            int ex = orc_mx_scale_exponent(amax);
+            sf[r * sf_ld + b] = (uint8_t)(ex + 127);
+            float mul = ldexpf(1.0f, -ex);
+            for (int64_t k = 0; k < 32; ++k) q[r * C + b * 32 + k] = orc_e4m3_from_f32(w[r * C + b * 32 + k] * mul);
+        }
+    }
+}
+
 /* ------------------------------------------------------------------------- */
 /* Router: softmax over the E logits of a token -> top-k -> renormalise (the  */
 /* router sits in front of the grouped GEMM; the "top_k" column of the        */
@@ -411,11 +471,14 @@ void orc_router_topk(const float* logits, int64_t M, int32_t E, int32_t k, int32
 /* a_kind 1: e4m3 codes with E8M0 scales per 1x32 block,                       */
 /*           a_sf[a_sf_row[row] * a_sf_ld + k/32];                             */
 /* a_kind 2: bf16 bit patterns (exact).                                        */
-/* w_kind 0: e4m3 codes, w_kind 1: int8; both times w_scale[e*N + n].          */
+/* w_kind 0: e4m3 codes, w_kind 1: int8; both times w_scale[e*N + n];         */
+/* w_kind 2: e4m3 codes with E8M0 scales per 1x32 block along K,               */
+/*           w_sf[(e*N + n) * w_sf_ld + k/32] (times w_scale[e*N + n] if given).*/
 /* ------------------------------------------------------------------------- */
 void orc_moe_gemm(int a_kind, const void* a, int64_t lda, const float* a_scale,
                   const uint8_t* a_sf, int64_t a_sf_ld, const int64_t* a_sf_row,
                   int w_kind, const void* w, const float* w_scale,
+                  const uint8_t* w_sf, int64_t w_sf_ld,
                   const int32_t* topk_ids, const float* topk_w,
                   const int64_t* slots, int64_t n_slots, const int64_t* a_row,
                   int64_t N, int64_t K, double* out) {
@@ -440,11 +503,15 @@ void orc_moe_gemm(int a_kind, const void* a, int64_t lda, const float* a_scale,
         double ws = topk_w ? (double)topk_w[s] : 1.0;
         for (int64_t n = 0; n < N; ++n) {
             const int64_t wrow = ((int64_t)e * N + n) * K;
-            const double sw = (double)w_scale[(int64_t)e * N + n];
+            const double sw = w_scale ? (double)w_scale[(int64_t)e * N + n] : 1.0;
             double acc = 0.0;
             if (w_kind == 0) {
                 const uint8_t* wq = (const uint8_t*)w + wrow;
                 for (int64_t k = 0; k < K; ++k) acc += arow[k] * (lut[wq[k]] * sw);
+            } else if (w_kind == 2) {
+                const uint8_t* wq = (const uint8_t*)w + wrow;
+                const uint8_t* ws = w_sf + ((int64_t)e * N + n) * w_sf_ld;
+                for (int64_t k = 0; k < K; ++k) acc += arow[k] * (lut[wq[k]] * orc_e8m0_to_f64(ws[k / 32]) * sw);
             } else {
                 const int8_t* wq = (const int8_t*)w + wrow;
                 for (int64_t k = 0; k < K; ++k) acc += arow[k] * ((double)wq[k] * sw);
