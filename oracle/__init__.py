@@ -92,6 +92,7 @@ def lib():
             L.orc_quant_mxfp8_rows.argtypes = [vp, i64, i64, i64, vp, vp, i32, vp, vp, i64]
             L.orc_quant_mxfp8_cols_bf16.argtypes = [vp, i64, i64, i64, vp, vp, i64, i64]
             L.orc_quant_rows_mxfp8_f32.argtypes = [vp, i64, i64, vp, vp, i64]
+            L.orc_mx_weight_sf_tiled.argtypes = [vp, i64, i64, i64, i64, vp]
             L.orc_router_topk.argtypes = [vp, i64, i32, i32, vp, vp]
             L.orc_srelu_f32.argtypes = [ctypes.c_float]
             L.orc_srelu_f32.restype = ctypes.c_float
@@ -327,6 +328,15 @@ def quant_rows_mxfp8_f32(w: np.ndarray):
     sf = np.zeros((R, ld), dtype=np.uint8)
     lib().orc_quant_rows_mxfp8_f32(_p(w), R, C, _p(q), _p(sf), ld)
     return q, sf
+
+
+def mx_weight_sf_tiled(sf: np.ndarray, E: int, N: int, K: int):
+    """E8M0 weight factors [E*N, ld] -> the GEMM's tiled blocks (uint8, flat)."""
+    sf = np.ascontiguousarray(sf, dtype=np.uint8)
+    nb, kb = (N + 255) // 256, (K + 127) // 128
+    out = np.zeros(E * nb * kb * 1024, dtype=np.uint8)
+    lib().orc_mx_weight_sf_tiled(_p(sf), E, N, K, sf.shape[-1], _p(out))
+    return out
 
 
 def router_topk(logits: np.ndarray, k: int):

@@ -424,6 +424,30 @@ void orc_quant_rows_mxfp8_f32(const float* w, int64_t R, int64_t C, uint8_t* q, 
     }
 }
 
+/* MXFP8 weight factors in the tiled order the grouped GEMM reads (one
+ * contiguous 1024-byte block per 256 weight rows x 128 K columns): block
+ * ((e * NB + nb) * KB + kb) * 1024 with NB = ceil(N/256), KB = ceil(K/128);
+ * inside it byte h*512 + i*16 + c*4 + b holds the factor of weight row
+ * nb*256 + h*128 + 32c + i (h in 0..1, i in 0..31, c in 0..3) for K block
+ * 4kb + b (b in 0..3), and 127 (2^0) for rows at or past N.  sf is
+ * [E*N, sf_ld] with sf_ld >= 4*KB. */
+void orc_mx_weight_sf_tiled(const uint8_t* sf, int64_t E, int64_t N, int64_t K, int64_t sf_ld, uint8_t* out) {
+    const int64_t NB = (N + 255) / 256, KB = (K + 127) / 128;
+    for (int64_t e = 0; e < E; ++e)
+        for (int64_t nb = 0; nb < NB; ++nb)
+            for (int64_t kb = 0; kb < KB; ++kb) {
+                uint8_t* blk = out + ((e * NB + nb) * KB + kb) * 1024;
+                for (int h = 0; h < 2; ++h)
+                    for (int i = 0; i < 32; ++i)
+                        for (int c = 0; c < 4; ++c)
+                            for (int b = 0; b < 4; ++b) {
+                                const int64_t n = nb * 256 + h * 128 + 32 * c + i;
+                                blk[h * 512 + i * 16 + c * 4 + b] =
+                                    (n < N) ? sf[(e * N + n) * sf_ld + 4 * kb + b] : (uint8_t)127;
+                            }
+            }
+}
+
 /* ------------------------------------------------------------------------- */
 /* Router: softmax over the E logits of a token -> top-k -> renormalise (the  */
 /* router sits in front of the grouped GEMM; the "top_k" column of the        */

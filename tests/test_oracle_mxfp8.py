@@ -119,3 +119,17 @@ def test_gemm_mx_weights_vs_bruteforce(orc):
     assert np.allclose(out, ref.reshape(M, top_k, N).sum(axis=1), rtol=1e-12, atol=1e-12)
     # and the reconstruction error of the MX weights is within e4m3's half-ulp bound per block
     assert np.all(np.abs(W - w.astype(np.float64)) <= np.abs(w) * 2.0 ** -4 + 2.0 ** -9 * np.abs(W).max())
+
+
+@pytest.mark.parametrize("E,N,K", [(2, 256, 128), (3, 300, 416), (1, 16, 32)])
+def test_weight_sf_tiling_is_a_permutation_with_2pow0_padding(orc, E, N, K):
+    """Undo the tiling with array reshapes (blocks [E][NB][KB][h][i][c][b]) and
+    recover the natural factors; rows past N hold 127 (2^0)."""
+    ld = (K // 32 + 3) // 4 * 4
+    sf = np.random.default_rng(E * N + K).integers(0, 255, size=(E * N, ld), dtype=np.uint8)
+    t = orc.mx_weight_sf_tiled(sf, E, N, K)
+    NB, KB = -(-N // 256), -(-K // 128)
+    v = t.reshape(E, NB, KB, 2, 32, 4, 4).transpose(0, 1, 3, 5, 4, 2, 6)   # e nb h c i kb b
+    nat = v.reshape(E, NB * 256, KB * 4)
+    assert np.array_equal(nat[:, :N, :], sf.reshape(E, N, ld)[:, :, : KB * 4])
+    assert np.all(nat[:, N:, :] == 127)
