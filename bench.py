@@ -379,7 +379,15 @@ def run_suite(reps: int = 20, only: str | None = None) -> None:
                         reps, flush)
             line("activation + MXFP8 8x4000x4096", name, ms, rows * width * 2 + rows * I + 8 * 4096 * (I // 32), 0,
                  "fp8")
-        del y
+        # plain MXFP8 input (rowwise, per-expert padded factors) and columnwise factors
+        xq, xsf = q.quant_mxfp8(y, expert_offsets=eoff, sf_padded_offsets=soff, sf_rows=8 * 4096)
+        ms = _timed(lambda: q.quant_mxfp8(y, expert_offsets=eoff, sf_padded_offsets=soff, q=xq, sf=xsf), reps, flush)
+        line("MXFP8 quantisation 8x4000x4096", "quant_mxfp8 rowwise", ms, rows * width * 3 + 8 * 4096 * (width // 32),
+             0, "fp8")
+        cq, csf = q.quant_mxfp8_colwise(y)
+        ms = _timed(lambda: q.quant_mxfp8_colwise(y, q=cq, sf=csf), reps, flush)
+        line("MXFP8 quantisation 8x4000x4096", "quant_mxfp8_colwise", ms, rows * width * 3 + csf.numel(), 0, "fp8")
+        del y, xq, cq
 
     # Router front: fp32 logits [M, 8] -> top-2 -> align -> sorted e4m3 rows,
     # fused into one launch at decode sizes, against the separate launches.
@@ -459,6 +467,21 @@ def run_suite(reps: int = 20, only: str | None = None) -> None:
             line(wl.name, "moe_gemm_w8a8 down mxfp8 (grouped A -> token sum)", ms,
                  hit * Nd * I + hit * Nd * 4 + T * (I + I // 32) + T * 8 + M * Nd * 2, 2.0 * T * I * Nd, "fp8")
             del w2q, w2s
+            # the same down projection with MXFP8 weights too (both operands block-scaled)
+            w2mq = torch.empty(E, Nd, I, dtype=torch.uint8, device=dev)
+            w2msf = torch.empty(E * Nd, q.mx_sf_ld(I), dtype=torch.uint8, device=dev)
+            for e in range(E):
+                w = torch.randn(Nd, I, device=dev) * (1.0 / np.sqrt(I))
+                q.quant_weight_mxfp8(w, q=w2mq[e], sf=w2msf[e * Nd:(e + 1) * Nd])
+            w2mt = q.mx_weight_sf_tiled(w2msf, E, Nd, I)
+            ms = _timed(lambda: q.moe_gemm_w8a8(hq, None, w2mq, None, al, twd, M=M, top_k=TOP_K, BM=BM,
+                                                a_layout=q.A_GROUPED, out_layout=q.OUT_TOKEN_SUM, out=out,
+                                                accum=acc, a_scale_mode=q.SCALE_MX_1X32, a_sf=sf,
+                                                a_sf_padded_offsets=al["padded_offsets"],
+                                                w_scale_mode=q.SCALE_MX_1X32, w_sf=w2mt), reps, flush)
+            line(wl.name, "moe_gemm_w8a8 down, MXFP8 activations and weights (token sum)", ms,
+                 hit * Nd * I + hit * Nd * (I // 32) + T * (I + I // 32) + T * 8 + M * Nd * 2, 2.0 * T * I * Nd, "fp8")
+            del w2mq, w2msf, w2mt
         del up
 
 

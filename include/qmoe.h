@@ -56,6 +56,7 @@ typedef enum {
 /* activation scale modes */
 #define QMOE_SCALE_PER_TOKEN 0 /* one fp32 scale per A row */
 #define QMOE_SCALE_MX_1X32 1   /* one E8M0 byte per 32 elements along K */
+#define QMOE_SCALE_PER_ROW 0   /* weights: one fp32 scale per output channel */
 /* A row layouts */
 #define QMOE_A_TOKEN_GATHER 0 /* slot s reads A row s / top_k ([M, K])        */
 #define QMOE_A_GROUPED 1      /* slot s reads its compact expert-grouped row ([T, K]) */
@@ -185,6 +186,54 @@ qmoe_status_t qmoe_quant_weight_fp8(const float* w, int64_t rows, int64_t cols,
 qmoe_status_t qmoe_quant_weight_int8(const float* w, int64_t rows, int64_t cols,
                                      int8_t* q, float* scale, qmoe_stream_t stream);
 
+/* MXFP8 weights ("[PyTorch] Let GroupedLinear accept MXFP8 input and
+ * gradient", Description: block-scaled operands): every row of fp32 W
+ * (rows = E*N, cols = K, K % 32 == 0) in 1x32 blocks along K; per block
+ * e = the smallest integer with 448 * 2^e >= amax (clamped to [-127, 127];
+ * 0 for an all-zero block), byte e + 127 at sf[row * sf_ld + k/32], codes
+ * e4m3(w * 2^-e).  sf_ld >= roundup(K/32, 4); the columns past K/32 are
+ * written as zero.  q [rows, K] e4m3, 16-byte aligned; w 16-byte aligned. */
+qmoe_status_t qmoe_quant_weight_mxfp8(const float* w, int64_t rows, int64_t cols, uint8_t* q, uint8_t* sf,
+                                      int64_t sf_ld, qmoe_stream_t stream);
+
+/* Plain MXFP8 quantisation of bf16 rows (the "MXFP8 input" of the same page,
+ * quantised as one concatenated tensor): the rowwise rule of
+ * qmoe_quant_weight_mxfp8 on x [rows, I] (I % 32 == 0, ldx >= I, ldx % 8 == 0)
+ * with the per-expert scale-factor layout of qmoe_silu_mul_quant's MX mode:
+ * row r of expert e has its factors at sf row sf_padded_offsets[e] + (r -
+ * expert_offsets[e]), each expert's block padded with zero rows to
+ * sf_padded_offsets[e+1], row stride sf_ld >= roundup(I/32, 4) (pad columns
+ * zero).  q [rows, I]. */
+qmoe_status_t qmoe_quant_mxfp8(const uint16_t* x, int64_t rows, int64_t I, int64_t ldx, uint8_t* q, uint8_t* sf,
+                               int64_t sf_ld, const int32_t* expert_offsets, const int32_t* sf_padded_offsets,
+                               int32_t E, int32_t* d_status, qmoe_stream_t stream);
+
+/* Columnwise MXFP8 (the colwise scaling factors of the same page: a [128,
+ * 128] tensor has colwise factors of shape [4, 128]): in every column, blocks
+ * of 32 consecutive rows (the last block holds the rows that are left) with
+ * the same rule; factor of block rb of column c at sf[rb * sf_ld + c], codes
+ * q[r * cols + c] = e4m3(x[r, c] * 2^-e) (same shape as x).  sf_rows >=
+ * ceil(rows/32) and sf_ld >= cols; every factor outside the blocks is written
+ * as zero (the page pads the block rows to a multiple of 4). */
+qmoe_status_t qmoe_quant_mxfp8_colwise(const uint16_t* x, int64_t rows, int64_t cols, int64_t ldx, uint8_t* q,
+                                       uint8_t* sf, int64_t sf_rows, int64_t sf_ld, qmoe_stream_t stream);
+
+/* MXFP8 weight factors rearranged, once per weight matrix, into the order the
+ * grouped GEMM streams them: one contiguous 1024-byte block per 256 weight
+ * rows x 128 K columns, block ((e * NB + nb) * KB + kb) * 1024 with
+ * NB = ceil(N/256), KB = ceil(K/128); inside a block, byte
+ * h*512 + i*16 + c*4 + b is the factor of weight row nb*256 + h*128 + 32c + i
+ * (h < 2, i < 32, c < 4) for K block 4kb + b (b < 4), and 127 (2^0) for rows
+ * at or past N.  Each 512-byte half is the 32 x 16-byte matrix that
+ * tcgen05.cp 32x128b.warpx4 copies into TMEM for the block-scaled MMA, so the
+ * GEMM moves a stage's weight factors with one bulk copy.
+ *   sf: [E*N, sf_ld] from qmoe_quant_weight_mxfp8 (sf_ld >= 4*KB, a multiple
+ *   of 4, 4-byte aligned); out: qmoe_mx_weight_sf_tiled_bytes(E, N, K) bytes,
+ *   16-byte aligned.  K % 32 == 0. */
+int64_t qmoe_mx_weight_sf_tiled_bytes(int64_t E, int64_t N, int64_t K);
+qmoe_status_t qmoe_mx_weight_sf_tiled(const uint8_t* sf, int64_t E, int64_t N, int64_t K, int64_t sf_ld, uint8_t* out,
+                                      qmoe_stream_t stream);
+
 /* ------------------------------------------------------------------------ */
 /* grouped GEMM                                                             */
 /* ------------------------------------------------------------------------ */
@@ -219,6 +268,14 @@ typedef struct {
      * aligned).  The library zeroes it, adds every routed slot result into it
      * in fp32, and writes out = bf16(accum) with a second launch. */
     float* accum;
+    /* Weight scales.  QMOE_SCALE_PER_ROW (0): w_scale [E, N] fp32 per output
+     * channel.  QMOE_SCALE_MX_1X32: MXFP8 weights (qmoe_quant_weight_mxfp8);
+     * w_sf holds their E8M0 factors in the tiled order of
+     * qmoe_mx_weight_sf_tiled (16-byte aligned); w_scale is then optional (an
+     * extra fp32 factor per output channel, or NULL).  FP8 GEMM with MX
+     * activations only. */
+    int32_t w_scale_mode;
+    const uint8_t* w_sf;
 } qmoe_gemm_args;
 
 /* FP8 W8A8 grouped GEMM (tables "FP8_W8A8 Benchmark" / "Model Results" of
@@ -238,7 +295,10 @@ typedef struct {
  * expert_offsets[e]), one byte per 32 elements along K (row stride a_sf_ld, a
  * multiple of 4 and >= roundup(K/32, 4)); a_scale is unused.  The scales are
  * applied inside the tensor-core MMA (block-scaled kind::mxf8f6f4).  Needs
- * K % 32 == 0 and BM >= 128 (else QMOE_ERR_UNSUPPORTED). */
+ * K % 32 == 0 and BM >= 128 (else QMOE_ERR_UNSUPPORTED).  With MX activations
+ * the weights may be MXFP8 too (w_scale_mode QMOE_SCALE_MX_1X32): both
+ * operands then carry their block scales into the MMA; MX weights with
+ * per-token activations return QMOE_ERR_UNSUPPORTED. */
 qmoe_status_t qmoe_moe_gemm_w8a8(const qmoe_gemm_args* args, qmoe_stream_t stream);
 
 /* FP8 W8A8 grouped GEMM with the TOKEN_SUM layout that allocates nothing.

@@ -32,7 +32,8 @@ EXPORTED = (
     "qmoe_quant_act_fp8", "qmoe_quant_act_fp8_sorted", "qmoe_moe_align_quant_fp8", "qmoe_moe_router_topk", "qmoe_moe_route_align_quant_fp8", "qmoe_gather_sorted_bf16", "qmoe_quant_weight_fp8", "qmoe_quant_weight_int8", "qmoe_moe_gemm_w8a8",
     "qmoe_moe_gemm_w8a16", "qmoe_silu_mul_quant", "qmoe_srelu_quant", "qmoe_debug_e4m3_encode", "qmoe_debug_int8_to_bf16",
     "qmoe_debug_silu_mul", "qmoe_debug_div_by_scale", "qmoe_debug_wait_timeout",
-    "qmoe_moe_gemm_w8a8_token_sum_noalloc",
+    "qmoe_moe_gemm_w8a8_token_sum_noalloc", "qmoe_quant_weight_mxfp8", "qmoe_quant_mxfp8", "qmoe_quant_mxfp8_colwise",
+    "qmoe_mx_weight_sf_tiled_bytes", "qmoe_mx_weight_sf_tiled",
 )
 NOALLOC_ACCUM_MAX_ELEMS = 4 << 20
 
@@ -56,6 +57,7 @@ class GemmArgs(ctypes.Structure):
         ("E", ctypes.c_int32), ("top_k", ctypes.c_int32), ("BM", ctypes.c_int32),
         ("d_status", ctypes.c_void_p),
         ("accum", ctypes.c_void_p),
+        ("w_scale_mode", ctypes.c_int32), ("w_sf", ctypes.c_void_p),
     ]
 
 
@@ -81,6 +83,12 @@ def load_library(path: str | None = None):
             L.qmoe_moe_align_quant_fp8.argtypes = [vp, i64, i64, i64, vp, i32, i32, i32, vp, vp, vp, vp, vp, vp,
                                                    vp, vp, vp]
             L.qmoe_moe_router_topk.argtypes = [vp, i64, i32, i32, vp, vp, vp]
+            L.qmoe_quant_weight_mxfp8.argtypes = [vp, i64, i64, vp, vp, i64, vp]
+            L.qmoe_quant_mxfp8.argtypes = [vp, i64, i64, i64, vp, vp, i64, vp, vp, i32, vp, vp]
+            L.qmoe_quant_mxfp8_colwise.argtypes = [vp, i64, i64, i64, vp, vp, i64, i64, vp]
+            L.qmoe_mx_weight_sf_tiled_bytes.argtypes = [i64, i64, i64]
+            L.qmoe_mx_weight_sf_tiled_bytes.restype = i64
+            L.qmoe_mx_weight_sf_tiled.argtypes = [vp, i64, i64, i64, i64, vp, vp]
             L.qmoe_moe_route_align_quant_fp8.argtypes = [vp, vp, i64, i64, i64, i32, i32, i32, vp, vp, vp, vp, vp,
                                                          vp, vp, vp, vp, vp, vp]
             L.qmoe_gather_sorted_bf16.argtypes = [vp, i64, i64, i64, vp, vp, i32, i64, vp, vp]
@@ -280,10 +288,73 @@ def quant_weight_int8(w: torch.Tensor, stream=None):
     return q, s
 
 
+def quant_weight_mxfp8(w: torch.Tensor, q=None, sf=None, stream=None):
+    """fp32 [..., K] weight rows -> (e4m3 codes uint8 same shape, E8M0 [rows, roundup(K/32, 4)])."""
+    _need(w, torch.float32, "w")
+    K = w.shape[-1]
+    rows = w.numel() // K
+    q = q if q is not None else torch.empty(w.shape, dtype=torch.uint8, device=w.device)
+    sf = sf if sf is not None else torch.empty(rows, mx_sf_ld(K), dtype=torch.uint8, device=w.device)
+    _check(load_library().qmoe_quant_weight_mxfp8(_ptr(w), rows, K, _ptr(q), _ptr(sf), sf.stride(0),
+                                                  _stream(stream)), "quant_weight_mxfp8")
+    return q, sf
+
+
+def quant_mxfp8(x: torch.Tensor, *, expert_offsets, sf_padded_offsets, sf_rows: int | None = None, q=None, sf=None,
+                d_status=None, stream=None):
+    """bf16 [rows, I] -> (e4m3 [rows, I], E8M0 rowwise factors padded per expert), no activation."""
+    if not x.is_cuda or x.dtype != torch.bfloat16 or x.dim() != 2 or x.stride(1) != 1:
+        raise QmoeError("x must be a 2-D CUDA bf16 tensor with unit column stride")
+    _need(expert_offsets, torch.int32, "expert_offsets")
+    _need(sf_padded_offsets, torch.int32, "sf_padded_offsets")
+    rows, I = x.shape
+    q = q if q is not None else torch.empty(rows, I, dtype=torch.uint8, device=x.device)
+    if sf is None:
+        if sf_rows is None:
+            raise QmoeError("sf_rows (capacity of the scale-factor matrix) is required when sf is not given")
+        sf = torch.empty(sf_rows, mx_sf_ld(I), dtype=torch.uint8, device=x.device)
+    st = load_library().qmoe_quant_mxfp8(_ptr(x), rows, I, x.stride(0), _ptr(q), _ptr(sf), sf.stride(0),
+                                         _ptr(expert_offsets), _ptr(sf_padded_offsets), expert_offsets.numel() - 1,
+                                         _ptr(d_status), _stream(stream))
+    _check(st, "quant_mxfp8")
+    return q, sf
+
+
+def mx_weight_sf_tiled(sf: torch.Tensor, E: int, N: int, K: int, out=None, stream=None):
+    """E8M0 weight factors [E*N, ld] -> the flat uint8 tiled blocks moe_gemm_w8a8 streams."""
+    _need(sf, torch.uint8, "sf")
+    L = load_library()
+    nbytes = int(L.qmoe_mx_weight_sf_tiled_bytes(E, N, K))
+    out = out if out is not None else torch.empty(nbytes, dtype=torch.uint8, device=sf.device)
+    _check(L.qmoe_mx_weight_sf_tiled(_ptr(sf), E, N, K, sf.stride(0), _ptr(out), _stream(stream)),
+           "mx_weight_sf_tiled")
+    return out
+
+
+def mx_colwise_sf_shape(rows: int, cols: int):
+    """ceil(rows/32) blocks padded to a multiple of 4 rows, columns padded to 128."""
+    return ((rows + 31) // 32 + 3) // 4 * 4, (cols + 127) // 128 * 128
+
+
+def quant_mxfp8_colwise(x: torch.Tensor, q=None, sf=None, stream=None):
+    """bf16 [rows, cols] -> (e4m3 [rows, cols] in 32x1 column blocks, E8M0 [mx_colwise_sf_shape])."""
+    if not x.is_cuda or x.dtype != torch.bfloat16 or x.dim() != 2 or x.stride(1) != 1:
+        raise QmoeError("x must be a 2-D CUDA bf16 tensor with unit column stride")
+    rows, cols = x.shape
+    q = q if q is not None else torch.empty(rows, cols, dtype=torch.uint8, device=x.device)
+    if sf is None:
+        sr, sc = mx_colwise_sf_shape(rows, cols)
+        sf = torch.empty(sr, sc, dtype=torch.uint8, device=x.device)
+    st = load_library().qmoe_quant_mxfp8_colwise(_ptr(x), rows, cols, x.stride(0), _ptr(q), _ptr(sf), sf.shape[0],
+                                                 sf.stride(0), _stream(stream))
+    _check(st, "quant_mxfp8_colwise")
+    return q, sf
+
+
 # ------------------------------------------------------------------ GEMM ---
 def _gemm(fn_name, *, a, a_scale, w, w_scale, align, topk_weights, out, M, top_k, BM, a_layout, out_layout,
           a_scale_mode=SCALE_PER_TOKEN, a_sf=None, a_sf_padded_offsets=None, d_status=None, accum=None,
-          stream=None):
+          stream=None, w_scale_mode=0, w_sf=None):
     E, N, K = w.shape
     if out_layout == OUT_TOKEN_SUM and accum is None:
         accum = torch.empty(M, N, dtype=torch.float32, device=out.device)
@@ -298,7 +369,9 @@ def _gemm(fn_name, *, a, a_scale, w, w_scale, align, topk_weights, out, M, top_k
     args.a_sf_padded_offsets = None if a_sf_padded_offsets is None else a_sf_padded_offsets.data_ptr()
     args.a_layout = a_layout
     args.w = w.data_ptr()
-    args.w_scale = w_scale.data_ptr()
+    args.w_scale = None if w_scale is None else w_scale.data_ptr()
+    args.w_scale_mode = w_scale_mode
+    args.w_sf = None if w_sf is None else w_sf.data_ptr()
     args.sorted_ids = align["sorted_ids"].data_ptr()
     args.expert_ids = align["expert_ids"].data_ptr()
     args.num_post_padded = align["num_post_padded"].data_ptr()
@@ -328,12 +401,15 @@ def moe_gemm_w8a8(a_q: torch.Tensor, a_scale: torch.Tensor | None, w_q: torch.Te
                   a_layout: int = A_TOKEN_GATHER, out_layout: int = OUT_SLOT, out: torch.Tensor | None = None,
                   d_status: torch.Tensor | None = None, accum: torch.Tensor | None = None,
                   a_scale_mode: int = SCALE_PER_TOKEN, a_sf: torch.Tensor | None = None,
-                  a_sf_padded_offsets: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+                  a_sf_padded_offsets: torch.Tensor | None = None, w_scale_mode: int = SCALE_PER_TOKEN,
+                  w_sf: torch.Tensor | None = None, stream=None) -> torch.Tensor:
     """FP8 W8A8 grouped GEMM.  a_q uint8 e4m3 [rows, K] (token rows for TOKEN_GATHER,
     compact grouped rows for GROUPED), a_scale fp32 [rows], w_q uint8 e4m3 [E, N, K],
     w_scale fp32 [E, N], align = moe_align_block_size(..., BM), topk_weights fp32 [M, top_k]
     or None.  Returns bf16 [T, N] (SLOT/GROUPED) or [M, N] (TOKEN_SUM; accum is the
-    fp32 [M, N] scratch the sum needs, allocated here when not given)."""
+    fp32 [M, N] scratch the sum needs, allocated here when not given).  MXFP8 weights:
+    w_scale_mode=SCALE_MX_1X32 with w_sf = mx_weight_sf_tiled(factors of quant_weight_mxfp8),
+    w_scale then optional; needs MX activations."""
     _need(a_q, torch.uint8, "a_q")
     _need(w_q, torch.uint8, "w_q")
     if a_scale_mode == SCALE_PER_TOKEN:
@@ -341,14 +417,19 @@ def moe_gemm_w8a8(a_q: torch.Tensor, a_scale: torch.Tensor | None, w_q: torch.Te
     else:
         _need(a_sf, torch.uint8, "a_sf")
         _need(a_sf_padded_offsets, torch.int32, "a_sf_padded_offsets")
-    _need(w_scale, torch.float32, "w_scale")
+    if w_scale_mode == SCALE_MX_1X32:
+        _need(w_sf, torch.uint8, "w_sf")
+        if w_scale is not None:
+            _need(w_scale, torch.float32, "w_scale")
+    else:
+        _need(w_scale, torch.float32, "w_scale")
     if topk_weights is not None:
         _need(topk_weights, torch.float32, "topk_weights")
     out = _out_for(out, out_layout, M, top_k, w_q.shape[1], a_q.device)
     return _gemm("qmoe_moe_gemm_w8a8", a=a_q, a_scale=a_scale, w=w_q, w_scale=w_scale, align=align,
                  topk_weights=topk_weights, out=out, M=M, top_k=top_k, BM=BM, a_layout=a_layout,
                  out_layout=out_layout, d_status=d_status, accum=accum, a_scale_mode=a_scale_mode, a_sf=a_sf,
-                 a_sf_padded_offsets=a_sf_padded_offsets, stream=stream)
+                 a_sf_padded_offsets=a_sf_padded_offsets, stream=stream, w_scale_mode=w_scale_mode, w_sf=w_sf)
 
 
 def moe_gemm_w8a8_token_sum_noalloc(a_q: torch.Tensor, a_scale: torch.Tensor, w_q: torch.Tensor,

@@ -527,6 +527,12 @@ struct ActSReLU {
     }
 };
 
+// No activation: plain MXFP8 / per-token quantisation of bf16 rows.
+struct ActIdentity {
+    static constexpr bool kGated = false;
+    QMOE_DI static void apply8(const uint4 xw, const uint4, float (&h)[8]) { unpack8(xw, h); }
+};
+
 template <class Act>
 __global__ void __launch_bounds__(kRowThreads)
     act_quant_token_kernel(const uint16_t* __restrict__ y, int64_t I, int64_t ldy, uint8_t* __restrict__ q,
@@ -896,6 +902,13 @@ qmoe_status_t qmoe_srelu_quant(const uint16_t* y, int64_t rows, int64_t I, int64
                                qmoe_stream_t stream) {
     return run_act_quant<ActSReLU>(y, rows, I, ldy, mode, q, scale, sf, sf_ld, expert_offsets, sf_padded_offsets,
                                    E, d_status, stream);
+}
+
+qmoe_status_t qmoe_quant_mxfp8(const uint16_t* x, int64_t rows, int64_t I, int64_t ldx, uint8_t* q, uint8_t* sf,
+                               int64_t sf_ld, const int32_t* expert_offsets, const int32_t* sf_padded_offsets,
+                               int32_t E, int32_t* d_status, qmoe_stream_t stream) {
+    return run_act_quant<ActIdentity>(x, rows, I, ldx, QMOE_SCALE_MX_1X32, q, nullptr, sf, sf_ld, expert_offsets,
+                                      sf_padded_offsets, E, d_status, stream);
 }
 
 qmoe_status_t qmoe_debug_e4m3_encode(const float* x, uint8_t* q, int64_t n, qmoe_stream_t stream) {

@@ -64,6 +64,7 @@ struct GemmParams {
     const uint8_t* a_sf;         // MX: E8M0 scale rows of the grouped activations
     int64_t a_sf_ld;
     const int32_t* a_sf_poff;    // MX: first scale row of each expert
+    const uint8_t* w_sf;         // MX weights: E8M0 factors in 1 KB tiled blocks, or nullptr (2^0)
     int32_t num_k_blocks;
     int32_t* d_status;
 };
@@ -93,7 +94,11 @@ struct GemmCfg {
     static constexpr int kLag = kStages >= 6 ? 3 : (kStages >= 5 ? 2 : 1);
     static constexpr int kBProdThreads = 64;
     static constexpr int kEpiThreads = kMX ? 256 : 128;   // MX: two groups of four warps, one per column half
-    static constexpr int kSfBytes = 512;                   // MX: one stage's activation scales in shared memory
+    // MX: a stage's scales in shared memory, as 512-byte blocks of 32 x 16
+    // bytes: the 128 activation rows, then the two 128-row halves of the 256
+    // weight rows (MXFP8 weights only)
+    static constexpr int kSfBytes = 512;
+    static constexpr int kSfStageBytes = 3 * kSfBytes;
     // W8A16 converter group: 8 warps for the wide tile (256 weight rows per
     // stage), 4 for the swapped one; groups alternate stages
     static constexpr int kConvThreads = (kBF16 && kWide) ? 256 : 128;
@@ -111,9 +116,9 @@ struct GemmCfg {
     static constexpr uint32_t kIdesc =
         kMX ? make_idesc_mx(128, kMmaN) : make_idesc(kBF16 ? kFmtBF16 : kFmtE4M3, 128, kMmaN);
     static_assert(!kMX || (kWide && !kBF16), "MX scales: FP8 wide tile only");
-    static_assert(!kMX || kSfbCol + 8 <= 512, "TMEM columns");
+    static_assert(!kMX || kSfbCol + 8 * kStages <= 512, "TMEM columns");  // per-stage weight scales
     static constexpr int kDynSmem =
-        kStages * kStageBytes + kRawStages * kRawBytes + (kMX ? (kStages + 1) * kSfBytes : 0) + 1024;
+        kStages * kStageBytes + kRawStages * kRawBytes + (kMX ? kStages * kSfStageBytes + kSfBytes : 0) + 1024;
     static_assert(kStages >= 2, "need at least two pipeline stages");
     static_assert(!kBF16 || kRawStages >= 2, "need at least two raw weight stages");
     static_assert(kMmaN % 16 == 0 && kMmaN >= 16 && kMmaN <= 256, "MMA N must be a multiple of 16 in [16, 256]");
@@ -206,7 +211,7 @@ __global__ void __launch_bounds__(GemmCfg<kBF16, kWide, BN, kMX>::kThreads, 1)
     const int lane = threadIdx.x & 31;
     // MX scale staging: S stage buffers, then the constant weight-scale block
     auto sf_smem = [&](int s) {
-        return smem + S * C::kStageBytes + C::kRawStages * C::kRawBytes + s * C::kSfBytes;
+        return smem + S * C::kStageBytes + C::kRawStages * C::kRawBytes + s * C::kSfStageBytes;
     };
 
     if (threadIdx.x == 0) {
@@ -276,7 +281,8 @@ __global__ void __launch_bounds__(GemmCfg<kBF16, kWide, BN, kMX>::kThreads, 1)
         if (lane == 0) {
             int it = 0;
             bool ok = true;
-            const uint32_t tx = C::kWBytes + (p.a_tma ? C::kActBytes : 0);
+            // MXFP8 weights add the stage's 1 KB block of tiled weight factors
+            const uint32_t tx = C::kWBytes + (p.a_tma ? C::kActBytes : 0) + (kMX && p.w_sf ? 2 * C::kSfBytes : 0);
             for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
                 int sb, nb;
                 const int e = tile_expert(tile, sb, nb);
@@ -299,6 +305,10 @@ __global__ void __launch_bounds__(GemmCfg<kBF16, kWide, BN, kMX>::kThreads, 1)
                         mbar_arrive_expect_tx(&bar_full[s], tx);
                         tma_load_3d(&tmap_w, &bar_full[s], w_tile(s), kb * C::kBK, nb * WR, e);
                         if (p.a_tma) tma_load_2d(&tmap_a, &bar_full[s], act_tile(s), kb * C::kBK, arow0);
+                        if (kMX && p.w_sf)
+                            bulk_load(sf_smem(s) + C::kSfBytes,
+                                      p.w_sf + ((static_cast<int64_t>(e) * n_blocks + nb) * nkb + kb) * 2 * C::kSfBytes,
+                                      2 * C::kSfBytes, &bar_full[s]);
                     }
                 }
             }
@@ -312,7 +322,7 @@ __global__ void __launch_bounds__(GemmCfg<kBF16, kWide, BN, kMX>::kThreads, 1)
         if (lane == 0) {
             int it = 0, tcount = 0;
             bool ok = true;
-            if (kMX) {  // constant weight scales: two 4-column copies of the 2^0 block
+            if (kMX && !p.w_sf) {  // per-channel weights: constant block scales 2^0, two 4-column copies
                 const uint64_t sd = desc_rows16_noswizzle(smem_u32(sf_smem(S)));
                 tmem_cp_32x128b_x4(tmem_base + C::kSfbCol, sd);
                 tmem_cp_32x128b_x4(tmem_base + C::kSfbCol + 4, sd);
@@ -331,8 +341,15 @@ __global__ void __launch_bounds__(GemmCfg<kBF16, kWide, BN, kMX>::kThreads, 1)
                     if (!mbar_wait(&bar_full[s], ph, abort, p.d_status)) { ok = false; break; }
                     if (kBF16 && !mbar_wait(&bar_conv[s], ph, abort, p.d_status)) { ok = false; break; }
                     tc_fence_after();
-                    if constexpr (kMX)  // this stage's activation scales, ahead of its MMAs in the same pipe
+                    if constexpr (kMX) {  // this stage's scales, ahead of its MMAs in the same pipe
                         tmem_cp_32x128b_x4(tmem_base + C::kSfaCol + 4 * s, desc_rows16_noswizzle(smem_u32(sf_smem(s))));
+                        if (p.w_sf) {  // weight rows 0-127 -> columns +0..3, rows 128-255 -> +4..7
+                            tmem_cp_32x128b_x4(tmem_base + C::kSfbCol + 8 * s,
+                                               desc_rows16_noswizzle(smem_u32(sf_smem(s) + C::kSfBytes)));
+                            tmem_cp_32x128b_x4(tmem_base + C::kSfbCol + 8 * s + 4,
+                                               desc_rows16_noswizzle(smem_u32(sf_smem(s) + 2 * C::kSfBytes)));
+                        }
+                    }
                     const uint64_t dw = desc_kmajor_sw128(smem_u32(w_tile(s)));
                     const uint64_t dx = desc_kmajor_sw128(smem_u32(act_tile(s)));
                     const uint64_t da = kWide ? dx : dw;
@@ -340,8 +357,11 @@ __global__ void __launch_bounds__(GemmCfg<kBF16, kWide, BN, kMX>::kThreads, 1)
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
                         if (kMX)
-                            mma_mxf8(d_tmem, da + 2 * k, db + 2 * k, C::kIdesc | (static_cast<uint32_t>(k) << 29),
-                                     tmem_base + C::kSfaCol + 4 * s, tmem_base + C::kSfbCol, (kb | k) != 0);
+                            // scale byte k of each 4-byte scale word: A's id at bits 29-30, B's at bits 4-5
+                            mma_mxf8(d_tmem, da + 2 * k, db + 2 * k,
+                                     C::kIdesc | (static_cast<uint32_t>(k) << 29) | (static_cast<uint32_t>(k) << 4),
+                                     tmem_base + C::kSfaCol + 4 * s, tmem_base + C::kSfbCol + (p.w_sf ? 8 * s : 0),
+                                     (kb | k) != 0);
                         else if (kBF16) mma_f16(d_tmem, da + 2 * k, db + 2 * k, C::kIdesc, (kb | k) != 0);
                         else mma_f8f6f4(d_tmem, da + 2 * k, db + 2 * k, C::kIdesc, (kb | k) != 0);
                     }
@@ -492,7 +512,7 @@ __global__ void __launch_bounds__(GemmCfg<kBF16, kWide, BN, kMX>::kThreads, 1)
                 named_bar_sync(2, C::kEpiThreads);
                 for (int c = et; c < WR; c += C::kEpiThreads) {
                     const int64_t n = static_cast<int64_t>(nb) * WR + c;
-                    s_wsc[c] = (n < p.N) ? p.w_scale[static_cast<int64_t>(e) * p.N + n] : 0.0f;
+                    s_wsc[c] = (n < p.N) ? (p.w_scale ? p.w_scale[static_cast<int64_t>(e) * p.N + n] : 1.0f) : 0.0f;
                 }
                 named_bar_sync(2, C::kEpiThreads);
                 const int pos = sb * SR + q * 32 + lane;
@@ -776,6 +796,12 @@ inline qmoe_status_t run_moe_gemm(const qmoe_gemm_args* a, cudaStream_t st) {
     const int64_t elem = kBF16 ? 2 : 1;
     if (a->lda < a->K || (a->lda * elem) % 16 != 0) return QMOE_ERR_INVALID_ARG;
     const bool mx = !kBF16 && a->a_scale_mode == QMOE_SCALE_MX_1X32;
+    const bool wmx = a->w_scale_mode == QMOE_SCALE_MX_1X32;
+    if (a->w_scale_mode != QMOE_SCALE_PER_ROW && !wmx) return QMOE_ERR_INVALID_ARG;
+    if (wmx) {  // MXFP8 weights: FP8 GEMM with MX activations only
+        if (kBF16 || !mx) return QMOE_ERR_UNSUPPORTED;
+        if (!a->w_sf || !aligned16(a->w_sf)) return QMOE_ERR_INVALID_ARG;
+    }
     if (kBF16) {
         if (a->a_scale_mode != QMOE_SCALE_PER_TOKEN) return QMOE_ERR_UNSUPPORTED;
     } else if (mx) {
@@ -790,7 +816,7 @@ inline qmoe_status_t run_moe_gemm(const qmoe_gemm_args* a, cudaStream_t st) {
     const int64_t T = a->M * a->top_k;
     if (T >= (int64_t(1) << 30) || a->N * a->K * a->E >= (int64_t(1) << 40)) return QMOE_ERR_UNSUPPORTED;
     if (T == 0) return QMOE_OK;
-    if (!a->a || !a->w || !a->w_scale || !a->out || !a->sorted_ids || !a->expert_ids || !a->num_post_padded ||
+    if (!a->a || !a->w || (!a->w_scale && !wmx) || !a->out || !a->sorted_ids || !a->expert_ids || !a->num_post_padded ||
         !a->expert_offsets || !a->padded_offsets)
         return QMOE_ERR_INVALID_ARG;
     if (!aligned16(a->a) || !aligned16(a->w) || !aligned16(a->out)) return QMOE_ERR_INVALID_ARG;
@@ -816,6 +842,7 @@ inline qmoe_status_t run_moe_gemm(const qmoe_gemm_args* a, cudaStream_t st) {
     p.padded_offsets = a->padded_offsets;
     p.topk_w = a->topk_weights;
     p.w_scale = a->w_scale;
+    p.w_sf = wmx ? a->w_sf : nullptr;
     p.out = a->out;
     p.accum = a->accum;
     p.N = a->N;
