@@ -34,7 +34,7 @@ _lock = threading.Lock()
 _lib = None
 
 A_FP8_TOKEN, A_FP8_MX, A_BF16 = 0, 1, 2
-W_FP8, W_INT8, W_MX = 0, 1, 2
+W_FP8, W_INT8, W_MX, W_INT4 = 0, 1, 2, 3
 
 
 def build(force: bool = False) -> str:
@@ -93,6 +93,7 @@ def lib():
             L.orc_quant_mxfp8_cols_bf16.argtypes = [vp, i64, i64, i64, vp, vp, i64, i64]
             L.orc_quant_rows_mxfp8_f32.argtypes = [vp, i64, i64, vp, vp, i64]
             L.orc_mx_weight_sf_tiled.argtypes = [vp, i64, i64, i64, i64, vp]
+            L.orc_quant_rows_int4_f32.argtypes = [vp, i64, i64, vp, vp]
             L.orc_router_topk.argtypes = [vp, i64, i32, i32, vp, vp]
             L.orc_srelu_f32.argtypes = [ctypes.c_float]
             L.orc_srelu_f32.restype = ctypes.c_float
@@ -330,6 +331,17 @@ def quant_rows_mxfp8_f32(w: np.ndarray):
     return q, sf
 
 
+def quant_rows_int4_f32(w: np.ndarray):
+    """fp32 [..., K] rows -> (packed int4 uint8 [..., K/2], fp32 group scales [..., K/128])."""
+    w = np.ascontiguousarray(w, dtype=np.float32)
+    K = w.shape[-1]
+    R = w.size // K
+    q = np.zeros(w.shape[:-1] + (K // 2,), dtype=np.uint8)
+    s = np.zeros(w.shape[:-1] + (K // 128,), dtype=np.float32)
+    lib().orc_quant_rows_int4_f32(_p(w), R, K, _p(q), _p(s))
+    return q, s
+
+
 def mx_weight_sf_tiled(sf: np.ndarray, E: int, N: int, K: int):
     """E8M0 weight factors [E*N, ld] -> the GEMM's tiled blocks (uint8, flat)."""
     sf = np.ascontiguousarray(sf, dtype=np.uint8)
@@ -411,7 +423,7 @@ def moe_gemm(*, a_kind, a, a_scale=None, a_sf=None, a_sf_row=None, w_kind, w, w_
     M, top_k = ids.shape
     T = M * top_k
     N = w.shape[1]
-    K = w.shape[2]
+    K = w.shape[2] * (2 if w_kind == W_INT4 else 1)   # packed int4: two values per byte
     pos = compact_row_of_slot(ids, E)
     if a_layout == "token":
         a_row = np.arange(T, dtype=np.int64) // top_k

@@ -238,6 +238,45 @@ void orc_quant_rows_int8_f32(const float* x, int64_t rows, int64_t cols, int64_t
     }
 }
 
+/* Symmetric INT4 in groups of 128 along the row (the "int4wo" weight-only
+ * recipe named in "Enabling MOE Quantization using linear decomposition",
+ * Summary; group size and symmetric range are this build's reading):
+ * per group scale = amax/7 (1 for an all-zero group), q = clamp(rint(x/scale),
+ * -7, 7); two's-complement nibbles packed two per byte, element 2j in the low
+ * nibble of byte j.  q is [rows, cols/2] bytes, scale [rows, cols/128]. */
+void orc_quant_rows_int4_f32(const float* x, int64_t rows, int64_t cols, uint8_t* q, float* scale) {
+    const int64_t G = cols / 128;
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; ++r) {
+        for (int64_t g = 0; g < G; ++g) {
+            const float* xg = x + r * cols + g * 128;
+            float amax = 0.0f;
+            for (int64_t c = 0; c < 128; ++c) {
+                float a = fabsf(xg[c]);
+                if (a > amax) amax = a;
+            }
+            float s = (amax == 0.0f) ? 1.0f : amax / 7.0f;
+            scale[r * G + g] = s;
+            for (int64_t c = 0; c < 128; c += 2) {
+                int v[2];
+                for (int t = 0; t < 2; ++t) {
+                    float f = rintf(xg[c + t] / s);
+                    if (f > 7.0f) f = 7.0f;
+                    if (f < -7.0f) f = -7.0f;
+                    v[t] = (int)f;
+                }
+                q[r * (cols / 2) + (g * 128 + c) / 2] = (uint8_t)((v[0] & 0xF) | ((v[1] & 0xF) << 4));
+            }
+        }
+    }
+}
+
+/* Value of nibble k of a packed INT4 row (two's complement). */
+static int int4_at(const uint8_t* row, int64_t k) {
+    int n = (row[k / 2] >> ((k & 1) * 4)) & 0xF;
+    return (n >= 8) ? n - 16 : n;
+}
+
 /* ------------------------------------------------------------------------- */
 /* exp in a fixed fp32 operation sequence.                                     */
 /*  clamp x to [-104, 89]; n = rint(x * log2(e));                              */
@@ -498,6 +537,8 @@ void orc_router_topk(const float* logits, int64_t M, int32_t E, int32_t k, int32
 /* w_kind 0: e4m3 codes, w_kind 1: int8; both times w_scale[e*N + n];         */
 /* w_kind 2: e4m3 codes with E8M0 scales per 1x32 block along K,               */
 /*           w_sf[(e*N + n) * w_sf_ld + k/32] (times w_scale[e*N + n] if given).*/
+/* w_kind 3: packed INT4 rows of K/2 bytes with one fp32 scale per group of    */
+/*           128 along K, w_scale[(e*N + n) * (K/128) + k/128].                */
 /* ------------------------------------------------------------------------- */
 void orc_moe_gemm(int a_kind, const void* a, int64_t lda, const float* a_scale,
                   const uint8_t* a_sf, int64_t a_sf_ld, const int64_t* a_sf_row,
@@ -527,9 +568,13 @@ void orc_moe_gemm(int a_kind, const void* a, int64_t lda, const float* a_scale,
         double ws = topk_w ? (double)topk_w[s] : 1.0;
         for (int64_t n = 0; n < N; ++n) {
             const int64_t wrow = ((int64_t)e * N + n) * K;
-            const double sw = w_scale ? (double)w_scale[(int64_t)e * N + n] : 1.0;
+            const double sw = (w_scale && w_kind != 3) ? (double)w_scale[(int64_t)e * N + n] : 1.0;
             double acc = 0.0;
-            if (w_kind == 0) {
+            if (w_kind == 3) {
+                const uint8_t* wq = (const uint8_t*)w + ((int64_t)e * N + n) * (K / 2);
+                const float* gs = w_scale + ((int64_t)e * N + n) * (K / 128);
+                for (int64_t k = 0; k < K; ++k) acc += arow[k] * ((double)int4_at(wq, k) * (double)gs[k / 128]);
+            } else if (w_kind == 0) {
                 const uint8_t* wq = (const uint8_t*)w + wrow;
                 for (int64_t k = 0; k < K; ++k) acc += arow[k] * (lut[wq[k]] * sw);
             } else if (w_kind == 2) {

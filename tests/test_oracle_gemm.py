@@ -161,3 +161,46 @@ def test_tolerance_helper_rejects_planted_error(orc):
     bad[3, 3] += 0.5
     ok, ratio = orc.gemm_tolerance_ok(bad, ref)
     assert not ok and ratio > 1
+
+
+def test_int4_quant_rule_and_packing(orc):
+    """Symmetric groups of 128: scale = amax/7, codes rint(w/scale) clamped to
+    [-7, 7], nibbles packed low-first; reconstruction within half a step."""
+    w = inputs.expert_weights_f32(2, 24, 384, seed=41)
+    w[0, 0, :128] = 0.0
+    w[1, 3, 128:256] *= 1e-20
+    q, s = orc.quant_rows_int4_f32(w)
+    assert q.shape == (2, 24, 192) and s.shape == (2, 24, 3)
+    lo = (q & 0xF).astype(np.int16)
+    hi = (q >> 4).astype(np.int16)
+    v = np.empty(w.shape, dtype=np.int16)
+    v[..., 0::2] = np.where(lo >= 8, lo - 16, lo)
+    v[..., 1::2] = np.where(hi >= 8, hi - 16, hi)
+    assert v.min() >= -7 and v.max() <= 7
+    g = w.reshape(2, 24, 3, 128)
+    amax = np.abs(g).max(axis=-1)
+    exp_s = np.where(amax == 0, np.float32(1), (amax / np.float32(7)).astype(np.float32))
+    assert np.array_equal(s, exp_s)
+    ref = np.clip(np.rint((g / s[..., None]).astype(np.float32)), -7, 7).reshape(w.shape)
+    assert np.array_equal(v, ref.astype(np.int16))
+    rec = v.reshape(2, 24, 3, 128) * s[..., None].astype(np.float64)
+    assert np.all(np.abs(rec - g) <= 0.5 * s[..., None] * (1 + 1e-6))
+    assert np.all(v[0, 0, :128] == 0) and s[0, 0, 0] == 1.0
+
+
+def test_int4_w4a16_vs_bruteforce(orc):
+    M, K, N, E, top_k = 9, 256, 20, 3, 2
+    a = inputs.activations_bf16(M, K, 42)
+    w = inputs.expert_weights_f32(E, N, K, 42)
+    ids, tw = inputs.routing(M, E, top_k, 42)
+    q, s = orc.quant_rows_int4_f32(w)
+    lo = (q & 0xF).astype(np.int16)
+    hi = (q >> 4).astype(np.int16)
+    v = np.empty((E, N, K), dtype=np.float64)
+    v[..., 0::2] = np.where(lo >= 8, lo - 16, lo)
+    v[..., 1::2] = np.where(hi >= 8, hi - 16, hi)
+    W = v * np.repeat(s.astype(np.float64), 128, axis=-1)
+    A = inputs.bf16_bits_to_f32(a).astype(np.float64)
+    ref = dense_moe(A, W, ids, tw)
+    out = orc.moe_gemm(a_kind=orc.A_BF16, a=a, w_kind=orc.W_INT4, w=q, w_scale=s, topk_ids=ids, topk_w=tw, E=E)
+    assert np.allclose(out, ref.reshape(M * top_k, N), rtol=1e-12, atol=1e-12)
