@@ -538,7 +538,8 @@ void orc_router_topk(const float* logits, int64_t M, int32_t E, int32_t k, int32
 /* w_kind 2: e4m3 codes with E8M0 scales per 1x32 block along K,               */
 /*           w_sf[(e*N + n) * w_sf_ld + k/32] (times w_scale[e*N + n] if given).*/
 /* w_kind 3: packed INT4 rows of K/2 bytes with one fp32 scale per group of    */
-/*           128 along K, w_scale[(e*N + n) * (K/128) + k/128].                */
+/*           128 along K, w_scale[(e*N + n) * (K/128) + k/128]; the weight the */
+/*           bf16 GEMM multiplies is bf16(q * scale) (fp32 product, RN).       */
 /* ------------------------------------------------------------------------- */
 void orc_moe_gemm(int a_kind, const void* a, int64_t lda, const float* a_scale,
                   const uint8_t* a_sf, int64_t a_sf_ld, const int64_t* a_sf_row,
@@ -573,7 +574,10 @@ void orc_moe_gemm(int a_kind, const void* a, int64_t lda, const float* a_scale,
             if (w_kind == 3) {
                 const uint8_t* wq = (const uint8_t*)w + ((int64_t)e * N + n) * (K / 2);
                 const float* gs = w_scale + ((int64_t)e * N + n) * (K / 128);
-                for (int64_t k = 0; k < K; ++k) acc += arow[k] * ((double)int4_at(wq, k) * (double)gs[k / 128]);
+                for (int64_t k = 0; k < K; ++k) {
+                    const float wf = (float)int4_at(wq, k) * gs[k / 128];
+                    acc += arow[k] * (double)orc_bf16_to_f32(orc_bf16_from_f32(wf));
+                }
             } else if (w_kind == 0) {
                 const uint8_t* wq = (const uint8_t*)w + wrow;
                 for (int64_t k = 0; k < K; ++k) acc += arow[k] * (lut[wq[k]] * sw);

@@ -199,7 +199,9 @@ def test_int4_w4a16_vs_bruteforce(orc):
     v = np.empty((E, N, K), dtype=np.float64)
     v[..., 0::2] = np.where(lo >= 8, lo - 16, lo)
     v[..., 1::2] = np.where(hi >= 8, hi - 16, hi)
-    W = v * np.repeat(s.astype(np.float64), 128, axis=-1)
+    # the weight the bf16 GEMM multiplies: bf16(q * scale), the product in fp32 (torch's bf16 cast)
+    wf = (v.astype(np.float32) * np.repeat(s, 128, axis=-1)).astype(np.float32)
+    W = torch.from_numpy(wf).to(torch.bfloat16).to(torch.float64).numpy()
     A = inputs.bf16_bits_to_f32(a).astype(np.float64)
     ref = dense_moe(A, W, ids, tw)
     out = orc.moe_gemm(a_kind=orc.A_BF16, a=a, w_kind=orc.W_INT4, w=q, w_scale=s, topk_ids=ids, topk_w=tw, E=E)
