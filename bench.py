@@ -362,6 +362,30 @@ def run_suite(reps: int = 20, only: str | None = None) -> None:
         line(wl.name, f"moe_gemm_w8a16 BM={BM} padded A", ms, nbytes, 2.0 * wl.M * TOP_K * wl.K * wl.N, "bf16")
         del wq, ws
 
+    # INT4 W4A16 (int4wo, groups of 128 along K) on the same shapes
+    for wl in inputs.int8_w8a16_sweep():
+        if only and only not in wl.name.replace("int8 w8a16", "int4 w4a16"):
+            continue
+        wq = torch.empty(E, wl.N, wl.K // 2, dtype=torch.uint8, device=dev)
+        ws = torch.empty(E, wl.N, wl.K // 128, dtype=torch.float32, device=dev)
+        for e in range(E):
+            w = torch.randn(wl.N, wl.K, device=dev) * (1.0 / np.sqrt(wl.K))
+            q.quant_weight_int4(w, q=wq[e], scale=ws[e])
+        a = torch.from_numpy(inputs.activations_bf16(wl.M, wl.K, wl.seed).view(np.int16)).to(dev).view(torch.bfloat16)
+        ids, tw = inputs.routing(wl.M, E, TOP_K, wl.seed)
+        BM = 128
+        al = q.moe_align_block_size(torch.from_numpy(ids).to(dev), E, BM)
+        twd = torch.from_numpy(tw).to(dev)
+        out = torch.empty(wl.M * TOP_K, wl.N, dtype=torch.bfloat16, device=dev)
+        hit = len(np.unique(ids))
+        nbytes = hit * wl.N * wl.K // 2 + hit * wl.N * (wl.K // 128) * 4 + wl.M * wl.K * 2 + wl.M * TOP_K * (8 + 2 * wl.N)
+        ap = q.gather_sorted_bf16(a, al, TOP_K)
+        ms = _timed(lambda: q.moe_gemm_w4a16(ap, wq, ws, al, twd, M=wl.M, top_k=TOP_K, BM=BM, a_layout=q.A_PADDED,
+                                             out=out), reps, flush)
+        line(wl.name.replace("int8 w8a16", "int4 w4a16"), f"moe_gemm_w4a16 BM={BM} padded A", ms, nbytes,
+             2.0 * wl.M * TOP_K * wl.K * wl.N, "bf16")
+        del wq, ws
+
     # Fused activation + MXFP8 on the TransformerEngine GroupedLinear page's input
     # (8 experts x 4000 rows, width 4096): SReLU on [32000, 4096]; SwiGLU on the
     # same input read as gate|up, [32000, 2 x 2048].  Page: ~142 us (SReLU) and

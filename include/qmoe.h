@@ -186,6 +186,17 @@ qmoe_status_t qmoe_quant_weight_fp8(const float* w, int64_t rows, int64_t cols,
 qmoe_status_t qmoe_quant_weight_int8(const float* w, int64_t rows, int64_t cols,
                                      int8_t* q, float* scale, qmoe_stream_t stream);
 
+/* INT4 weight-only quantisation (the "int4wo" recipe named in "Enabling MOE
+ * Quantization using linear decomposition", Summary; the pages do not define
+ * it -- this library reads it as symmetric groups of 128 along K): every
+ * fp32 row of cols (a multiple of 128) values, per 128-wide group
+ * scale = amax/7 (IEEE division; 1 for an all-zero group),
+ * q = clamp(rint(w/scale), -7, 7), two's-complement nibbles packed two per
+ * byte with element 2j in the low nibble of byte j.
+ *   q [rows, cols/2] bytes and w 16-byte aligned; scale [rows, cols/128] fp32. */
+qmoe_status_t qmoe_quant_weight_int4(const float* w, int64_t rows, int64_t cols, uint8_t* q, float* scale,
+                                     qmoe_stream_t stream);
+
 /* MXFP8 weights ("[PyTorch] Let GroupedLinear accept MXFP8 input and
  * gradient", Description: block-scaled operands): every row of fp32 W
  * (rows = E*N, cols = K, K % 32 == 0) in 1x32 blocks along K; per block
@@ -300,6 +311,16 @@ typedef struct {
  * operands then carry their block scales into the MMA; MX weights with
  * per-token activations return QMOE_ERR_UNSUPPORTED. */
 qmoe_status_t qmoe_moe_gemm_w8a8(const qmoe_gemm_args* args, qmoe_stream_t stream);
+
+/* INT4 W4A16 grouped GEMM (weight-only int4 against bf16 activations):
+ *   out = w[s] * sum_k a_bf16[k] * bf16(q4[e, n, k] * scale[e, n, k/128])
+ * with fp32 accumulation and a bf16 result.  args->w holds the packed int4
+ * weights [E, N, K/2] of qmoe_quant_weight_int4 and args->w_scale their group
+ * scales [E, N, K/128]; the converter warps form each bf16 weight as the fp32
+ * product q * scale rounded to bf16 (RN) before the tensor-core MMA.
+ * Activation and output layouts as qmoe_moe_gemm_w8a16.  Limits: K % 128 == 0,
+ * BM in {128, 256} (else QMOE_ERR_UNSUPPORTED), w_scale_mode PER_ROW. */
+qmoe_status_t qmoe_moe_gemm_w4a16(const qmoe_gemm_args* args, qmoe_stream_t stream);
 
 /* FP8 W8A8 grouped GEMM with the TOKEN_SUM layout that allocates nothing.
  * The pages have no counterpart to this entry point; it exists for callers

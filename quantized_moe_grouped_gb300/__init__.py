@@ -33,7 +33,7 @@ EXPORTED = (
     "qmoe_moe_gemm_w8a16", "qmoe_silu_mul_quant", "qmoe_srelu_quant", "qmoe_debug_e4m3_encode", "qmoe_debug_int8_to_bf16",
     "qmoe_debug_silu_mul", "qmoe_debug_div_by_scale", "qmoe_debug_wait_timeout",
     "qmoe_moe_gemm_w8a8_token_sum_noalloc", "qmoe_quant_weight_mxfp8", "qmoe_quant_mxfp8", "qmoe_quant_mxfp8_colwise",
-    "qmoe_mx_weight_sf_tiled_bytes", "qmoe_mx_weight_sf_tiled",
+    "qmoe_mx_weight_sf_tiled_bytes", "qmoe_mx_weight_sf_tiled", "qmoe_quant_weight_int4", "qmoe_moe_gemm_w4a16",
 )
 NOALLOC_ACCUM_MAX_ELEMS = 4 << 20
 
@@ -89,6 +89,7 @@ def load_library(path: str | None = None):
             L.qmoe_mx_weight_sf_tiled_bytes.argtypes = [i64, i64, i64]
             L.qmoe_mx_weight_sf_tiled_bytes.restype = i64
             L.qmoe_mx_weight_sf_tiled.argtypes = [vp, i64, i64, i64, i64, vp, vp]
+            L.qmoe_quant_weight_int4.argtypes = [vp, i64, i64, vp, vp, vp]
             L.qmoe_moe_route_align_quant_fp8.argtypes = [vp, vp, i64, i64, i64, i32, i32, i32, vp, vp, vp, vp, vp,
                                                          vp, vp, vp, vp, vp, vp]
             L.qmoe_gather_sorted_bf16.argtypes = [vp, i64, i64, i64, vp, vp, i32, i64, vp, vp]
@@ -288,6 +289,19 @@ def quant_weight_int8(w: torch.Tensor, stream=None):
     return q, s
 
 
+def quant_weight_int4(w: torch.Tensor, q=None, scale=None, stream=None):
+    """fp32 [..., K] rows (K % 128 == 0) -> (packed int4 uint8 [..., K/2], fp32 group scales [..., K/128])."""
+    _need(w, torch.float32, "w")
+    K = w.shape[-1]
+    rows = w.numel() // K
+    q = q if q is not None else torch.empty(w.shape[:-1] + (K // 2,), dtype=torch.uint8, device=w.device)
+    scale = scale if scale is not None else torch.empty(w.shape[:-1] + (K // 128,), dtype=torch.float32,
+                                                        device=w.device)
+    _check(load_library().qmoe_quant_weight_int4(_ptr(w), rows, K, _ptr(q), _ptr(scale), _stream(stream)),
+           "quant_weight_int4")
+    return q, scale
+
+
 def quant_weight_mxfp8(w: torch.Tensor, q=None, sf=None, stream=None):
     """fp32 [..., K] weight rows -> (e4m3 codes uint8 same shape, E8M0 [rows, roundup(K/32, 4)])."""
     _need(w, torch.float32, "w")
@@ -354,8 +368,9 @@ def quant_mxfp8_colwise(x: torch.Tensor, q=None, sf=None, stream=None):
 # ------------------------------------------------------------------ GEMM ---
 def _gemm(fn_name, *, a, a_scale, w, w_scale, align, topk_weights, out, M, top_k, BM, a_layout, out_layout,
           a_scale_mode=SCALE_PER_TOKEN, a_sf=None, a_sf_padded_offsets=None, d_status=None, accum=None,
-          stream=None, w_scale_mode=0, w_sf=None):
-    E, N, K = w.shape
+          stream=None, w_scale_mode=0, w_sf=None, K=None):
+    E, N, Kw = w.shape
+    K = Kw if K is None else K
     if out_layout == OUT_TOKEN_SUM and accum is None:
         accum = torch.empty(M, N, dtype=torch.float32, device=out.device)
     args = GemmArgs()
@@ -481,6 +496,24 @@ def moe_gemm_w8a16(a: torch.Tensor, w_q: torch.Tensor, w_scale: torch.Tensor, al
     return _gemm("qmoe_moe_gemm_w8a16", a=a, a_scale=None, w=w_q, w_scale=w_scale, align=align,
                  topk_weights=topk_weights, out=out, M=M, top_k=top_k, BM=BM, a_layout=a_layout,
                  out_layout=out_layout, d_status=d_status, accum=accum, stream=stream)
+
+
+def moe_gemm_w4a16(a: torch.Tensor, w_q: torch.Tensor, w_scale: torch.Tensor, align: dict,
+                   topk_weights: torch.Tensor | None, *, M: int, top_k: int, BM: int,
+                   a_layout: int = A_TOKEN_GATHER, out_layout: int = OUT_SLOT, out: torch.Tensor | None = None,
+                   d_status: torch.Tensor | None = None, accum: torch.Tensor | None = None,
+                   stream=None) -> torch.Tensor:
+    """INT4 W4A16 grouped GEMM: a bf16 [rows, K], w_q packed int4 uint8 [E, N, K/2],
+    w_scale fp32 group scales [E, N, K/128] (quant_weight_int4); BM 128 or 256."""
+    _need(a, torch.bfloat16, "a")
+    _need(w_q, torch.uint8, "w_q")
+    _need(w_scale, torch.float32, "w_scale")
+    if topk_weights is not None:
+        _need(topk_weights, torch.float32, "topk_weights")
+    out = _out_for(out, out_layout, M, top_k, w_q.shape[1], a.device)
+    return _gemm("qmoe_moe_gemm_w4a16", a=a, a_scale=None, w=w_q, w_scale=w_scale, align=align,
+                 topk_weights=topk_weights, out=out, M=M, top_k=top_k, BM=BM, a_layout=a_layout,
+                 out_layout=out_layout, d_status=d_status, accum=accum, stream=stream, K=2 * w_q.shape[2])
 
 
 # ------------------------------------------------------ SwiGLU + quant ---

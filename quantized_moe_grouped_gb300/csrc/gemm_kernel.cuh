@@ -27,7 +27,11 @@
 //   warps 8+    W8A16: int8 -> bf16 converters (raw ring -> main ring), two
 //               groups (eight warps each for the wide tile, four for the
 //               swapped one) taking alternate stages
-//   warps 8-11  MX: the activation scale writers (global -> TMEM)
+//   warp  2     MX: the scale writer (activation factors -> shared memory;
+//               the MMA thread copies them into TMEM), warps 8-11 a second
+//               epilogue group
+//   W4A16 (kI4): the converters also apply each row's scale per 128-wide
+//               group of K while turning packed int4 into bf16
 //
 // Every wait is bounded (mbar_wait); on a timeout the CTA raises an abort
 // flag, all roles leave their loops, copies in flight are drained and TMEM is
@@ -65,13 +69,17 @@ struct GemmParams {
     int64_t a_sf_ld;
     const int32_t* a_sf_poff;    // MX: first scale row of each expert
     const uint8_t* w_sf;         // MX weights: E8M0 factors in 1 KB tiled blocks, or nullptr (2^0)
+    const float* w_gscale;       // W4A16: fp32 scale per weight row and group of 128 along K
+    int32_t w_groups;            // W4A16: K / 128
     int32_t num_k_blocks;
     int32_t* d_status;
 };
 
 constexpr int kGemmMaxE = 256;  // experts per call (the align's limit)
 
-template <bool kBF16, bool kWide, int BN, bool kMX = false>
+// kI4: W4A16 -- packed int4 weight tiles (32 bytes per row per stage) with a
+// scale per 128-wide group along K, applied by the converters (wide tile only).
+template <bool kBF16, bool kWide, int BN, bool kMX = false, bool kI4 = false>
 struct GemmCfg {
     static constexpr int kSlotRows = kWide ? 128 : BN;      // slots per tile
     static constexpr int kWRows = kWide ? 256 : 128;        // weight rows (output channels) per tile
@@ -79,7 +87,8 @@ struct GemmCfg {
     static constexpr int kBK = kBF16 ? 64 : 128;            // K elements per stage (128 bytes of MMA operand)
     static constexpr int kWBytes = kWRows * 128;
     static constexpr int kActBytes = kSlotRows * 128;
-    static constexpr int kRawBytes = kBF16 ? kWRows * 64 : 0;  // int8 weight tile before conversion
+    static constexpr int kRawRowBytes = kI4 ? 32 : 64;     // raw weight bytes per row per stage
+    static constexpr int kRawBytes = kBF16 ? kWRows * kRawRowBytes : 0;  // int8/int4 tile before conversion
     // Main ring: MMA operand tiles (weights -- converted to bf16 for W8A16 --
     // and activations).  W8A16 adds a separate, deeper ring of raw int8 weight
     // tiles so that the weight stream keeps many bytes in flight while the
@@ -116,6 +125,7 @@ struct GemmCfg {
     static constexpr uint32_t kIdesc =
         kMX ? make_idesc_mx(128, kMmaN) : make_idesc(kBF16 ? kFmtBF16 : kFmtE4M3, 128, kMmaN);
     static_assert(!kMX || (kWide && !kBF16), "MX scales: FP8 wide tile only");
+    static_assert(!kI4 || (kBF16 && kWide), "W4A16: wide bf16 tile only");
     static_assert(!kMX || kSfbCol + 8 * kStages <= 512, "TMEM columns");  // per-stage weight scales
     static constexpr int kDynSmem =
         kStages * kStageBytes + kRawStages * kRawBytes + (kMX ? kStages * kSfStageBytes + kSfBytes : 0) + 1024;
@@ -185,11 +195,11 @@ QMOE_DI void tmem_wait_ld_regs(uint32_t (&r)[32]) {
                    "+r"(r[29]), "+r"(r[30]), "+r"(r[31]));
 }
 
-template <bool kBF16, bool kWide, int BN, bool kMX>
-__global__ void __launch_bounds__(GemmCfg<kBF16, kWide, BN, kMX>::kThreads, 1)
+template <bool kBF16, bool kWide, int BN, bool kMX, bool kI4>
+__global__ void __launch_bounds__(GemmCfg<kBF16, kWide, BN, kMX, kI4>::kThreads, 1)
     moe_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_a,
                     const GemmParams p) {
-    using C = GemmCfg<kBF16, kWide, BN, kMX>;
+    using C = GemmCfg<kBF16, kWide, BN, kMX, kI4>;
     constexpr int S = C::kStages;
     constexpr int SR = C::kSlotRows;
     constexpr int WR = C::kWRows;
@@ -297,7 +307,7 @@ __global__ void __launch_bounds__(GemmCfg<kBF16, kWide, BN, kMX>::kThreads, 1)
                         const uint32_t rph = (it / R) & 1;
                         if (!mbar_wait(&bar_raw_empty[r], rph ^ 1, abort, p.d_status)) { ok = false; break; }
                         mbar_arrive_expect_tx(&bar_raw_full[r], C::kRawBytes);
-                        tma_load_3d(&tmap_w, &bar_raw_full[r], raw_tile(r), kb * C::kBK, nb * WR, e);
+                        tma_load_3d(&tmap_w, &bar_raw_full[r], raw_tile(r), kb * C::kRawRowBytes, nb * WR, e);
                     } else {
                         const int s = it % S;
                         const uint32_t ph = (it / S) & 1;
@@ -659,7 +669,8 @@ __global__ void __launch_bounds__(GemmCfg<kBF16, kWide, BN, kMX>::kThreads, 1)
             bool ok = true;
             for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
                 int sb, nb;
-                if (tile_expert(tile, sb, nb) < 0) continue;
+                const int e = tile_expert(tile, sb, nb);
+                if (e < 0) continue;
                 for (int kb = 0; kb < nkb; ++kb, ++it) {
                     if ((it & 1) != group) continue;
                     const int s = it % S;
@@ -671,6 +682,34 @@ __global__ void __launch_bounds__(GemmCfg<kBF16, kWide, BN, kMX>::kThreads, 1)
                     if (!mbar_wait(&bar_empty[s], ph ^ 1, abort, p.d_status)) { ok = false; break; }
                     const uint8_t* raw = raw_tile(r);
                     uint8_t* dst = w_tile(s);
+                    if constexpr (kI4) {
+                        // two threads per 32-byte row (32 int4 each), each with the
+                        // row's scale for this stage's 128-wide group (kb / 2)
+                        const int c2 = ct & 1;
+                        constexpr int kRows4 = C::kConvThreads / 2;
+#pragma unroll
+                        for (int i = 0; i < WR / kRows4; ++i) {
+                            const int rr = (ct >> 1) + kRows4 * i;
+                            const int64_t n = static_cast<int64_t>(nb) * WR + rr;
+                            const float sc = (n < p.N) ? __ldg(p.w_gscale + (static_cast<int64_t>(e) * p.N + n) *
+                                                                               p.w_groups + (kb >> 1))
+                                                       : 0.0f;
+                            const uint4 w = *reinterpret_cast<const uint4*>(raw + rr * 32 + c2 * 16);
+                            uint32_t o[4][4];
+                            int4x8_to_bf16x8_scaled(w.x, sc, o[0]);
+                            int4x8_to_bf16x8_scaled(w.y, sc, o[1]);
+                            int4x8_to_bf16x8_scaled(w.z, sc, o[2]);
+                            int4x8_to_bf16x8_scaled(w.w, sc, o[3]);
+#pragma unroll
+                            for (int t = 0; t < 4; ++t)
+                                *reinterpret_cast<uint4*>(dst + rr * 128 + (((4 * c2 + t) ^ (rr & 7)) << 4)) =
+                                    make_uint4(o[t][0], o[t][1], o[t][2], o[t][3]);
+                        }
+                        fence_proxy_async_smem();
+                        mbar_arrive(&bar_conv[s]);
+                        mbar_arrive(&bar_raw_empty[r]);
+                        continue;
+                    }
                     const int c = ct & 3;
                     constexpr int kRowsPerPass = C::kConvThreads / 4;  // four threads per 64-byte row
 #pragma unroll
@@ -750,10 +789,10 @@ inline bool make_act_map(CUtensorMap* map, const void* a, int64_t rows, int64_t 
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <bool kBF16, bool kWide, int BN, bool kMX = false>
+template <bool kBF16, bool kWide, int BN, bool kMX = false, bool kI4 = false>
 inline qmoe_status_t launch_gemm(const void* w, int64_t E, int64_t N, int64_t K, const GemmParams& p,
                                  int64_t max_padded, int64_t a_rows, int64_t lda, cudaStream_t st) {
-    using C = GemmCfg<kBF16, kWide, BN, kMX>;
+    using C = GemmCfg<kBF16, kWide, BN, kMX, kI4>;
     static std::mutex mu;
     static bool attr_set[64] = {false};
     int dev = 0;
@@ -761,14 +800,16 @@ inline qmoe_status_t launch_gemm(const void* w, int64_t E, int64_t N, int64_t K,
     {
         std::lock_guard<std::mutex> g(mu);
         if (!attr_set[dev]) {
-            if (cudaFuncSetAttribute(moe_gemm_kernel<kBF16, kWide, BN, kMX>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+            if (cudaFuncSetAttribute(moe_gemm_kernel<kBF16, kWide, BN, kMX, kI4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      C::kDynSmem) != cudaSuccess)
                 return QMOE_ERR_CUDA;
             attr_set[dev] = true;
         }
     }
     CUtensorMap map, amap;
-    if (!make_weight_map(&map, w, E, N, K, C::kBK, C::kWRows, !kBF16)) return QMOE_ERR_CUDA;
+    // rows of K weight bytes (FP8, INT8) or K/2 (packed INT4); box: one stage's bytes per row
+    if (!make_weight_map(&map, w, E, N, kI4 ? K / 2 : K, kBF16 ? C::kRawRowBytes : C::kBK, C::kWRows, !kBF16))
+        return QMOE_ERR_CUDA;
     memset(&amap, 0, sizeof(amap));
     if (p.a_tma && !make_act_map(&amap, p.a, a_rows, K, lda, kBF16 ? 2 : 1, C::kSlotRows)) return QMOE_ERR_CUDA;
     const int sms = device_sm_count();
@@ -776,7 +817,7 @@ inline qmoe_status_t launch_gemm(const void* w, int64_t E, int64_t N, int64_t K,
     const int64_t max_tiles = ((max_padded + C::kSlotRows - 1) / C::kSlotRows) * ((N + C::kWRows - 1) / C::kWRows);
     const int64_t grid = max_tiles < sms ? max_tiles : sms;
     if (grid <= 0) return QMOE_OK;
-    moe_gemm_kernel<kBF16, kWide, BN, kMX><<<static_cast<unsigned>(grid), C::kThreads, C::kDynSmem, st>>>(map, amap, p);
+    moe_gemm_kernel<kBF16, kWide, BN, kMX, kI4><<<static_cast<unsigned>(grid), C::kThreads, C::kDynSmem, st>>>(map, amap, p);
     return launch_status();
 }
 
@@ -784,8 +825,14 @@ inline qmoe_status_t launch_gemm(const void* w, int64_t E, int64_t N, int64_t K,
 qmoe_status_t launch_token_sum_finalize(const float* accum, uint16_t* out, int64_t n, cudaStream_t st);
 
 // Shared argument checks and dispatch for both precisions.
-template <bool kBF16>
+template <bool kBF16, bool kI4 = false>
 inline qmoe_status_t run_moe_gemm(const qmoe_gemm_args* a, cudaStream_t st) {
+    static_assert(!kI4 || kBF16, "W4A16 is a bf16-activation GEMM");
+    if (kI4 && a && a->struct_size >= sizeof(qmoe_gemm_args)) {
+        // packed int4 weights with a scale per 128-wide group of K: wide tile only
+        if (a->BM != 128 && a->BM != 256) return QMOE_ERR_UNSUPPORTED;
+        if (a->K % 128 != 0 || a->w_scale_mode != QMOE_SCALE_PER_ROW) return QMOE_ERR_INVALID_ARG;
+    }
     if (!a || a->struct_size < sizeof(qmoe_gemm_args)) return QMOE_ERR_INVALID_ARG;
     if (a->M < 0 || a->N < 16 || a->N % 16 != 0 || a->K < 16 || a->K % 16 != 0) return QMOE_ERR_INVALID_ARG;
     if (a->E < 1 || a->E > kGemmMaxE || a->top_k < 1 || a->top_k > a->E) return QMOE_ERR_INVALID_ARG;
@@ -841,7 +888,9 @@ inline qmoe_status_t run_moe_gemm(const qmoe_gemm_args* a, cudaStream_t st) {
     p.expert_offsets = a->expert_offsets;
     p.padded_offsets = a->padded_offsets;
     p.topk_w = a->topk_weights;
-    p.w_scale = a->w_scale;
+    p.w_scale = kI4 ? nullptr : a->w_scale;   // W4A16: the group scales are applied by the converters
+    p.w_gscale = kI4 ? a->w_scale : nullptr;
+    p.w_groups = kI4 ? static_cast<int32_t>(a->K / 128) : 0;
     p.w_sf = wmx ? a->w_sf : nullptr;
     p.out = a->out;
     p.accum = a->accum;
@@ -860,6 +909,11 @@ inline qmoe_status_t run_moe_gemm(const qmoe_gemm_args* a, cudaStream_t st) {
     // the kernel numbers its tiles (slot blocks x weight blocks) with 32-bit ints
     if (max_padded / 16 * ((a->N + 127) / 128) >= (int64_t(1) << 31)) return QMOE_ERR_UNSUPPORTED;
     qmoe_status_t r;
+    if constexpr (kI4) {
+        r = launch_gemm<true, true, 128, false, true>(a->w, a->E, a->N, a->K, p, max_padded, a_rows, a->lda, st);
+        if (r != QMOE_OK || !tsum) return r;
+        return launch_token_sum_finalize(a->accum, a->out, a->M * a->N, st);
+    }
     if constexpr (!kBF16) {
         if (mx) {
             r = launch_gemm<false, true, 128, true>(a->w, a->E, a->N, a->K, p, max_padded, a_rows, a->lda, st);
