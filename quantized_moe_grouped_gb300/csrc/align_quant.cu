@@ -27,6 +27,8 @@ __global__ void __launch_bounds__(kAlignThreads, 1)
                  int64_t sorted_cap, int32_t* __restrict__ expert_ids, int64_t blocks_cap,
                  int32_t* __restrict__ num_post_padded, int32_t* __restrict__ expert_offsets,
                  int32_t* __restrict__ padded_offsets, int32_t* d_status) {
+    pdl_launch_dependents();
+    pdl_wait();  // inputs from, and buffers shared with, the previous kernel
     __shared__ int s_cnt[kAlignMaxE];
     __shared__ int s_poff[kAlignMaxE + 1];
     __shared__ int s_cursor[kAlignMaxE];
@@ -136,6 +138,10 @@ QMOE_DI float block_max(float v, float* red) {
     return red[32];
 }
 
+QMOE_DI void unpack8(const uint4 w, float (&v)[8]) {
+    v[0] = bf16_lo(w.x); v[1] = bf16_hi(w.x); v[2] = bf16_lo(w.y); v[3] = bf16_hi(w.y);
+    v[4] = bf16_lo(w.z); v[5] = bf16_hi(w.z); v[6] = bf16_lo(w.w); v[7] = bf16_hi(w.w);
+}
 QMOE_DI void load8(const uint16_t* p, float (&v)[8]) {
     const uint4 w = *reinterpret_cast<const uint4*>(p);
     v[0] = bf16_lo(w.x); v[1] = bf16_hi(w.x); v[2] = bf16_lo(w.y); v[3] = bf16_hi(w.y);
@@ -201,6 +207,8 @@ __global__ void __launch_bounds__(kRowThreads)
     quant_rows_fp8_sorted_kernel(const uint16_t* __restrict__ x, int64_t cols, int64_t ldx,
                                  const int32_t* __restrict__ sorted_ids, const int32_t* __restrict__ npp,
                                  int64_t T, int top_k, uint8_t* __restrict__ q, float* __restrict__ scale) {
+    pdl_launch_dependents();
+    pdl_wait();  // inputs from, and buffers shared with, the previous kernel
     __shared__ float red[33];
     const int64_t p = blockIdx.x;
     if (p >= *npp) return;
@@ -213,7 +221,37 @@ __global__ void __launch_bounds__(kRowThreads)
         return;
     }
     const uint16_t* xr = x + static_cast<int64_t>(s / top_k) * ldx;
+    // rows of up to kRegVec * 8 * kRowThreads values are read once, into registers
+    constexpr int kRegVec = 4;
     float amax = 0.0f;
+    if (cols <= static_cast<int64_t>(kRegVec) * 8 * kRowThreads) {
+        uint4 xv[kRegVec];
+#pragma unroll
+        for (int j = 0; j < kRegVec; ++j) {
+            const int64_t c = (static_cast<int64_t>(j) * kRowThreads + threadIdx.x) * 8;
+            xv[j] = (c < cols) ? *reinterpret_cast<const uint4*>(xr + c) : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int j = 0; j < kRegVec; ++j) {
+            float v[8];
+            unpack8(xv[j], v);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
+        }
+        amax = block_max(amax, red);
+        const float sc = (amax == 0.0f) ? 1.0f : __fdiv_rn(amax, 448.0f);
+        const float rinv = __frcp_rn(sc);
+        if (threadIdx.x == 0) scale[p] = sc;
+#pragma unroll
+        for (int j = 0; j < kRegVec; ++j) {
+            const int64_t c = (static_cast<int64_t>(j) * kRowThreads + threadIdx.x) * 8;
+            if (c >= cols) break;
+            float v[8];
+            unpack8(xv[j], v);
+            *reinterpret_cast<uint2*>(qr + c) = quant8(v, sc, rinv);
+        }
+        return;
+    }
     for (int64_t c = static_cast<int64_t>(threadIdx.x) * 8; c < cols; c += kRowThreads * 8) {
         float v[8];
         load8(xr + c, v);
@@ -324,13 +362,31 @@ __global__ void __launch_bounds__(kRowThreads)
                              int32_t* __restrict__ num_post_padded, int32_t* __restrict__ expert_offsets,
                              int32_t* __restrict__ padded_offsets, uint8_t* __restrict__ q,
                              float* __restrict__ scale, int32_t* d_status) {
+    pdl_launch_dependents();
+    pdl_wait();  // inputs from, and buffers shared with, the previous kernel
     __shared__ int s_ids[kFusedMaxT];
     __shared__ int s_cnt[kAlignMaxE];
     __shared__ int s_poff[kAlignMaxE + 1];
     __shared__ int s_rank[8];
-    __shared__ float red[33];
+    __shared__ int s_redc[kRowThreads / 32][8];
+    __shared__ float s_reda[kRowThreads / 32];
+    __shared__ float s_sc;
     const int T = static_cast<int>(M) * top_k;
     const int tid = threadIdx.x;
+    // Token CTAs load their row first (rows of up to kRegVec * 8 * kRowThreads
+    // values stay in registers), so the load latency overlaps the histogram
+    // and the ranking instead of following them.
+    constexpr int kRegVec = 4;
+    const bool in_regs = cols <= static_cast<int64_t>(kRegVec) * 8 * kRowThreads;
+    uint4 xv[kRegVec];
+    if (blockIdx.x < M && in_regs) {
+        const uint16_t* xr0 = x + static_cast<int64_t>(blockIdx.x) * ldx;
+#pragma unroll
+        for (int j = 0; j < kRegVec; ++j) {
+            const int64_t c = (static_cast<int64_t>(j) * kRowThreads + tid) * 8;
+            xv[j] = (c < cols) ? *reinterpret_cast<const uint4*>(xr0 + c) : make_uint4(0u, 0u, 0u, 0u);
+        }
+    }
     for (int e = tid; e < E; e += blockDim.x) s_cnt[e] = 0;
     __syncthreads();
     if constexpr (kRoute) {
@@ -412,43 +468,91 @@ __global__ void __launch_bounds__(kRowThreads)
         }
         return;
     }
-    // token b: padded positions of its slots
-    for (int j = 0; j < top_k; ++j) {
-        const int s = static_cast<int>(b) * top_k + j;
-        const int e = s_ids[s];
-        int c = 0;
-        if (e >= 0 && e < E)
-            for (int i = tid; i < s; i += blockDim.x) c += (s_ids[i] == e);
+    // token b: the rank of each of its top_k slots among the earlier slots of
+    // the same expert, and the row amax, in one block reduction
+    const int s0 = static_cast<int>(b) * top_k;
+    int es[8], cnt[8];
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xFFFFFFFFu, c, o);
-        if ((tid & 31) == 0) red[tid >> 5] = __int_as_float(c);
-        __syncthreads();
-        if (tid == 0) {
-            int tot = 0;
-            for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) tot += __float_as_int(red[w]);
-            s_rank[j] = (e >= 0 && e < E) ? s_poff[e] + tot : -1;
-            if (e >= 0 && e < E) sorted_ids[s_poff[e] + tot] = s;
-        }
-        __syncthreads();
+    for (int j = 0; j < 8; ++j) {
+        es[j] = (j < top_k) ? s_ids[s0 + j] : -1;
+        cnt[j] = 0;
+    }
+    for (int i = tid; i < s0 + top_k; i += blockDim.x) {
+        const int ei = s_ids[i];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) cnt[j] += (j < top_k && i < s0 + j && ei == es[j]) ? 1 : 0;
     }
     const uint16_t* xr = x + b * ldx;
     float amax = 0.0f;
-    for (int64_t c = static_cast<int64_t>(tid) * 8; c < cols; c += kRowThreads * 8) {
-        float v[8];
-        load8(xr + c, v);
+    if (in_regs) {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
+        for (int j = 0; j < kRegVec; ++j) {
+            float v[8];
+            unpack8(xv[j], v);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
+        }
+    } else {
+        for (int64_t c = static_cast<int64_t>(tid) * 8; c < cols; c += kRowThreads * 8) {
+            float v[8];
+            load8(xr + c, v);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
+        }
     }
-    amax = block_max(amax, red);
-    const float sc = (amax == 0.0f) ? 1.0f : __fdiv_rn(amax, 448.0f);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+#pragma unroll
+        for (int j = 0; j < 8; ++j) cnt[j] += __shfl_xor_sync(0xFFFFFFFFu, cnt[j], o);
+    }
+    const int warp = tid >> 5;
+    if ((tid & 31) == 0) {
+        s_reda[warp] = amax;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) s_redc[warp][j] = cnt[j];
+    }
+    __syncthreads();
+    if (tid < top_k) {
+        int tot = 0;
+        for (int w = 0; w < kRowThreads / 32; ++w) tot += s_redc[w][tid];
+        const int e = s_ids[s0 + tid];
+        const bool ok = e >= 0 && e < E;
+        s_rank[tid] = ok ? s_poff[e] + tot : -1;
+        if (ok) sorted_ids[s_poff[e] + tot] = s0 + tid;
+    } else if (tid == 32) {
+        float a = 0.0f;
+        for (int w = 0; w < kRowThreads / 32; ++w) a = fmaxf(a, s_reda[w]);
+        s_sc = (a == 0.0f) ? 1.0f : __fdiv_rn(a, 448.0f);
+    }
+    __syncthreads();
+    const float sc = s_sc;
     const float rinv = __frcp_rn(sc);
     if (tid < top_k && s_rank[tid] >= 0) scale[s_rank[tid]] = sc;
-    for (int64_t c = static_cast<int64_t>(tid) * 8; c < cols; c += kRowThreads * 8) {
-        float v[8];
-        load8(xr + c, v);
-        const uint2 o = quant8(v, sc, rinv);
-        for (int j = 0; j < top_k; ++j)
-            if (s_rank[j] >= 0) *reinterpret_cast<uint2*>(q + static_cast<int64_t>(s_rank[j]) * cols + c) = o;
+    int rk[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) rk[j] = (j < top_k) ? s_rank[j] : -1;
+    if (in_regs) {
+#pragma unroll
+        for (int j = 0; j < kRegVec; ++j) {
+            const int64_t c = (static_cast<int64_t>(j) * kRowThreads + tid) * 8;
+            if (c >= cols) break;
+            float v[8];
+            unpack8(xv[j], v);
+            const uint2 o = quant8(v, sc, rinv);
+#pragma unroll
+            for (int t = 0; t < 8; ++t)
+                if (rk[t] >= 0) *reinterpret_cast<uint2*>(q + static_cast<int64_t>(rk[t]) * cols + c) = o;
+        }
+    } else {
+        for (int64_t c = static_cast<int64_t>(tid) * 8; c < cols; c += kRowThreads * 8) {
+            float v[8];
+            load8(xr + c, v);
+            const uint2 o = quant8(v, sc, rinv);
+#pragma unroll
+            for (int t = 0; t < 8; ++t)
+                if (rk[t] >= 0) *reinterpret_cast<uint2*>(q + static_cast<int64_t>(rk[t]) * cols + c) = o;
+        }
     }
 }
 
@@ -496,10 +600,6 @@ __global__ void __launch_bounds__(kRowThreads)
 // MX: one CTA per row, one thread per 1x32 block (h in registers); the CTA
 // also zeroes its row's pad columns and a share of its expert's pad rows.
 // ======================================================================
-QMOE_DI void unpack8(const uint4 w, float (&v)[8]) {
-    v[0] = bf16_lo(w.x); v[1] = bf16_hi(w.x); v[2] = bf16_lo(w.y); v[3] = bf16_hi(w.y);
-    v[4] = bf16_lo(w.z); v[5] = bf16_hi(w.z); v[6] = bf16_lo(w.w); v[7] = bf16_hi(w.w);
-}
 // h for 8 elements from raw gate / up words (already loaded).
 QMOE_DI void silu8w(const uint4 gw, const uint4 uw, float (&h)[8]) {
     float gv[8], uv[8];
@@ -757,9 +857,8 @@ qmoe_status_t qmoe_moe_align_block_size(const int32_t* topk_ids, int64_t T, int3
     if ((T > 0 && !topk_ids) || !sorted_ids || !expert_ids || !num_post_padded || !expert_offsets ||
         !padded_offsets)
         return QMOE_ERR_INVALID_ARG;
-    align_kernel<<<1, kAlignThreads, 0, stream>>>(topk_ids, T, E, BM, sorted_ids, cap, expert_ids, cap / BM,
-                                                  num_post_padded, expert_offsets, padded_offsets, d_status);
-    return launch_status();
+    return launch_pdl(align_kernel, dim3(1), dim3(kAlignThreads), 0, stream, topk_ids, T, E, BM, sorted_ids, cap,
+                      expert_ids, cap / BM, num_post_padded, expert_offsets, padded_offsets, d_status);
 }
 
 qmoe_status_t qmoe_quant_act_fp8(const uint16_t* x, int64_t rows, int64_t cols, int64_t ldx, uint8_t* q,
@@ -784,9 +883,8 @@ qmoe_status_t qmoe_quant_act_fp8_sorted(const uint16_t* x, int64_t M, int64_t co
     if (!x || !sorted_ids || !num_post_padded || !q || !scale || !aligned16(x) || !aligned16(q) ||
         cap > 0x7FFFFFFF)
         return QMOE_ERR_INVALID_ARG;
-    quant_rows_fp8_sorted_kernel<<<static_cast<unsigned>(cap), kRowThreads, 0, stream>>>(
-        x, cols, ldx, sorted_ids, num_post_padded, M * top_k, top_k, q, scale);
-    return launch_status();
+    return launch_pdl(quant_rows_fp8_sorted_kernel, dim3(static_cast<unsigned>(cap)), dim3(kRowThreads), 0, stream, x,
+                      cols, ldx, sorted_ids, num_post_padded, M * top_k, top_k, q, scale);
 }
 
 qmoe_status_t qmoe_moe_align_quant_fp8(const uint16_t* x, int64_t M, int64_t cols, int64_t ldx,
@@ -808,10 +906,10 @@ qmoe_status_t qmoe_moe_align_quant_fp8(const uint16_t* x, int64_t M, int64_t col
         if (st != QMOE_OK) return st;
         return qmoe_quant_act_fp8_sorted(x, M, cols, ldx, sorted_ids, num_post_padded, top_k, cap, q, scale, stream);
     }
-    align_quant_fused_kernel<false><<<static_cast<unsigned>(M + 1), kRowThreads, 0, stream>>>(
-        x, M, cols, ldx, topk_ids, nullptr, nullptr, nullptr, top_k, E, BM, sorted_ids, cap, expert_ids,
-        num_post_padded, expert_offsets, padded_offsets, q, scale, d_status);
-    return launch_status();
+    return launch_pdl(align_quant_fused_kernel<false>, dim3(static_cast<unsigned>(M + 1)), dim3(kRowThreads), 0, stream,
+                      x, M, cols, ldx, topk_ids, static_cast<const float*>(nullptr), static_cast<int32_t*>(nullptr),
+                      static_cast<float*>(nullptr), top_k, E, BM, sorted_ids, cap, expert_ids, num_post_padded,
+                      expert_offsets, padded_offsets, q, scale, d_status);
 }
 
 qmoe_status_t qmoe_moe_router_topk(const float* logits, int64_t M, int32_t E, int32_t top_k, int32_t* topk_ids,
@@ -847,10 +945,10 @@ qmoe_status_t qmoe_moe_route_align_quant_fp8(const float* logits, const uint16_t
         if (st != QMOE_OK) return st;
         return qmoe_quant_act_fp8_sorted(x, M, cols, ldx, sorted_ids, num_post_padded, top_k, cap, q, scale, stream);
     }
-    align_quant_fused_kernel<true><<<static_cast<unsigned>(M + 1), kRowThreads, 0, stream>>>(
-        x, M, cols, ldx, nullptr, logits, topk_ids, topk_weights, top_k, E, BM, sorted_ids, cap, expert_ids,
-        num_post_padded, expert_offsets, padded_offsets, q, scale, d_status);
-    return launch_status();
+    return launch_pdl(align_quant_fused_kernel<true>, dim3(static_cast<unsigned>(M + 1)), dim3(kRowThreads), 0, stream,
+                      x, M, cols, ldx, static_cast<const int32_t*>(nullptr), logits, topk_ids, topk_weights, top_k, E,
+                      BM, sorted_ids, cap, expert_ids, num_post_padded, expert_offsets, padded_offsets, q, scale,
+                      d_status);
 }
 
 qmoe_status_t qmoe_gather_sorted_bf16(const uint16_t* x, int64_t M, int64_t cols, int64_t ldx,

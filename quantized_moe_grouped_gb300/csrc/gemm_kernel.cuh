@@ -244,12 +244,17 @@ __global__ void __launch_bounds__(GemmCfg<kBF16, kWide, BN, kMX, kI4>::kThreads,
         s_abort = 0;
         fence_mbar_init();
     }
-    for (int i = threadIdx.x; i <= p.E; i += blockDim.x) s_poff[i] = p.padded_offsets[i];
     if constexpr (kMX) {  // weight scales 2^0: E8M0 byte 127 everywhere
         if (threadIdx.x < C::kSfBytes / 4) reinterpret_cast<uint32_t*>(sf_smem(S))[threadIdx.x] = 0x7F7F7F7Fu;
         fence_proxy_async_smem();
     }
     if (warp == 1) tmem_alloc(&s_tmem_base, C::kTmemCols);
+    // Everything above touches only this CTA's own resources and overlaps the
+    // previous kernel on the stream; from here on the kernel reads the align
+    // outputs, activations and weights and writes its outputs.
+    pdl_launch_dependents();
+    pdl_wait();
+    for (int i = threadIdx.x; i <= p.E; i += blockDim.x) s_poff[i] = p.padded_offsets[i];
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -817,8 +822,8 @@ inline qmoe_status_t launch_gemm(const void* w, int64_t E, int64_t N, int64_t K,
     const int64_t max_tiles = ((max_padded + C::kSlotRows - 1) / C::kSlotRows) * ((N + C::kWRows - 1) / C::kWRows);
     const int64_t grid = max_tiles < sms ? max_tiles : sms;
     if (grid <= 0) return QMOE_OK;
-    moe_gemm_kernel<kBF16, kWide, BN, kMX, kI4><<<static_cast<unsigned>(grid), C::kThreads, C::kDynSmem, st>>>(map, amap, p);
-    return launch_status();
+    return launch_pdl(moe_gemm_kernel<kBF16, kWide, BN, kMX, kI4>, dim3(static_cast<unsigned>(grid)),
+                      dim3(C::kThreads), C::kDynSmem, st, map, amap, p);
 }
 
 // out[i] = bf16(accum[i]) for the TOKEN_SUM layout (defined in gemm_w8a8.cu).

@@ -6,6 +6,8 @@ namespace qmoe {
 
 // out = bf16(accum), 8 elements per step (n % 8 == 0, 16-byte aligned), else 1.
 __global__ void token_sum_finalize_kernel(const float* __restrict__ accum, uint16_t* __restrict__ out, int64_t n) {
+    pdl_launch_dependents();
+    pdl_wait();  // the GEMM's sums are complete
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     const int64_t i0 = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
     if ((n & 7) == 0) {
@@ -31,8 +33,7 @@ qmoe_status_t launch_token_sum_finalize(const float* accum, uint16_t* out, int64
     int64_t blocks = (work + 255) / 256;
     const int64_t cap = static_cast<int64_t>(sms > 0 ? sms : 132) * 8;
     if (blocks > cap) blocks = cap;
-    token_sum_finalize_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(accum, out, n);
-    return launch_status();
+    return launch_pdl(token_sum_finalize_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, st, accum, out, n);
 }
 
 }  // namespace qmoe

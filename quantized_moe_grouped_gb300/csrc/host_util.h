@@ -33,4 +33,25 @@ inline qmoe_status_t launch_status() {
     return cudaPeekAtLastError() == cudaSuccess ? QMOE_OK : QMOE_ERR_CUDA;
 }
 
+// Launch with programmatic stream serialisation: the kernel may begin while
+// the previous kernel on the stream is still running; it must execute
+// griddepcontrol.wait (pdl_wait) before it reads or writes memory the previous
+// kernel touches, and may signal griddepcontrol.launch_dependents so that the
+// next kernel can begin early in turn.
+template <typename... KArgs, typename... Args>
+inline qmoe_status_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                                Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...) == cudaSuccess ? QMOE_OK : QMOE_ERR_CUDA;
+}
+
 }  // namespace qmoe
