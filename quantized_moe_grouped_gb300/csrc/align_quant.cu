@@ -633,8 +633,11 @@ struct ActIdentity {
     QMOE_DI static void apply8(const uint4 xw, const uint4, float (&h)[8]) { unpack8(xw, h); }
 };
 
-template <class Act>
-__global__ void __launch_bounds__(kRowThreads)
+// kT threads per row.  Long SwiGLU rows (ALU-bound) run 512: with the row's
+// fp32 h in shared memory that keeps 32 warps resident per SM instead of 24;
+// short rows keep 256 so that no thread idles.
+template <class Act, int kT>
+__global__ void __launch_bounds__(kT)
     act_quant_token_kernel(const uint16_t* __restrict__ y, int64_t I, int64_t ldy, uint8_t* __restrict__ q,
                            float* __restrict__ scale) {
     extern __shared__ float s_h[];
@@ -642,11 +645,11 @@ __global__ void __launch_bounds__(kRowThreads)
     const int64_t row = blockIdx.x;
     const uint16_t* yr = y + row * ldy;
     float amax = 0.0f;
-    for (int64_t c0 = static_cast<int64_t>(threadIdx.x) * 8; c0 < I; c0 += kRowThreads * 8 * kSiluBatch) {
+    for (int64_t c0 = static_cast<int64_t>(threadIdx.x) * 8; c0 < I; c0 += kT * 8 * kSiluBatch) {
         uint4 gw[kSiluBatch], uw[kSiluBatch];
 #pragma unroll
         for (int j = 0; j < kSiluBatch; ++j) {
-            const int64_t c = c0 + static_cast<int64_t>(j) * kRowThreads * 8;
+            const int64_t c = c0 + static_cast<int64_t>(j) * kT * 8;
             if (c < I) {
                 gw[j] = *reinterpret_cast<const uint4*>(yr + c);
                 uw[j] = Act::kGated ? *reinterpret_cast<const uint4*>(yr + I + c) : make_uint4(0u, 0u, 0u, 0u);
@@ -654,7 +657,7 @@ __global__ void __launch_bounds__(kRowThreads)
         }
 #pragma unroll
         for (int j = 0; j < kSiluBatch; ++j) {
-            const int64_t c = c0 + static_cast<int64_t>(j) * kRowThreads * 8;
+            const int64_t c = c0 + static_cast<int64_t>(j) * kT * 8;
             if (c < I) {
                 float h[8];
                 Act::apply8(gw[j], uw[j], h);
@@ -670,7 +673,7 @@ __global__ void __launch_bounds__(kRowThreads)
     const float rinv = __frcp_rn(s);
     if (threadIdx.x == 0) scale[row] = s;
     uint8_t* qr = q + row * I;
-    for (int64_t c = static_cast<int64_t>(threadIdx.x) * 8; c < I; c += kRowThreads * 8) {
+    for (int64_t c = static_cast<int64_t>(threadIdx.x) * 8; c < I; c += kT * 8) {
         const float4 a = *reinterpret_cast<const float4*>(s_h + c);
         const float4 b = *reinterpret_cast<const float4*>(s_h + c + 4);
         const float h[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
@@ -814,12 +817,17 @@ static qmoe_status_t run_act_quant(const uint16_t* y, int64_t rows, int64_t I, i
         if (!scale) return QMOE_ERR_INVALID_ARG;
         const size_t smem = static_cast<size_t>(I) * sizeof(float);
         if (smem > 200 * 1024) return QMOE_ERR_UNSUPPORTED;
+        const bool wide = Act::kGated && I >= 8192;
         if (smem > 48 * 1024) {
-            if (cudaFuncSetAttribute(act_quant_token_kernel<Act>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     static_cast<int>(smem)) != cudaSuccess)
+            if (cudaFuncSetAttribute(wide ? act_quant_token_kernel<Act, 512> : act_quant_token_kernel<Act, kRowThreads>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess)
                 return QMOE_ERR_CUDA;
         }
-        act_quant_token_kernel<Act><<<static_cast<unsigned>(rows), kRowThreads, smem, stream>>>(y, I, ldy, q, scale);
+        if (wide)
+            act_quant_token_kernel<Act, 512><<<static_cast<unsigned>(rows), 512, smem, stream>>>(y, I, ldy, q, scale);
+        else
+            act_quant_token_kernel<Act, kRowThreads><<<static_cast<unsigned>(rows), kRowThreads, smem, stream>>>(
+                y, I, ldy, q, scale);
         return launch_status();
     }
     if (mode == QMOE_SCALE_MX_1X32) {

@@ -117,7 +117,7 @@ def test_quant_weights_bitexact(q, orc, E, N, K):
     assert np.array_equal(wq8.cpu().numpy(), rq8) and np.array_equal(ws8.cpu().numpy(), rs8)
 
 
-@pytest.mark.parametrize("R,I", [(64, 256), (300, 1024), (8, 14336), (3, 40)])
+@pytest.mark.parametrize("R,I", [(64, 256), (300, 1024), (8, 14336), (3, 40), (5, 8200)])
 def test_silu_quant_token_bitexact(q, orc, R, I):
     y = inputs.activations_bf16(R, 2 * I, seed=R + I)
     y[0, :] = 0
