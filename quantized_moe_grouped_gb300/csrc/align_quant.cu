@@ -201,71 +201,97 @@ __global__ void __launch_bounds__(kRowThreads)
     }
 }
 
-// Per-token FP8 quantisation written in padded sorted order (one CTA per
-// padded position; the token row is re-quantised for each of its slots).
+// Per-token FP8 quantisation written in padded sorted order: one warp per
+// padded position (8 per CTA, grid-stride), so no block barrier sits between
+// a row's loads and its stores.  Rows of up to kWarpVec * 8 * 32 values are
+// read once into registers with all loads in flight; longer rows are read in
+// batches of kWarpVec loads per lane, twice (amax, then codes; the second
+// pass mostly hits L1/L2).  The amax is a warp shuffle reduction.  The token
+// row is quantised again for each of its slots (the second read hits L2).
+constexpr int kWarpVec = 4;
 __global__ void __launch_bounds__(kRowThreads)
     quant_rows_fp8_sorted_kernel(const uint16_t* __restrict__ x, int64_t cols, int64_t ldx,
                                  const int32_t* __restrict__ sorted_ids, const int32_t* __restrict__ npp,
                                  int64_t T, int top_k, uint8_t* __restrict__ q, float* __restrict__ scale) {
     pdl_launch_dependents();
     pdl_wait();  // inputs from, and buffers shared with, the previous kernel
-    __shared__ float red[33];
-    const int64_t p = blockIdx.x;
-    if (p >= *npp) return;
-    const int s = sorted_ids[p];
-    uint8_t* qr = q + p * cols;
-    if (s < 0 || s >= T) {  // pad position
-        for (int64_t c = static_cast<int64_t>(threadIdx.x) * 16; c < cols; c += kRowThreads * 16)
-            *reinterpret_cast<uint4*>(qr + c) = make_uint4(0u, 0u, 0u, 0u);
-        if (threadIdx.x == 0) scale[p] = 0.0f;
-        return;
-    }
-    const uint16_t* xr = x + static_cast<int64_t>(s / top_k) * ldx;
-    // rows of up to kRegVec * 8 * kRowThreads values are read once, into registers
-    constexpr int kRegVec = 4;
-    float amax = 0.0f;
-    if (cols <= static_cast<int64_t>(kRegVec) * 8 * kRowThreads) {
-        uint4 xv[kRegVec];
+    const int lane = threadIdx.x & 31;
+    const int64_t warps = static_cast<int64_t>(gridDim.x) * (kRowThreads / 32);
+    const int64_t n = *npp;
+    const bool in_regs = cols <= static_cast<int64_t>(kWarpVec) * 8 * 32;
+    for (int64_t p = static_cast<int64_t>(blockIdx.x) * (kRowThreads / 32) + (threadIdx.x >> 5); p < n;
+         p += warps) {
+        const int s = sorted_ids[p];
+        uint8_t* qr = q + p * cols;
+        if (s < 0 || s >= T) {  // pad position
+            for (int64_t c = static_cast<int64_t>(lane) * 16; c < cols; c += 32 * 16)
+                *reinterpret_cast<uint4*>(qr + c) = make_uint4(0u, 0u, 0u, 0u);
+            if (lane == 0) scale[p] = 0.0f;
+            continue;
+        }
+        const uint16_t* xr = x + static_cast<int64_t>(s / top_k) * ldx;
+        float amax = 0.0f;
+        uint4 xv[kWarpVec];
+        if (in_regs) {
 #pragma unroll
-        for (int j = 0; j < kRegVec; ++j) {
-            const int64_t c = (static_cast<int64_t>(j) * kRowThreads + threadIdx.x) * 8;
-            xv[j] = (c < cols) ? *reinterpret_cast<const uint4*>(xr + c) : make_uint4(0u, 0u, 0u, 0u);
+            for (int j = 0; j < kWarpVec; ++j) {
+                const int64_t c = (static_cast<int64_t>(j) * 32 + lane) * 8;
+                xv[j] = (c < cols) ? *reinterpret_cast<const uint4*>(xr + c) : make_uint4(0u, 0u, 0u, 0u);
+            }
+#pragma unroll
+            for (int j = 0; j < kWarpVec; ++j) {
+                float v[8];
+                unpack8(xv[j], v);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
+            }
+        } else {
+            for (int64_t c0 = 0; c0 < cols; c0 += static_cast<int64_t>(kWarpVec) * 32 * 8) {
+#pragma unroll
+                for (int j = 0; j < kWarpVec; ++j) {
+                    const int64_t c = c0 + (static_cast<int64_t>(j) * 32 + lane) * 8;
+                    xv[j] = (c < cols) ? *reinterpret_cast<const uint4*>(xr + c) : make_uint4(0u, 0u, 0u, 0u);
+                }
+#pragma unroll
+                for (int j = 0; j < kWarpVec; ++j) {
+                    float v[8];
+                    unpack8(xv[j], v);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
+                }
+            }
         }
 #pragma unroll
-        for (int j = 0; j < kRegVec; ++j) {
-            float v[8];
-            unpack8(xv[j], v);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
-        }
-        amax = block_max(amax, red);
+        for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
         const float sc = (amax == 0.0f) ? 1.0f : __fdiv_rn(amax, 448.0f);
         const float rinv = __frcp_rn(sc);
-        if (threadIdx.x == 0) scale[p] = sc;
+        if (lane == 0) scale[p] = sc;
+        if (in_regs) {
 #pragma unroll
-        for (int j = 0; j < kRegVec; ++j) {
-            const int64_t c = (static_cast<int64_t>(j) * kRowThreads + threadIdx.x) * 8;
-            if (c >= cols) break;
-            float v[8];
-            unpack8(xv[j], v);
-            *reinterpret_cast<uint2*>(qr + c) = quant8(v, sc, rinv);
+            for (int j = 0; j < kWarpVec; ++j) {
+                const int64_t c = (static_cast<int64_t>(j) * 32 + lane) * 8;
+                if (c >= cols) break;
+                float v[8];
+                unpack8(xv[j], v);
+                *reinterpret_cast<uint2*>(qr + c) = quant8(v, sc, rinv);
+            }
+        } else {
+            for (int64_t c0 = 0; c0 < cols; c0 += static_cast<int64_t>(kWarpVec) * 32 * 8) {
+#pragma unroll
+                for (int j = 0; j < kWarpVec; ++j) {
+                    const int64_t c = c0 + (static_cast<int64_t>(j) * 32 + lane) * 8;
+                    xv[j] = (c < cols) ? *reinterpret_cast<const uint4*>(xr + c) : make_uint4(0u, 0u, 0u, 0u);
+                }
+#pragma unroll
+                for (int j = 0; j < kWarpVec; ++j) {
+                    const int64_t c = c0 + (static_cast<int64_t>(j) * 32 + lane) * 8;
+                    if (c >= cols) break;
+                    float v[8];
+                    unpack8(xv[j], v);
+                    *reinterpret_cast<uint2*>(qr + c) = quant8(v, sc, rinv);
+                }
+            }
         }
-        return;
-    }
-    for (int64_t c = static_cast<int64_t>(threadIdx.x) * 8; c < cols; c += kRowThreads * 8) {
-        float v[8];
-        load8(xr + c, v);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
-    }
-    amax = block_max(amax, red);
-    const float sc = (amax == 0.0f) ? 1.0f : __fdiv_rn(amax, 448.0f);
-    const float rinv = __frcp_rn(sc);
-    if (threadIdx.x == 0) scale[p] = sc;
-    for (int64_t c = static_cast<int64_t>(threadIdx.x) * 8; c < cols; c += kRowThreads * 8) {
-        float v[8];
-        load8(xr + c, v);
-        *reinterpret_cast<uint2*>(qr + c) = quant8(v, sc, rinv);
     }
 }
 
@@ -891,8 +917,12 @@ qmoe_status_t qmoe_quant_act_fp8_sorted(const uint16_t* x, int64_t M, int64_t co
     if (!x || !sorted_ids || !num_post_padded || !q || !scale || !aligned16(x) || !aligned16(q) ||
         cap > 0x7FFFFFFF)
         return QMOE_ERR_INVALID_ARG;
-    return launch_pdl(quant_rows_fp8_sorted_kernel, dim3(static_cast<unsigned>(cap)), dim3(kRowThreads), 0, stream, x,
-                      cols, ldx, sorted_ids, num_post_padded, M * top_k, top_k, q, scale);
+    // enough warps to cover every padded position once, at most 8 CTAs per SM (grid-stride beyond)
+    const int64_t want = (cap + kRowThreads / 32 - 1) / (kRowThreads / 32);
+    const int64_t most = static_cast<int64_t>(device_sm_count() > 0 ? device_sm_count() : 132) * 8;
+    const int64_t blocks = want < most ? want : most;
+    return launch_pdl(quant_rows_fp8_sorted_kernel, dim3(static_cast<unsigned>(blocks)), dim3(kRowThreads), 0, stream,
+                      x, cols, ldx, sorted_ids, num_post_padded, M * top_k, top_k, q, scale);
 }
 
 qmoe_status_t qmoe_moe_align_quant_fp8(const uint16_t* x, int64_t M, int64_t cols, int64_t ldx,
