@@ -81,7 +81,10 @@ constexpr int kGemmMaxE = 256;  // experts per call (the align's limit)
 // scale per 128-wide group along K, applied by the converters (wide tile only).
 template <bool kBF16, bool kWide, int BN, bool kMX = false, bool kI4 = false>
 struct GemmCfg {
-    static constexpr int kSlotRows = kWide ? 128 : BN;      // slots per tile
+    // kW2 (wide, BN = 256): two 128-slot halves share every weight stage, one
+    // accumulator each -- one weight pass serves both slot blocks of a 256 block
+    static constexpr bool kW2 = kWide && BN == 256;
+    static constexpr int kSlotRows = BN;                     // slots per tile
     static constexpr int kWRows = kWide ? 256 : 128;        // weight rows (output channels) per tile
     static constexpr int kMmaN = kWide ? 256 : BN;
     static constexpr int kBK = kBF16 ? 64 : 128;            // K elements per stage (128 bytes of MMA operand)
@@ -102,7 +105,8 @@ struct GemmCfg {
     // ahead of the gather warps, so the lag shrinks when the ring is short.
     static constexpr int kLag = kStages >= 6 ? 3 : (kStages >= 5 ? 2 : 1);
     static constexpr int kBProdThreads = 64;
-    static constexpr int kEpiThreads = kMX ? 256 : 128;   // MX: two groups of four warps, one per column half
+    // MX: two groups of four warps, one per column half; kW2: one per slot half
+    static constexpr int kEpiThreads = (kMX || kW2) ? 256 : 128;
     // MX: a stage's scales in shared memory, as 512-byte blocks of 32 x 16
     // bytes: the 128 activation rows, then the two 128-row halves of the 256
     // weight rows (MXFP8 weights only)
@@ -112,20 +116,22 @@ struct GemmCfg {
     // stage), 4 for the swapped one; groups alternate stages
     static constexpr int kConvThreads = (kBF16 && kWide) ? 256 : 128;
     static constexpr int kConvGroups = kBF16 ? 2 : 1;       // converter groups alternate stages
-    static constexpr int kThreads = kBF16 ? 256 + 2 * kConvThreads : (kMX ? 384 : 256);
+    static constexpr int kThreads = kBF16 ? 256 + 2 * kConvThreads : ((kMX || kW2) ? 384 : 256);
     static constexpr int kAccCols = kMmaN;                  // TMEM columns per accumulator
     // MX: one accumulator (256 columns), then four scale columns per stage for
     // the 128 activation rows (4-column aligned) and 8 columns of constant
     // weight scales 2^0 (8-column aligned), all copied in from shared memory
     // by the MMA thread.
-    static constexpr int kAccBufs = kMX ? 1 : 2;
+    static constexpr int kAccBufs = (kMX || kW2) ? 1 : 2;   // kW2: the one buffer is both halves' accumulators
     static constexpr int kSfaCol = kAccCols;
     static constexpr int kSfbCol = (kAccCols + 4 * kStages + 7) / 8 * 8;
-    static constexpr int kTmemCols = kMX ? 512 : (2 * kAccCols < 32 ? 32 : 2 * kAccCols);
+    static constexpr int kTmemCols = (kMX || kW2) ? 512 : (2 * kAccCols < 32 ? 32 : 2 * kAccCols);
     static constexpr uint32_t kIdesc =
         kMX ? make_idesc_mx(128, kMmaN) : make_idesc(kBF16 ? kFmtBF16 : kFmtE4M3, 128, kMmaN);
     static_assert(!kMX || (kWide && !kBF16), "MX scales: FP8 wide tile only");
     static_assert(!kI4 || (kBF16 && kWide), "W4A16: wide bf16 tile only");
+    static_assert(!kWide || BN == 128 || BN == 256, "wide tile: 128 or 256 slots");
+    static_assert(!kW2 || (!kBF16 && !kMX), "two-half tile: FP8 with per-row scales only");
     static_assert(!kMX || kSfbCol + 8 * kStages <= 512, "TMEM columns");  // per-stage weight scales
     static constexpr int kDynSmem =
         kStages * kStageBytes + kRawStages * kRawBytes + (kMX ? kStages * kSfStageBytes + kSfBytes : 0) + 1024;
@@ -214,6 +220,7 @@ __global__ void __launch_bounds__(GemmCfg<kBF16, kWide, BN, kMX, kI4>::kThreads,
     __shared__ int32_t s_crow[kWide ? 1 : SR];     // swapped epilogue: output row per column (-1: padding)
     __shared__ float s_wsc[kWide ? WR : 1];        // wide epilogue: w_scale per column
     __shared__ int32_t s_poff[kGemmMaxE + 1];      // padded_offsets: first padded position of each expert
+    __shared__ int32_t s_ppre[C::kW2 ? kGemmMaxE + 1 : 1];  // kW2: tile pairs of the experts before e
 
     const uint32_t raw_addr = smem_u32(smem_raw);
     uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
@@ -255,6 +262,22 @@ __global__ void __launch_bounds__(GemmCfg<kBF16, kWide, BN, kMX, kI4>::kThreads,
     pdl_launch_dependents();
     pdl_wait();
     for (int i = threadIdx.x; i <= p.E; i += blockDim.x) s_poff[i] = p.padded_offsets[i];
+    if (C::kW2 && warp == 0) {
+        // s_ppre[i] = sum over experts e < i of ceil(128-slot blocks of e / 2), a warp scan per 32 experts
+        int base = 0;
+        for (int c = 0; c <= p.E; c += 32) {
+            const int i = c + lane;
+            const int v = i < p.E ? ((p.padded_offsets[i + 1] - p.padded_offsets[i]) / 128 + 1) / 2 : 0;
+            int x = v;
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+                const int y = __shfl_up_sync(0xFFFFFFFFu, x, d);
+                if (lane >= d) x += y;
+            }
+            if (i <= p.E) s_ppre[i] = base + x - v;
+            base += __shfl_sync(0xFFFFFFFFu, x, 31);
+        }
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -262,7 +285,8 @@ __global__ void __launch_bounds__(GemmCfg<kBF16, kWide, BN, kMX, kI4>::kThreads,
     volatile int* abort = &s_abort;
 
     const int n_blocks = static_cast<int>((p.N + WR - 1) / WR);
-    const int num_tiles = s_poff[p.E] / SR * n_blocks;
+    const int num_tiles = C::kW2 ? s_ppre[p.E] * n_blocks : s_poff[p.E] / SR * n_blocks;
+    constexpr int SRB = C::kW2 ? 128 : SR;  // padded rows per unit of the slot-block index sb
     const int nkb = p.num_k_blocks;
     auto w_tile = [&](int s) { return smem + s * C::kStageBytes; };
     auto act_tile = [&](int s) { return smem + s * C::kStageBytes + C::kWBytes; };
@@ -275,7 +299,24 @@ __global__ void __launch_bounds__(GemmCfg<kBF16, kWide, BN, kMX, kI4>::kThreads,
     // the tile is to be skipped: (tiles narrower than BM) a tile whose first
     // slot is padding -- valid slots precede the padding inside an expert's
     // region, so the whole tile is padding then.
+    //
+    // kW2: the tiles of an expert are the pairs of consecutive 128-slot blocks
+    // of its region (the last pair may hold one block), numbered like the
+    // blocks above; sb is then the index of the pair's first 128-slot block.
     auto tile_expert = [&](int tile, int& sb, int& nb) {
+        if constexpr (C::kW2) {
+            int lo = 0, hi = p.E - 1;
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (s_ppre[mid] * n_blocks <= tile) lo = mid;
+                else hi = mid - 1;
+            }
+            const int np = s_ppre[lo + 1] - s_ppre[lo];
+            const int local = tile - s_ppre[lo] * n_blocks;
+            nb = local / np;
+            sb = s_poff[lo] / 128 + 2 * (local % np);
+            return lo;
+        }
         int lo = 0, hi = p.E - 1;
         while (lo < hi) {
             const int mid = (lo + hi + 1) >> 1;
@@ -289,6 +330,11 @@ __global__ void __launch_bounds__(GemmCfg<kBF16, kWide, BN, kMX, kI4>::kThreads,
         sb = sb0 + local % nsb;
         if (SR < p.BM && p.sorted_ids[sb * SR] >= p.T) return -1;
         return lo;
+    };
+    // kW2: whether the tile's second 128-slot block lies in expert e's region
+    // and holds a valid slot (valid slots precede the padding in a region)
+    auto second_half = [&](int e, int sb) {
+        return sb + 1 < s_poff[e + 1] / 128 && p.sorted_ids[(sb + 1) * 128] < p.T;
     };
 
     if (warp == 0) {
@@ -304,8 +350,8 @@ __global__ void __launch_bounds__(GemmCfg<kBF16, kWide, BN, kMX, kI4>::kThreads,
                 if (e < 0) continue;
                 // first activation row of the tile: padded position, or compact grouped row
                 const int arow0 = (p.a_layout == QMOE_A_PADDED)
-                                      ? sb * SR
-                                      : p.expert_offsets[e] + (sb * SR - p.padded_offsets[e]);
+                                      ? sb * SRB
+                                      : p.expert_offsets[e] + (sb * SRB - p.padded_offsets[e]);
                 for (int kb = 0; kb < nkb; ++kb, ++it) {
                     if constexpr (kBF16) {  // raw int8 weights into their own ring
                         const int r = it % R;
@@ -344,12 +390,14 @@ __global__ void __launch_bounds__(GemmCfg<kBF16, kWide, BN, kMX, kI4>::kThreads,
             }
             for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
                 int sb, nb;
-                if (tile_expert(tile, sb, nb) < 0) continue;
+                const int e = tile_expert(tile, sb, nb);
+                if (e < 0) continue;
                 const int acc = tcount % C::kAccBufs;
                 const uint32_t aph = (tcount / C::kAccBufs) & 1;
                 if (!mbar_wait(&bar_tempty[acc], aph ^ 1, abort, p.d_status)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * C::kAccCols);
+                const bool half2 = C::kW2 && second_half(e, sb);  // kW2: accumulator at columns +256
                 for (int kb = 0; kb < nkb; ++kb, ++it) {
                     const int s = it % S;
                     const uint32_t ph = (it / S) & 1;
@@ -379,6 +427,14 @@ __global__ void __launch_bounds__(GemmCfg<kBF16, kWide, BN, kMX, kI4>::kThreads,
                                      (kb | k) != 0);
                         else if (kBF16) mma_f16(d_tmem, da + 2 * k, db + 2 * k, C::kIdesc, (kb | k) != 0);
                         else mma_f8f6f4(d_tmem, da + 2 * k, db + 2 * k, C::kIdesc, (kb | k) != 0);
+                    }
+                    if constexpr (C::kW2) {
+                        if (half2) {
+                            const uint64_t dx2 = desc_kmajor_sw128(smem_u32(act_tile(s) + 128 * 128));
+#pragma unroll
+                            for (int k = 0; k < 4; ++k)
+                                mma_f8f6f4(d_tmem + 256, dx2 + 2 * k, dw + 2 * k, C::kIdesc, (kb | k) != 0);
+                        }
                     }
                     tc_commit(&bar_empty[s]);
                 }
@@ -508,10 +564,11 @@ __global__ void __launch_bounds__(GemmCfg<kBF16, kWide, BN, kMX, kI4>::kThreads,
         cp_async_wait<0>();
         fence_proxy_async_smem();
         for (int j = (it > C::kLag ? it - C::kLag : 0); j < it; ++j) mbar_arrive(&bar_full[j % S]);
-    } else if (warp < 8 || kMX) {
+    } else if (warp < 8 || kMX || C::kW2) {
         // ------------------------------------------------- epilogue ---
         const int et = threadIdx.x - 128;
         const int q = warp & 3;  // TMEM lane quadrant of this warp
+        const int hs = C::kW2 ? (warp - 4) >> 2 : 0;  // kW2: slot half (accumulator) of this group
         int tcount = 0;
         for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
             if (*abort) break;
@@ -521,7 +578,7 @@ __global__ void __launch_bounds__(GemmCfg<kBF16, kWide, BN, kMX, kI4>::kThreads,
             const int acc = tcount % C::kAccBufs;
             const uint32_t aph = (tcount / C::kAccBufs) & 1;
             const uint32_t t_base =
-                tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * C::kAccCols);
+                tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * C::kAccCols + hs * 256);
             if constexpr (kWide) {
                 // lane = slot row, columns = 256 output channels
                 named_bar_sync(2, C::kEpiThreads);
@@ -530,8 +587,9 @@ __global__ void __launch_bounds__(GemmCfg<kBF16, kWide, BN, kMX, kI4>::kThreads,
                     s_wsc[c] = (n < p.N) ? (p.w_scale ? p.w_scale[static_cast<int64_t>(e) * p.N + n] : 1.0f) : 0.0f;
                 }
                 named_bar_sync(2, C::kEpiThreads);
-                const int pos = sb * SR + q * 32 + lane;
-                const int s = p.sorted_ids[pos];
+                const int pos = sb * SRB + hs * 128 + q * 32 + lane;
+                const bool in_tile = !C::kW2 || hs == 0 || second_half(e, sb);
+                const int s = in_tile ? p.sorted_ids[pos] : -1;
                 const bool valid = s >= 0 && s < p.T;
                 float rs = 0.0f;
                 int64_t orow = 0;
@@ -819,7 +877,9 @@ inline qmoe_status_t launch_gemm(const void* w, int64_t E, int64_t N, int64_t K,
     if (p.a_tma && !make_act_map(&amap, p.a, a_rows, K, lda, kBF16 ? 2 : 1, C::kSlotRows)) return QMOE_ERR_CUDA;
     const int sms = device_sm_count();
     if (sms <= 0) return QMOE_ERR_CUDA;
-    const int64_t max_tiles = ((max_padded + C::kSlotRows - 1) / C::kSlotRows) * ((N + C::kWRows - 1) / C::kWRows);
+    // (kW2: the last pair of an expert may hold a single 128-slot block)
+    const int64_t max_tiles = ((max_padded + C::kSlotRows - 1) / C::kSlotRows + (C::kW2 ? E : 0)) *
+                              ((N + C::kWRows - 1) / C::kWRows);
     const int64_t grid = max_tiles < sms ? max_tiles : sms;
     if (grid <= 0) return QMOE_OK;
     return launch_pdl(moe_gemm_kernel<kBF16, kWide, BN, kMX, kI4>, dim3(static_cast<unsigned>(grid)),
@@ -922,6 +982,16 @@ inline qmoe_status_t run_moe_gemm(const qmoe_gemm_args* a, cudaStream_t st) {
     if constexpr (!kBF16) {
         if (mx) {
             r = launch_gemm<false, true, 128, true>(a->w, a->E, a->N, a->K, p, max_padded, a_rows, a->lda, st);
+            if (r != QMOE_OK || !tsum) return r;
+            return launch_token_sum_finalize(a->accum, a->out, a->M * a->N, st);
+        }
+    }
+    if constexpr (!kBF16) {
+        // long K (e.g. a down projection): one weight pass for two 128-slot
+        // blocks, which halves the weight-operand reads per MMA; at short K the
+        // single accumulator buffer costs more than that saves
+        if (a->BM >= 128 && p.a_tma && a->K >= 8192) {
+            r = launch_gemm<false, true, 256>(a->w, a->E, a->N, a->K, p, max_padded, a_rows, a->lda, st);
             if (r != QMOE_OK || !tsum) return r;
             return launch_token_sum_finalize(a->accum, a->out, a->M * a->N, st);
         }

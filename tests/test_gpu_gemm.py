@@ -295,6 +295,69 @@ def test_w8a8_mx_activations(q, orc, M, I, N, E, BM, zipf, out_layout):
     check(bf16_to_np_f32(out), ref)
 
 
+@pytest.mark.parametrize("a_layout,out_layout", [(2, 0), (2, 2), (1, 1), (1, 2)])
+@pytest.mark.parametrize("M,K,N,E,top_k,zipf,BM,rows", [
+    (700, 8288, 272, 8, 2, None, 128, None),     # ~175 slots per expert: pairs with both halves; ragged K and N
+    (300, 8192, 256, 4, 1, None, 256, None),     # ~75 slots per expert: every second half empty
+    (1000, 8192, 3072, 8, 2, 1.2, 128, 24),      # Zipf skew, more tiles than SMs: 24 sampled tokens
+    (150, 8192, 272, 16, 2, None, 128, None),    # five experts that receive nothing
+])
+def test_w8a8_two_half_tile(q, orc, a_layout, out_layout, M, K, N, E, top_k, zipf, BM, rows):
+    """K >= 8192 with activation rows loaded by TMA (PADDED from
+    quant_act_fp8_sorted, or GROUPED) runs the two-half tile: one weight pass
+    serves two consecutive 128-slot blocks of an expert, one accumulator each,
+    and the second is skipped when it lies outside the expert's region or holds
+    only padding.  Whole outputs, or the rows of sampled tokens."""
+    T = M * top_k
+    seed = M + 13 * N
+    ids = tw = None
+    if E == 16:
+        ids, tw = inputs.routing(M, 11, top_k, seed)
+        ids = np.where(ids < 5, ids, ids + 5).astype(np.int32)   # experts 5..9 empty
+    p = fp8_problem(q, orc, M, K, N, E, top_k, seed=seed, zipf=zipf, ids=ids, tw=tw)
+    al = q.moe_align_block_size(to_dev(p["ids"]), E, BM)
+    if a_layout == q.A_PADDED:
+        a_in, s_in = q.quant_act_fp8_sorted(to_dev_bf16(p["a"]), al, top_k)
+        ref_al = orc.moe_align(p["ids"], E, BM)
+        n = ref_al["num_post_padded"]
+        srt = ref_al["sorted_ids"][:n]
+        valid = srt < T
+        ra = np.zeros((a_in.shape[0], K), dtype=np.uint8)
+        rs = np.zeros(a_in.shape[0], dtype=np.float32)
+        ra[:n][valid] = p["raq"][srt[valid] // top_k]
+        rs[:n][valid] = p["rsa"][srt[valid] // top_k]
+        assert np.array_equal(a_in.cpu().numpy()[:n][valid], ra[:n][valid])
+        ref_layout = "padded"
+    else:
+        order = np.empty(T, dtype=np.int64)
+        order[orc.compact_row_of_slot(p["ids"], E)] = np.arange(T)
+        src = order // top_k                               # compact row -> token row
+        a_in, s_in = p["aq"][to_dev(src)].contiguous(), p["sa"][to_dev(src)].contiguous()
+        ra, rs = p["raq"][src], p["rsa"][src]
+        ref_layout = "grouped"
+    st = status()
+    out = q.moe_gemm_w8a8(a_in, s_in, p["wq"], p["ws"], al, to_dev(p["tw"]), M=M, top_k=top_k, BM=BM,
+                          a_layout=a_layout, out_layout=out_layout, d_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    got = bf16_to_np_f32(out)
+    args = dict(a_kind=orc.A_FP8_TOKEN, a=ra, a_scale=rs, w_kind=orc.W_FP8, w=p["rwq"], w_scale=p["rws"],
+                topk_ids=p["ids"], topk_w=p["tw"], E=E, a_layout=ref_layout, BM=BM)
+    if rows is None:
+        ref = orc.moe_gemm(out_layout={0: "slot", 1: "grouped", 2: "token_sum"}[out_layout], **args)
+        check(got, ref)
+        return
+    toks = np.random.default_rng(seed).choice(M, rows, replace=False)
+    slots = (toks[:, None] * top_k + np.arange(top_k)[None, :]).ravel()
+    per_slot = orc.moe_gemm(slots=slots, **args)
+    if out_layout == q.OUT_TOKEN_SUM:
+        check(got[toks], per_slot.reshape(rows, top_k, N).sum(axis=1))
+    elif out_layout == q.OUT_GROUPED:
+        check(got[orc.compact_row_of_slot(p["ids"], E)[slots]], per_slot)
+    else:
+        check(got[slots], per_slot)
+
+
 @pytest.mark.parametrize("M,K,N,E,top_k,BM,out_layout", [(64, 4096, 256, 8, 2, 32, 0), (200, 272, 208, 8, 2, 64, 2),
                                                          (520, 256, 400, 8, 2, 128, 0), (90, 160, 272, 5, 3, 256, 2),
                                                          (33, 512, 128, 4, 2, 16, 0)])
