@@ -460,6 +460,14 @@ def run_suite(reps: int = 20, only: str | None = None) -> None:
                                             a_layout=q.A_PADDED, out_layout=q.OUT_GROUPED, out=up), reps, flush)
         line(wl.name, "moe_gemm_w8a8 up (padded A -> grouped out)", ms,
              hit * 2 * I * K + hit * 2 * I * 4 + T * (K + 4) + T * 2 * I * 2, 2.0 * T * K * 2 * I, "fp8")
+        if wl.act_scale == "mx":  # the same projection with SwiGLU + MXFP8 in its epilogue
+            fq = torch.empty(T, I, dtype=torch.uint8, device=dev)
+            fsf = torch.empty(q.align_max_padded(T, E, 128), q.mx_sf_ld(I), dtype=torch.uint8, device=dev)
+            ms = _timed(lambda: q.moe_gemm_w8a8_silu_mxfp8(aq, sa, w1q, w1s, al, M=M, top_k=TOP_K,
+                                                           a_layout=q.A_PADDED, q=fq, sf=fsf), reps, flush)
+            line(wl.name, "moe_gemm_w8a8 up + SwiGLU + MXFP8 epilogue (padded A -> grouped e4m3 + E8M0)", ms,
+                 hit * 2 * I * K + hit * 2 * I * 4 + T * (K + 4) + T * I + T * (I // 32), 2.0 * T * K * 2 * I, "fp8")
+            del fq, fsf
         del w1q, w1s
         if wl.act_scale == "token":
             hq, hs = q.silu_mul_quant(up)

@@ -392,6 +392,29 @@ qmoe_status_t qmoe_srelu_quant(const uint16_t* y, int64_t rows, int64_t I, int64
                                const int32_t* sf_padded_offsets, int32_t E, int32_t* d_status,
                                qmoe_stream_t stream);
 
+/* FP8 up projection with SwiGLU + MXFP8 in the GEMM epilogue: the fused
+ * activation + MXFP8 quantisation of "[PyTorch] Let GroupedLinear accept
+ * MXFP8 input and gradient" (TransformerEngine PR 2099, Description) moved
+ * into the producing GEMM.  The result is the same as
+ *   qmoe_moe_gemm_w8a8(args) with out_layout QMOE_OUT_GROUPED -> y bf16 [T, N]
+ *   qmoe_silu_mul_quant(y, rows = T, I = N/2, mode QMOE_SCALE_MX_1X32, ...)
+ * bit for bit, but y never reaches memory: each bf16 value is rounded exactly
+ * as that GEMM stores it and the SwiGLU and the 1x32 block factors are
+ * computed from it in registers.  args describes the [gate | up] projection
+ * (w [E, N, K] with gate rows [0, N/2) and up rows [N/2, N), per-row
+ * w_scale, per-token a_scale, any activation layout); args->out and
+ * args->accum are unused (out may be NULL) and out_layout must be
+ * QMOE_OUT_GROUPED.  Outputs, as qmoe_silu_mul_quant's MX mode with
+ * I = N/2: q [T, I] e4m3 codes in compact grouped rows (16-byte aligned) and
+ * sf [.., sf_ld] E8M0 factors, row r of expert e at sf row
+ * sf_padded_offsets[e] + (r - expert_offsets[e]); the expert's pad rows up to
+ * sf_padded_offsets[e+1] and the columns past I/32 are zeroed.
+ * sf_padded_offsets must be the padded_offsets of the BM = 128 align the GEMM
+ * uses.  Limits: BM == 128, N % 256 == 0, sf_ld >= N/64, FP8 per-token
+ * activations and per-row weights (MX operands: QMOE_ERR_UNSUPPORTED). */
+qmoe_status_t qmoe_moe_gemm_w8a8_silu_mxfp8(const qmoe_gemm_args* args, uint8_t* q, uint8_t* sf, int64_t sf_ld,
+                                           const int32_t* sf_padded_offsets, qmoe_stream_t stream);
+
 /* ------------------------------------------------------------------------ */
 /* element-level hooks used by the exhaustive tests                         */
 /* ------------------------------------------------------------------------ */

@@ -34,6 +34,7 @@ EXPORTED = (
     "qmoe_debug_silu_mul", "qmoe_debug_div_by_scale", "qmoe_debug_wait_timeout",
     "qmoe_moe_gemm_w8a8_token_sum_noalloc", "qmoe_quant_weight_mxfp8", "qmoe_quant_mxfp8", "qmoe_quant_mxfp8_colwise",
     "qmoe_mx_weight_sf_tiled_bytes", "qmoe_mx_weight_sf_tiled", "qmoe_quant_weight_int4", "qmoe_moe_gemm_w4a16",
+    "qmoe_moe_gemm_w8a8_silu_mxfp8",
 )
 NOALLOC_ACCUM_MAX_ELEMS = 4 << 20
 
@@ -98,6 +99,7 @@ def load_library(path: str | None = None):
             L.qmoe_moe_gemm_w8a8.argtypes = [ctypes.POINTER(GemmArgs), vp]
             L.qmoe_moe_gemm_w8a16.argtypes = [ctypes.POINTER(GemmArgs), vp]
             L.qmoe_moe_gemm_w8a8_token_sum_noalloc.argtypes = [ctypes.POINTER(GemmArgs), vp]
+            L.qmoe_moe_gemm_w8a8_silu_mxfp8.argtypes = [ctypes.POINTER(GemmArgs), vp, vp, i64, vp, vp]
             L.qmoe_silu_mul_quant.argtypes = [vp, i64, i64, i64, i32, vp, vp, vp, i64, vp, vp, i32, vp, vp]
             L.qmoe_srelu_quant.argtypes = [vp, i64, i64, i64, i32, vp, vp, vp, i64, vp, vp, i32, vp, vp]
             L.qmoe_debug_e4m3_encode.argtypes = [vp, vp, i64, vp]
@@ -368,7 +370,7 @@ def quant_mxfp8_colwise(x: torch.Tensor, q=None, sf=None, stream=None):
 # ------------------------------------------------------------------ GEMM ---
 def _gemm(fn_name, *, a, a_scale, w, w_scale, align, topk_weights, out, M, top_k, BM, a_layout, out_layout,
           a_scale_mode=SCALE_PER_TOKEN, a_sf=None, a_sf_padded_offsets=None, d_status=None, accum=None,
-          stream=None, w_scale_mode=0, w_sf=None, K=None):
+          stream=None, w_scale_mode=0, w_sf=None, K=None, extra=()):
     E, N, Kw = w.shape
     K = Kw if K is None else K
     if out_layout == OUT_TOKEN_SUM and accum is None:
@@ -393,13 +395,13 @@ def _gemm(fn_name, *, a, a_scale, w, w_scale, align, topk_weights, out, M, top_k
     args.expert_offsets = align["expert_offsets"].data_ptr()
     args.padded_offsets = align["padded_offsets"].data_ptr()
     args.topk_weights = None if topk_weights is None else topk_weights.data_ptr()
-    args.out = out.data_ptr()
+    args.out = None if out is None else out.data_ptr()
     args.out_layout = out_layout
     args.M, args.N, args.K = M, N, K
     args.E, args.top_k, args.BM = E, top_k, BM
     args.d_status = None if d_status is None else d_status.data_ptr()
     args.accum = None if accum is None else accum.data_ptr()
-    st = getattr(load_library(), fn_name)(ctypes.byref(args), _stream(stream))
+    st = getattr(load_library(), fn_name)(ctypes.byref(args), *extra, _stream(stream))
     _check(st, fn_name)
     return out
 
@@ -445,6 +447,35 @@ def moe_gemm_w8a8(a_q: torch.Tensor, a_scale: torch.Tensor | None, w_q: torch.Te
                  topk_weights=topk_weights, out=out, M=M, top_k=top_k, BM=BM, a_layout=a_layout,
                  out_layout=out_layout, d_status=d_status, accum=accum, a_scale_mode=a_scale_mode, a_sf=a_sf,
                  a_sf_padded_offsets=a_sf_padded_offsets, stream=stream, w_scale_mode=w_scale_mode, w_sf=w_sf)
+
+
+def moe_gemm_w8a8_silu_mxfp8(a_q: torch.Tensor, a_scale: torch.Tensor, w_q: torch.Tensor, w_scale: torch.Tensor,
+                             align: dict, *, M: int, top_k: int, a_layout: int = A_TOKEN_GATHER,
+                             topk_weights: torch.Tensor | None = None, q: torch.Tensor | None = None,
+                             sf: torch.Tensor | None = None, sf_rows: int | None = None,
+                             d_status: torch.Tensor | None = None, stream=None):
+    """FP8 [gate | up] projection (w_q [E, 2I, K], gate rows first) with SwiGLU +
+    MXFP8 in the GEMM epilogue; align from moe_align_block_size(..., 128).
+    Returns (q [T, I] uint8 e4m3 codes in compact grouped rows, sf [sf_rows,
+    mx_sf_ld(I)] uint8 E8M0), the bytes silu_mul_quant(SCALE_MX_1X32) writes for
+    the bf16 output of moe_gemm_w8a8(..., out_layout=OUT_GROUPED)."""
+    _need(a_q, torch.uint8, "a_q")
+    _need(a_scale, torch.float32, "a_scale")
+    _need(w_q, torch.uint8, "w_q")
+    _need(w_scale, torch.float32, "w_scale")
+    if topk_weights is not None:
+        _need(topk_weights, torch.float32, "topk_weights")
+    E, N, _ = w_q.shape
+    I, T = N // 2, M * top_k
+    q = q if q is not None else torch.empty(T, I, dtype=torch.uint8, device=a_q.device)
+    if sf is None:
+        rows = sf_rows if sf_rows is not None else align_max_padded(T, E, 128)
+        sf = torch.empty(rows, mx_sf_ld(I), dtype=torch.uint8, device=a_q.device)
+    _gemm("qmoe_moe_gemm_w8a8_silu_mxfp8", a=a_q, a_scale=a_scale, w=w_q, w_scale=w_scale, align=align,
+          topk_weights=topk_weights, out=None, M=M, top_k=top_k, BM=128, a_layout=a_layout, out_layout=OUT_GROUPED,
+          d_status=d_status, stream=stream,
+          extra=(_ptr(q), _ptr(sf), sf.stride(0), _ptr(align["padded_offsets"])))
+    return q, sf
 
 
 def moe_gemm_w8a8_token_sum_noalloc(a_q: torch.Tensor, a_scale: torch.Tensor, w_q: torch.Tensor,

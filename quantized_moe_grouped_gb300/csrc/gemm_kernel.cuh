@@ -73,13 +73,23 @@ struct GemmParams {
     int32_t w_groups;            // W4A16: K / 128
     int32_t num_k_blocks;
     int32_t* d_status;
+    // SwiGLU + MXFP8 epilogue (kSwi): output h = silu(gate) * up of the grouped
+    // rows as e4m3 codes [T, N/2] and E8M0 factors [rows, act_sf_ld]
+    uint8_t* act_q;
+    uint8_t* act_sf;
+    int64_t act_sf_ld;
+    const int32_t* act_sf_poff;  // first factor row of each expert
 };
 
 constexpr int kGemmMaxE = 256;  // experts per call (the align's limit)
 
 // kI4: W4A16 -- packed int4 weight tiles (32 bytes per row per stage) with a
 // scale per 128-wide group along K, applied by the converters (wide tile only).
-template <bool kBF16, bool kWide, int BN, bool kMX = false, bool kI4 = false>
+// kSwi: FP8 wide tile whose 256 weight rows are 128 gate rows [nb*128, +128)
+// and the matching 128 up rows [N/2 + nb*128, +128) of a fused [gate | up]
+// projection, with a SwiGLU + MXFP8 epilogue (one 1x32 block = 32 columns of
+// one thread's row).
+template <bool kBF16, bool kWide, int BN, bool kMX = false, bool kI4 = false, bool kSwi = false>
 struct GemmCfg {
     // kW2 (wide, BN = 256): two 128-slot halves share every weight stage, one
     // accumulator each -- one weight pass serves both slot blocks of a 256 block
@@ -132,6 +142,7 @@ struct GemmCfg {
     static_assert(!kI4 || (kBF16 && kWide), "W4A16: wide bf16 tile only");
     static_assert(!kWide || BN == 128 || BN == 256, "wide tile: 128 or 256 slots");
     static_assert(!kW2 || (!kBF16 && !kMX), "two-half tile: FP8 with per-row scales only");
+    static_assert(!kSwi || (kWide && BN == 128 && !kBF16 && !kMX), "SwiGLU epilogue: FP8 wide 128-slot tile only");
     static_assert(!kMX || kSfbCol + 8 * kStages <= 512, "TMEM columns");  // per-stage weight scales
     static constexpr int kDynSmem =
         kStages * kStageBytes + kRawStages * kRawBytes + (kMX ? kStages * kSfStageBytes + kSfBytes : 0) + 1024;
@@ -201,11 +212,11 @@ QMOE_DI void tmem_wait_ld_regs(uint32_t (&r)[32]) {
                    "+r"(r[29]), "+r"(r[30]), "+r"(r[31]));
 }
 
-template <bool kBF16, bool kWide, int BN, bool kMX, bool kI4>
+template <bool kBF16, bool kWide, int BN, bool kMX, bool kI4, bool kSwi>
 __global__ void __launch_bounds__(GemmCfg<kBF16, kWide, BN, kMX, kI4>::kThreads, 1)
     moe_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_a,
                     const GemmParams p) {
-    using C = GemmCfg<kBF16, kWide, BN, kMX, kI4>;
+    using C = GemmCfg<kBF16, kWide, BN, kMX, kI4, kSwi>;
     constexpr int S = C::kStages;
     constexpr int SR = C::kSlotRows;
     constexpr int WR = C::kWRows;
@@ -364,7 +375,13 @@ __global__ void __launch_bounds__(GemmCfg<kBF16, kWide, BN, kMX, kI4>::kThreads,
                         const uint32_t ph = (it / S) & 1;
                         if (!mbar_wait(&bar_empty[s], ph ^ 1, abort, p.d_status)) { ok = false; break; }
                         mbar_arrive_expect_tx(&bar_full[s], tx);
-                        tma_load_3d(&tmap_w, &bar_full[s], w_tile(s), kb * C::kBK, nb * WR, e);
+                        if constexpr (kSwi) {  // gate rows, then the matching up rows
+                            tma_load_3d(&tmap_w, &bar_full[s], w_tile(s), kb * C::kBK, nb * 128, e);
+                            tma_load_3d(&tmap_w, &bar_full[s], w_tile(s) + 128 * 128, kb * C::kBK,
+                                        static_cast<int>(p.N / 2) + nb * 128, e);
+                        } else {
+                            tma_load_3d(&tmap_w, &bar_full[s], w_tile(s), kb * C::kBK, nb * WR, e);
+                        }
                         if (p.a_tma) tma_load_2d(&tmap_a, &bar_full[s], act_tile(s), kb * C::kBK, arow0);
                         if (kMX && p.w_sf)
                             bulk_load(sf_smem(s) + C::kSfBytes,
@@ -583,7 +600,8 @@ __global__ void __launch_bounds__(GemmCfg<kBF16, kWide, BN, kMX, kI4>::kThreads,
                 // lane = slot row, columns = 256 output channels
                 named_bar_sync(2, C::kEpiThreads);
                 for (int c = et; c < WR; c += C::kEpiThreads) {
-                    const int64_t n = static_cast<int64_t>(nb) * WR + c;
+                    const int64_t n = !kSwi ? static_cast<int64_t>(nb) * WR + c
+                                            : (c < 128 ? 0 : p.N / 2) + static_cast<int64_t>(nb) * 128 + (c & 127);
                     s_wsc[c] = (n < p.N) ? (p.w_scale ? p.w_scale[static_cast<int64_t>(e) * p.N + n] : 1.0f) : 0.0f;
                 }
                 named_bar_sync(2, C::kEpiThreads);
@@ -650,6 +668,54 @@ __global__ void __launch_bounds__(GemmCfg<kBF16, kWide, BN, kMX, kI4>::kThreads,
                             }
                         }
                     }
+                } else if constexpr (kSwi) {
+                    // y = bf16(acc * w_scale * row scale), rounded exactly as
+                    // the plain epilogue stores it, then h = silu(y_gate) * y_up
+                    // in fp32 and each 1x32 block's E8M0 factor and e4m3 codes,
+                    // the same operations as the SwiGLU + MXFP8 kernel applies to
+                    // the stored y.  Padding rows of the expert get factor 0.
+                    const int64_t I = p.N / 2;
+                    const int64_t local = pos - p.padded_offsets[e];
+                    uint8_t* sfr = p.act_sf + (static_cast<int64_t>(p.act_sf_poff[e]) + local) * p.act_sf_ld;
+                    uint8_t* qr = p.act_q + (static_cast<int64_t>(p.expert_offsets[e]) + local) * I +
+                                  static_cast<int64_t>(nb) * 128;
+                    auto bf16r = [](float x) { return __bfloat162float(__float2bfloat16_rn(x)); };
+#pragma unroll 1
+                    for (int j = 0; j < 4; ++j) {
+                        float vg[32], vu[32];
+                        tmem_ld32(t_base + 32 * j, vg);
+                        tmem_ld32(t_base + 128 + 32 * j, vu);
+                        if (j == 3) {  // accumulator read out: the MMA may reuse it
+                            tc_fence_before();
+                            mbar_arrive(&bar_tempty[acc]);
+                        }
+                        if (!valid) {
+                            sfr[nb * 4 + j] = 0;
+                            continue;
+                        }
+                        float amax = 0.0f;
+#pragma unroll
+                        for (int i = 0; i < 32; i += 2) {
+                            const float g0 = bf16r(vg[i] * s_wsc[32 * j + i] * rs);
+                            const float g1 = bf16r(vg[i + 1] * s_wsc[32 * j + i + 1] * rs);
+                            const float u0 = bf16r(vu[i] * s_wsc[128 + 32 * j + i] * rs);
+                            const float u1 = bf16r(vu[i + 1] * s_wsc[128 + 32 * j + i + 1] * rs);
+                            silu_mul2(g0, g1, u0, u1, vg[i], vg[i + 1]);
+                            amax = fmaxf(amax, fmaxf(fabsf(vg[i]), fabsf(vg[i + 1])));
+                        }
+                        const int ex = mx_block_exponent(amax);
+                        const float mul = pow2_neg(ex);
+                        sfr[nb * 4 + j] = static_cast<uint8_t>(ex + 127);
+                        uint32_t o[8];
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            o[i] = e4m3x4(__fmul_rn(vg[4 * i], mul), __fmul_rn(vg[4 * i + 1], mul),
+                                          __fmul_rn(vg[4 * i + 2], mul), __fmul_rn(vg[4 * i + 3], mul));
+                        *reinterpret_cast<uint4*>(qr + 32 * j) = make_uint4(o[0], o[1], o[2], o[3]);
+                        *reinterpret_cast<uint4*>(qr + 32 * j + 16) = make_uint4(o[4], o[5], o[6], o[7]);
+                    }
+                    if (nb == n_blocks - 1)  // factor columns past I/32 (row padding of the factor matrix)
+                        for (int64_t c = I / 32; c < p.act_sf_ld; ++c) sfr[c] = 0;
                 } else {
                     for (int c0 = 0; c0 < WR; c0 += 32) {
                         float v[32];
@@ -852,10 +918,10 @@ inline bool make_act_map(CUtensorMap* map, const void* a, int64_t rows, int64_t 
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <bool kBF16, bool kWide, int BN, bool kMX = false, bool kI4 = false>
+template <bool kBF16, bool kWide, int BN, bool kMX = false, bool kI4 = false, bool kSwi = false>
 inline qmoe_status_t launch_gemm(const void* w, int64_t E, int64_t N, int64_t K, const GemmParams& p,
                                  int64_t max_padded, int64_t a_rows, int64_t lda, cudaStream_t st) {
-    using C = GemmCfg<kBF16, kWide, BN, kMX, kI4>;
+    using C = GemmCfg<kBF16, kWide, BN, kMX, kI4, kSwi>;
     static std::mutex mu;
     static bool attr_set[64] = {false};
     int dev = 0;
@@ -863,7 +929,8 @@ inline qmoe_status_t launch_gemm(const void* w, int64_t E, int64_t N, int64_t K,
     {
         std::lock_guard<std::mutex> g(mu);
         if (!attr_set[dev]) {
-            if (cudaFuncSetAttribute(moe_gemm_kernel<kBF16, kWide, BN, kMX, kI4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+            if (cudaFuncSetAttribute(moe_gemm_kernel<kBF16, kWide, BN, kMX, kI4, kSwi>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      C::kDynSmem) != cudaSuccess)
                 return QMOE_ERR_CUDA;
             attr_set[dev] = true;
@@ -871,7 +938,9 @@ inline qmoe_status_t launch_gemm(const void* w, int64_t E, int64_t N, int64_t K,
     }
     CUtensorMap map, amap;
     // rows of K weight bytes (FP8, INT8) or K/2 (packed INT4); box: one stage's bytes per row
-    if (!make_weight_map(&map, w, E, N, kI4 ? K / 2 : K, kBF16 ? C::kRawRowBytes : C::kBK, C::kWRows, !kBF16))
+    // (kSwi: 128-row boxes, the gate and up halves of a tile loaded separately)
+    if (!make_weight_map(&map, w, E, N, kI4 ? K / 2 : K, kBF16 ? C::kRawRowBytes : C::kBK, kSwi ? 128 : C::kWRows,
+                         !kBF16))
         return QMOE_ERR_CUDA;
     memset(&amap, 0, sizeof(amap));
     if (p.a_tma && !make_act_map(&amap, p.a, a_rows, K, lda, kBF16 ? 2 : 1, C::kSlotRows)) return QMOE_ERR_CUDA;
@@ -882,16 +951,24 @@ inline qmoe_status_t launch_gemm(const void* w, int64_t E, int64_t N, int64_t K,
                               ((N + C::kWRows - 1) / C::kWRows);
     const int64_t grid = max_tiles < sms ? max_tiles : sms;
     if (grid <= 0) return QMOE_OK;
-    return launch_pdl(moe_gemm_kernel<kBF16, kWide, BN, kMX, kI4>, dim3(static_cast<unsigned>(grid)),
+    return launch_pdl(moe_gemm_kernel<kBF16, kWide, BN, kMX, kI4, kSwi>, dim3(static_cast<unsigned>(grid)),
                       dim3(C::kThreads), C::kDynSmem, st, map, amap, p);
 }
 
 // out[i] = bf16(accum[i]) for the TOKEN_SUM layout (defined in gemm_w8a8.cu).
 qmoe_status_t launch_token_sum_finalize(const float* accum, uint16_t* out, int64_t n, cudaStream_t st);
 
+// Outputs of the SwiGLU + MXFP8 epilogue (qmoe_moe_gemm_w8a8_silu_mxfp8).
+struct SwiGluOut {
+    uint8_t* q;
+    uint8_t* sf;
+    int64_t sf_ld;
+    const int32_t* sf_poff;
+};
+
 // Shared argument checks and dispatch for both precisions.
 template <bool kBF16, bool kI4 = false>
-inline qmoe_status_t run_moe_gemm(const qmoe_gemm_args* a, cudaStream_t st) {
+inline qmoe_status_t run_moe_gemm(const qmoe_gemm_args* a, cudaStream_t st, const SwiGluOut* so = nullptr) {
     static_assert(!kI4 || kBF16, "W4A16 is a bf16-activation GEMM");
     if (kI4 && a && a->struct_size >= sizeof(qmoe_gemm_args)) {
         // packed int4 weights with a scale per 128-wide group of K: wide tile only
@@ -928,10 +1005,16 @@ inline qmoe_status_t run_moe_gemm(const qmoe_gemm_args* a, cudaStream_t st) {
     const int64_t T = a->M * a->top_k;
     if (T >= (int64_t(1) << 30) || a->N * a->K * a->E >= (int64_t(1) << 40)) return QMOE_ERR_UNSUPPORTED;
     if (T == 0) return QMOE_OK;
-    if (!a->a || !a->w || (!a->w_scale && !wmx) || !a->out || !a->sorted_ids || !a->expert_ids || !a->num_post_padded ||
-        !a->expert_offsets || !a->padded_offsets)
+    if (!a->a || !a->w || (!a->w_scale && !wmx) || (!a->out && !so) || !a->sorted_ids || !a->expert_ids ||
+        !a->num_post_padded || !a->expert_offsets || !a->padded_offsets)
         return QMOE_ERR_INVALID_ARG;
-    if (!aligned16(a->a) || !aligned16(a->w) || !aligned16(a->out)) return QMOE_ERR_INVALID_ARG;
+    if (!aligned16(a->a) || !aligned16(a->w) || (a->out && !aligned16(a->out))) return QMOE_ERR_INVALID_ARG;
+    if (so) {  // fused [gate | up] projection of grouped rows: FP8 per-row scales, 128-slot tiles
+        if (kBF16 || mx || wmx) return QMOE_ERR_UNSUPPORTED;
+        if (a->out_layout != QMOE_OUT_GROUPED || a->BM != 128 || a->N % 256 != 0) return QMOE_ERR_INVALID_ARG;
+        if (!so->q || !so->sf || !so->sf_poff || !aligned16(so->q) || so->sf_ld < a->N / 64)
+            return QMOE_ERR_INVALID_ARG;
+    }
 
     const bool tsum = a->out_layout == QMOE_OUT_TOKEN_SUM;
     if (tsum) {
@@ -969,6 +1052,10 @@ inline qmoe_status_t run_moe_gemm(const qmoe_gemm_args* a, cudaStream_t st) {
     p.a_tma = a->a_layout != QMOE_A_TOKEN_GATHER;
     p.num_k_blocks = static_cast<int32_t>((a->K + (kBF16 ? 63 : 127)) / (kBF16 ? 64 : 128));
     p.d_status = a->d_status;
+    p.act_q = so ? so->q : nullptr;
+    p.act_sf = so ? so->sf : nullptr;
+    p.act_sf_ld = so ? so->sf_ld : 0;
+    p.act_sf_poff = so ? so->sf_poff : nullptr;
     const int64_t max_padded = (T + static_cast<int64_t>(a->E) * (a->BM - 1) + a->BM - 1) / a->BM * a->BM;
     const int64_t a_rows = a->a_layout == QMOE_A_PADDED ? max_padded : (a->a_layout == QMOE_A_GROUPED ? T : a->M);
     // the kernel numbers its tiles (slot blocks x weight blocks) with 32-bit ints
@@ -980,6 +1067,8 @@ inline qmoe_status_t run_moe_gemm(const qmoe_gemm_args* a, cudaStream_t st) {
         return launch_token_sum_finalize(a->accum, a->out, a->M * a->N, st);
     }
     if constexpr (!kBF16) {
+        if (so) return launch_gemm<false, true, 128, false, false, true>(a->w, a->E, a->N, a->K, p, max_padded, a_rows,
+                                                                         a->lda, st);
         if (mx) {
             r = launch_gemm<false, true, 128, true>(a->w, a->E, a->N, a->K, p, max_padded, a_rows, a->lda, st);
             if (r != QMOE_OK || !tsum) return r;

@@ -41,3 +41,10 @@ qmoe_status_t launch_token_sum_finalize(const float* accum, uint16_t* out, int64
 extern "C" qmoe_status_t qmoe_moe_gemm_w8a8(const qmoe_gemm_args* args, qmoe_stream_t stream) {
     return qmoe::run_moe_gemm<false>(args, stream);
 }
+
+extern "C" qmoe_status_t qmoe_moe_gemm_w8a8_silu_mxfp8(const qmoe_gemm_args* args, uint8_t* q, uint8_t* sf,
+                                                      int64_t sf_ld, const int32_t* sf_padded_offsets,
+                                                      qmoe_stream_t stream) {
+    const qmoe::SwiGluOut so{q, sf, sf_ld, sf_padded_offsets};
+    return qmoe::run_moe_gemm<false>(args, stream, &so);
+}

@@ -121,11 +121,13 @@ def sampled_token_slots(M, seed):
     return toks, (toks[:, None] * TOP_K + np.arange(TOP_K)[None, :]).ravel()
 
 
-def layer_up(q, orc, wl):
+def layer_up(q, orc, wl, fused_mx=False):
     """The layer's first stages as bench.py launches them: moe_align_block_size
     (BM=128), quant_act_fp8_sorted into padded sorted rows, then the up GEMM
     (padded A -> grouped out).  Align and the quantised rows are checked in
-    full, the up projection on 16 sampled slots."""
+    full, the up projection on 16 sampled slots.  fused_mx: also the same
+    projection with SwiGLU + MXFP8 in its epilogue, whose (codes, factors) are
+    returned last."""
     M, K, I = wl.M, wl.K, wl.inter
     T, BM = M * TOP_K, 128
     ids, tw = inputs.routing(M, E, TOP_K, wl.seed, wl.zipf_s)
@@ -147,6 +149,9 @@ def layer_up(q, orc, wl):
     st = status()
     up = q.moe_gemm_w8a8(aq, sa, w1q, w1s, al, None, M=M, top_k=TOP_K, BM=BM, a_layout=q.A_PADDED,
                          out_layout=q.OUT_GROUPED, d_status=st)
+    fused = None
+    if fused_mx:
+        fused = q.moe_gemm_w8a8_silu_mxfp8(aq, sa, w1q, w1s, al, M=M, top_k=TOP_K, a_layout=q.A_PADDED, d_status=st)
     torch.cuda.synchronize()
     assert int(st.item()) == 0
     del w1q, aq
@@ -155,7 +160,7 @@ def layer_up(q, orc, wl):
     ref_up = orc.moe_gemm(a_kind=orc.A_FP8_TOKEN, a=raq, a_scale=rsa, w_kind=orc.W_FP8, w=r1q, w_scale=r1s,
                           topk_ids=ids, topk_w=None, E=E, slots=slots)
     check_rows(bf16_to_np_f32(up[torch.from_numpy(pos[slots]).to(dev())]), ref_up)
-    return ids, tw, al, ref_al, up
+    return (ids, tw, al, ref_al, up) + ((fused,) if fused_mx else ())
 
 
 def test_mixtral_8x7b_layer_full_size(q, orc):
@@ -185,13 +190,14 @@ def test_mixtral_8x7b_layer_full_size(q, orc):
 def test_mixtral_8x22b_mx_layer_full_size(q, orc):
     """M=4096 with Zipf(1.2)-skewed routing, K=6144, I=16384, N=6144: align,
     sorted quant, up GEMM, then SwiGLU + MXFP8 over the grouped rows (codes and
-    E8M0 factors bit-exact on every row), then the block-scaled down GEMM with
+    E8M0 factors bit-exact on every row; the up GEMM's fused SwiGLU + MXFP8
+    epilogue gives the same bytes), then the block-scaled down GEMM with
     per-row FP8 weights and again with MXFP8 weights (tiled factors), each on 8
     sampled tokens."""
     wl = inputs.mixtral_8x22b_layer()
     M, I, Nd = wl.M, wl.inter, wl.N
     T = M * TOP_K
-    ids, tw, al, ref_al, up = layer_up(q, orc, wl)
+    ids, tw, al, ref_al, up, (fq, fsf) = layer_up(q, orc, wl, fused_mx=True)
     eoff, poff = ref_al["expert_offsets"], ref_al["padded_offsets"]
     hq, sf = q.silu_mul_quant(up, q.SCALE_MX_1X32, expert_offsets=al["expert_offsets"],
                               sf_padded_offsets=al["padded_offsets"], sf_rows=q.align_max_padded(T, E, 128))
@@ -199,6 +205,9 @@ def test_mixtral_8x22b_mx_layer_full_size(q, orc):
     del up
     assert np.array_equal(hq.cpu().numpy(), rq)
     assert np.array_equal(sf.cpu().numpy()[: poff[-1]], rsf)
+    # the same intermediate from the up GEMM's SwiGLU + MXFP8 epilogue
+    assert torch.equal(fq, hq) and torch.equal(fsf[: poff[-1]], sf[: poff[-1]])
+    del fq, fsf
     sf_row = np.empty(T, dtype=np.int64)
     for e in range(E):
         sf_row[eoff[e]:eoff[e + 1]] = poff[e] + np.arange(eoff[e + 1] - eoff[e])

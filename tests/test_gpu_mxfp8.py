@@ -129,3 +129,78 @@ def test_gemm_mx_weights_need_mx_activations(q, orc):
     wsf = torch.zeros(1024, dtype=torch.uint8, device="cuda")
     with pytest.raises(qq.QmoeError):
         q.moe_gemm_w8a8(aq, sa, wq, None, al, None, M=M, top_k=2, BM=128, w_scale_mode=q.SCALE_MX_1X32, w_sf=wsf)
+
+
+@pytest.mark.parametrize("M,K,I,E,top_k,zipf,a_layout,routed,pad_cols", [
+    (256, 256, 384, 8, 2, None, 2, False, 0),     # padded A, ragged expert counts
+    (150, 160, 256, 5, 3, None, 0, True, 4),      # token-gather A, ragged K, routing weights, wider factor rows
+    (300, 512, 1024, 16, 2, None, 1, False, 0),   # grouped A, five experts without slots
+    (1024, 256, 2560, 8, 2, 1.2, 2, False, 0),    # Zipf skew, more tiles than SMs
+])
+def test_gemm_silu_mxfp8_epilogue_bitexact(q, orc, M, K, I, E, top_k, zipf, a_layout, routed, pad_cols):
+    """FP8 [gate | up] projection with SwiGLU + MXFP8 in the GEMM epilogue: codes
+    and E8M0 factors (incl. the zeroed pad rows and pad columns) identical to
+    the oracle's SwiGLU + MXFP8 of the bf16 output the same GEMM stores without
+    the fused epilogue; that output itself within the GEMM tolerance of the
+    oracle's fp64 GEMM."""
+    T, N = M * top_k, 2 * I
+    seed = M + K + I
+    if E == 16:
+        ids, tw = inputs.routing(M, 11, top_k, seed)
+        ids = np.where(ids < 5, ids, ids + 5).astype(np.int32)
+    else:
+        ids, tw = inputs.routing(M, E, top_k, seed, zipf)
+    a = inputs.activations_bf16(M, K, seed)
+    w = inputs.expert_weights_f32(E, N, K, seed)
+    wq, ws = q.quant_weight_fp8(to_dev(w))
+    aq, sa = q.quant_act_fp8(to_dev_bf16(a))
+    rwq, rws = orc.quant_rows_fp8_f32(w)
+    raq, rsa = orc.quant_rows_fp8_bf16(a)
+    al = q.moe_align_block_size(to_dev(ids), E, 128)
+    ref_al = orc.moe_align(ids, E, 128)
+    eoff, poff = ref_al["expert_offsets"], ref_al["padded_offsets"]
+    twd = to_dev(tw) if routed else None
+    if a_layout == q.A_PADDED:
+        a_in, s_in = q.quant_act_fp8_sorted(to_dev_bf16(a), al, top_k)
+    elif a_layout == q.A_GROUPED:
+        order = np.empty(T, dtype=np.int64)
+        order[orc.compact_row_of_slot(ids, E)] = np.arange(T)
+        src = to_dev(order // top_k)
+        a_in, s_in = aq[src].contiguous(), sa[src].contiguous()
+    else:
+        a_in, s_in = aq, sa
+    st = status()
+    y = q.moe_gemm_w8a8(a_in, s_in, wq, ws, al, twd, M=M, top_k=top_k, BM=128, a_layout=a_layout,
+                        out_layout=q.OUT_GROUPED, d_status=st)
+    rows = q.align_max_padded(T, E, 128)
+    ld = q.mx_sf_ld(I) + pad_cols
+    sf = torch.full((rows, ld), 0xAB, dtype=torch.uint8, device=aq.device)
+    hq, sf = q.moe_gemm_w8a8_silu_mxfp8(a_in, s_in, wq, ws, al, M=M, top_k=top_k, a_layout=a_layout,
+                                         topk_weights=twd, sf=sf, d_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    ref_y = orc.moe_gemm(a_kind=orc.A_FP8_TOKEN, a=raq, a_scale=rsa, w_kind=orc.W_FP8, w=rwq, w_scale=rws,
+                         topk_ids=ids, topk_w=tw if routed else None, E=E, out_layout="grouped")
+    import oracle
+    ok, ratio = oracle.gemm_tolerance_ok(bf16_to_np_f32(y), ref_y)
+    assert ok, f"unfused GEMM: worst |err|/bound = {ratio:.3f}"
+    y_bits = y.view(torch.int16).cpu().numpy().view(np.uint16)
+    rq, rsf = orc.silu_mul_quant_mx(y_bits, eoff, poff)
+    assert np.array_equal(hq.cpu().numpy(), rq)
+    got_sf = sf.cpu().numpy()
+    n = int(poff[-1])
+    assert np.array_equal(got_sf[:n, :q.mx_sf_ld(I)], rsf)
+    assert not got_sf[:n, q.mx_sf_ld(I):].any()                    # pad columns zeroed
+    assert np.all(got_sf[n:] == 0xAB)                             # rows past the last expert untouched
+
+
+def test_gemm_silu_mxfp8_rejects(q):
+    """Host checks: BM must be 128, N a multiple of 256, FP8 per-token operands."""
+    import quantized_moe_grouped_gb300 as qq
+    M, K, E = 16, 64, 2
+    ids, _ = inputs.routing(M, E, 2, seed=4)
+    aq, sa = q.quant_act_fp8(to_dev_bf16(inputs.activations_bf16(M, K, 4)))
+    wq, ws = q.quant_weight_fp8(to_dev(inputs.expert_weights_f32(E, 384, K, 4)))   # N = 384: not a multiple of 256
+    al = q.moe_align_block_size(to_dev(ids), E, 128)
+    with pytest.raises(qq.QmoeError):
+        q.moe_gemm_w8a8_silu_mxfp8(aq, sa, wq, ws, al, M=M, top_k=2)
