@@ -460,6 +460,17 @@ def run_suite(reps: int = 20, only: str | None = None) -> None:
                                             a_layout=q.A_PADDED, out_layout=q.OUT_GROUPED, out=up), reps, flush)
         line(wl.name, "moe_gemm_w8a8 up (padded A -> grouped out)", ms,
              hit * 2 * I * K + hit * 2 * I * 4 + T * (K + 4) + T * 2 * I * 2, 2.0 * T * K * 2 * I, "fp8")
+        if wl.act_scale == "token":  # the same projection with SwiGLU in its epilogue + the per-token pass
+            fq = torch.empty(T, I, dtype=torch.uint8, device=dev)
+            fs = torch.empty(T, dtype=torch.float32, device=dev)
+            hs_scr = torch.empty(T * I + T, dtype=torch.float32, device=dev)
+            ms = _timed(lambda: q.moe_gemm_w8a8_silu_fp8_token(aq, sa, w1q, w1s, al, M=M, top_k=TOP_K,
+                                                               a_layout=q.A_PADDED, q=fq, scale=fs,
+                                                               h_scratch=hs_scr), reps, flush)
+            line(wl.name, "moe_gemm_w8a8 up + SwiGLU epilogue + per-token FP8 pass (2 launches + memset)", ms,
+                 hit * 2 * I * K + hit * 2 * I * 4 + T * (K + 4) + 2 * T * I * 4 + T * (I + 4), 2.0 * T * K * 2 * I,
+                 "fp8")
+            del fq, fs, hs_scr
         if wl.act_scale == "mx":  # the same projection with SwiGLU + MXFP8 in its epilogue
             fq = torch.empty(T, I, dtype=torch.uint8, device=dev)
             fsf = torch.empty(q.align_max_padded(T, E, 128), q.mx_sf_ld(I), dtype=torch.uint8, device=dev)

@@ -415,6 +415,22 @@ qmoe_status_t qmoe_srelu_quant(const uint16_t* y, int64_t rows, int64_t I, int64
 qmoe_status_t qmoe_moe_gemm_w8a8_silu_mxfp8(const qmoe_gemm_args* args, uint8_t* q, uint8_t* sf, int64_t sf_ld,
                                            const int32_t* sf_padded_offsets, qmoe_stream_t stream);
 
+/* The same fused [gate | up] projection with the per-token requantisation:
+ * the result is that of qmoe_moe_gemm_w8a8 (QMOE_OUT_GROUPED) followed by
+ * qmoe_silu_mul_quant(mode QMOE_SCALE_PER_TOKEN), bit for bit.  A row's scale
+ * needs the amax of all its I = N/2 values, so the GEMM epilogue writes
+ * h = silu(y_gate) * y_up in fp32 (y rounded to bf16 exactly as the GEMM
+ * stores it) and reduces each row's amax |h|; a second launch forms
+ * scale[r] = amax_r/448 (1 for an all-zero row) and q = e4m3(h/scale).
+ *   q [T, I] e4m3 codes and scale [T] fp32, compact grouped rows.
+ *   h_scratch: caller-owned fp32 scratch of T*I + T floats (16-byte aligned),
+ *   overwritten (h, then the T row maxima, zeroed on the stream first).
+ * args as for qmoe_moe_gemm_w8a8_silu_mxfp8 (out unused, out_layout
+ * QMOE_OUT_GROUPED, BM == 128, N % 256 == 0, FP8 per-token operands).  Host
+ * errors return before anything is launched. */
+qmoe_status_t qmoe_moe_gemm_w8a8_silu_fp8_token(const qmoe_gemm_args* args, uint8_t* q, float* scale,
+                                               float* h_scratch, qmoe_stream_t stream);
+
 /* ------------------------------------------------------------------------ */
 /* element-level hooks used by the exhaustive tests                         */
 /* ------------------------------------------------------------------------ */

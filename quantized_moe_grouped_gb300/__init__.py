@@ -34,7 +34,7 @@ EXPORTED = (
     "qmoe_debug_silu_mul", "qmoe_debug_div_by_scale", "qmoe_debug_wait_timeout",
     "qmoe_moe_gemm_w8a8_token_sum_noalloc", "qmoe_quant_weight_mxfp8", "qmoe_quant_mxfp8", "qmoe_quant_mxfp8_colwise",
     "qmoe_mx_weight_sf_tiled_bytes", "qmoe_mx_weight_sf_tiled", "qmoe_quant_weight_int4", "qmoe_moe_gemm_w4a16",
-    "qmoe_moe_gemm_w8a8_silu_mxfp8",
+    "qmoe_moe_gemm_w8a8_silu_mxfp8", "qmoe_moe_gemm_w8a8_silu_fp8_token",
 )
 NOALLOC_ACCUM_MAX_ELEMS = 4 << 20
 
@@ -100,6 +100,7 @@ def load_library(path: str | None = None):
             L.qmoe_moe_gemm_w8a16.argtypes = [ctypes.POINTER(GemmArgs), vp]
             L.qmoe_moe_gemm_w8a8_token_sum_noalloc.argtypes = [ctypes.POINTER(GemmArgs), vp]
             L.qmoe_moe_gemm_w8a8_silu_mxfp8.argtypes = [ctypes.POINTER(GemmArgs), vp, vp, i64, vp, vp]
+            L.qmoe_moe_gemm_w8a8_silu_fp8_token.argtypes = [ctypes.POINTER(GemmArgs), vp, vp, vp, vp]
             L.qmoe_silu_mul_quant.argtypes = [vp, i64, i64, i64, i32, vp, vp, vp, i64, vp, vp, i32, vp, vp]
             L.qmoe_srelu_quant.argtypes = [vp, i64, i64, i64, i32, vp, vp, vp, i64, vp, vp, i32, vp, vp]
             L.qmoe_debug_e4m3_encode.argtypes = [vp, vp, i64, vp]
@@ -476,6 +477,38 @@ def moe_gemm_w8a8_silu_mxfp8(a_q: torch.Tensor, a_scale: torch.Tensor, w_q: torc
           d_status=d_status, stream=stream,
           extra=(_ptr(q), _ptr(sf), sf.stride(0), _ptr(align["padded_offsets"])))
     return q, sf
+
+
+def moe_gemm_w8a8_silu_fp8_token(a_q: torch.Tensor, a_scale: torch.Tensor, w_q: torch.Tensor,
+                                 w_scale: torch.Tensor, align: dict, *, M: int, top_k: int,
+                                 a_layout: int = A_TOKEN_GATHER, topk_weights: torch.Tensor | None = None,
+                                 q: torch.Tensor | None = None, scale: torch.Tensor | None = None,
+                                 h_scratch: torch.Tensor | None = None, d_status: torch.Tensor | None = None,
+                                 stream=None):
+    """FP8 [gate | up] projection (w_q [E, 2I, K]) with SwiGLU in the GEMM
+    epilogue and per-token FP8 requantisation; align from
+    moe_align_block_size(..., 128).  Returns (q [T, I] uint8, scale [T] fp32),
+    the bytes silu_mul_quant(SCALE_PER_TOKEN) writes for the bf16 output of
+    moe_gemm_w8a8(..., out_layout=OUT_GROUPED).  h_scratch: fp32, at least
+    T*I + T elements (allocated here when not given)."""
+    _need(a_q, torch.uint8, "a_q")
+    _need(a_scale, torch.float32, "a_scale")
+    _need(w_q, torch.uint8, "w_q")
+    _need(w_scale, torch.float32, "w_scale")
+    if topk_weights is not None:
+        _need(topk_weights, torch.float32, "topk_weights")
+    E, N, _ = w_q.shape
+    I, T = N // 2, M * top_k
+    q = q if q is not None else torch.empty(T, I, dtype=torch.uint8, device=a_q.device)
+    scale = scale if scale is not None else torch.empty(T, dtype=torch.float32, device=a_q.device)
+    if h_scratch is None:
+        h_scratch = torch.empty(T * I + T, dtype=torch.float32, device=a_q.device)
+    elif h_scratch.dtype != torch.float32 or h_scratch.numel() < T * I + T:
+        raise QmoeError("h_scratch must be fp32 with at least T*I + T elements")
+    _gemm("qmoe_moe_gemm_w8a8_silu_fp8_token", a=a_q, a_scale=a_scale, w=w_q, w_scale=w_scale, align=align,
+          topk_weights=topk_weights, out=None, M=M, top_k=top_k, BM=128, a_layout=a_layout, out_layout=OUT_GROUPED,
+          d_status=d_status, stream=stream, extra=(_ptr(q), _ptr(scale), _ptr(h_scratch)))
+    return q, scale
 
 
 def moe_gemm_w8a8_token_sum_noalloc(a_q: torch.Tensor, a_scale: torch.Tensor, w_q: torch.Tensor,

@@ -707,6 +707,44 @@ __global__ void __launch_bounds__(kT)
     }
 }
 
+// Second pass of the per-token SwiGLU quantisation when h comes from the up
+// GEMM's epilogue (qmoe_moe_gemm_w8a8_silu_fp8_token): rows of fp32 h whose
+// amax |h| the epilogue has already reduced, scale = amax/448 (1 for an
+// all-zero row), q = e4m3(h / scale) -- the same operations as the quantisation
+// pass of act_quant_token_kernel.  One thread per 8 elements, flat grid.
+__global__ void __launch_bounds__(256)
+    quant_h_token_kernel(const float* __restrict__ h, const float* __restrict__ amax, int64_t rows, int64_t I,
+                         uint8_t* __restrict__ q, float* __restrict__ scale) {
+    pdl_launch_dependents();
+    pdl_wait();
+    const int64_t per_row = I / 8;
+    for (int64_t g = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; g < rows * per_row;
+         g += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t r = g / per_row;
+        const int64_t c = (g - r * per_row) * 8;
+        const float a = amax[r];
+        const float s = (a == 0.0f) ? 1.0f : __fdiv_rn(a, 448.0f);
+        const float rinv = __frcp_rn(s);
+        const float4 x0 = __ldcs(reinterpret_cast<const float4*>(h + r * I + c));
+        const float4 x1 = __ldcs(reinterpret_cast<const float4*>(h + r * I + c + 4));
+        const float v[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+        *reinterpret_cast<uint2*>(q + r * I + c) = quant8(v, s, rinv);
+        if (c == 0) scale[r] = s;
+    }
+}
+
+qmoe_status_t launch_quant_h_token(const float* h, const float* amax, int64_t rows, int64_t I, uint8_t* q,
+                                   float* scale, cudaStream_t st) {
+    if (rows <= 0) return QMOE_OK;
+    const int64_t n = rows * (I / 8);
+    const int sms = device_sm_count();
+    int64_t blocks = (n + 255) / 256;
+    const int64_t cap = static_cast<int64_t>(sms > 0 ? sms : 132) * 16;
+    if (blocks > cap) blocks = cap;
+    return launch_pdl(quant_h_token_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, st, h, amax, rows, I,
+                      q, scale);
+}
+
 constexpr int kMxThreads = 256;
 
 // One thread per (row, 1x32 block) item over a flat grid, so short rows keep

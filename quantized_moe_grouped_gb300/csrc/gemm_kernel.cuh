@@ -73,23 +73,28 @@ struct GemmParams {
     int32_t w_groups;            // W4A16: K / 128
     int32_t num_k_blocks;
     int32_t* d_status;
-    // SwiGLU + MXFP8 epilogue (kSwi): output h = silu(gate) * up of the grouped
-    // rows as e4m3 codes [T, N/2] and E8M0 factors [rows, act_sf_ld]
+    // SwiGLU epilogues (kAct): h = silu(gate) * up of the grouped rows, as
+    // MXFP8 (kAct 1: e4m3 codes [T, N/2], E8M0 factors [rows, act_sf_ld]) or
+    // as fp32 (kAct 2: act_h [T, N/2] and each row's running amax |h| in
+    // act_amax [T], for the per-token quantisation that follows)
     uint8_t* act_q;
     uint8_t* act_sf;
     int64_t act_sf_ld;
     const int32_t* act_sf_poff;  // first factor row of each expert
+    float* act_h;
+    float* act_amax;
 };
 
 constexpr int kGemmMaxE = 256;  // experts per call (the align's limit)
 
 // kI4: W4A16 -- packed int4 weight tiles (32 bytes per row per stage) with a
 // scale per 128-wide group along K, applied by the converters (wide tile only).
-// kSwi: FP8 wide tile whose 256 weight rows are 128 gate rows [nb*128, +128)
-// and the matching 128 up rows [N/2 + nb*128, +128) of a fused [gate | up]
-// projection, with a SwiGLU + MXFP8 epilogue (one 1x32 block = 32 columns of
-// one thread's row).
-template <bool kBF16, bool kWide, int BN, bool kMX = false, bool kI4 = false, bool kSwi = false>
+// kAct != 0: FP8 wide tile whose 256 weight rows are 128 gate rows
+// [nb*128, +128) and the matching 128 up rows [N/2 + nb*128, +128) of a fused
+// [gate | up] projection, with a SwiGLU epilogue: kAct 1 quantises h to MXFP8
+// (one 1x32 block = 32 columns of one thread's row), kAct 2 writes fp32 h and
+// the row amax.
+template <bool kBF16, bool kWide, int BN, bool kMX = false, bool kI4 = false, int kAct = 0>
 struct GemmCfg {
     // kW2 (wide, BN = 256): two 128-slot halves share every weight stage, one
     // accumulator each -- one weight pass serves both slot blocks of a 256 block
@@ -115,8 +120,9 @@ struct GemmCfg {
     // ahead of the gather warps, so the lag shrinks when the ring is short.
     static constexpr int kLag = kStages >= 6 ? 3 : (kStages >= 5 ? 2 : 1);
     static constexpr int kBProdThreads = 64;
-    // MX: two groups of four warps, one per column half; kW2: one per slot half
-    static constexpr int kEpiThreads = (kMX || kW2) ? 256 : 128;
+    // MX: two groups of four warps, one per column half; kW2: one per slot
+    // half; kAct (SwiGLU epilogues): one per half of the tile's 128 h columns
+    static constexpr int kEpiThreads = (kMX || kW2 || kAct != 0) ? 256 : 128;
     // MX: a stage's scales in shared memory, as 512-byte blocks of 32 x 16
     // bytes: the 128 activation rows, then the two 128-row halves of the 256
     // weight rows (MXFP8 weights only)
@@ -126,7 +132,7 @@ struct GemmCfg {
     // stage), 4 for the swapped one; groups alternate stages
     static constexpr int kConvThreads = (kBF16 && kWide) ? 256 : 128;
     static constexpr int kConvGroups = kBF16 ? 2 : 1;       // converter groups alternate stages
-    static constexpr int kThreads = kBF16 ? 256 + 2 * kConvThreads : ((kMX || kW2) ? 384 : 256);
+    static constexpr int kThreads = kBF16 ? 256 + 2 * kConvThreads : ((kMX || kW2 || kAct != 0) ? 384 : 256);
     static constexpr int kAccCols = kMmaN;                  // TMEM columns per accumulator
     // MX: one accumulator (256 columns), then four scale columns per stage for
     // the 128 activation rows (4-column aligned) and 8 columns of constant
@@ -142,7 +148,7 @@ struct GemmCfg {
     static_assert(!kI4 || (kBF16 && kWide), "W4A16: wide bf16 tile only");
     static_assert(!kWide || BN == 128 || BN == 256, "wide tile: 128 or 256 slots");
     static_assert(!kW2 || (!kBF16 && !kMX), "two-half tile: FP8 with per-row scales only");
-    static_assert(!kSwi || (kWide && BN == 128 && !kBF16 && !kMX), "SwiGLU epilogue: FP8 wide 128-slot tile only");
+    static_assert(kAct == 0 || (kWide && BN == 128 && !kBF16 && !kMX), "SwiGLU epilogue: FP8 wide 128-slot tile only");
     static_assert(!kMX || kSfbCol + 8 * kStages <= 512, "TMEM columns");  // per-stage weight scales
     static constexpr int kDynSmem =
         kStages * kStageBytes + kRawStages * kRawBytes + (kMX ? kStages * kSfStageBytes + kSfBytes : 0) + 1024;
@@ -212,11 +218,11 @@ QMOE_DI void tmem_wait_ld_regs(uint32_t (&r)[32]) {
                    "+r"(r[29]), "+r"(r[30]), "+r"(r[31]));
 }
 
-template <bool kBF16, bool kWide, int BN, bool kMX, bool kI4, bool kSwi>
-__global__ void __launch_bounds__(GemmCfg<kBF16, kWide, BN, kMX, kI4>::kThreads, 1)
+template <bool kBF16, bool kWide, int BN, bool kMX, bool kI4, int kAct>
+__global__ void __launch_bounds__(GemmCfg<kBF16, kWide, BN, kMX, kI4, kAct>::kThreads, 1)
     moe_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_a,
                     const GemmParams p) {
-    using C = GemmCfg<kBF16, kWide, BN, kMX, kI4, kSwi>;
+    using C = GemmCfg<kBF16, kWide, BN, kMX, kI4, kAct>;
     constexpr int S = C::kStages;
     constexpr int SR = C::kSlotRows;
     constexpr int WR = C::kWRows;
@@ -375,7 +381,7 @@ __global__ void __launch_bounds__(GemmCfg<kBF16, kWide, BN, kMX, kI4>::kThreads,
                         const uint32_t ph = (it / S) & 1;
                         if (!mbar_wait(&bar_empty[s], ph ^ 1, abort, p.d_status)) { ok = false; break; }
                         mbar_arrive_expect_tx(&bar_full[s], tx);
-                        if constexpr (kSwi) {  // gate rows, then the matching up rows
+                        if constexpr (kAct != 0) {  // gate rows, then the matching up rows
                             tma_load_3d(&tmap_w, &bar_full[s], w_tile(s), kb * C::kBK, nb * 128, e);
                             tma_load_3d(&tmap_w, &bar_full[s], w_tile(s) + 128 * 128, kb * C::kBK,
                                         static_cast<int>(p.N / 2) + nb * 128, e);
@@ -581,7 +587,7 @@ __global__ void __launch_bounds__(GemmCfg<kBF16, kWide, BN, kMX, kI4>::kThreads,
         cp_async_wait<0>();
         fence_proxy_async_smem();
         for (int j = (it > C::kLag ? it - C::kLag : 0); j < it; ++j) mbar_arrive(&bar_full[j % S]);
-    } else if (warp < 8 || kMX || C::kW2) {
+    } else if (warp < 8 || kMX || C::kW2 || kAct != 0) {
         // ------------------------------------------------- epilogue ---
         const int et = threadIdx.x - 128;
         const int q = warp & 3;  // TMEM lane quadrant of this warp
@@ -600,7 +606,7 @@ __global__ void __launch_bounds__(GemmCfg<kBF16, kWide, BN, kMX, kI4>::kThreads,
                 // lane = slot row, columns = 256 output channels
                 named_bar_sync(2, C::kEpiThreads);
                 for (int c = et; c < WR; c += C::kEpiThreads) {
-                    const int64_t n = !kSwi ? static_cast<int64_t>(nb) * WR + c
+                    const int64_t n = kAct == 0 ? static_cast<int64_t>(nb) * WR + c
                                             : (c < 128 ? 0 : p.N / 2) + static_cast<int64_t>(nb) * 128 + (c & 127);
                     s_wsc[c] = (n < p.N) ? (p.w_scale ? p.w_scale[static_cast<int64_t>(e) * p.N + n] : 1.0f) : 0.0f;
                 }
@@ -668,7 +674,7 @@ __global__ void __launch_bounds__(GemmCfg<kBF16, kWide, BN, kMX, kI4>::kThreads,
                             }
                         }
                     }
-                } else if constexpr (kSwi) {
+                } else if constexpr (kAct == 1) {
                     // y = bf16(acc * w_scale * row scale), rounded exactly as
                     // the plain epilogue stores it, then h = silu(y_gate) * y_up
                     // in fp32 and each 1x32 block's E8M0 factor and e4m3 codes,
@@ -680,12 +686,13 @@ __global__ void __launch_bounds__(GemmCfg<kBF16, kWide, BN, kMX, kI4>::kThreads,
                     uint8_t* qr = p.act_q + (static_cast<int64_t>(p.expert_offsets[e]) + local) * I +
                                   static_cast<int64_t>(nb) * 128;
                     auto bf16r = [](float x) { return __bfloat162float(__float2bfloat16_rn(x)); };
+                    const int j0 = 2 * ((warp - 4) >> 2);  // this group's two 32-column blocks
 #pragma unroll 1
-                    for (int j = 0; j < 4; ++j) {
+                    for (int j = j0; j < j0 + 2; ++j) {
                         float vg[32], vu[32];
                         tmem_ld32(t_base + 32 * j, vg);
                         tmem_ld32(t_base + 128 + 32 * j, vu);
-                        if (j == 3) {  // accumulator read out: the MMA may reuse it
+                        if (j == j0 + 1) {  // accumulator read out: the MMA may reuse it
                             tc_fence_before();
                             mbar_arrive(&bar_tempty[acc]);
                         }
@@ -714,8 +721,43 @@ __global__ void __launch_bounds__(GemmCfg<kBF16, kWide, BN, kMX, kI4>::kThreads,
                         *reinterpret_cast<uint4*>(qr + 32 * j) = make_uint4(o[0], o[1], o[2], o[3]);
                         *reinterpret_cast<uint4*>(qr + 32 * j + 16) = make_uint4(o[4], o[5], o[6], o[7]);
                     }
-                    if (nb == n_blocks - 1)  // factor columns past I/32 (row padding of the factor matrix)
+                    if (nb == n_blocks - 1 && j0 == 0)  // factor columns past I/32 (row padding of the factor matrix)
                         for (int64_t c = I / 32; c < p.act_sf_ld; ++c) sfr[c] = 0;
+                } else if constexpr (kAct == 2) {
+                    // y and h as for kAct 1; h goes to act_h in fp32 and the
+                    // amax |h| of this group's 64 columns of the row into
+                    // act_amax[row] by an integer max on the bit patterns
+                    // (monotone for floats >= 0)
+                    const int64_t I = p.N / 2;
+                    const int64_t compact = p.expert_offsets[e] + (pos - p.padded_offsets[e]);
+                    float* hr = p.act_h + compact * I + static_cast<int64_t>(nb) * 128;
+                    auto bf16r = [](float x) { return __bfloat162float(__float2bfloat16_rn(x)); };
+                    float amax = 0.0f;
+                    const int j0 = 2 * ((warp - 4) >> 2);  // this group's two 32-column blocks
+#pragma unroll 1
+                    for (int j = j0; j < j0 + 2; ++j) {
+                        float vg[32], vu[32];
+                        tmem_ld32(t_base + 32 * j, vg);
+                        tmem_ld32(t_base + 128 + 32 * j, vu);
+                        if (j == j0 + 1) {  // accumulator read out: the MMA may reuse it
+                            tc_fence_before();
+                            mbar_arrive(&bar_tempty[acc]);
+                        }
+                        if (!valid) continue;
+#pragma unroll
+                        for (int i = 0; i < 32; i += 2) {
+                            const float g0 = bf16r(vg[i] * s_wsc[32 * j + i] * rs);
+                            const float g1 = bf16r(vg[i + 1] * s_wsc[32 * j + i + 1] * rs);
+                            const float u0 = bf16r(vu[i] * s_wsc[128 + 32 * j + i] * rs);
+                            const float u1 = bf16r(vu[i + 1] * s_wsc[128 + 32 * j + i + 1] * rs);
+                            silu_mul2(g0, g1, u0, u1, vg[i], vg[i + 1]);
+                            amax = fmaxf(amax, fmaxf(fabsf(vg[i]), fabsf(vg[i + 1])));
+                        }
+#pragma unroll
+                        for (int i = 0; i < 32; i += 4)
+                            *reinterpret_cast<float4*>(hr + 32 * j + i) = make_float4(vg[i], vg[i + 1], vg[i + 2], vg[i + 3]);
+                    }
+                    if (valid) atomicMax(reinterpret_cast<int*>(p.act_amax) + compact, __float_as_int(amax));
                 } else {
                     for (int c0 = 0; c0 < WR; c0 += 32) {
                         float v[32];
@@ -918,10 +960,10 @@ inline bool make_act_map(CUtensorMap* map, const void* a, int64_t rows, int64_t 
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <bool kBF16, bool kWide, int BN, bool kMX = false, bool kI4 = false, bool kSwi = false>
+template <bool kBF16, bool kWide, int BN, bool kMX = false, bool kI4 = false, int kAct = 0>
 inline qmoe_status_t launch_gemm(const void* w, int64_t E, int64_t N, int64_t K, const GemmParams& p,
                                  int64_t max_padded, int64_t a_rows, int64_t lda, cudaStream_t st) {
-    using C = GemmCfg<kBF16, kWide, BN, kMX, kI4, kSwi>;
+    using C = GemmCfg<kBF16, kWide, BN, kMX, kI4, kAct>;
     static std::mutex mu;
     static bool attr_set[64] = {false};
     int dev = 0;
@@ -929,7 +971,7 @@ inline qmoe_status_t launch_gemm(const void* w, int64_t E, int64_t N, int64_t K,
     {
         std::lock_guard<std::mutex> g(mu);
         if (!attr_set[dev]) {
-            if (cudaFuncSetAttribute(moe_gemm_kernel<kBF16, kWide, BN, kMX, kI4, kSwi>,
+            if (cudaFuncSetAttribute(moe_gemm_kernel<kBF16, kWide, BN, kMX, kI4, kAct>,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      C::kDynSmem) != cudaSuccess)
                 return QMOE_ERR_CUDA;
@@ -938,8 +980,8 @@ inline qmoe_status_t launch_gemm(const void* w, int64_t E, int64_t N, int64_t K,
     }
     CUtensorMap map, amap;
     // rows of K weight bytes (FP8, INT8) or K/2 (packed INT4); box: one stage's bytes per row
-    // (kSwi: 128-row boxes, the gate and up halves of a tile loaded separately)
-    if (!make_weight_map(&map, w, E, N, kI4 ? K / 2 : K, kBF16 ? C::kRawRowBytes : C::kBK, kSwi ? 128 : C::kWRows,
+    // (kAct: 128-row boxes, the gate and up halves of a tile loaded separately)
+    if (!make_weight_map(&map, w, E, N, kI4 ? K / 2 : K, kBF16 ? C::kRawRowBytes : C::kBK, kAct ? 128 : C::kWRows,
                          !kBF16))
         return QMOE_ERR_CUDA;
     memset(&amap, 0, sizeof(amap));
@@ -951,24 +993,30 @@ inline qmoe_status_t launch_gemm(const void* w, int64_t E, int64_t N, int64_t K,
                               ((N + C::kWRows - 1) / C::kWRows);
     const int64_t grid = max_tiles < sms ? max_tiles : sms;
     if (grid <= 0) return QMOE_OK;
-    return launch_pdl(moe_gemm_kernel<kBF16, kWide, BN, kMX, kI4, kSwi>, dim3(static_cast<unsigned>(grid)),
+    return launch_pdl(moe_gemm_kernel<kBF16, kWide, BN, kMX, kI4, kAct>, dim3(static_cast<unsigned>(grid)),
                       dim3(C::kThreads), C::kDynSmem, st, map, amap, p);
 }
 
 // out[i] = bf16(accum[i]) for the TOKEN_SUM layout (defined in gemm_w8a8.cu).
 qmoe_status_t launch_token_sum_finalize(const float* accum, uint16_t* out, int64_t n, cudaStream_t st);
 
-// Outputs of the SwiGLU + MXFP8 epilogue (qmoe_moe_gemm_w8a8_silu_mxfp8).
+// Outputs of the SwiGLU epilogues: MXFP8 codes and factors
+// (qmoe_moe_gemm_w8a8_silu_mxfp8), or, with h set, fp32 h and the row amax
+// that qmoe_moe_gemm_w8a8_silu_fp8_token quantises per token afterwards.
 struct SwiGluOut {
     uint8_t* q;
     uint8_t* sf;
     int64_t sf_ld;
     const int32_t* sf_poff;
+    float* h;
+    float* amax;
 };
 
-// Shared argument checks and dispatch for both precisions.
+// Shared argument checks and dispatch for both precisions;
+// check_only: validate the arguments and return without launching anything.
 template <bool kBF16, bool kI4 = false>
-inline qmoe_status_t run_moe_gemm(const qmoe_gemm_args* a, cudaStream_t st, const SwiGluOut* so = nullptr) {
+inline qmoe_status_t run_moe_gemm(const qmoe_gemm_args* a, cudaStream_t st, const SwiGluOut* so = nullptr,
+                                  bool check_only = false) {
     static_assert(!kI4 || kBF16, "W4A16 is a bf16-activation GEMM");
     if (kI4 && a && a->struct_size >= sizeof(qmoe_gemm_args)) {
         // packed int4 weights with a scale per 128-wide group of K: wide tile only
@@ -1012,9 +1060,11 @@ inline qmoe_status_t run_moe_gemm(const qmoe_gemm_args* a, cudaStream_t st, cons
     if (so) {  // fused [gate | up] projection of grouped rows: FP8 per-row scales, 128-slot tiles
         if (kBF16 || mx || wmx) return QMOE_ERR_UNSUPPORTED;
         if (a->out_layout != QMOE_OUT_GROUPED || a->BM != 128 || a->N % 256 != 0) return QMOE_ERR_INVALID_ARG;
-        if (!so->q || !so->sf || !so->sf_poff || !aligned16(so->q) || so->sf_ld < a->N / 64)
+        if (so->h ? (!aligned16(so->h) || !so->amax || !aligned4(so->amax))
+                  : (!so->q || !so->sf || !so->sf_poff || !aligned16(so->q) || so->sf_ld < a->N / 64))
             return QMOE_ERR_INVALID_ARG;
     }
+    if (check_only) return QMOE_OK;
 
     const bool tsum = a->out_layout == QMOE_OUT_TOKEN_SUM;
     if (tsum) {
@@ -1056,6 +1106,8 @@ inline qmoe_status_t run_moe_gemm(const qmoe_gemm_args* a, cudaStream_t st, cons
     p.act_sf = so ? so->sf : nullptr;
     p.act_sf_ld = so ? so->sf_ld : 0;
     p.act_sf_poff = so ? so->sf_poff : nullptr;
+    p.act_h = so ? so->h : nullptr;
+    p.act_amax = so ? so->amax : nullptr;
     const int64_t max_padded = (T + static_cast<int64_t>(a->E) * (a->BM - 1) + a->BM - 1) / a->BM * a->BM;
     const int64_t a_rows = a->a_layout == QMOE_A_PADDED ? max_padded : (a->a_layout == QMOE_A_GROUPED ? T : a->M);
     // the kernel numbers its tiles (slot blocks x weight blocks) with 32-bit ints
@@ -1067,8 +1119,12 @@ inline qmoe_status_t run_moe_gemm(const qmoe_gemm_args* a, cudaStream_t st, cons
         return launch_token_sum_finalize(a->accum, a->out, a->M * a->N, st);
     }
     if constexpr (!kBF16) {
-        if (so) return launch_gemm<false, true, 128, false, false, true>(a->w, a->E, a->N, a->K, p, max_padded, a_rows,
-                                                                         a->lda, st);
+        if (so && so->h)
+            return launch_gemm<false, true, 128, false, false, 2>(a->w, a->E, a->N, a->K, p, max_padded, a_rows, a->lda,
+                                                                  st);
+        if (so)
+            return launch_gemm<false, true, 128, false, false, 1>(a->w, a->E, a->N, a->K, p, max_padded, a_rows, a->lda,
+                                                                  st);
         if (mx) {
             r = launch_gemm<false, true, 128, true>(a->w, a->E, a->N, a->K, p, max_padded, a_rows, a->lda, st);
             if (r != QMOE_OK || !tsum) return r;

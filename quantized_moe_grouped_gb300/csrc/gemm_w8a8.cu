@@ -26,6 +26,10 @@ __global__ void token_sum_finalize_kernel(const float* __restrict__ accum, uint1
     }
 }
 
+// Per-token quantisation of the fp32 h rows (defined in align_quant.cu).
+qmoe_status_t launch_quant_h_token(const float* h, const float* amax, int64_t rows, int64_t I, uint8_t* q,
+                                   float* scale, cudaStream_t st);
+
 qmoe_status_t launch_token_sum_finalize(const float* accum, uint16_t* out, int64_t n, cudaStream_t st) {
     if (n <= 0) return QMOE_OK;
     const int sms = device_sm_count();
@@ -45,6 +49,24 @@ extern "C" qmoe_status_t qmoe_moe_gemm_w8a8(const qmoe_gemm_args* args, qmoe_str
 extern "C" qmoe_status_t qmoe_moe_gemm_w8a8_silu_mxfp8(const qmoe_gemm_args* args, uint8_t* q, uint8_t* sf,
                                                       int64_t sf_ld, const int32_t* sf_padded_offsets,
                                                       qmoe_stream_t stream) {
-    const qmoe::SwiGluOut so{q, sf, sf_ld, sf_padded_offsets};
+    const qmoe::SwiGluOut so{q, sf, sf_ld, sf_padded_offsets, nullptr, nullptr};
     return qmoe::run_moe_gemm<false>(args, stream, &so);
+}
+
+extern "C" qmoe_status_t qmoe_moe_gemm_w8a8_silu_fp8_token(const qmoe_gemm_args* args, uint8_t* q, float* scale,
+                                                          float* h_scratch, qmoe_stream_t stream) {
+    if (!args || args->struct_size < sizeof(qmoe_gemm_args)) return QMOE_ERR_INVALID_ARG;
+    if (!q || !scale || !h_scratch || !qmoe::aligned16(q) || !qmoe::aligned16(h_scratch) || args->M < 0 ||
+        args->top_k < 1 || args->N % 256 != 0)
+        return QMOE_ERR_INVALID_ARG;
+    const int64_t T = args->M * args->top_k;
+    const int64_t I = args->N / 2;
+    float* amax = h_scratch + T * I;  // the row maxima follow the h rows
+    const qmoe::SwiGluOut so{nullptr, nullptr, 0, nullptr, h_scratch, amax};
+    qmoe_status_t r = qmoe::run_moe_gemm<false>(args, stream, &so, true);
+    if (r != QMOE_OK || T == 0) return r;
+    if (cudaMemsetAsync(amax, 0, static_cast<size_t>(T) * sizeof(float), stream) != cudaSuccess) return QMOE_ERR_CUDA;
+    r = qmoe::run_moe_gemm<false>(args, stream, &so);
+    if (r != QMOE_OK) return r;
+    return qmoe::launch_quant_h_token(h_scratch, amax, T, I, q, scale, stream);
 }

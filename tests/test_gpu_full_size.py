@@ -121,13 +121,13 @@ def sampled_token_slots(M, seed):
     return toks, (toks[:, None] * TOP_K + np.arange(TOP_K)[None, :]).ravel()
 
 
-def layer_up(q, orc, wl, fused_mx=False):
+def layer_up(q, orc, wl, fused=None):
     """The layer's first stages as bench.py launches them: moe_align_block_size
     (BM=128), quant_act_fp8_sorted into padded sorted rows, then the up GEMM
     (padded A -> grouped out).  Align and the quantised rows are checked in
-    full, the up projection on 16 sampled slots.  fused_mx: also the same
-    projection with SwiGLU + MXFP8 in its epilogue, whose (codes, factors) are
-    returned last."""
+    full, the up projection on 16 sampled slots.  fused ("mx" or "token"):
+    also the same projection with SwiGLU and that requantisation in its
+    epilogue, whose (codes, factors or scales) are returned last."""
     M, K, I = wl.M, wl.K, wl.inter
     T, BM = M * TOP_K, 128
     ids, tw = inputs.routing(M, E, TOP_K, wl.seed, wl.zipf_s)
@@ -149,9 +149,13 @@ def layer_up(q, orc, wl, fused_mx=False):
     st = status()
     up = q.moe_gemm_w8a8(aq, sa, w1q, w1s, al, None, M=M, top_k=TOP_K, BM=BM, a_layout=q.A_PADDED,
                          out_layout=q.OUT_GROUPED, d_status=st)
-    fused = None
-    if fused_mx:
-        fused = q.moe_gemm_w8a8_silu_mxfp8(aq, sa, w1q, w1s, al, M=M, top_k=TOP_K, a_layout=q.A_PADDED, d_status=st)
+    fused_out = None
+    if fused == "mx":
+        fused_out = q.moe_gemm_w8a8_silu_mxfp8(aq, sa, w1q, w1s, al, M=M, top_k=TOP_K, a_layout=q.A_PADDED,
+                                               d_status=st)
+    elif fused == "token":
+        fused_out = q.moe_gemm_w8a8_silu_fp8_token(aq, sa, w1q, w1s, al, M=M, top_k=TOP_K, a_layout=q.A_PADDED,
+                                                   d_status=st)
     torch.cuda.synchronize()
     assert int(st.item()) == 0
     del w1q, aq
@@ -160,21 +164,25 @@ def layer_up(q, orc, wl, fused_mx=False):
     ref_up = orc.moe_gemm(a_kind=orc.A_FP8_TOKEN, a=raq, a_scale=rsa, w_kind=orc.W_FP8, w=r1q, w_scale=r1s,
                           topk_ids=ids, topk_w=None, E=E, slots=slots)
     check_rows(bf16_to_np_f32(up[torch.from_numpy(pos[slots]).to(dev())]), ref_up)
-    return (ids, tw, al, ref_al, up) + ((fused,) if fused_mx else ())
+    return (ids, tw, al, ref_al, up) + ((fused_out,) if fused else ())
 
 
 def test_mixtral_8x7b_layer_full_size(q, orc):
     """M=4096, K=4096, I=14336, N=4096: align, sorted quant, up GEMM, then
-    SwiGLU + per-token FP8 (bit-exact on every row), then the down GEMM
+    SwiGLU + per-token FP8 (bit-exact on every row; the up GEMM's fused SwiGLU
+    epilogue and per-token pass give the same bytes), then the down GEMM
     (grouped A -> sum over top_k with routing weights) on 8 sampled tokens.
     Each stage's oracle takes the GPU's previous-stage output."""
     wl = inputs.mixtral_8x7b_layer()
     M, I, Nd = wl.M, wl.inter, wl.N
-    ids, tw, al, _, up = layer_up(q, orc, wl)
+    ids, tw, al, _, up, (fq, fs) = layer_up(q, orc, wl, fused="token")
     hq, hs = q.silu_mul_quant(up)
     rhq, rhs = orc.silu_mul_quant_token(up.view(torch.int16).cpu().numpy().view(np.uint16))
     del up
     assert np.array_equal(hq.cpu().numpy(), rhq) and np.array_equal(hs.cpu().numpy(), rhs)
+    # the same intermediate from the up GEMM's SwiGLU epilogue + per-token pass
+    assert torch.equal(fq, hq) and torch.equal(fs, hs)
+    del fq, fs
     w2q, w2s, r2q, r2s = fp8_weights(q, orc, Nd, I, wl.seed, weight_set=1)
     st = status()
     down = q.moe_gemm_w8a8(hq, hs, w2q, w2s, al, to_dev(tw), M=M, top_k=TOP_K, BM=128, a_layout=q.A_GROUPED,
@@ -197,7 +205,7 @@ def test_mixtral_8x22b_mx_layer_full_size(q, orc):
     wl = inputs.mixtral_8x22b_layer()
     M, I, Nd = wl.M, wl.inter, wl.N
     T = M * TOP_K
-    ids, tw, al, ref_al, up, (fq, fsf) = layer_up(q, orc, wl, fused_mx=True)
+    ids, tw, al, ref_al, up, (fq, fsf) = layer_up(q, orc, wl, fused="mx")
     eoff, poff = ref_al["expert_offsets"], ref_al["padded_offsets"]
     hq, sf = q.silu_mul_quant(up, q.SCALE_MX_1X32, expert_offsets=al["expert_offsets"],
                               sf_padded_offsets=al["padded_offsets"], sf_rows=q.align_max_padded(T, E, 128))

@@ -386,3 +386,59 @@ def test_w8a16_padded_sorted_activations(q, orc, M, K, N, E, top_k, BM, out_layo
     ref = orc.moe_gemm(a_kind=orc.A_BF16, a=a_full, w_kind=orc.W_INT8, w=rwq, w_scale=rws, topk_ids=ids, topk_w=tw,
                        E=E, a_layout="padded", BM=BM, out_layout={0: "slot", 2: "token_sum"}[out_layout])
     check(bf16_to_np_f32(out), ref)
+
+
+@pytest.mark.parametrize("M,K,I,E,top_k,zipf,a_layout,routed", [
+    (256, 256, 384, 8, 2, None, 2, False),     # padded A, ragged expert counts
+    (150, 160, 256, 5, 3, None, 0, True),      # token-gather A, ragged K, routing weights
+    (300, 512, 1024, 16, 2, None, 1, False),   # grouped A, five experts without slots
+    (1024, 256, 2560, 8, 2, 1.2, 2, False),    # Zipf skew, more tiles than SMs
+])
+def test_gemm_silu_fp8_token_epilogue_bitexact(q, orc, M, K, I, E, top_k, zipf, a_layout, routed):
+    """FP8 [gate | up] projection with SwiGLU in the GEMM epilogue (fp32 h and
+    row maxima) and the per-token requantisation pass: codes and scales
+    identical to the oracle's per-token SwiGLU quantisation of the bf16 output
+    the same GEMM stores without the fused epilogue."""
+    T, N = M * top_k, 2 * I
+    seed = 7 * M + K + I
+    if E == 16:
+        ids, tw = inputs.routing(M, 11, top_k, seed)
+        ids = np.where(ids < 5, ids, ids + 5).astype(np.int32)
+        p = fp8_problem(q, orc, M, K, N, E, top_k, seed=seed, ids=ids, tw=tw)
+    else:
+        p = fp8_problem(q, orc, M, K, N, E, top_k, seed=seed, zipf=zipf)
+    al = q.moe_align_block_size(to_dev(p["ids"]), E, 128)
+    twd = to_dev(p["tw"]) if routed else None
+    if a_layout == q.A_PADDED:
+        a_in, s_in = q.quant_act_fp8_sorted(to_dev_bf16(p["a"]), al, top_k)
+    elif a_layout == q.A_GROUPED:
+        order = np.empty(T, dtype=np.int64)
+        order[orc.compact_row_of_slot(p["ids"], E)] = np.arange(T)
+        src = to_dev(order // top_k)
+        a_in, s_in = p["aq"][src].contiguous(), p["sa"][src].contiguous()
+    else:
+        a_in, s_in = p["aq"], p["sa"]
+    st = status()
+    y = q.moe_gemm_w8a8(a_in, s_in, p["wq"], p["ws"], al, twd, M=M, top_k=top_k, BM=128, a_layout=a_layout,
+                        out_layout=q.OUT_GROUPED, d_status=st)
+    hq, hs = q.moe_gemm_w8a8_silu_fp8_token(a_in, s_in, p["wq"], p["ws"], al, M=M, top_k=top_k, a_layout=a_layout,
+                                            topk_weights=twd, d_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    rq, rs = orc.silu_mul_quant_token(y.view(torch.int16).cpu().numpy().view(np.uint16))
+    assert np.array_equal(hs.cpu().numpy(), rs)
+    assert np.array_equal(hq.cpu().numpy(), rq)
+
+
+def test_gemm_silu_fp8_token_rejects_before_launch(q, orc):
+    """A host-side argument error (K % 16 != 0) returns before anything is
+    launched: the scratch keeps its contents."""
+    import quantized_moe_grouped_gb300 as qq
+    M, K, N, E = 32, 40, 256, 2
+    p = fp8_problem(q, orc, M, K, N, E, 2, seed=12)
+    al = q.moe_align_block_size(to_dev(p["ids"]), E, 128)
+    scratch = torch.full((M * 2 * (N // 2) + M * 2,), 3.0, device=dev())
+    with pytest.raises(qq.QmoeError):
+        q.moe_gemm_w8a8_silu_fp8_token(p["aq"], p["sa"], p["wq"], p["ws"], al, M=M, top_k=2, h_scratch=scratch)
+    torch.cuda.synchronize()
+    assert bool((scratch == 3.0).all())
