@@ -166,8 +166,10 @@ qmoe_status_t qmoe_moe_router_topk(const float* logits, int64_t M, int32_t E, in
                                    float* topk_weights, qmoe_stream_t stream);
 
 /* Router + moe_align_block_size + per-token quantisation in padded sorted
- * order in one launch for T = M*top_k <= 4096 (larger T: three launches), the
- * decode-sized front of the grouped GEMM.  Outputs are those of
+ * order, the decode-sized front of the grouped GEMM: one launch for M <= 64
+ * (every CTA routes all M tokens itself), two for larger M with
+ * T = M*top_k <= 4096 (the router, then align + quantisation in one launch),
+ * three for larger T.  Outputs are those of
  * qmoe_moe_router_topk followed by qmoe_moe_align_quant_fp8 (pad rows of q and
  * scale not written).  Limits as there. */
 qmoe_status_t qmoe_moe_route_align_quant_fp8(const float* logits, const uint16_t* x, int64_t M, int64_t cols,

@@ -375,6 +375,7 @@ __global__ void router_topk_kernel(const float* __restrict__ logits, int64_t M, 
 // unwritten (the grouped GEMM never stores their results).
 // ======================================================================
 constexpr int kFusedMaxT = 4096;
+constexpr int kRouteFusedMaxM = 64;  // largest M routed inside the align + quantisation launch
 
 // kRoute: the ids come from routing fp32 logits [M, E] in the same launch --
 // every CTA routes all tokens (its histogram needs them) and CTA m writes
@@ -1020,6 +1021,15 @@ qmoe_status_t qmoe_moe_route_align_quant_fp8(const float* logits, const uint16_t
                                        padded_offsets, d_status, stream);
         if (st != QMOE_OK) return st;
         return qmoe_quant_act_fp8_sorted(x, M, cols, ldx, sorted_ids, num_post_padded, top_k, cap, q, scale, stream);
+    }
+    if (M > kRouteFusedMaxM) {
+        // every CTA of the one-launch form routes all M tokens (work ~ M^2):
+        // past a few dozen tokens the router's own launch is cheaper
+        // (measured at M=512: 14.3 us for router + align/quant against 22.5)
+        const qmoe_status_t st = qmoe_moe_router_topk(logits, M, E, top_k, topk_ids, topk_weights, stream);
+        if (st != QMOE_OK) return st;
+        return qmoe_moe_align_quant_fp8(x, M, cols, ldx, topk_ids, top_k, E, BM, sorted_ids, expert_ids,
+                                        num_post_padded, expert_offsets, padded_offsets, q, scale, d_status, stream);
     }
     return launch_pdl(align_quant_fused_kernel<true>, dim3(static_cast<unsigned>(M + 1)), dim3(kRowThreads), 0, stream,
                       x, M, cols, ldx, static_cast<const int32_t*>(nullptr), logits, topk_ids, topk_weights, top_k, E,
