@@ -56,15 +56,15 @@ extern "C" qmoe_status_t qmoe_moe_gemm_w8a8_silu_mxfp8(const qmoe_gemm_args* arg
 extern "C" qmoe_status_t qmoe_moe_gemm_w8a8_silu_fp8_token(const qmoe_gemm_args* args, uint8_t* q, float* scale,
                                                           float* h_scratch, qmoe_stream_t stream) {
     if (!args || args->struct_size < sizeof(qmoe_gemm_args)) return QMOE_ERR_INVALID_ARG;
-    if (!q || !scale || !h_scratch || !qmoe::aligned16(q) || !qmoe::aligned16(h_scratch) || args->M < 0 ||
-        args->top_k < 1 || args->N % 256 != 0)
-        return QMOE_ERR_INVALID_ARG;
+    if (args->M < 0 || args->top_k < 1 || args->N % 256 != 0) return QMOE_ERR_INVALID_ARG;
     const int64_t T = args->M * args->top_k;
+    if (T == 0) return qmoe::run_moe_gemm<false>(args, stream, nullptr, true);  // nothing to write
+    if (!q || !scale || !h_scratch || !qmoe::aligned16(q) || !qmoe::aligned16(h_scratch)) return QMOE_ERR_INVALID_ARG;
     const int64_t I = args->N / 2;
     float* amax = h_scratch + T * I;  // the row maxima follow the h rows
     const qmoe::SwiGluOut so{nullptr, nullptr, 0, nullptr, h_scratch, amax};
     qmoe_status_t r = qmoe::run_moe_gemm<false>(args, stream, &so, true);
-    if (r != QMOE_OK || T == 0) return r;
+    if (r != QMOE_OK) return r;
     if (cudaMemsetAsync(amax, 0, static_cast<size_t>(T) * sizeof(float), stream) != cudaSuccess) return QMOE_ERR_CUDA;
     r = qmoe::run_moe_gemm<false>(args, stream, &so);
     if (r != QMOE_OK) return r;

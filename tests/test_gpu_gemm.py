@@ -442,3 +442,74 @@ def test_gemm_silu_fp8_token_rejects_before_launch(q, orc):
         q.moe_gemm_w8a8_silu_fp8_token(p["aq"], p["sa"], p["wq"], p["ws"], al, M=M, top_k=2, h_scratch=scratch)
     torch.cuda.synchronize()
     assert bool((scratch == 3.0).all())
+
+
+@pytest.mark.parametrize("M,K,N,E,top_k,BM", [(40, 64, 48, 256, 8, 16), (40, 64, 48, 256, 8, 128),
+                                              (3, 16, 16, 2, 1, 16), (5, 16, 32, 2, 2, 256)])
+@pytest.mark.parametrize("a_layout,out_layout", [(0, 0), (1, 1), (0, 2)])
+def test_w8a8_extreme_shapes(q, orc, M, K, N, E, top_k, BM, a_layout, out_layout):
+    """The largest expert count (E = 256) with top_k = 8 (most experts get no
+    slot or one), and the smallest N and K (16) the tiles accept."""
+    p = fp8_problem(q, orc, M, K, N, E, top_k, seed=M * 31 + E + N)
+    T = M * top_k
+    al = q.moe_align_block_size(to_dev(p["ids"]), E, BM)
+    if a_layout == q.A_GROUPED:
+        order = np.empty(T, dtype=np.int64)
+        order[orc.compact_row_of_slot(p["ids"], E)] = np.arange(T)
+        src = order // top_k
+        a_in, s_in = p["aq"][to_dev(src)].contiguous(), p["sa"][to_dev(src)].contiguous()
+        ra, rs = p["raq"][src], p["rsa"][src]
+    else:
+        a_in, s_in, ra, rs = p["aq"], p["sa"], p["raq"], p["rsa"]
+    st = status()
+    out = q.moe_gemm_w8a8(a_in, s_in, p["wq"], p["ws"], al, to_dev(p["tw"]), M=M, top_k=top_k, BM=BM,
+                          a_layout=a_layout, out_layout=out_layout, d_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    ref = orc.moe_gemm(a_kind=orc.A_FP8_TOKEN, a=ra, a_scale=rs, w_kind=orc.W_FP8, w=p["rwq"], w_scale=p["rws"],
+                       topk_ids=p["ids"], topk_w=p["tw"], E=E, a_layout="grouped" if a_layout == 1 else "token",
+                       out_layout={0: "slot", 1: "grouped", 2: "token_sum"}[out_layout])
+    check(bf16_to_np_f32(out), ref)
+
+
+def test_w8a16_extreme_shapes(q, orc):
+    """W8A16 with E = 256 and top_k = 8."""
+    M, K, N, E, top_k, BM = 40, 64, 48, 256, 8, 128
+    a = inputs.activations_bf16(M, K, seed=77)
+    w = inputs.expert_weights_f32(E, N, K, seed=77)
+    ids, tw = inputs.routing(M, E, top_k, seed=77)
+    wq, ws = q.quant_weight_int8(to_dev(w))
+    rwq, rws = orc.quant_rows_int8_f32(w)
+    al = q.moe_align_block_size(to_dev(ids), E, BM)
+    st = status()
+    out = q.moe_gemm_w8a16(to_dev_bf16(a), wq, ws, al, to_dev(tw), M=M, top_k=top_k, BM=BM, d_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    ref = orc.moe_gemm(a_kind=orc.A_BF16, a=a, w_kind=orc.W_INT8, w=rwq, w_scale=rws, topk_ids=ids, topk_w=tw, E=E)
+    check(bf16_to_np_f32(out), ref)
+
+
+def test_gemms_with_no_tokens(q, orc):
+    """M = 0 (T = 0): every GEMM entry point returns OK and writes nothing."""
+    K, N, E, top_k = 128, 256, 4, 2
+    ids = np.zeros((0, top_k), dtype=np.int32)
+    al = q.moe_align_block_size(to_dev(ids), E, 128)
+    assert int(al["num_post_padded"].item()) == 0
+    w = inputs.expert_weights_f32(E, N, K, seed=3)
+    wq, ws = q.quant_weight_fp8(to_dev(w))
+    wq8, ws8 = q.quant_weight_int8(to_dev(w))
+    aq = torch.zeros(1, K, dtype=torch.uint8, device=dev())
+    sa = torch.ones(1, dtype=torch.float32, device=dev())
+    abf = torch.zeros(1, K, dtype=torch.bfloat16, device=dev())
+    tw = torch.zeros(1, top_k, dtype=torch.float32, device=dev())
+    sentinel = torch.full((4, N), 7.0, dtype=torch.bfloat16, device=dev())
+    for layout in (q.OUT_SLOT, q.OUT_GROUPED, q.OUT_TOKEN_SUM):
+        out = sentinel.clone()
+        q.moe_gemm_w8a8(aq, sa, wq, ws, al, tw, M=0, top_k=top_k, BM=128, out_layout=layout, out=out)
+        q.moe_gemm_w8a16(abf, wq8, ws8, al, tw, M=0, top_k=top_k, BM=128, out_layout=layout, out=out)
+        torch.cuda.synchronize()
+        assert torch.equal(out, sentinel)
+    hq, hs = q.moe_gemm_w8a8_silu_fp8_token(aq, sa, wq, ws, al, M=0, top_k=top_k)
+    fq, fsf = q.moe_gemm_w8a8_silu_mxfp8(aq, sa, wq, ws, al, M=0, top_k=top_k)
+    torch.cuda.synchronize()
+    assert hq.numel() == 0 and hs.numel() == 0 and fq.numel() == 0
