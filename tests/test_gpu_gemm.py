@@ -225,7 +225,8 @@ def test_w8a8_decode_full_size_sampled(q, orc):
 
 
 @pytest.mark.parametrize("M,K,N,E,top_k,BM,out_layout", [(64, 128, 256, 8, 2, 32, 0), (200, 272, 208, 8, 2, 64, 2),
-                                                         (333, 512, 400, 8, 2, 128, 0), (90, 160, 272, 5, 3, 256, 2)])
+                                                         (333, 512, 400, 8, 2, 128, 0), (90, 160, 272, 5, 3, 256, 2),
+                                                         (300, 6144, 128, 8, 2, 128, 2), (64, 8320, 128, 8, 2, 128, 0)])
 def test_w8a8_padded_sorted_activations(q, orc, M, K, N, E, top_k, BM, out_layout):
     """quant_act_fp8_sorted (bit-exact against the oracle's per-token codes placed
     at the padded sorted positions) feeding the GEMM's PADDED activation layout."""
