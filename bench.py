@@ -273,12 +273,14 @@ def run_reference(args) -> None:
 
 
 # ----------------------------------------------------------------- suite ---
-def _timed(fn, reps, flush=None):
-    """Median device time (ms) of fn() over reps runs, each after an L2 flush.
-    A 30 us device sleep before the start event keeps the GPU busy while the
-    host enqueues fn's launches, so short kernels are timed without the host's
-    launch latency."""
+def _timed(fn, reps, flush=None, warmup=5):
+    """Median device time (ms) of fn() over reps runs after `warmup` untimed
+    runs, each timed run after an L2 flush.  A 30 us device sleep before the
+    start event keeps the GPU busy while the host enqueues fn's launches, so
+    short kernels are timed without the host's launch latency."""
     import torch
+    for _ in range(warmup):
+        fn()
     ts = []
     for _ in range(reps):
         if flush is not None:
@@ -294,7 +296,7 @@ def _timed(fn, reps, flush=None):
     return statistics.median(ts)
 
 
-def run_suite(reps: int = 20, only: str | None = None) -> None:
+def run_suite(reps: int = 50, only: str | None = None) -> None:
     """Per-entry-point timings of the other workloads (not the bench line):
     INT8 W8A16 sweep, Mixtral-8x7B- and 8x22B-shaped FP8 layers.  Weights are
     N(0, 1/K) drawn with torch's seeded device generator (timing only); every
@@ -538,7 +540,7 @@ def main() -> None:
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--suite", action="store_true", help="per-kernel timings of the other workloads instead")
     ap.add_argument("--only", default=None, help="--suite: workloads whose name contains this text")
-    ap.add_argument("--reps", type=int, default=20, help="--suite: timed repetitions per kernel")
+    ap.add_argument("--reps", type=int, default=50, help="--suite: timed repetitions per kernel (median)")
     args = ap.parse_args()
     if args.suite:
         run_suite(args.reps, args.only)
