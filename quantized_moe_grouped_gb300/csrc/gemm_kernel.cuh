@@ -83,6 +83,10 @@ struct GemmParams {
     const int32_t* act_sf_poff;  // first factor row of each expert
     float* act_h;
     float* act_amax;
+    // > 0: before waiting for the previous kernel, prefetch this many k-blocks of
+    // the CTA's first weight tile into L2, the tile taken as if every expert had
+    // one slot block (decode-sized launches; a wrong guess only costs bandwidth)
+    int32_t l2_prefetch_kb;
 };
 
 constexpr int kGemmMaxE = 256;  // experts per call (the align's limit)
@@ -163,6 +167,14 @@ struct GemmCfg {
 QMOE_DI bool mbar_wait_drain(uint64_t* bar, uint32_t parity, int32_t* d_status) {
     int dummy = 0;
     return mbar_wait(bar, parity, &dummy, d_status);
+}
+
+// L2 prefetch of one box of a tiled tensor map (no shared memory, no barrier).
+QMOE_DI void tma_prefetch_l2_3d(const CUtensorMap* map, int x, int y, int z) {
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y), "r"(z)
+                 : "memory");
 }
 
 QMOE_DI uint32_t pack_bf16x2(float lo, float hi) {
@@ -277,6 +289,17 @@ __global__ void __launch_bounds__(GemmCfg<kBF16, kWide, BN, kMX, kI4, kAct>::kTh
     // previous kernel on the stream; from here on the kernel reads the align
     // outputs, activations and weights and writes its outputs.
     pdl_launch_dependents();
+    if (p.l2_prefetch_kb > 0 && threadIdx.x == 0) {
+        // the weights are not written by the previous kernel: while it finishes,
+        // bring the likely first weight tile into L2 (expert-major order with one
+        // slot block per expert: tile t = expert t / n_blocks, weight block t % n_blocks)
+        const int nbk = static_cast<int>((p.N + WR - 1) / WR);
+        const int e0 = static_cast<int>(blockIdx.x) / nbk;
+        const int nb0 = static_cast<int>(blockIdx.x) % nbk;
+        if (e0 < p.E)
+            for (int kb = 0; kb < p.l2_prefetch_kb && kb < p.num_k_blocks; ++kb)
+                tma_prefetch_l2_3d(&tmap_w, kb * C::kBK, nb0 * WR, e0);
+    }
     pdl_wait();
     for (int i = threadIdx.x; i <= p.E; i += blockDim.x) s_poff[i] = p.padded_offsets[i];
     if (C::kW2 && warp == 0) {
@@ -1108,6 +1131,13 @@ inline qmoe_status_t run_moe_gemm(const qmoe_gemm_args* a, cudaStream_t st, cons
     p.act_sf_poff = so ? so->sf_poff : nullptr;
     p.act_h = so ? so->h : nullptr;
     p.act_amax = so ? so->amax : nullptr;
+    // decode-sized FP8 launches (at most one slot block per expert on average):
+    // about 128 KB of weights per CTA prefetched into L2 ahead of the wait
+    {
+        const int64_t slot_rows = a->BM >= 128 ? 128 : a->BM;
+        const int64_t w_stage = (a->BM >= 128 ? 256 : 128) * 128;
+        p.l2_prefetch_kb = (!kBF16 && !mx && !so && T <= slot_rows * a->E) ? static_cast<int32_t>(131072 / w_stage) : 0;
+    }
     const int64_t max_padded = (T + static_cast<int64_t>(a->E) * (a->BM - 1) + a->BM - 1) / a->BM * a->BM;
     const int64_t a_rows = a->a_layout == QMOE_A_PADDED ? max_padded : (a->a_layout == QMOE_A_GROUPED ? T : a->M);
     // the kernel numbers its tiles (slot blocks x weight blocks) with 32-bit ints
