@@ -148,6 +148,10 @@ struct GemmCfg {
     static constexpr int kTmemCols = (kMX || kW2) ? 512 : (2 * kAccCols < 32 ? 32 : 2 * kAccCols);
     static constexpr uint32_t kIdesc =
         kMX ? make_idesc_mx(128, kMmaN) : make_idesc(kBF16 ? kFmtBF16 : kFmtE4M3, 128, kMmaN);
+    // Tail split (plain FP8 wide tile): quarter tiles of 64 weight rows (MMA N = 64)
+    static constexpr bool kTailSplit = kWide && !kBF16 && !kMX && kAct == 0 && !kW2;
+    static constexpr int kQRows = 64;
+    static constexpr uint32_t kIdescQ = make_idesc(kFmtE4M3, 128, kQRows);
     static_assert(!kMX || (kWide && !kBF16), "MX scales: FP8 wide tile only");
     static_assert(!kI4 || (kBF16 && kWide), "W4A16: wide bf16 tile only");
     static_assert(!kWide || BN == 128 || BN == 256, "wide tile: 128 or 256 slots");
@@ -233,7 +237,7 @@ QMOE_DI void tmem_wait_ld_regs(uint32_t (&r)[32]) {
 template <bool kBF16, bool kWide, int BN, bool kMX, bool kI4, int kAct>
 __global__ void __launch_bounds__(GemmCfg<kBF16, kWide, BN, kMX, kI4, kAct>::kThreads, 1)
     moe_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_a,
-                    const GemmParams p) {
+                    const __grid_constant__ CUtensorMap tmap_wq, const GemmParams p) {
     using C = GemmCfg<kBF16, kWide, BN, kMX, kI4, kAct>;
     constexpr int S = C::kStages;
     constexpr int SR = C::kSlotRows;
@@ -376,6 +380,27 @@ __global__ void __launch_bounds__(GemmCfg<kBF16, kWide, BN, kMX, kI4, kAct>::kTh
     auto second_half = [&](int e, int sb) {
         return sb + 1 < s_poff[e + 1] / 128 && p.sorted_ids[(sb + 1) * 128] < p.T;
     };
+    // Tail split (kTailSplit): when the last partial wave of the round robin
+    // holds at most a quarter of the CTAs' worth of tiles, each of those tiles
+    // runs as four quarter tiles of 64 weight rows (loaded through tmap_wq, MMA
+    // N = 64), so the launch ends about a quarter of a tile's time after the
+    // full waves instead of a whole tile's.  Every role walks the same work
+    // items: items below full_tiles are the tiles above, item full_tiles + 4i + q
+    // is quarter q of tile full_tiles + i.  qt = -1 for a whole tile.
+    const int grid_n = static_cast<int>(gridDim.x);
+    const int tail_r = (C::kTailSplit && num_tiles % grid_n != 0 && 4 * (num_tiles % grid_n) <= grid_n)
+                           ? num_tiles % grid_n
+                           : 0;
+    const int full_tiles = num_tiles - tail_r;
+    const int num_work = full_tiles + 4 * tail_r;
+    auto work_tile = [&](int w, int& sb, int& nb, int& qt) {
+        qt = -1;
+        if (w >= full_tiles) {
+            qt = (w - full_tiles) & 3;
+            w = full_tiles + ((w - full_tiles) >> 2);
+        }
+        return tile_expert(w, sb, nb);
+    };
 
     if (warp == 0) {
         // ------------------------------------------------ TMA producer ---
@@ -384,9 +409,10 @@ __global__ void __launch_bounds__(GemmCfg<kBF16, kWide, BN, kMX, kI4, kAct>::kTh
             bool ok = true;
             // MXFP8 weights add the stage's 1 KB block of tiled weight factors
             const uint32_t tx = C::kWBytes + (p.a_tma ? C::kActBytes : 0) + (kMX && p.w_sf ? 2 * C::kSfBytes : 0);
-            for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+            for (int tile = blockIdx.x; ok && tile < num_work; tile += gridDim.x) {
                 int sb, nb;
-                const int e = tile_expert(tile, sb, nb);
+                int qt;
+                const int e = work_tile(tile, sb, nb, qt);
                 if (e < 0) continue;
                 // first activation row of the tile: padded position, or compact grouped row
                 const int arow0 = (p.a_layout == QMOE_A_PADDED)
@@ -403,11 +429,14 @@ __global__ void __launch_bounds__(GemmCfg<kBF16, kWide, BN, kMX, kI4, kAct>::kTh
                         const int s = it % S;
                         const uint32_t ph = (it / S) & 1;
                         if (!mbar_wait(&bar_empty[s], ph ^ 1, abort, p.d_status)) { ok = false; break; }
-                        mbar_arrive_expect_tx(&bar_full[s], tx);
+                        // a quarter tile brings a quarter of the weight rows
+                        mbar_arrive_expect_tx(&bar_full[s], qt < 0 ? tx : tx - (C::kWBytes - C::kWBytes / 4));
                         if constexpr (kAct != 0) {  // gate rows, then the matching up rows
                             tma_load_3d(&tmap_w, &bar_full[s], w_tile(s), kb * C::kBK, nb * 128, e);
                             tma_load_3d(&tmap_w, &bar_full[s], w_tile(s) + 128 * 128, kb * C::kBK,
                                         static_cast<int>(p.N / 2) + nb * 128, e);
+                        } else if (C::kTailSplit && qt >= 0) {
+                            tma_load_3d(&tmap_wq, &bar_full[s], w_tile(s), kb * C::kBK, nb * WR + qt * C::kQRows, e);
                         } else {
                             tma_load_3d(&tmap_w, &bar_full[s], w_tile(s), kb * C::kBK, nb * WR, e);
                         }
@@ -434,9 +463,10 @@ __global__ void __launch_bounds__(GemmCfg<kBF16, kWide, BN, kMX, kI4, kAct>::kTh
                 tmem_cp_32x128b_x4(tmem_base + C::kSfbCol, sd);
                 tmem_cp_32x128b_x4(tmem_base + C::kSfbCol + 4, sd);
             }
-            for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+            for (int tile = blockIdx.x; ok && tile < num_work; tile += gridDim.x) {
                 int sb, nb;
-                const int e = tile_expert(tile, sb, nb);
+                int qt;
+                const int e = work_tile(tile, sb, nb, qt);
                 if (e < 0) continue;
                 const int acc = tcount % C::kAccBufs;
                 const uint32_t aph = (tcount / C::kAccBufs) & 1;
@@ -472,7 +502,8 @@ __global__ void __launch_bounds__(GemmCfg<kBF16, kWide, BN, kMX, kI4, kAct>::kTh
                                      tmem_base + C::kSfaCol + 4 * s, tmem_base + C::kSfbCol + (p.w_sf ? 8 * s : 0),
                                      (kb | k) != 0);
                         else if (kBF16) mma_f16(d_tmem, da + 2 * k, db + 2 * k, C::kIdesc, (kb | k) != 0);
-                        else mma_f8f6f4(d_tmem, da + 2 * k, db + 2 * k, C::kIdesc, (kb | k) != 0);
+                        else mma_f8f6f4(d_tmem, da + 2 * k, db + 2 * k, (C::kTailSplit && qt >= 0) ? C::kIdescQ : C::kIdesc,
+                                        (kb | k) != 0);
                     }
                     if constexpr (C::kW2) {
                         if (half2) {
@@ -501,9 +532,10 @@ __global__ void __launch_bounds__(GemmCfg<kBF16, kWide, BN, kMX, kI4, kAct>::kTh
         // their slot frees, so their latency stays off the MMA's path.
         int it = 0;
         bool ok = true;
-        for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+        for (int tile = blockIdx.x; ok && tile < num_work; tile += gridDim.x) {
             int sb, nb;
-            const int e = tile_expert(tile, sb, nb);
+            int qt;
+                const int e = work_tile(tile, sb, nb, qt);
             if (e < 0) continue;
             const int cnt = p.expert_offsets[e + 1] - p.expert_offsets[e];
             const uint8_t* sfrow[4];
@@ -544,9 +576,10 @@ __global__ void __launch_bounds__(GemmCfg<kBF16, kWide, BN, kMX, kI4, kAct>::kTh
         if (warp == 2 && lane == 0) {
             int it = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+            for (int tile = blockIdx.x; ok && tile < num_work; tile += gridDim.x) {
                 int sb, nb;
-                const int e = tile_expert(tile, sb, nb);
+                int qt;
+                const int e = work_tile(tile, sb, nb, qt);
                 if (e < 0) continue;
                 const int arow0 = (p.a_layout == QMOE_A_PADDED)
                                       ? sb * SR
@@ -569,10 +602,11 @@ __global__ void __launch_bounds__(GemmCfg<kBF16, kWide, BN, kMX, kI4, kAct>::kTh
         const int pt = threadIdx.x - 64;
         int it = 0;
         bool ok = !p.a_tma;
-        for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+        for (int tile = blockIdx.x; ok && tile < num_work; tile += gridDim.x) {
             if (*abort) break;
             int sb, nb;
-            const int e = tile_expert(tile, sb, nb);
+            int qt;
+                const int e = work_tile(tile, sb, nb, qt);
             if (e < 0) continue;
             named_bar_sync(1, C::kBProdThreads);
             for (int j = pt; j < SR; j += C::kBProdThreads) {
@@ -616,10 +650,11 @@ __global__ void __launch_bounds__(GemmCfg<kBF16, kWide, BN, kMX, kI4, kAct>::kTh
         const int q = warp & 3;  // TMEM lane quadrant of this warp
         const int hs = C::kW2 ? (warp - 4) >> 2 : 0;  // kW2: slot half (accumulator) of this group
         int tcount = 0;
-        for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+        for (int tile = blockIdx.x; tile < num_work; tile += gridDim.x) {
             if (*abort) break;
             int sb, nb;
-            const int e = tile_expert(tile, sb, nb);
+            int qt;
+                const int e = work_tile(tile, sb, nb, qt);
             if (e < 0) continue;
             const int acc = tcount % C::kAccBufs;
             const uint32_t aph = (tcount / C::kAccBufs) & 1;
@@ -629,7 +664,7 @@ __global__ void __launch_bounds__(GemmCfg<kBF16, kWide, BN, kMX, kI4, kAct>::kTh
                 // lane = slot row, columns = 256 output channels
                 named_bar_sync(2, C::kEpiThreads);
                 for (int c = et; c < WR; c += C::kEpiThreads) {
-                    const int64_t n = kAct == 0 ? static_cast<int64_t>(nb) * WR + c
+                    const int64_t n = kAct == 0 ? static_cast<int64_t>(nb) * WR + (qt >= 0 ? qt * C::kQRows : 0) + c
                                             : (c < 128 ? 0 : p.N / 2) + static_cast<int64_t>(nb) * 128 + (c & 127);
                     s_wsc[c] = (n < p.N) ? (p.w_scale ? p.w_scale[static_cast<int64_t>(e) * p.N + n] : 1.0f) : 0.0f;
                 }
@@ -650,8 +685,11 @@ __global__ void __launch_bounds__(GemmCfg<kBF16, kWide, BN, kMX, kI4, kAct>::kTh
                 }
                 if (!mbar_wait(&bar_tfull[acc], aph, abort, p.d_status)) break;
                 tc_fence_after();
-                const int64_t col0 = orow * p.N + static_cast<int64_t>(nb) * WR;
-                const int64_t n_left = p.N - static_cast<int64_t>(nb) * WR;
+                // first output channel of the tile (a quarter tile starts qt * 64 rows in)
+                const int64_t nbase = static_cast<int64_t>(nb) * WR + (qt >= 0 ? qt * C::kQRows : 0);
+                const int ncols = qt >= 0 ? C::kQRows : WR;  // accumulator columns of this tile
+                const int64_t col0 = orow * p.N + nbase;
+                const int64_t n_left = p.N - nbase;
                 const bool tsum = p.out_layout == QMOE_OUT_TOKEN_SUM;
                 // scale and write 8 consecutive output channels starting at column cc
                 auto emit8 = [&](int cc, const float* v) {
@@ -782,10 +820,10 @@ __global__ void __launch_bounds__(GemmCfg<kBF16, kWide, BN, kMX, kI4, kAct>::kTh
                     }
                     if (valid) atomicMax(reinterpret_cast<int*>(p.act_amax) + compact, __float_as_int(amax));
                 } else {
-                    for (int c0 = 0; c0 < WR; c0 += 32) {
+                    for (int c0 = 0; c0 < ncols; c0 += 32) {
                         float v[32];
                         tmem_ld32(t_base + c0, v);
-                        if (c0 + 32 == WR) {  // accumulator read out: the MMA may reuse it while the stores finish
+                        if (c0 + 32 == ncols) {  // accumulator read out: the MMA may reuse it while the stores finish
                             tc_fence_before();
                             mbar_arrive(&bar_tempty[acc]);
                         }
@@ -861,9 +899,10 @@ __global__ void __launch_bounds__(GemmCfg<kBF16, kWide, BN, kMX, kI4, kAct>::kTh
             const int ct = threadIdx.x - 256 - group * C::kConvThreads;
             int it = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+            for (int tile = blockIdx.x; ok && tile < num_work; tile += gridDim.x) {
                 int sb, nb;
-                const int e = tile_expert(tile, sb, nb);
+                int qt;
+                const int e = work_tile(tile, sb, nb, qt);
                 if (e < 0) continue;
                 for (int kb = 0; kb < nkb; ++kb, ++it) {
                     if ((it & 1) != group) continue;
@@ -1009,15 +1048,20 @@ inline qmoe_status_t launch_gemm(const void* w, int64_t E, int64_t N, int64_t K,
         return QMOE_ERR_CUDA;
     memset(&amap, 0, sizeof(amap));
     if (p.a_tma && !make_act_map(&amap, p.a, a_rows, K, lda, kBF16 ? 2 : 1, C::kSlotRows)) return QMOE_ERR_CUDA;
+    CUtensorMap mapq;  // quarter-tile weight boxes (tail split)
+    memset(&mapq, 0, sizeof(mapq));
+    if (C::kTailSplit && !make_weight_map(&mapq, w, E, N, K, C::kBK, C::kQRows, true)) return QMOE_ERR_CUDA;
     const int sms = device_sm_count();
     if (sms <= 0) return QMOE_ERR_CUDA;
     // (kW2: the last pair of an expert may hold a single 128-slot block)
     const int64_t max_tiles = ((max_padded + C::kSlotRows - 1) / C::kSlotRows + (C::kW2 ? E : 0)) *
                               ((N + C::kWRows - 1) / C::kWRows);
-    const int64_t grid = max_tiles < sms ? max_tiles : sms;
+    // (tail split: up to four CTAs per tile when all tiles fit in a quarter of a wave)
+    const int64_t max_work = max_tiles * (C::kTailSplit ? 4 : 1);
+    const int64_t grid = max_work < sms ? max_work : sms;
     if (grid <= 0) return QMOE_OK;
     return launch_pdl(moe_gemm_kernel<kBF16, kWide, BN, kMX, kI4, kAct>, dim3(static_cast<unsigned>(grid)),
-                      dim3(C::kThreads), C::kDynSmem, st, map, amap, p);
+                      dim3(C::kThreads), C::kDynSmem, st, map, amap, mapq, p);
 }
 
 // out[i] = bf16(accum[i]) for the TOKEN_SUM layout (defined in gemm_w8a8.cu).
