@@ -452,6 +452,9 @@ qmoe_status_t qmoe_debug_wait_timeout(int32_t* d_status, int64_t limit_ns, qmoe_
 /* q = x / s through the kernels' division by a row scale (correctly rounded,
  * like IEEE fp32 division), n values. */
 qmoe_status_t qmoe_debug_div_by_scale(const float* x, float s, float* q, int64_t n, qmoe_stream_t stream);
+/* y[i] = 1/d[i] with the reciprocal the SiLU uses (correctly rounded, for
+ * d >= 1): the exhaustive check of that sequence. */
+qmoe_status_t qmoe_debug_rcp_ge1(const float* d, float* y, int64_t n, qmoe_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -34,7 +34,7 @@ EXPORTED = (
     "qmoe_debug_silu_mul", "qmoe_debug_div_by_scale", "qmoe_debug_wait_timeout",
     "qmoe_moe_gemm_w8a8_token_sum_noalloc", "qmoe_quant_weight_mxfp8", "qmoe_quant_mxfp8", "qmoe_quant_mxfp8_colwise",
     "qmoe_mx_weight_sf_tiled_bytes", "qmoe_mx_weight_sf_tiled", "qmoe_quant_weight_int4", "qmoe_moe_gemm_w4a16",
-    "qmoe_moe_gemm_w8a8_silu_mxfp8", "qmoe_moe_gemm_w8a8_silu_fp8_token",
+    "qmoe_moe_gemm_w8a8_silu_mxfp8", "qmoe_moe_gemm_w8a8_silu_fp8_token", "qmoe_debug_rcp_ge1",
 )
 NOALLOC_ACCUM_MAX_ELEMS = 4 << 20
 
@@ -107,6 +107,7 @@ def load_library(path: str | None = None):
             L.qmoe_debug_int8_to_bf16.argtypes = [vp, vp, i64, vp]
             L.qmoe_debug_silu_mul.argtypes = [vp, vp, vp, i64, vp]
             L.qmoe_debug_div_by_scale.argtypes = [vp, ctypes.c_float, vp, i64, vp]
+            L.qmoe_debug_rcp_ge1.argtypes = [vp, vp, i64, vp]
             L.qmoe_debug_wait_timeout.argtypes = [vp, i64, vp]
             for name in EXPORTED:
                 if name not in ("qmoe_status_string", "qmoe_version", "qmoe_align_max_padded"):
@@ -651,6 +652,13 @@ def debug_silu_mul(g: torch.Tensor, u: torch.Tensor, stream=None) -> torch.Tenso
     _check(load_library().qmoe_debug_silu_mul(_ptr(g), _ptr(u), _ptr(h), g.numel(), _stream(stream)),
            "debug_silu_mul")
     return h
+
+
+def debug_rcp_ge1(d: torch.Tensor, stream=None) -> torch.Tensor:
+    _need(d, torch.float32, "d")
+    y = torch.empty_like(d)
+    _check(load_library().qmoe_debug_rcp_ge1(_ptr(d), _ptr(y), d.numel(), _stream(stream)), "debug_rcp_ge1")
+    return y
 
 
 def debug_div_by_scale(x: torch.Tensor, s: float, stream=None) -> torch.Tensor:

@@ -929,6 +929,11 @@ __global__ void debug_silu_kernel(const float* __restrict__ g, const float* __re
         else h[i] = silu_mul(g[i], u[i]);
     }
 }
+__global__ void debug_rcp_kernel(const float* __restrict__ d, float* __restrict__ y, int64_t n) {
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+        y[i] = rcp_rn_ge1(d[i]);
+}
 __global__ void debug_div_kernel(const float* __restrict__ x, float s, float* __restrict__ q, int64_t n) {
     const float rinv = __frcp_rn(s);
     for (int64_t i = 2 * (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x); i < n;
@@ -1228,6 +1233,13 @@ qmoe_status_t qmoe_debug_silu_mul(const float* g, const float* u, float* h, int6
 qmoe_status_t qmoe_debug_wait_timeout(int32_t* d_status, int64_t limit_ns, qmoe_stream_t stream) {
     if (!d_status || limit_ns < 0 || limit_ns > 1000000000) return QMOE_ERR_INVALID_ARG;
     debug_wait_timeout_kernel<<<1, 32, 0, stream>>>(d_status, static_cast<uint64_t>(limit_ns));
+    return launch_status();
+}
+
+qmoe_status_t qmoe_debug_rcp_ge1(const float* d, float* y, int64_t n, qmoe_stream_t stream) {
+    if (n < 0 || (n > 0 && (!d || !y))) return QMOE_ERR_INVALID_ARG;
+    if (n == 0) return QMOE_OK;
+    debug_rcp_kernel<<<grid_for(n, 256), 256, 0, stream>>>(d, y, n);
     return launch_status();
 }
 

@@ -192,6 +192,28 @@ def test_fused_align_quant_bitexact(q, orc, M, K, E, top_k, BM):
     assert np.array_equal(ss.cpu().numpy()[valid], rs[srt[valid] // top_k])
 
 
+def test_silu_reciprocal_exhaustive(q):
+    """The reciprocal in the SiLU, 1/d with d = 1 + exp(-g) >= 1, equals IEEE
+    fp32 division (numpy) bit for bit for every fp32 d in [1, 2^126), and for
+    the largest values and +inf (which take the IEEE reciprocal)."""
+    lo = int(np.float32(1.0).view(np.uint32))
+    hi = int(np.float32(2.0 ** 126).view(np.uint32))
+    chunk = 1 << 26
+    one = np.float32(1.0)
+    for start in range(lo, hi, chunk):
+        n = min(chunk, hi - start)
+        d = torch.arange(start, start + n, dtype=torch.int64, device=dev()).to(torch.int32).view(torch.float32)
+        got = q.debug_rcp_ge1(d).cpu().numpy()
+        dn = d.cpu().numpy()
+        ref = one / dn
+        bad = np.nonzero(got.view(np.uint32) != ref.view(np.uint32))[0]
+        assert bad.size == 0, (dn[bad[:4]], got[bad[:4]], ref[bad[:4]])
+    edge = np.array([2.0 ** 126, 1.5 * 2.0 ** 126, 2.0 ** 127, 3.0e38, np.finfo(np.float32).max, np.inf],
+                    dtype=np.float32)
+    got = q.debug_rcp_ge1(to_dev(edge)).cpu().numpy()
+    assert np.array_equal(got.view(np.uint32), (one / edge).view(np.uint32))
+
+
 @pytest.mark.parametrize("s", [np.float32(1.0), np.float32(1.0 / 448.0), np.float32(3.0), np.float32(0.0123456),
                                np.nextafter(np.float32(2.0), np.float32(0)), np.float32(7.0e-3) / np.float32(448.0)])
 def test_division_by_row_scale_exhaustive(q, s):
