@@ -341,6 +341,33 @@ def run_suite(reps: int = 50, only: str | None = None) -> None:
             wq[e], ws[e] = q.quant_weight_int8(w)
         return wq, ws
 
+    # FP8 decode GEMM by activation layout: token rows gathered by the GEMM's
+    # cp.async warps against rows quantised into padded sorted order
+    for wl in inputs.decode_fp8_sweep():
+        if only and only not in wl.name:
+            continue
+        if wl.M not in (64, 512):
+            continue
+        wq8, ws8 = weights_fp8(E, wl.N, wl.K)
+        a = torch.from_numpy(inputs.activations_bf16(wl.M, wl.K, wl.seed).view(np.int16)).to(dev).view(torch.bfloat16)
+        ids, tw = inputs.routing(wl.M, E, TOP_K, wl.seed)
+        BM = 32 if wl.M <= 64 else 128
+        al = q.moe_align_block_size(torch.from_numpy(ids).to(dev), E, BM)
+        twd = torch.from_numpy(tw).to(dev)
+        out = torch.empty(wl.M * TOP_K, wl.N, dtype=torch.bfloat16, device=dev)
+        hit = len(np.unique(ids))
+        nbytes = hit * wl.N * wl.K + hit * wl.N * 4 + wl.M * (wl.K + 4) + wl.M * TOP_K * (8 + 2 * wl.N)
+        aq, sa = q.quant_act_fp8(a)
+        ms = _timed(lambda: q.moe_gemm_w8a8(aq, sa, wq8, ws8, al, twd, M=wl.M, top_k=TOP_K, BM=BM, out=out), reps,
+                    flush)
+        line(wl.name, f"moe_gemm_w8a8 BM={BM} token-gather A", ms, nbytes,
+             2.0 * wl.M * TOP_K * wl.K * wl.N, "fp8")
+        aqp, sap = q.quant_act_fp8_sorted(a, al, TOP_K)
+        ms = _timed(lambda: q.moe_gemm_w8a8(aqp, sap, wq8, ws8, al, twd, M=wl.M, top_k=TOP_K, BM=BM,
+                                            a_layout=q.A_PADDED, out=out), reps, flush)
+        line(wl.name, f"moe_gemm_w8a8 BM={BM} padded A", ms, nbytes, 2.0 * wl.M * TOP_K * wl.K * wl.N, "fp8")
+        del wq8, ws8
+
     # INT8 W8A16 sweep
     for wl in inputs.int8_w8a16_sweep():
         if only and only not in wl.name:

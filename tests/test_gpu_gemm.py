@@ -514,3 +514,20 @@ def test_gemms_with_no_tokens(q, orc):
     fq, fsf = q.moe_gemm_w8a8_silu_mxfp8(aq, sa, wq, ws, al, M=0, top_k=top_k)
     torch.cuda.synchronize()
     assert hq.numel() == 0 and hs.numel() == 0 and fq.numel() == 0
+
+
+@pytest.mark.parametrize("BM", [16, 128])
+def test_w8a8_token_gather_single_token_deep_k(q, orc, BM):
+    """One token (M=1, top_k=2) over several k-blocks with token-gathered
+    activation rows: every gathered row is row 0."""
+    M, K, N, E, top_k = 1, 512, 256, 4, 2
+    p = fp8_problem(q, orc, M, K, N, E, top_k, seed=21)
+    al = q.moe_align_block_size(to_dev(p["ids"]), E, BM)
+    st = status()
+    out = q.moe_gemm_w8a8(p["aq"], p["sa"], p["wq"], p["ws"], al, to_dev(p["tw"]), M=M, top_k=top_k, BM=BM,
+                          d_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    ref = orc.moe_gemm(a_kind=orc.A_FP8_TOKEN, a=p["raq"], a_scale=p["rsa"], w_kind=orc.W_FP8, w=p["rwq"],
+                       w_scale=p["rws"], topk_ids=p["ids"], topk_w=p["tw"], E=E)
+    check(bf16_to_np_f32(out), ref)
