@@ -535,7 +535,7 @@ __global__ void __launch_bounds__(GemmCfg<kBF16, kWide, BN, kMX, kI4, kAct>::kTh
         for (int tile = blockIdx.x; ok && tile < num_work; tile += gridDim.x) {
             int sb, nb;
             int qt;
-                const int e = work_tile(tile, sb, nb, qt);
+            const int e = work_tile(tile, sb, nb, qt);
             if (e < 0) continue;
             const int cnt = p.expert_offsets[e + 1] - p.expert_offsets[e];
             const uint8_t* sfrow[4];
@@ -606,7 +606,7 @@ __global__ void __launch_bounds__(GemmCfg<kBF16, kWide, BN, kMX, kI4, kAct>::kTh
             if (*abort) break;
             int sb, nb;
             int qt;
-                const int e = work_tile(tile, sb, nb, qt);
+            const int e = work_tile(tile, sb, nb, qt);
             if (e < 0) continue;
             named_bar_sync(1, C::kBProdThreads);
             for (int j = pt; j < SR; j += C::kBProdThreads) {
@@ -654,7 +654,7 @@ __global__ void __launch_bounds__(GemmCfg<kBF16, kWide, BN, kMX, kI4, kAct>::kTh
             if (*abort) break;
             int sb, nb;
             int qt;
-                const int e = work_tile(tile, sb, nb, qt);
+            const int e = work_tile(tile, sb, nb, qt);
             if (e < 0) continue;
             const int acc = tcount % C::kAccBufs;
             const uint32_t aph = (tcount / C::kAccBufs) & 1;
