@@ -123,7 +123,10 @@ struct GemmCfg {
     // cp.async completion lag (stages): the MMA can run kStages - kLag - 1 stages
     // ahead of the gather warps, so the lag shrinks when the ring is short.
     static constexpr int kLag = kStages >= 6 ? 3 : (kStages >= 5 ? 2 : 1);
-    static constexpr int kBProdThreads = 64;
+    // TOKEN_GATHER activation gather: warps 2-3, and for FP8 two more warps
+    // after the epilogue warps (the last two of the block)
+    static constexpr int kExtraGather = (!kBF16 && !kMX) ? 64 : 0;
+    static constexpr int kBProdThreads = 64 + kExtraGather;
     // MX: two groups of four warps, one per column half; kW2: one per slot
     // half; kAct (SwiGLU epilogues): one per half of the tile's 128 h columns
     static constexpr int kEpiThreads = (kMX || kW2 || kAct != 0) ? 256 : 128;
@@ -136,7 +139,9 @@ struct GemmCfg {
     // stage), 4 for the swapped one; groups alternate stages
     static constexpr int kConvThreads = (kBF16 && kWide) ? 256 : 128;
     static constexpr int kConvGroups = kBF16 ? 2 : 1;       // converter groups alternate stages
-    static constexpr int kThreads = kBF16 ? 256 + 2 * kConvThreads : ((kMX || kW2 || kAct != 0) ? 384 : 256);
+    static constexpr int kThreads =
+        kBF16 ? 256 + 2 * kConvThreads : ((kMX || kW2 || kAct != 0) ? 384 : 256) + kExtraGather;
+    static constexpr int kFirstExtraGatherWarp = (kThreads - kExtraGather) / 32;
     static constexpr int kAccCols = kMmaN;                  // TMEM columns per accumulator
     // MX: one accumulator (256 columns), then four scale columns per stage for
     // the 128 activation rows (4-column aligned) and 8 columns of constant
@@ -597,9 +602,9 @@ __global__ void __launch_bounds__(GemmCfg<kBF16, kWide, BN, kMX, kI4, kAct>::kTh
                 while (global_timer_ns() - t0 < 2000000ull) {}
             }
         }
-    } else if (warp < 4) {
+    } else if (warp < 4 || (C::kExtraGather > 0 && warp >= C::kFirstExtraGatherWarp)) {
         // ------------------------------- activation gather (TOKEN_GATHER) ---
-        const int pt = threadIdx.x - 64;
+        const int pt = warp < 4 ? threadIdx.x - 64 : 64 + threadIdx.x - 32 * C::kFirstExtraGatherWarp;
         int it = 0;
         bool ok = !p.a_tma;
         for (int tile = blockIdx.x; ok && tile < num_work; tile += gridDim.x) {
