@@ -59,8 +59,8 @@ typedef enum {
 #define QMOE_SCALE_PER_ROW 0   /* weights: one fp32 scale per output channel */
 /* A row layouts.  GROUPED and PADDED rows reach the GEMM as TMA boxes and are
  * the fast layouts; TOKEN_GATHER rows are gathered by cp.async warps inside the
- * GEMM (measured on the FP8 decode shape: 1.05x the padded time at M=64,
- * 1.7x at M=512 with BM=128). */
+ * GEMM (measured on the FP8 decode shape: 1.02x the padded time at M=64,
+ * 1.3x at M=512 with BM=128). */
 #define QMOE_A_TOKEN_GATHER 0 /* slot s reads A row s / top_k ([M, K])        */
 #define QMOE_A_GROUPED 1      /* slot s reads its compact expert-grouped row ([T, K]) */
 #define QMOE_A_PADDED 2       /* slot at padded sorted position p reads row p
