@@ -123,9 +123,9 @@ struct GemmCfg {
     // cp.async completion lag (stages): the MMA can run kStages - kLag - 1 stages
     // ahead of the gather warps, so the lag shrinks when the ring is short.
     static constexpr int kLag = kStages >= 6 ? 3 : (kStages >= 5 ? 2 : 1);
-    // TOKEN_GATHER activation gather: warps 2-3, and for FP8 two more warps
-    // after the epilogue warps (the last two of the block)
-    static constexpr int kExtraGather = (!kBF16 && !kMX) ? 64 : 0;
+    // TOKEN_GATHER activation gather: warps 2-3, and two more warps after all
+    // the others (the last two of the block); MX tiles never gather
+    static constexpr int kExtraGather = !kMX ? 64 : 0;
     static constexpr int kBProdThreads = 64 + kExtraGather;
     // MX: two groups of four warps, one per column half; kW2: one per slot
     // half; kAct (SwiGLU epilogues): one per half of the tile's 128 h columns
@@ -140,7 +140,7 @@ struct GemmCfg {
     static constexpr int kConvThreads = (kBF16 && kWide) ? 256 : 128;
     static constexpr int kConvGroups = kBF16 ? 2 : 1;       // converter groups alternate stages
     static constexpr int kThreads =
-        kBF16 ? 256 + 2 * kConvThreads : ((kMX || kW2 || kAct != 0) ? 384 : 256) + kExtraGather;
+        (kBF16 ? 256 + 2 * kConvThreads : ((kMX || kW2 || kAct != 0) ? 384 : 256)) + kExtraGather;
     static constexpr int kFirstExtraGatherWarp = (kThreads - kExtraGather) / 32;
     static constexpr int kAccCols = kMmaN;                  // TMEM columns per accumulator
     // MX: one accumulator (256 columns), then four scale columns per stage for
