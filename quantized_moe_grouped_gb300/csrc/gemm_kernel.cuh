@@ -123,9 +123,9 @@ struct GemmCfg {
     // cp.async completion lag (stages): the MMA can run kStages - kLag - 1 stages
     // ahead of the gather warps, so the lag shrinks when the ring is short.
     static constexpr int kLag = kStages >= 6 ? 3 : (kStages >= 5 ? 2 : 1);
-    // TOKEN_GATHER activation gather: warps 2-3, and two more warps after all
-    // the others (the last two of the block); MX tiles never gather
-    static constexpr int kExtraGather = !kMX ? 64 : 0;
+    // TOKEN_GATHER activation gather: warps 2-3, and more warps after all the
+    // others (the last two of the block, four for W8A16); MX tiles never gather
+    static constexpr int kExtraGather = kMX ? 0 : (kBF16 ? 128 : 64);
     static constexpr int kBProdThreads = 64 + kExtraGather;
     // MX: two groups of four warps, one per column half; kW2: one per slot
     // half; kAct (SwiGLU epilogues): one per half of the tile's 128 h columns
