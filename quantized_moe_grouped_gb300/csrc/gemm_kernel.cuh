@@ -1144,7 +1144,7 @@ inline qmoe_status_t run_moe_gemm(const qmoe_gemm_args* a, cudaStream_t st, cons
         if (cudaMemsetAsync(a->accum, 0, static_cast<size_t>(a->M * a->N) * sizeof(float), st) != cudaSuccess)
             return QMOE_ERR_CUDA;
     }
-    GemmParams p;
+    GemmParams p{};  // every field set below; value-initialised so that none can be left undefined
     p.a = static_cast<const uint8_t*>(a->a);
     p.lda_bytes = a->lda * elem;
     p.a_row_bytes = a->K * elem;
