@@ -42,11 +42,39 @@ def test_silu_sequence_bitexact(q, orc):
     gs = np.concatenate([
         (g.random(1 << 22, dtype=np.float32) * 220 - 110),
         g.standard_normal(1 << 21).astype(np.float32) * 3,
-        np.array([0.0, -0.0, 89.0, -89.0, 104.0, -104.0, 1e-30, -1e-30, 3e38, -3e38], np.float32)])
+        np.array([0.0, -0.0, 89.0, -89.0, 104.0, -104.0, 1e-30, -1e-30, 3e38, -3e38], np.float32),
+        # -g * log2 e rounds to a half-integer (41.5, 45.5, 53.5, 67.5): n = rint of the
+        # rounded product, not of the exact one
+        np.array([3253084151, 3254537786, 3256112480, 3258656341], np.uint32).view(np.float32)])
     us = g.standard_normal(gs.size).astype(np.float32)
     got = q.debug_silu_mul(to_dev(gs), to_dev(us)).cpu().numpy()
     ref = orc.silu_mul_f32_array(gs, us)
     assert np.array_equal(got.view(np.uint32), ref.view(np.uint32))
+
+
+def test_silu_sequence_exhaustive(q, orc):
+    """h = silu(g) * u on the GPU equals the oracle's op sequence bit for bit
+    for every fp32 g in [-104, 89] (the range the exp reduction does not
+    clamp; both signs of zero included), each g paired with a multiplier u in
+    [1, 2) whose mantissa is taken from g's bit pattern (so the final product
+    rounds too)."""
+    chunk = 1 << 26
+    spans = [(0, int(np.float32(89.0).view(np.uint32)) + 1),
+             (0x80000000, int(np.float32(-104.0).view(np.uint32)) + 1)]
+    for lo, hi in spans:
+        for start in range(lo, hi, chunk):
+            n = min(chunk, hi - start)
+            b = torch.arange(start, start + n, dtype=torch.int64, device=dev())
+            ub = 0x3F800000 | ((b ^ (b >> 9)) & 0x7FFFFF)
+            g = torch.where(b >= (1 << 31), b - (1 << 32), b).to(torch.int32).view(torch.float32)
+            u = ub.to(torch.int32).view(torch.float32)
+            got = q.debug_silu_mul(g, u).cpu().numpy().view(np.uint32)
+            del b, ub, g, u
+            bits = np.arange(start, start + n, dtype=np.uint64).astype(np.uint32)
+            un = (np.uint32(0x3F800000) | ((bits ^ (bits >> np.uint32(9))) & np.uint32(0x7FFFFF))).view(np.float32)
+            ref = orc.silu_mul_f32_array(bits.view(np.float32), un).view(np.uint32)
+            bad = np.nonzero(got != ref)[0]
+            assert bad.size == 0, (hex(start), bits[bad[:4]], got[bad[:4]], ref[bad[:4]])
 
 
 @pytest.mark.parametrize("M,E,BM", [(64, 8, 16), (64, 8, 32), (200, 8, 64), (4096, 8, 128), (4096, 8, 256),

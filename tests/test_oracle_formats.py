@@ -121,6 +121,23 @@ def test_exp_within_2ulp_of_fp64(orc):
     assert worst <= 2.0, worst
 
 
+def test_exp_faithful_exhaustive(orc):
+    """Every fp32 x in [-87, 88] (about 2.2e9 values, exp(x) a normal fp32):
+    the oracle's exp is within one ulp of fp64 exp, i.e. faithfully rounded."""
+    import multiprocessing as mp
+    import os
+
+    from tests.exhaustive_util import exp_chunk_worst_ulp
+    spans = [(0, int(np.float32(88.0).view(np.uint32)) + 1),
+             (0x80000000, int(np.float32(-87.0).view(np.uint32)) + 1)]
+    ch = 1 << 22
+    jobs = [(s, min(s + ch, hi)) for lo, hi in spans for s in range(lo, hi, ch)]
+    with mp.get_context("spawn").Pool(min(8, os.cpu_count() or 1)) as pool:
+        res = pool.map(exp_chunk_worst_ulp, jobs, chunksize=8)
+    worst, at = max(res)
+    assert worst < 1.0, (worst, at)
+
+
 def test_exp_special_values(orc):
     assert orc.exp_f32([0.0])[0] == 1.0
     assert np.isinf(orc.exp_f32([89.0])[0]) and np.isinf(orc.exp_f32([1000.0])[0])
