@@ -32,6 +32,37 @@ def test_quant_weight_mxfp8_bitexact(q, orc, E, N, K):
     assert np.array_equal(sf.cpu().numpy(), rsf)
 
 
+def test_quant_weight_mxfp8_block_exponent_edges(q, orc):
+    """The E8M0 block exponent at its edges, codes and factors bit-exact: block
+    maxima m * 2^x in every fp32 binade x = -126..127 with m = 1, the mantissas
+    either side of 1.75 (448 = 1.75 * 2^8, where the exponent steps), 1.75
+    itself, the largest mantissa and a random one; subnormal maxima (exponent
+    clamped to -127) and the largest finite value.  Each maximum sits at a
+    random position of its 32-block with a random sign and 31 smaller values."""
+    rng = np.random.default_rng(17)
+    f = np.float32
+    ms = [f(1.0), np.nextafter(f(1.75), f(0)), f(1.75), np.nextafter(f(1.75), f(2)), np.nextafter(f(2.0), f(0))]
+    amax = [np.ldexp(m, x).astype(np.float32) for x in range(-126, 128) for m in ms + [f(1 + rng.random())]]
+    amax += [np.float32(v) for v in (np.array([1, 2, 3, 7, 1 << 20, (1 << 23) - 1], np.uint32).view(np.float32))]
+    amax += [np.finfo(np.float32).max]
+    amax = np.array(amax, dtype=np.float32)
+    assert np.all(np.isfinite(amax)) and np.all(amax > 0)
+    blocks = (rng.random((amax.size, 32)).astype(np.float32) * amax[:, None]).astype(np.float32)
+    blocks *= np.where(rng.random(blocks.shape) < 0.5, f(-1), f(1))
+    pos = rng.integers(0, 32, amax.size)
+    blocks[np.arange(amax.size), pos] = amax * np.where(rng.random(amax.size) < 0.5, f(-1), f(1))
+    per_row = 32
+    rows = -(-amax.size // per_row)
+    w = np.zeros((rows * per_row, 32), dtype=np.float32)
+    w[:amax.size] = blocks
+    w = w.reshape(rows, per_row * 32)
+    qq, sf = q.quant_weight_mxfp8(to_dev(w))
+    torch.cuda.synchronize()
+    rq, rsf = orc.quant_rows_mxfp8_f32(w)
+    assert np.array_equal(sf.cpu().numpy(), rsf)
+    assert np.array_equal(qq.cpu().numpy(), rq)
+
+
 @pytest.mark.parametrize("cnt,I", [([5, 0, 130, 1], 96), ([4000] * 8, 4096 // 8), ([64, 64], 128)])
 def test_quant_mxfp8_rows_bitexact(q, orc, cnt, I):
     R = sum(cnt)
