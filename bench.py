@@ -247,9 +247,33 @@ class OracleBench:
         return self.sweep_bytes / t_sweep / 1e9, t_sweep, sample
 
 
+def dist_env() -> tuple[int, int, int]:
+    """(world size, rank, local rank) from torchrun's environment; (1, 0, 0) without it."""
+    return (int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    """The largest x over all ranks (the job's time is its slowest rank's);
+    x itself on one rank.  Every rank must call it."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank: float, seconds: float, world: int) -> float:
+    """Units per second of the whole job: every rank processes units_per_rank
+    (weak scaling) in at most `seconds` (the max over ranks)."""
+    return world * units_per_rank / seconds
+
+
 def run_reference(args) -> None:
-    rank = int(os.environ.get("RANK", "0"))
-    if rank != 0:
+    _, rank, _ = dist_env()
+    if rank != 0:  # the oracle runs on rank 0 alone; the other ranks exit without work
         return
     steps, warmup = args.steps, args.warmup
     per_step = min(6.0, 120.0 / max(1, steps + warmup))  # one slot batch at least
@@ -580,9 +604,7 @@ def main() -> None:
     import torch
     import torch.distributed as dist
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
+    world, rank, local = dist_env()
     if world > 1:
         torch.cuda.set_device(local)
         dist.init_process_group("nccl")
@@ -631,10 +653,7 @@ def main() -> None:
     ms = t0.elapsed_time(t1)
     gemm_ms = [sum(evs[s][i][0].elapsed_time(evs[s][i][1]) for s in range(args.steps)) / args.steps
                for i in range(n_sh)]
-    if world > 1:
-        tt = torch.tensor([ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
+    ms = max_over_ranks(ms, world, dev)
 
     # end-to-end through the public API with pinned host buffers
     h2d = sum(sh["a_h"].numel() * 2 + sh["ids_h"].numel() * 4 + sh["tw_h"].numel() * 4 for sh in shapes)
@@ -681,16 +700,13 @@ def main() -> None:
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
-    if world > 1:
-        tt = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_ms = float(tt.item())
+    e2e_ms = max_over_ranks(e2e_ms, world, dev)
 
     step_bytes = sum(sh["bytes"] for sh in shapes)
     step_flops = sum(sh["flops"] for sh in shapes)
     ms_step = ms / args.steps
-    value = world * step_bytes / (ms_step * 1e-3) / 1e9
-    tflops = world * step_flops / (ms_step * 1e-3) / 1e12
+    value = whole_job_rate(step_bytes, ms_step * 1e-3, world) / 1e9
+    tflops = whole_job_rate(step_flops, ms_step * 1e-3, world) / 1e12
     peak, peak_kind = measured_peaks()
     gemm_total_ms = sum(gemm_ms)
     achieved = step_bytes / (gemm_total_ms * 1e-3) / 1e9
@@ -720,7 +736,7 @@ def main() -> None:
             "sweep": sweep,
             "vs_baseline_note": f"page aggregate over the same sweep: {page_gbs:.0f} GB/s, {page_tflops:.0f} TFLOPS "
                                 "(ROCm GPU, unnamed)",
-            "e2e": {"value": world * step_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+            "e2e": {"value": whole_job_rate(step_bytes, e2e_ms * 1e-3, world) / 1e9, "unit": "GB/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": 2 * n_sh * args.steps,
             "clocks": clk,
