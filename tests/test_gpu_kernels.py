@@ -243,7 +243,10 @@ def test_silu_reciprocal_exhaustive(q):
 
 
 @pytest.mark.parametrize("s", [np.float32(1.0), np.float32(1.0 / 448.0), np.float32(3.0), np.float32(0.0123456),
-                               np.nextafter(np.float32(2.0), np.float32(0)), np.float32(7.0e-3) / np.float32(448.0)])
+                               np.nextafter(np.float32(2.0), np.float32(0)), np.float32(7.0e-3) / np.float32(448.0),
+                               # a huge scale (Markstein path from |x| >= 2^-99 s > 1) and a subnormal
+                               # one (every dividend below the threshold: IEEE path throughout)
+                               np.float32(1.37 * 2.0 ** 100), np.float32(1.5 * 2.0 ** -130)])
 def test_division_by_row_scale_exhaustive(q, s):
     """The kernels' division by a row scale s equals IEEE fp32 division (numpy)
     bit for bit for every fp32 dividend the kernels can pass, |x| <= 512 s
