@@ -62,3 +62,75 @@ def test_host_validation_rejects_before_launch(lib):
     assert lib.qmoe_silu_mul_quant(vp(16), 4, 12, 24, 0, vp(16), vp(16), None, 0, None, None, 1, None, None) == 1
     # nothing to do is fine
     assert lib.qmoe_quant_act_fp8(None, 0, 64, 64, None, None, None) == 0
+
+
+# Calls that each break one documented rule (the same calls with that one field
+# valid pass every host check); every one must come back with the listed status
+# from the host checks, before any CUDA call, so they are safe with or without
+# a GPU.
+_P = 1 << 20          # a 16-byte-aligned dummy address (never dereferenced on the host)
+_U = (1 << 20) + 8    # 8-byte aligned only
+
+
+def _gemm_args(q, **kw):
+    a = q.GemmArgs()
+    a.struct_size = ctypes.sizeof(q.GemmArgs)
+    base = dict(a=_P, lda=256, a_scale=_P, a_scale_mode=0, a_layout=0, w=_P, w_scale=_P, sorted_ids=_P,
+                expert_ids=_P, num_post_padded=_P, expert_offsets=_P, padded_offsets=_P, topk_weights=None,
+                out=_P, out_layout=0, M=4, N=256, K=256, E=8, top_k=2, BM=128, d_status=None, accum=None,
+                w_scale_mode=0, w_sf=None)
+    base.update(kw)
+    for k, v in base.items():
+        setattr(a, k, v)
+    return ctypes.byref(a)
+
+
+_CASES = {
+    "w8a8: weights not 16-byte aligned": (1, lambda L, q: L.qmoe_moe_gemm_w8a8(_gemm_args(q, w=_U), None)),
+    "w8a8: no sorted_ids": (1, lambda L, q: L.qmoe_moe_gemm_w8a8(_gemm_args(q, sorted_ids=None), None)),
+    "w8a8: top_k > E": (1, lambda L, q: L.qmoe_moe_gemm_w8a8(_gemm_args(q, top_k=9), None)),
+    "w8a8: E > 256": (1, lambda L, q: L.qmoe_moe_gemm_w8a8(_gemm_args(q, E=257), None)),
+    "w8a8: unknown out layout": (1, lambda L, q: L.qmoe_moe_gemm_w8a8(_gemm_args(q, out_layout=7), None)),
+    "w8a8: token sum without accum": (1, lambda L, q: L.qmoe_moe_gemm_w8a8(_gemm_args(q, out_layout=2), None)),
+    "w8a16: MX activation scales": (2, lambda L, q: L.qmoe_moe_gemm_w8a16(
+        _gemm_args(q, a_scale=None, a_scale_mode=1), None)),
+    "w8a16: lda < K": (1, lambda L, q: L.qmoe_moe_gemm_w8a16(_gemm_args(q, a_scale=None, lda=128), None)),
+    "w8a16: activations not 16-byte aligned": (1, lambda L, q: L.qmoe_moe_gemm_w8a16(
+        _gemm_args(q, a_scale=None, a=_U), None)),
+    "w4a16: BM below 128": (2, lambda L, q: L.qmoe_moe_gemm_w4a16(_gemm_args(q, a_scale=None, BM=64), None)),
+    "w4a16: K not a multiple of 128": (1, lambda L, q: L.qmoe_moe_gemm_w4a16(
+        _gemm_args(q, a_scale=None, K=192, lda=192), None)),
+    "fused per-token SwiGLU: K % 16 != 0": (1, lambda L, q: L.qmoe_moe_gemm_w8a8_silu_fp8_token(
+        _gemm_args(q, K=40, lda=48, out=None, out_layout=1), ctypes.c_void_p(_P), ctypes.c_void_p(_P),
+        ctypes.c_void_p(_P), None)),
+    "fused per-token SwiGLU: slot output layout": (1, lambda L, q: L.qmoe_moe_gemm_w8a8_silu_fp8_token(
+        _gemm_args(q, out=None, out_layout=0), ctypes.c_void_p(_P), ctypes.c_void_p(_P), ctypes.c_void_p(_P),
+        None)),
+    "fused MX SwiGLU: gate|up width not a multiple of 256": (1, lambda L, q: L.qmoe_moe_gemm_w8a8_silu_mxfp8(
+        _gemm_args(q, N=272, out=None, out_layout=1), ctypes.c_void_p(_P), ctypes.c_void_p(_P), 16,
+        ctypes.c_void_p(_P), None)),
+    "router: top_k > E": (1, lambda L, q: L.qmoe_moe_router_topk(_P, 4, 8, 9, _P, _P, None)),
+    "router: no experts": (1, lambda L, q: L.qmoe_moe_router_topk(_P, 4, 0, 1, _P, _P, None)),
+    "align: BM above 1024": (1, lambda L, q: L.qmoe_moe_align_block_size(_P, 8, 8, 2048, _P, _P, _P, _P, _P,
+                                                                          None, None)),
+    "int4 weights: K not a multiple of 128": (1, lambda L, q: L.qmoe_quant_weight_int4(_P, 4, 192, _P, _P, None)),
+    "int8 weights: no columns": (1, lambda L, q: L.qmoe_quant_weight_int8(_P, 4, 0, _P, _P, None)),
+    "MXFP8 weights: K not a multiple of 32": (1, lambda L, q: L.qmoe_quant_weight_mxfp8(_P, 4, 48, _P, _P, 4,
+                                                                                       None)),
+    "MXFP8 rows: width not a multiple of 32": (1, lambda L, q: L.qmoe_quant_mxfp8(
+        _P, 4, 48, 48, _P, _P, 4, _P, _P, 1, None, None)),
+    "gather_sorted_bf16: lda < K": (1, lambda L, q: L.qmoe_gather_sorted_bf16(_P, 4, 256, 128, _P, _P, 2, 256,
+                                                                              _P, None)),
+    "quant_act_fp8: ldx < cols": (1, lambda L, q: L.qmoe_quant_act_fp8(_P, 4, 256, 128, _P, _P, None)),
+    "silu_mul_quant: unknown mode": (1, lambda L, q: L.qmoe_silu_mul_quant(_P, 4, 64, 128, 5, _P, _P, None, 0,
+                                                                           None, None, 1, None, None)),
+    "srelu_quant: unknown mode": (1, lambda L, q: L.qmoe_srelu_quant(_P, 4, 64, 64, 5, _P, _P, None, 0, None,
+                                                                     None, 1, None, None)),
+}
+
+
+@pytest.mark.parametrize("case", sorted(_CASES))
+def test_host_validation_table(lib, case):
+    import quantized_moe_grouped_gb300 as q
+    want, call = _CASES[case]
+    assert call(lib, q) == want
