@@ -17,3 +17,25 @@ def exp_chunk_worst_ulp(span):
     d = np.abs(y - ref) * inv_ulp
     i = int(np.argmax(d))
     return float(d[i]), float(x[i])
+
+
+def e4m3_chunk_mismatches(span):
+    """Over the fp32 bit patterns [lo, hi) (NaNs skipped): the patterns where
+    the oracle's e4m3 code differs from torch's float8_e4m3fn cast (where the
+    cast is finite), or where the cast overflows to NaN and the oracle does not
+    give the saturated +-448 (0x7E / 0xFE) or |x| is below 464.  At most 4."""
+    import oracle
+    import torch
+    torch.set_num_threads(1)
+    lo, hi = span
+    bits = np.arange(lo, hi, dtype=np.uint32)
+    x = bits.view(np.float32)
+    keep = ~np.isnan(x)
+    bits, x = bits[keep], x[keep]
+    o = oracle.e4m3_from_f32_array(x)
+    t = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    fin = (t & 0x7F) != 0x7F
+    bad = fin & (o != t)
+    sat = np.where(x < 0, 0xFE, 0x7E).astype(np.uint8)
+    bad |= ~fin & ((o != sat) | (np.abs(x) < 464.0))
+    return [int(b) for b in bits[bad][:4]]

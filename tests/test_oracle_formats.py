@@ -121,6 +121,22 @@ def test_exp_within_2ulp_of_fp64(orc):
     assert worst <= 2.0, worst
 
 
+def test_e4m3_encode_exhaustive_vs_torch(orc):
+    """Every non-NaN fp32: the oracle's e4m3 code equals torch's float8_e4m3fn
+    cast wherever that cast is finite.  Where torch overflows to NaN (|x| past
+    the rounding midpoint between 448 and the NaN encoding, and infinities),
+    the oracle saturates to +-448 (0x7E / 0xFE), as satfinite prescribes."""
+    import multiprocessing as mp
+    import os
+
+    from tests.exhaustive_util import e4m3_chunk_mismatches
+    ch = 1 << 24
+    jobs = [(s, s + ch) for s in range(0, 1 << 32, ch)]
+    with mp.get_context("spawn").Pool(min(8, os.cpu_count() or 1)) as pool:
+        bad = [b for r in pool.map(e4m3_chunk_mismatches, jobs, chunksize=4) for b in r]
+    assert not bad, [hex(b) for b in bad[:8]]
+
+
 def test_exp_faithful_exhaustive(orc):
     """Every fp32 x in [-87, 88] (about 2.2e9 values, exp(x) a normal fp32):
     the oracle's exp is within one ulp of fp64 exp, i.e. faithfully rounded."""
