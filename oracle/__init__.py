@@ -76,6 +76,7 @@ def lib():
             L.orc_e8m0_to_f64.restype = ctypes.c_double
             L.orc_mx_scale_exponent.argtypes = [ctypes.c_float]
             L.orc_mx_scale_exponent.restype = ctypes.c_int
+            L.orc_mx_scale_exponent_array.argtypes = [vp, i64, vp]
             L.orc_exp_f32.argtypes = [ctypes.c_float]
             L.orc_exp_f32.restype = ctypes.c_float
             L.orc_silu_mul_f32.argtypes = [ctypes.c_float, ctypes.c_float]
@@ -166,6 +167,13 @@ def e8m0_to_f64(b) -> np.ndarray:
 
 def mx_scale_exponent(a: float) -> int:
     return int(lib().orc_mx_scale_exponent(float(a)))
+
+
+def mx_scale_exponent_array(a: np.ndarray) -> np.ndarray:
+    a = np.ascontiguousarray(a, dtype=np.float32)
+    e = np.empty(a.shape, dtype=np.int32)
+    lib().orc_mx_scale_exponent_array(_p(a), a.size, _p(e))
+    return e
 
 
 def exp_f32(x) -> np.ndarray:

@@ -134,6 +134,11 @@ int orc_mx_scale_exponent(float a) {
     return e;
 }
 
+/* orc_mx_scale_exponent over an array (marshalling only). */
+void orc_mx_scale_exponent_array(const float* a, int64_t n, int32_t* e) {
+    for (int64_t i = 0; i < n; ++i) e[i] = orc_mx_scale_exponent(a[i]);
+}
+
 /* ------------------------------------------------------------------------- */
 /* moe_align_block_size: sort token-slots by expert, pad each expert's group */
 /* to a multiple of the tile size BM.                                        */

@@ -39,3 +39,25 @@ def e4m3_chunk_mismatches(span):
     sat = np.where(x < 0, 0xFE, 0x7E).astype(np.uint8)
     bad |= ~fin & ((o != sat) | (np.abs(x) < 464.0))
     return [int(b) for b in bits[bad][:4]]
+
+
+def mx_exponent_chunk_mismatches(span):
+    """Over the fp32 bit patterns [lo, hi) of non-negative finite values: the
+    patterns where the oracle's MX block exponent differs from the smallest
+    integer e with 448 * 2^e >= a (exact float64 comparisons against
+    ldexp(448, e)), clamped to [-127, 127], and 0 for a = 0.  At most 4."""
+    import oracle
+    lo, hi = span
+    bits = np.arange(lo, hi, dtype=np.uint32)
+    a = bits.view(np.float32)
+    got = oracle.mx_scale_exponent_array(a)
+    a64 = a.astype(np.float64)
+    pos = a64 > 0
+    est = np.zeros(a.shape, dtype=np.int32)
+    est[pos] = np.ceil(np.log2(a64[pos]) - np.log2(448.0)).astype(np.int32)
+    for _ in range(2):  # the estimate is within one of the answer; settle it exactly
+        est[pos & (np.ldexp(448.0, est) < a64)] += 1
+        est[pos & (np.ldexp(448.0, est - 1) >= a64)] -= 1
+    ref = np.clip(est, -127, 127)
+    ref[~pos] = 0
+    return [int(b) for b in bits[got != ref][:4]]

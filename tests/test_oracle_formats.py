@@ -109,6 +109,22 @@ def test_mx_scale_exponent_vs_search(orc):
         assert orc.mx_scale_exponent(float(np.float32(a))) == _mx_exp_bruteforce(np.float32(a)), a
 
 
+def test_mx_scale_exponent_exhaustive(orc):
+    """Every non-negative finite fp32 a (about 2.1e9 values): the oracle's MX
+    block exponent is the smallest integer e with 448 * 2^e >= a, clamped to
+    [-127, 127], and 0 for a = 0 -- settled by exact comparisons in float64."""
+    import multiprocessing as mp
+    import os
+
+    from tests.exhaustive_util import mx_exponent_chunk_mismatches
+    ch = 1 << 24
+    end = 0x7F800000  # +inf
+    jobs = [(s, min(s + ch, end)) for s in range(0, end, ch)]
+    with mp.get_context("spawn").Pool(min(8, os.cpu_count() or 1)) as pool:
+        bad = [b for r in pool.map(mx_exponent_chunk_mismatches, jobs, chunksize=4) for b in r]
+    assert not bad, [hex(b) for b in bad[:8]]
+
+
 def test_exp_within_2ulp_of_fp64(orc):
     g = np.random.default_rng(9)
     xs = np.concatenate([np.linspace(-87.0, 88.0, 20001), g.uniform(-87, 88, 20000),
