@@ -61,3 +61,24 @@ def mx_exponent_chunk_mismatches(span):
     ref = np.clip(est, -127, 127)
     ref[~pos] = 0
     return [int(b) for b in bits[got != ref][:4]]
+
+
+def silu_chunk_worst(span):
+    """Over the fp32 bit patterns [lo, hi) of g: the largest error of the
+    oracle's silu(g) (u = 1) against fp64 g / (1 + exp(-g)), in ulps of the
+    fp64 value's binade where that value is a normal fp32, and in units of
+    2^-149 where it is subnormal; each with the g where it occurs."""
+    import oracle
+    lo, hi = span
+    x = np.arange(lo, hi, dtype=np.uint32).view(np.float32)
+    h = oracle.silu_mul_f32_array(x, np.ones_like(x)).astype(np.float64)
+    g = x.astype(np.float64)
+    ref = g / (1.0 + np.exp(-g))
+    normal = np.abs(ref) >= 2.0 ** -126
+    e = (ref.view(np.uint64) >> np.uint64(52)) & np.uint64(0x7FF)
+    inv_ulp = ((np.uint64(2046 + 23) - e) << np.uint64(52)).view(np.float64)
+    d = np.abs(h - ref)
+    dn = np.where(normal, d * inv_ulp, 0.0)
+    ds = np.where(normal, 0.0, d * 2.0 ** 149)
+    i, j = int(np.argmax(dn)), int(np.argmax(ds))
+    return (float(dn[i]), float(x[i])), (float(ds[j]), float(x[j]))

@@ -170,6 +170,31 @@ def test_exp_faithful_exhaustive(orc):
     assert worst < 1.0, (worst, at)
 
 
+def test_silu_accuracy_exhaustive(orc):
+    """Every fp32 g in [-87.3, 89], where sigma = 1/(1 + exp(-g)) is a normal
+    fp32: the oracle's silu(g) is within 3 ulp of fp64 g / (1 + exp(-g))
+    (within half of 2^-149 where the result is subnormal).  Below, exp(-g)
+    overflows from g < -88.72 on and the sequence gives -0 (|true value| <
+    2.7e-37)."""
+    import multiprocessing as mp
+    import os
+
+    from tests.exhaustive_util import silu_chunk_worst
+    spans = [(0, int(np.float32(89.0).view(np.uint32)) + 1),
+             (0x80000000, int(np.float32(-87.3).view(np.uint32)) + 1)]
+    ch = 1 << 23
+    jobs = [(s, min(s + ch, hi)) for lo, hi in spans for s in range(lo, hi, ch)]
+    with mp.get_context("spawn").Pool(min(8, os.cpu_count() or 1)) as pool:
+        res = pool.map(silu_chunk_worst, jobs, chunksize=4)
+    worst_n = max(r[0] for r in res)
+    worst_s = max(r[1] for r in res)
+    assert worst_n[0] <= 3.0, worst_n
+    assert worst_s[0] <= 0.5, worst_s
+    low = np.array([-88.73, -89.0, -95.5, -103.9, -104.0, -1e4], dtype=np.float32)
+    h = orc.silu_mul_f32_array(low, np.ones_like(low))
+    assert np.all(h == 0.0) and np.all(np.signbit(h))
+
+
 def test_exp_special_values(orc):
     assert orc.exp_f32([0.0])[0] == 1.0
     assert np.isinf(orc.exp_f32([89.0])[0]) and np.isinf(orc.exp_f32([1000.0])[0])
