@@ -117,11 +117,11 @@ def test_mx_scale_exponent_exhaustive(orc):
     import os
 
     from tests.exhaustive_util import mx_exponent_chunk_mismatches
-    ch = 1 << 24
+    ch = 1 << 22
     end = 0x7F800000  # +inf
     jobs = [(s, min(s + ch, end)) for s in range(0, end, ch)]
     with mp.get_context("spawn").Pool(min(8, os.cpu_count() or 1)) as pool:
-        bad = [b for r in pool.map(mx_exponent_chunk_mismatches, jobs, chunksize=4) for b in r]
+        bad = [b for r in pool.map(mx_exponent_chunk_mismatches, jobs, chunksize=16) for b in r]
     assert not bad, [hex(b) for b in bad[:8]]
 
 
@@ -182,10 +182,10 @@ def test_silu_accuracy_exhaustive(orc):
     from tests.exhaustive_util import silu_chunk_worst
     spans = [(0, int(np.float32(89.0).view(np.uint32)) + 1),
              (0x80000000, int(np.float32(-87.3).view(np.uint32)) + 1)]
-    ch = 1 << 23
+    ch = 1 << 22
     jobs = [(s, min(s + ch, hi)) for lo, hi in spans for s in range(lo, hi, ch)]
     with mp.get_context("spawn").Pool(min(8, os.cpu_count() or 1)) as pool:
-        res = pool.map(silu_chunk_worst, jobs, chunksize=4)
+        res = pool.map(silu_chunk_worst, jobs, chunksize=8)
     worst_n = max(r[0] for r in res)
     worst_s = max(r[1] for r in res)
     assert worst_n[0] <= 3.0, worst_n
