@@ -365,7 +365,9 @@ qmoe_status_t qmoe_moe_gemm_w8a16(const qmoe_gemm_args* args, qmoe_stream_t stre
 /* y[rows, 2I] bf16 (row stride ldy) holds gate (first I columns) and up (last
  * I columns); h = silu(gate) * up in fp32 (silu(g) = g / (1 + exp(-g)),
  * with exp evaluated by a fixed fp32 Cody-Waite + degree-7 Taylor sequence so
- * that the result is reproducible bit for bit), then
+ * that the result is reproducible bit for bit; silu(g) is within 3 ulp of
+ * the exact value for g in [-87.3, 89], and is -0 for g < -88.72, where
+ * exp(-g) overflows fp32 and the exact value is below 2.7e-37), then
  *  mode QMOE_SCALE_PER_TOKEN: scale[r] = amax_r/448, q = e4m3(h/scale);
  *  mode QMOE_SCALE_MX_1X32:   per 1x32 block along the row, e = smallest
  *    integer with 448*2^e >= block amax (clamped to [-127, 127], 0 for an
