@@ -142,10 +142,14 @@ def _need(t: torch.Tensor, dtype, name: str):
 
 # ----------------------------------------------------------------- align ---
 def align_max_padded(T: int, E: int, BM: int) -> int:
+    """Capacity of sorted_ids for T slots, E experts and tile BM (qmoe_align_max_padded):
+    T + E*(BM-1) rounded up to a multiple of BM."""
     return int(load_library().qmoe_align_max_padded(int(T), int(E), int(BM)))
 
 
 def alloc_align_outputs(T: int, E: int, BM: int, device="cuda") -> dict:
+    """Empty device buffers for moe_align_block_size: sorted_ids, expert_ids,
+    num_post_padded, expert_offsets, padded_offsets."""
     cap = align_max_padded(T, E, BM)
     i32 = torch.int32
     return dict(sorted_ids=torch.empty(cap, dtype=i32, device=device),
@@ -157,6 +161,10 @@ def alloc_align_outputs(T: int, E: int, BM: int, device="cuda") -> dict:
 
 def moe_align_block_size(topk_ids: torch.Tensor, E: int, BM: int, out: dict | None = None,
                          d_status: torch.Tensor | None = None, stream=None) -> dict:
+    """Sort token-slots by expert and pad every expert to a multiple of BM (qmoe_moe_align_block_size).
+
+    topk_ids int32 [M, top_k] on the device.  Returns the dict of alloc_align_outputs,
+    filled on the stream: slots in ascending order within an expert, pads = T."""
     _need(topk_ids, torch.int32, "topk_ids")
     T = topk_ids.numel()
     o = out if out is not None else alloc_align_outputs(T, E, BM, topk_ids.device)
@@ -283,6 +291,7 @@ def quant_weight_fp8(w: torch.Tensor, stream=None):
 
 
 def quant_weight_int8(w: torch.Tensor, stream=None):
+    """fp32 [..., K] weight rows -> (int8 codes, fp32 per-row scale amax/127), qmoe_quant_weight_int8."""
     _need(w, torch.float32, "w")
     K = w.shape[-1]
     rows = w.numel() // K
@@ -583,6 +592,7 @@ def moe_gemm_w4a16(a: torch.Tensor, w_q: torch.Tensor, w_scale: torch.Tensor, al
 
 # ------------------------------------------------------ SwiGLU + quant ---
 def mx_sf_ld(I: int) -> int:
+    """Row stride (bytes) of rowwise E8M0 factors for I columns: I/32 rounded up to a multiple of 4."""
     return (I // 32 + 3) // 4 * 4
 
 
@@ -631,6 +641,7 @@ def _act_quant(fn_name, gated, y, mode, expert_offsets, sf_padded_offsets, sf_ro
 
 # --------------------------------------------------------- element hooks ---
 def debug_e4m3_encode(x: torch.Tensor, stream=None) -> torch.Tensor:
+    """Test hook: the kernels' fp32 -> e4m3 conversion (RNE, satfinite) applied elementwise."""
     _need(x, torch.float32, "x")
     q = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
     _check(load_library().qmoe_debug_e4m3_encode(_ptr(x), _ptr(q), x.numel(), _stream(stream)), "debug_e4m3_encode")
@@ -638,6 +649,7 @@ def debug_e4m3_encode(x: torch.Tensor, stream=None) -> torch.Tensor:
 
 
 def debug_int8_to_bf16(x: torch.Tensor, stream=None) -> torch.Tensor:
+    """Test hook: the W8A16 converters' int8 -> bf16 conversion applied elementwise."""
     _need(x, torch.int8, "x")
     y = torch.empty(x.shape, dtype=torch.bfloat16, device=x.device)
     _check(load_library().qmoe_debug_int8_to_bf16(_ptr(x), _ptr(y), x.numel(), _stream(stream)),
@@ -646,6 +658,7 @@ def debug_int8_to_bf16(x: torch.Tensor, stream=None) -> torch.Tensor:
 
 
 def debug_silu_mul(g: torch.Tensor, u: torch.Tensor, stream=None) -> torch.Tensor:
+    """Test hook: h = silu(g) * u by the kernels' packed fp32 sequence, elementwise."""
     _need(g, torch.float32, "g")
     _need(u, torch.float32, "u")
     h = torch.empty_like(g)
@@ -655,6 +668,7 @@ def debug_silu_mul(g: torch.Tensor, u: torch.Tensor, stream=None) -> torch.Tenso
 
 
 def debug_rcp_ge1(d: torch.Tensor, stream=None) -> torch.Tensor:
+    """Test hook: the SiLU's reciprocal 1/d for d >= 1, elementwise."""
     _need(d, torch.float32, "d")
     y = torch.empty_like(d)
     _check(load_library().qmoe_debug_rcp_ge1(_ptr(d), _ptr(y), d.numel(), _stream(stream)), "debug_rcp_ge1")
@@ -662,6 +676,7 @@ def debug_rcp_ge1(d: torch.Tensor, stream=None) -> torch.Tensor:
 
 
 def debug_div_by_scale(x: torch.Tensor, s: float, stream=None) -> torch.Tensor:
+    """Test hook: the quantisers' division x / s by a row scale (packed pairs), elementwise."""
     _need(x, torch.float32, "x")
     q = torch.empty_like(x)
     _check(load_library().qmoe_debug_div_by_scale(_ptr(x), float(s), _ptr(q), x.numel(), _stream(stream)),
@@ -670,6 +685,7 @@ def debug_div_by_scale(x: torch.Tensor, s: float, stream=None) -> torch.Tensor:
 
 
 def debug_wait_timeout(d_status: torch.Tensor, limit_ns: int, stream=None) -> None:
+    """Test hook: one bounded mbarrier wait that nothing completes; sets QMOE_DEV_TIMEOUT in d_status."""
     _need(d_status, torch.int32, "d_status")
     _check(load_library().qmoe_debug_wait_timeout(_ptr(d_status), int(limit_ns), _stream(stream)),
            "debug_wait_timeout")
