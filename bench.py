@@ -230,20 +230,21 @@ class OracleBench:
         self.rng = np.random.default_rng(0)
 
     def run(self, seconds: float):
+        """Batches of one slot per thread, drawn at random from the M=64 shape's
+        slots, until `seconds` of oracle time have passed (at least one batch)."""
         o = self.oracle
-        n, elapsed, done = max(self.cores, 1), 0.0, 0
-        while elapsed < seconds and done < self.T:
-            take = min(n, self.T - done)
-            slots = self.rng.choice(self.T, take, replace=False)
+        n, elapsed, done = min(max(self.cores, 1), self.T), 0.0, 0
+        while done == 0 or elapsed < seconds:
+            slots = self.rng.choice(self.T, n, replace=False)
             t0 = time.perf_counter()
             o.moe_gemm(a_kind=o.A_FP8_TOKEN, a=self.raq, a_scale=self.rsa, w_kind=o.W_FP8, w=self.rwq,
                        w_scale=self.rws, topk_ids=self.ids, topk_w=self.tw, E=E, slots=slots)
             elapsed += time.perf_counter() - t0
-            done += take
+            done += n
         t_sweep = self.sweep_slots * elapsed / done
-        sample = (f"{done} random slots of the M=64 shape (K=4096, N=14336; fp64 dense per-slot loop) in "
-                  f"{elapsed:.1f} s on {self.cores} threads; per-slot time extrapolated to the "
-                  f"{self.sweep_slots} slots of the sweep")
+        sample = (f"{done} slots drawn at random from the {self.T} of the M=64 shape (K=4096, N=14336; fp64 "
+                  f"dense per-slot loop) in {elapsed:.1f} s on {self.cores} threads; per-slot time extrapolated "
+                  f"to the {self.sweep_slots} slots of the sweep")
         return self.sweep_bytes / t_sweep / 1e9, t_sweep, sample
 
 
