@@ -77,6 +77,7 @@ def lib():
             L.orc_mx_scale_exponent.argtypes = [ctypes.c_float]
             L.orc_mx_scale_exponent.restype = ctypes.c_int
             L.orc_mx_scale_exponent_array.argtypes = [vp, i64, vp]
+            L.orc_bf16_from_f32_array.argtypes = [vp, i64, vp]
             L.orc_exp_f32.argtypes = [ctypes.c_float]
             L.orc_exp_f32.restype = ctypes.c_float
             L.orc_silu_mul_f32.argtypes = [ctypes.c_float, ctypes.c_float]
@@ -120,6 +121,13 @@ def bf16_from_f32(x) -> np.ndarray:
     f = lib().orc_bf16_from_f32
     x = np.asarray(x, dtype=np.float32).ravel()
     return np.array([f(float(v)) for v in x], dtype=np.uint16)
+
+
+def bf16_from_f32_array(x: np.ndarray) -> np.ndarray:
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    h = np.empty(x.shape, dtype=np.uint16)
+    lib().orc_bf16_from_f32_array(_p(x), x.size, _p(h))
+    return h
 
 
 def bf16_to_f32(b) -> np.ndarray:

@@ -80,6 +80,11 @@ uint16_t orc_bf16_from_f32(float x) {
 
 float orc_bf16_to_f32(uint16_t h) { return f32_from_bits((uint32_t)h << 16); }
 
+/* orc_bf16_from_f32 over an array (marshalling only). */
+void orc_bf16_from_f32_array(const float* x, int64_t n, uint16_t* h) {
+    for (int64_t i = 0; i < n; ++i) h[i] = orc_bf16_from_f32(x[i]);
+}
+
 /* ------------------------------------------------------------------------- */
 /* OCP E4M3: 1 sign, 4 exponent (bias 7), 3 mantissa bits; no infinities;    */
 /* S.1111.111 is NaN; largest finite 1.75 * 2^8 = 448; subnormals m * 2^-9.  */

@@ -82,3 +82,19 @@ def silu_chunk_worst(span):
     ds = np.where(normal, 0.0, d * 2.0 ** 149)
     i, j = int(np.argmax(dn)), int(np.argmax(ds))
     return (float(dn[i]), float(x[i])), (float(ds[j]), float(x[j]))
+
+
+def bf16_chunk_mismatches(span):
+    """Over the fp32 bit patterns [lo, hi) (NaNs skipped): the patterns where
+    the oracle's bf16 encoding differs from torch's bfloat16 cast.  At most 4."""
+    import oracle
+    import torch
+    torch.set_num_threads(1)
+    lo, hi = span
+    bits = np.arange(lo, hi, dtype=np.uint32)
+    x = bits.view(np.float32)
+    keep = ~np.isnan(x)
+    bits, x = bits[keep], x[keep]
+    got = oracle.bf16_from_f32_array(x)
+    ref = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    return [int(b) for b in bits[got != ref][:4]]

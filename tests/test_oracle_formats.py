@@ -82,6 +82,20 @@ def test_bf16_encode_vs_torch(orc):
     assert np.array_equal(back, torch.from_numpy(xs).to(torch.bfloat16).float().numpy())
 
 
+def test_bf16_encode_exhaustive_vs_torch(orc):
+    """Every non-NaN fp32: the oracle's bf16 encoding (round to nearest even)
+    equals torch's bfloat16 cast."""
+    import multiprocessing as mp
+    import os
+
+    from tests.exhaustive_util import bf16_chunk_mismatches
+    ch = 1 << 24
+    jobs = [(s, s + ch) for s in range(0, 1 << 32, ch)]
+    with mp.get_context("spawn").Pool(min(8, os.cpu_count() or 1)) as pool:
+        bad = [b for r in pool.map(bf16_chunk_mismatches, jobs, chunksize=4) for b in r]
+    assert not bad, [hex(b) for b in bad[:8]]
+
+
 def test_e8m0_decode(orc):
     codes = np.arange(256, dtype=np.uint8)
     v = orc.e8m0_to_f64(codes)
