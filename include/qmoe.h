@@ -195,7 +195,9 @@ qmoe_status_t qmoe_quant_weight_int8(const float* w, int64_t rows, int64_t cols,
  * Quantization using linear decomposition", Summary; the pages do not define
  * it -- this library reads it as symmetric groups of 128 along K): every
  * fp32 row of cols (a multiple of 128) values, per 128-wide group
- * scale = amax/7 (IEEE division; 1 for an all-zero group),
+ * scale = amax/7 (IEEE division) rounded up to the nearest fp32 value with at
+ * most 5 significant bits (1 for an all-zero group), so that every
+ * dequantised weight q * scale is exactly a bf16 number;
  * q = clamp(rint(w/scale), -7, 7), two's-complement nibbles packed two per
  * byte with element 2j in the low nibble of byte j.
  *   q [rows, cols/2] bytes and w 16-byte aligned; scale [rows, cols/128] fp32. */
@@ -318,11 +320,13 @@ typedef struct {
 qmoe_status_t qmoe_moe_gemm_w8a8(const qmoe_gemm_args* args, qmoe_stream_t stream);
 
 /* INT4 W4A16 grouped GEMM (weight-only int4 against bf16 activations):
- *   out = w[s] * sum_k a_bf16[k] * bf16(q4[e, n, k] * scale[e, n, k/128])
+ *   out = w[s] * sum_k a_bf16[k] * (q4[e, n, k] * scale[e, n, k/128])
  * with fp32 accumulation and a bf16 result.  args->w holds the packed int4
  * weights [E, N, K/2] of qmoe_quant_weight_int4 and args->w_scale their group
  * scales [E, N, K/128]; the converter warps form each bf16 weight as the fp32
- * product q * scale rounded to bf16 (RN) before the tensor-core MMA.
+ * product q * scale rounded to bf16 (RN) before the tensor-core MMA, which is
+ * exact for the scales qmoe_quant_weight_int4 writes (other scales: the
+ * product is rounded to bf16).
  * Activation and output layouts as qmoe_moe_gemm_w8a16.  Limits: K % 128 == 0,
  * BM in {128, 256} (else QMOE_ERR_UNSUPPORTED), w_scale_mode PER_ROW. */
 qmoe_status_t qmoe_moe_gemm_w4a16(const qmoe_gemm_args* args, qmoe_stream_t stream);
@@ -341,6 +345,10 @@ qmoe_status_t qmoe_moe_gemm_w4a16(const qmoe_gemm_args* args, qmoe_stream_t stre
  *    launches nothing.
  *  - The first call on a device looks up the array's device address (with
  *    that device current); make that first call before any stream capture.
+ *    The address is kept per device and looked up again when the device's
+ *    context has changed (after cudaDeviceReset, for example, the array has
+ *    a new address); make the first call after such a reset before any
+ *    stream capture too.
  *  - All calls share the one array: the first M*N floats are zeroed on the
  *    stream at every call, but calls whose work overlaps on the GPU (other
  *    streams, other host threads) race on it and must be serialised by the

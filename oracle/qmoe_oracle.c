@@ -250,10 +250,23 @@ void orc_quant_rows_int8_f32(const float* x, int64_t rows, int64_t cols, int64_t
 
 /* Symmetric INT4 in groups of 128 along the row (the "int4wo" weight-only
  * recipe named in "Enabling MOE Quantization using linear decomposition",
- * Summary; group size and symmetric range are this build's reading):
- * per group scale = amax/7 (1 for an all-zero group), q = clamp(rint(x/scale),
- * -7, 7); two's-complement nibbles packed two per byte, element 2j in the low
- * nibble of byte j.  q is [rows, cols/2] bytes, scale [rows, cols/128]. */
+ * Summary; group size, symmetric range and scale format are this build's
+ * reading): per group s0 = amax/7 (IEEE division), and the stored scale is s0
+ * rounded up to the nearest fp32 value with at most 5 significant bits (1 for
+ * an all-zero group), so that every dequantised weight q * scale (|q| <= 7,
+ * at most 3 significant bits) has at most 8 significant bits and is a bf16
+ * number, the operand format of a weight-only GEMM on bf16 activations;
+ * q = clamp(rint(x/scale), -7, 7); two's-complement nibbles packed two per
+ * byte, element 2j in the low nibble of byte j.  q is [rows, cols/2] bytes,
+ * scale [rows, cols/128]. */
+static float round_up_5bits(float s) {
+    uint32_t b;
+    memcpy(&b, &s, 4);
+    if (b & 0x7FFFFu) b = (b | 0x7FFFFu) + 1u;  /* clear 19 low fraction bits, rounding up */
+    memcpy(&s, &b, 4);
+    return s;
+}
+
 void orc_quant_rows_int4_f32(const float* x, int64_t rows, int64_t cols, uint8_t* q, float* scale) {
     const int64_t G = cols / 128;
 #pragma omp parallel for schedule(static)
@@ -265,7 +278,7 @@ void orc_quant_rows_int4_f32(const float* x, int64_t rows, int64_t cols, uint8_t
                 float a = fabsf(xg[c]);
                 if (a > amax) amax = a;
             }
-            float s = (amax == 0.0f) ? 1.0f : amax / 7.0f;
+            float s = (amax == 0.0f) ? 1.0f : round_up_5bits(amax / 7.0f);
             scale[r * G + g] = s;
             for (int64_t c = 0; c < 128; c += 2) {
                 int v[2];
@@ -548,8 +561,8 @@ void orc_router_topk(const float* logits, int64_t M, int32_t E, int32_t k, int32
 /* w_kind 2: e4m3 codes with E8M0 scales per 1x32 block along K,               */
 /*           w_sf[(e*N + n) * w_sf_ld + k/32] (times w_scale[e*N + n] if given).*/
 /* w_kind 3: packed INT4 rows of K/2 bytes with one fp32 scale per group of    */
-/*           128 along K, w_scale[(e*N + n) * (K/128) + k/128]; the weight the */
-/*           bf16 GEMM multiplies is bf16(q * scale) (fp32 product, RN).       */
+/*           128 along K, w_scale[(e*N + n) * (K/128) + k/128]; dequantised   */
+/*           as q * scale in fp64 like every other kind.                      */
 /* ------------------------------------------------------------------------- */
 void orc_moe_gemm(int a_kind, const void* a, int64_t lda, const float* a_scale,
                   const uint8_t* a_sf, int64_t a_sf_ld, const int64_t* a_sf_row,
@@ -584,10 +597,7 @@ void orc_moe_gemm(int a_kind, const void* a, int64_t lda, const float* a_scale,
             if (w_kind == 3) {
                 const uint8_t* wq = (const uint8_t*)w + ((int64_t)e * N + n) * (K / 2);
                 const float* gs = w_scale + ((int64_t)e * N + n) * (K / 128);
-                for (int64_t k = 0; k < K; ++k) {
-                    const float wf = (float)int4_at(wq, k) * gs[k / 128];
-                    acc += arow[k] * (double)orc_bf16_to_f32(orc_bf16_from_f32(wf));
-                }
+                for (int64_t k = 0; k < K; ++k) acc += arow[k] * ((double)int4_at(wq, k) * (double)gs[k / 128]);
             } else if (w_kind == 0) {
                 const uint8_t* wq = (const uint8_t*)w + wrow;
                 for (int64_t k = 0; k < K; ++k) acc += arow[k] * (lut[wq[k]] * sw);

@@ -1,15 +1,19 @@
 // gemm_w4a16.cu -- INT4 weight-only ("int4wo") grouped GEMM entry point and
 // its weight quantiser: packed int4 weights with one fp32 scale per output
-// channel and 128-wide group of K, turned into bf16 (q * scale) by the
-// converter warps ahead of a tcgen05 kind::f16 MMA on bf16 activations.
+// channel and 128-wide group of K, turned into bf16 (q * scale, exact for the
+// quantiser's 5-bit scales) by the converter warps ahead of a tcgen05
+// kind::f16 MMA on bf16 activations.
 #include "gemm_kernel.cuh"
 
 namespace qmoe {
 
 constexpr int kI4QuantThreads = 128;
 
-// One thread per (row, 128-wide group): scale = amax/7 (IEEE division; 1 for an
-// all-zero group), q = clamp(rint(x/scale), -7, 7), nibbles packed low-first.
+// One thread per (row, 128-wide group): scale = amax/7 (IEEE division) rounded
+// up to the nearest value with at most 5 significant bits (1 for an all-zero
+// group), so that q * scale for |q| <= 7 has at most 8 significant bits and
+// the converters' bf16 rounding of it is exact; q = clamp(rint(x/scale), -7, 7),
+// nibbles packed low-first.
 __global__ void __launch_bounds__(kI4QuantThreads)
     quant_rows_int4_kernel(const float* __restrict__ w, int64_t rows, int64_t cols, uint8_t* __restrict__ q,
                            float* __restrict__ scale) {
@@ -25,7 +29,12 @@ __global__ void __launch_bounds__(kI4QuantThreads)
         const float4 t = src[i];
         a = fmaxf(a, fmaxf(fmaxf(fabsf(t.x), fabsf(t.y)), fmaxf(fabsf(t.z), fabsf(t.w))));
     }
-    const float s = (a == 0.0f) ? 1.0f : __fdiv_rn(a, 7.0f);
+    float s = 1.0f;
+    if (a != 0.0f) {
+        uint32_t b = __float_as_uint(__fdiv_rn(a, 7.0f));
+        if (b & 0x7FFFFu) b = (b | 0x7FFFFu) + 1u;  // clear the 19 low fraction bits, rounding up
+        s = __uint_as_float(b);
+    }
     scale[g] = s;
     uint4* dst = reinterpret_cast<uint4*>(q + r * (cols / 2) + grp * 64);
 #pragma unroll

@@ -163,9 +163,22 @@ def test_tolerance_helper_rejects_planted_error(orc):
     assert not ok and ratio > 1
 
 
+def _ceil_5_significant_bits(x: np.ndarray) -> np.ndarray:
+    """Smallest float with at most 5 significant bits that is >= x (x > 0, fp32),
+    found with exact float64 arithmetic: 2^(e-4) * ceil(x / 2^(e-4)) where
+    2^e <= x < 2^(e+1)."""
+    x = x.astype(np.float64)
+    e = np.floor(np.log2(x))
+    e = np.where(2.0 ** e > x, e - 1, e)
+    e = np.where(2.0 ** (e + 1) <= x, e + 1, e)
+    ulp = 2.0 ** (e - 4)
+    return (np.ceil(x / ulp) * ulp).astype(np.float32)
+
+
 def test_int4_quant_rule_and_packing(orc):
-    """Symmetric groups of 128: scale = amax/7, codes rint(w/scale) clamped to
-    [-7, 7], nibbles packed low-first; reconstruction within half a step."""
+    """Symmetric groups of 128: scale = amax/7 rounded up to 5 significant bits,
+    codes rint(w/scale) clamped to [-7, 7], nibbles packed low-first;
+    reconstruction within half a step; every q * scale a bf16 number."""
     w = inputs.expert_weights_f32(2, 24, 384, seed=41)
     w[0, 0, :128] = 0.0
     w[1, 3, 128:256] *= 1e-20
@@ -179,13 +192,20 @@ def test_int4_quant_rule_and_packing(orc):
     assert v.min() >= -7 and v.max() <= 7
     g = w.reshape(2, 24, 3, 128)
     amax = np.abs(g).max(axis=-1)
-    exp_s = np.where(amax == 0, np.float32(1), (amax / np.float32(7)).astype(np.float32))
+    s0 = np.where(amax == 0, np.float32(1), (amax / np.float32(7)).astype(np.float32))
+    exp_s = np.where(amax == 0, np.float32(1), _ceil_5_significant_bits(s0))
     assert np.array_equal(s, exp_s)
+    # at most 5 significant bits, never below amax/7, less than 2^-4 relative above it
+    assert np.all((s.view(np.uint32) & 0x7FFFF) == 0)
+    assert np.all(s >= s0) and np.all(s.astype(np.float64) < s0.astype(np.float64) * (1 + 2.0 ** -4))
     ref = np.clip(np.rint((g / s[..., None]).astype(np.float32)), -7, 7).reshape(w.shape)
     assert np.array_equal(v, ref.astype(np.int16))
     rec = v.reshape(2, 24, 3, 128) * s[..., None].astype(np.float64)
     assert np.all(np.abs(rec - g) <= 0.5 * s[..., None] * (1 + 1e-6))
     assert np.all(v[0, 0, :128] == 0) and s[0, 0, 0] == 1.0
+    # the dequantised weights are exact bf16 numbers (torch's bf16 cast leaves them unchanged)
+    exact = (v.reshape(2, 24, 3, 128) * s[..., None].astype(np.float64)).astype(np.float32)
+    assert np.array_equal(torch.from_numpy(exact).to(torch.bfloat16).float().numpy(), exact)
 
 
 def test_int4_w4a16_vs_bruteforce(orc):
@@ -199,9 +219,8 @@ def test_int4_w4a16_vs_bruteforce(orc):
     v = np.empty((E, N, K), dtype=np.float64)
     v[..., 0::2] = np.where(lo >= 8, lo - 16, lo)
     v[..., 1::2] = np.where(hi >= 8, hi - 16, hi)
-    # the weight the bf16 GEMM multiplies: bf16(q * scale), the product in fp32 (torch's bf16 cast)
-    wf = (v.astype(np.float32) * np.repeat(s, 128, axis=-1)).astype(np.float32)
-    W = torch.from_numpy(wf).to(torch.bfloat16).to(torch.float64).numpy()
+    # dequantised in fp64: q * scale
+    W = v * np.repeat(s, 128, axis=-1).astype(np.float64)
     A = inputs.bf16_bits_to_f32(a).astype(np.float64)
     ref = dense_moe(A, W, ids, tw)
     out = orc.moe_gemm(a_kind=orc.A_BF16, a=a, w_kind=orc.W_INT4, w=q, w_scale=s, topk_ids=ids, topk_w=tw, E=E)
