@@ -131,6 +131,12 @@ def _stream(stream: torch.cuda.Stream | None = None):
     return ctypes.c_void_p(s.cuda_stream)
 
 
+def _empty(*size, dtype, device) -> torch.Tensor:
+    """Every output and scratch tensor the binding allocates comes from here
+    (uninitialised device memory, like torch.empty)."""
+    return torch.empty(*size, dtype=dtype, device=device)
+
+
 def _need(t: torch.Tensor, dtype, name: str):
     if not isinstance(t, torch.Tensor) or not t.is_cuda:
         raise QmoeError(f"{name} must be a CUDA tensor")
@@ -152,11 +158,11 @@ def alloc_align_outputs(T: int, E: int, BM: int, device="cuda") -> dict:
     num_post_padded, expert_offsets, padded_offsets."""
     cap = align_max_padded(T, E, BM)
     i32 = torch.int32
-    return dict(sorted_ids=torch.empty(cap, dtype=i32, device=device),
-                expert_ids=torch.empty(cap // BM, dtype=i32, device=device),
-                num_post_padded=torch.empty(1, dtype=i32, device=device),
-                expert_offsets=torch.empty(E + 1, dtype=i32, device=device),
-                padded_offsets=torch.empty(E + 1, dtype=i32, device=device))
+    return dict(sorted_ids=_empty(cap, dtype=i32, device=device),
+                expert_ids=_empty(cap // BM, dtype=i32, device=device),
+                num_post_padded=_empty(1, dtype=i32, device=device),
+                expert_offsets=_empty(E + 1, dtype=i32, device=device),
+                padded_offsets=_empty(E + 1, dtype=i32, device=device))
 
 
 def moe_align_block_size(topk_ids: torch.Tensor, E: int, BM: int, out: dict | None = None,
@@ -181,8 +187,8 @@ def quant_act_fp8(x: torch.Tensor, q: torch.Tensor | None = None, scale: torch.T
     if not x.is_cuda or x.dtype != torch.bfloat16 or x.dim() != 2 or x.stride(1) != 1:
         raise QmoeError("x must be a 2-D CUDA bf16 tensor with unit column stride")
     rows, cols = x.shape
-    q = q if q is not None else torch.empty(rows, cols, dtype=torch.uint8, device=x.device)
-    scale = scale if scale is not None else torch.empty(rows, dtype=torch.float32, device=x.device)
+    q = q if q is not None else _empty(rows, cols, dtype=torch.uint8, device=x.device)
+    scale = scale if scale is not None else _empty(rows, dtype=torch.float32, device=x.device)
     st = load_library().qmoe_quant_act_fp8(_ptr(x), rows, cols, x.stride(0), _ptr(q), _ptr(scale), _stream(stream))
     _check(st, "quant_act_fp8")
     return q, scale
@@ -196,8 +202,8 @@ def quant_act_fp8_sorted(x: torch.Tensor, align: dict, top_k: int, q: torch.Tens
         raise QmoeError("x must be a 2-D CUDA bf16 tensor with unit column stride")
     M, cols = x.shape
     cap = align["sorted_ids"].numel()
-    q = q if q is not None else torch.empty(cap, cols, dtype=torch.uint8, device=x.device)
-    scale = scale if scale is not None else torch.empty(cap, dtype=torch.float32, device=x.device)
+    q = q if q is not None else _empty(cap, cols, dtype=torch.uint8, device=x.device)
+    scale = scale if scale is not None else _empty(cap, dtype=torch.float32, device=x.device)
     st = load_library().qmoe_quant_act_fp8_sorted(_ptr(x), M, cols, x.stride(0), _ptr(align["sorted_ids"]),
                                                   _ptr(align["num_post_padded"]), top_k, cap, _ptr(q), _ptr(scale),
                                                   _stream(stream))
@@ -218,8 +224,8 @@ def moe_align_quant_fp8(x: torch.Tensor, topk_ids: torch.Tensor, E: int, BM: int
     T = topk_ids.numel()
     o = align if align is not None else alloc_align_outputs(T, E, BM, x.device)
     cap = o["sorted_ids"].numel()
-    q = q if q is not None else torch.empty(cap, cols, dtype=torch.uint8, device=x.device)
-    scale = scale if scale is not None else torch.empty(cap, dtype=torch.float32, device=x.device)
+    q = q if q is not None else _empty(cap, cols, dtype=torch.uint8, device=x.device)
+    scale = scale if scale is not None else _empty(cap, dtype=torch.float32, device=x.device)
     st = load_library().qmoe_moe_align_quant_fp8(
         _ptr(x), M, cols, x.stride(0), _ptr(topk_ids), top_k, E, BM, _ptr(o["sorted_ids"]), _ptr(o["expert_ids"]),
         _ptr(o["num_post_padded"]), _ptr(o["expert_offsets"]), _ptr(o["padded_offsets"]), _ptr(q), _ptr(scale),
@@ -232,8 +238,8 @@ def moe_router_topk(logits: torch.Tensor, top_k: int, topk_ids=None, topk_weight
     """fp32 logits [M, E] -> (topk_ids int32 [M, top_k], topk_weights fp32 [M, top_k])."""
     _need(logits, torch.float32, "logits")
     M, E = logits.shape
-    ids = topk_ids if topk_ids is not None else torch.empty(M, top_k, dtype=torch.int32, device=logits.device)
-    w = topk_weights if topk_weights is not None else torch.empty(M, top_k, dtype=torch.float32, device=logits.device)
+    ids = topk_ids if topk_ids is not None else _empty(M, top_k, dtype=torch.int32, device=logits.device)
+    w = topk_weights if topk_weights is not None else _empty(M, top_k, dtype=torch.float32, device=logits.device)
     _check(load_library().qmoe_moe_router_topk(_ptr(logits), M, E, top_k, _ptr(ids), _ptr(w), _stream(stream)),
            "moe_router_topk")
     return ids, w
@@ -250,11 +256,11 @@ def moe_route_align_quant_fp8(logits: torch.Tensor, x: torch.Tensor, top_k: int,
     cols = x.shape[1]
     T = M * top_k
     o = align if align is not None else alloc_align_outputs(T, E, BM, x.device)
-    ids = topk_ids if topk_ids is not None else torch.empty(M, top_k, dtype=torch.int32, device=x.device)
-    w = topk_weights if topk_weights is not None else torch.empty(M, top_k, dtype=torch.float32, device=x.device)
+    ids = topk_ids if topk_ids is not None else _empty(M, top_k, dtype=torch.int32, device=x.device)
+    w = topk_weights if topk_weights is not None else _empty(M, top_k, dtype=torch.float32, device=x.device)
     cap = o["sorted_ids"].numel()
-    q = q if q is not None else torch.empty(cap, cols, dtype=torch.uint8, device=x.device)
-    scale = scale if scale is not None else torch.empty(cap, dtype=torch.float32, device=x.device)
+    q = q if q is not None else _empty(cap, cols, dtype=torch.uint8, device=x.device)
+    scale = scale if scale is not None else _empty(cap, dtype=torch.float32, device=x.device)
     st = load_library().qmoe_moe_route_align_quant_fp8(
         _ptr(logits), _ptr(x), M, cols, x.stride(0), E, top_k, BM, _ptr(ids), _ptr(w), _ptr(o["sorted_ids"]),
         _ptr(o["expert_ids"]), _ptr(o["num_post_padded"]), _ptr(o["expert_offsets"]), _ptr(o["padded_offsets"]),
@@ -270,7 +276,7 @@ def gather_sorted_bf16(x: torch.Tensor, align: dict, top_k: int, out: torch.Tens
         raise QmoeError("x must be a 2-D CUDA bf16 tensor with unit column stride")
     M, cols = x.shape
     cap = align["sorted_ids"].numel()
-    out = out if out is not None else torch.empty(cap, cols, dtype=torch.bfloat16, device=x.device)
+    out = out if out is not None else _empty(cap, cols, dtype=torch.bfloat16, device=x.device)
     st = load_library().qmoe_gather_sorted_bf16(_ptr(x), M, cols, x.stride(0), _ptr(align["sorted_ids"]),
                                                 _ptr(align["num_post_padded"]), top_k, cap, _ptr(out),
                                                 _stream(stream))
@@ -283,8 +289,8 @@ def quant_weight_fp8(w: torch.Tensor, stream=None):
     _need(w, torch.float32, "w")
     K = w.shape[-1]
     rows = w.numel() // K
-    q = torch.empty(w.shape, dtype=torch.uint8, device=w.device)
-    s = torch.empty(w.shape[:-1], dtype=torch.float32, device=w.device)
+    q = _empty(w.shape, dtype=torch.uint8, device=w.device)
+    s = _empty(w.shape[:-1], dtype=torch.float32, device=w.device)
     _check(load_library().qmoe_quant_weight_fp8(_ptr(w), rows, K, _ptr(q), _ptr(s), _stream(stream)),
            "quant_weight_fp8")
     return q, s
@@ -295,8 +301,8 @@ def quant_weight_int8(w: torch.Tensor, stream=None):
     _need(w, torch.float32, "w")
     K = w.shape[-1]
     rows = w.numel() // K
-    q = torch.empty(w.shape, dtype=torch.int8, device=w.device)
-    s = torch.empty(w.shape[:-1], dtype=torch.float32, device=w.device)
+    q = _empty(w.shape, dtype=torch.int8, device=w.device)
+    s = _empty(w.shape[:-1], dtype=torch.float32, device=w.device)
     _check(load_library().qmoe_quant_weight_int8(_ptr(w), rows, K, _ptr(q), _ptr(s), _stream(stream)),
            "quant_weight_int8")
     return q, s
@@ -307,8 +313,8 @@ def quant_weight_int4(w: torch.Tensor, q=None, scale=None, stream=None):
     _need(w, torch.float32, "w")
     K = w.shape[-1]
     rows = w.numel() // K
-    q = q if q is not None else torch.empty(w.shape[:-1] + (K // 2,), dtype=torch.uint8, device=w.device)
-    scale = scale if scale is not None else torch.empty(w.shape[:-1] + (K // 128,), dtype=torch.float32,
+    q = q if q is not None else _empty(w.shape[:-1] + (K // 2,), dtype=torch.uint8, device=w.device)
+    scale = scale if scale is not None else _empty(w.shape[:-1] + (K // 128,), dtype=torch.float32,
                                                         device=w.device)
     _check(load_library().qmoe_quant_weight_int4(_ptr(w), rows, K, _ptr(q), _ptr(scale), _stream(stream)),
            "quant_weight_int4")
@@ -320,8 +326,8 @@ def quant_weight_mxfp8(w: torch.Tensor, q=None, sf=None, stream=None):
     _need(w, torch.float32, "w")
     K = w.shape[-1]
     rows = w.numel() // K
-    q = q if q is not None else torch.empty(w.shape, dtype=torch.uint8, device=w.device)
-    sf = sf if sf is not None else torch.empty(rows, mx_sf_ld(K), dtype=torch.uint8, device=w.device)
+    q = q if q is not None else _empty(w.shape, dtype=torch.uint8, device=w.device)
+    sf = sf if sf is not None else _empty(rows, mx_sf_ld(K), dtype=torch.uint8, device=w.device)
     _check(load_library().qmoe_quant_weight_mxfp8(_ptr(w), rows, K, _ptr(q), _ptr(sf), sf.stride(0),
                                                   _stream(stream)), "quant_weight_mxfp8")
     return q, sf
@@ -335,11 +341,11 @@ def quant_mxfp8(x: torch.Tensor, *, expert_offsets, sf_padded_offsets, sf_rows: 
     _need(expert_offsets, torch.int32, "expert_offsets")
     _need(sf_padded_offsets, torch.int32, "sf_padded_offsets")
     rows, I = x.shape
-    q = q if q is not None else torch.empty(rows, I, dtype=torch.uint8, device=x.device)
+    q = q if q is not None else _empty(rows, I, dtype=torch.uint8, device=x.device)
     if sf is None:
         if sf_rows is None:
             raise QmoeError("sf_rows (capacity of the scale-factor matrix) is required when sf is not given")
-        sf = torch.empty(sf_rows, mx_sf_ld(I), dtype=torch.uint8, device=x.device)
+        sf = _empty(sf_rows, mx_sf_ld(I), dtype=torch.uint8, device=x.device)
     st = load_library().qmoe_quant_mxfp8(_ptr(x), rows, I, x.stride(0), _ptr(q), _ptr(sf), sf.stride(0),
                                          _ptr(expert_offsets), _ptr(sf_padded_offsets), expert_offsets.numel() - 1,
                                          _ptr(d_status), _stream(stream))
@@ -352,7 +358,7 @@ def mx_weight_sf_tiled(sf: torch.Tensor, E: int, N: int, K: int, out=None, strea
     _need(sf, torch.uint8, "sf")
     L = load_library()
     nbytes = int(L.qmoe_mx_weight_sf_tiled_bytes(E, N, K))
-    out = out if out is not None else torch.empty(nbytes, dtype=torch.uint8, device=sf.device)
+    out = out if out is not None else _empty(nbytes, dtype=torch.uint8, device=sf.device)
     _check(L.qmoe_mx_weight_sf_tiled(_ptr(sf), E, N, K, sf.stride(0), _ptr(out), _stream(stream)),
            "mx_weight_sf_tiled")
     return out
@@ -368,10 +374,10 @@ def quant_mxfp8_colwise(x: torch.Tensor, q=None, sf=None, stream=None):
     if not x.is_cuda or x.dtype != torch.bfloat16 or x.dim() != 2 or x.stride(1) != 1:
         raise QmoeError("x must be a 2-D CUDA bf16 tensor with unit column stride")
     rows, cols = x.shape
-    q = q if q is not None else torch.empty(rows, cols, dtype=torch.uint8, device=x.device)
+    q = q if q is not None else _empty(rows, cols, dtype=torch.uint8, device=x.device)
     if sf is None:
         sr, sc = mx_colwise_sf_shape(rows, cols)
-        sf = torch.empty(sr, sc, dtype=torch.uint8, device=x.device)
+        sf = _empty(sr, sc, dtype=torch.uint8, device=x.device)
     st = load_library().qmoe_quant_mxfp8_colwise(_ptr(x), rows, cols, x.stride(0), _ptr(q), _ptr(sf), sf.shape[0],
                                                  sf.stride(0), _stream(stream))
     _check(st, "quant_mxfp8_colwise")
@@ -385,7 +391,7 @@ def _gemm(fn_name, *, a, a_scale, w, w_scale, align, topk_weights, out, M, top_k
     E, N, Kw = w.shape
     K = Kw if K is None else K
     if out_layout == OUT_TOKEN_SUM and accum is None:
-        accum = torch.empty(M, N, dtype=torch.float32, device=out.device)
+        accum = _empty(M, N, dtype=torch.float32, device=out.device)
     args = GemmArgs()
     args.struct_size = ctypes.sizeof(GemmArgs)
     args.a = a.data_ptr()
@@ -421,7 +427,7 @@ def _out_for(out, out_layout, M, top_k, N, device):
     if out is not None:
         return out
     rows = M if out_layout == OUT_TOKEN_SUM else M * top_k
-    return torch.empty(rows, N, dtype=torch.bfloat16, device=device)
+    return _empty(rows, N, dtype=torch.bfloat16, device=device)
 
 
 def moe_gemm_w8a8(a_q: torch.Tensor, a_scale: torch.Tensor | None, w_q: torch.Tensor, w_scale: torch.Tensor,
@@ -478,10 +484,10 @@ def moe_gemm_w8a8_silu_mxfp8(a_q: torch.Tensor, a_scale: torch.Tensor, w_q: torc
         _need(topk_weights, torch.float32, "topk_weights")
     E, N, _ = w_q.shape
     I, T = N // 2, M * top_k
-    q = q if q is not None else torch.empty(T, I, dtype=torch.uint8, device=a_q.device)
+    q = q if q is not None else _empty(T, I, dtype=torch.uint8, device=a_q.device)
     if sf is None:
         rows = sf_rows if sf_rows is not None else align_max_padded(T, E, 128)
-        sf = torch.empty(rows, mx_sf_ld(I), dtype=torch.uint8, device=a_q.device)
+        sf = _empty(rows, mx_sf_ld(I), dtype=torch.uint8, device=a_q.device)
     _gemm("qmoe_moe_gemm_w8a8_silu_mxfp8", a=a_q, a_scale=a_scale, w=w_q, w_scale=w_scale, align=align,
           topk_weights=topk_weights, out=None, M=M, top_k=top_k, BM=128, a_layout=a_layout, out_layout=OUT_GROUPED,
           d_status=d_status, stream=stream,
@@ -509,10 +515,10 @@ def moe_gemm_w8a8_silu_fp8_token(a_q: torch.Tensor, a_scale: torch.Tensor, w_q: 
         _need(topk_weights, torch.float32, "topk_weights")
     E, N, _ = w_q.shape
     I, T = N // 2, M * top_k
-    q = q if q is not None else torch.empty(T, I, dtype=torch.uint8, device=a_q.device)
-    scale = scale if scale is not None else torch.empty(T, dtype=torch.float32, device=a_q.device)
+    q = q if q is not None else _empty(T, I, dtype=torch.uint8, device=a_q.device)
+    scale = scale if scale is not None else _empty(T, dtype=torch.float32, device=a_q.device)
     if h_scratch is None:
-        h_scratch = torch.empty(T * I + T, dtype=torch.float32, device=a_q.device)
+        h_scratch = _empty(T * I + T, dtype=torch.float32, device=a_q.device)
     elif h_scratch.dtype != torch.float32 or h_scratch.numel() < T * I + T:
         raise QmoeError("h_scratch must be fp32 with at least T*I + T elements")
     _gemm("qmoe_moe_gemm_w8a8_silu_fp8_token", a=a_q, a_scale=a_scale, w=w_q, w_scale=w_scale, align=align,
@@ -617,10 +623,10 @@ def _act_quant(fn_name, gated, y, mode, expert_offsets, sf_padded_offsets, sf_ro
         raise QmoeError("y must be a 2-D CUDA bf16 tensor with unit column stride")
     rows, width = y.shape
     I = width // 2 if gated else width
-    q = q if q is not None else torch.empty(rows, I, dtype=torch.uint8, device=y.device)
+    q = q if q is not None else _empty(rows, I, dtype=torch.uint8, device=y.device)
     fn = getattr(load_library(), fn_name)
     if mode == SCALE_PER_TOKEN:
-        scale = scale if scale is not None else torch.empty(rows, dtype=torch.float32, device=y.device)
+        scale = scale if scale is not None else _empty(rows, dtype=torch.float32, device=y.device)
         st = fn(_ptr(y), rows, I, y.stride(0), mode, _ptr(q), _ptr(scale), None, 0, None, None, 1, _ptr(d_status),
                 _stream(stream))
         _check(st, fn_name)
@@ -632,7 +638,7 @@ def _act_quant(fn_name, gated, y, mode, expert_offsets, sf_padded_offsets, sf_ro
     if sf is None:
         if sf_rows is None:
             raise QmoeError("sf_rows (capacity of the scale-factor matrix) is required when sf is not given")
-        sf = torch.empty(sf_rows, ld, dtype=torch.uint8, device=y.device)
+        sf = _empty(sf_rows, ld, dtype=torch.uint8, device=y.device)
     st = fn(_ptr(y), rows, I, y.stride(0), mode, _ptr(q), None, _ptr(sf), sf.stride(0), _ptr(expert_offsets),
             _ptr(sf_padded_offsets), E, _ptr(d_status), _stream(stream))
     _check(st, fn_name)
@@ -643,7 +649,7 @@ def _act_quant(fn_name, gated, y, mode, expert_offsets, sf_padded_offsets, sf_ro
 def debug_e4m3_encode(x: torch.Tensor, stream=None) -> torch.Tensor:
     """Test hook: the kernels' fp32 -> e4m3 conversion (RNE, satfinite) applied elementwise."""
     _need(x, torch.float32, "x")
-    q = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+    q = _empty(x.shape, dtype=torch.uint8, device=x.device)
     _check(load_library().qmoe_debug_e4m3_encode(_ptr(x), _ptr(q), x.numel(), _stream(stream)), "debug_e4m3_encode")
     return q
 
@@ -651,7 +657,7 @@ def debug_e4m3_encode(x: torch.Tensor, stream=None) -> torch.Tensor:
 def debug_int8_to_bf16(x: torch.Tensor, stream=None) -> torch.Tensor:
     """Test hook: the W8A16 converters' int8 -> bf16 conversion applied elementwise."""
     _need(x, torch.int8, "x")
-    y = torch.empty(x.shape, dtype=torch.bfloat16, device=x.device)
+    y = _empty(x.shape, dtype=torch.bfloat16, device=x.device)
     _check(load_library().qmoe_debug_int8_to_bf16(_ptr(x), _ptr(y), x.numel(), _stream(stream)),
            "debug_int8_to_bf16")
     return y
@@ -661,7 +667,7 @@ def debug_silu_mul(g: torch.Tensor, u: torch.Tensor, stream=None) -> torch.Tenso
     """Test hook: h = silu(g) * u by the kernels' packed fp32 sequence, elementwise."""
     _need(g, torch.float32, "g")
     _need(u, torch.float32, "u")
-    h = torch.empty_like(g)
+    h = _empty(g.shape, dtype=g.dtype, device=g.device)
     _check(load_library().qmoe_debug_silu_mul(_ptr(g), _ptr(u), _ptr(h), g.numel(), _stream(stream)),
            "debug_silu_mul")
     return h
@@ -670,7 +676,7 @@ def debug_silu_mul(g: torch.Tensor, u: torch.Tensor, stream=None) -> torch.Tenso
 def debug_rcp_ge1(d: torch.Tensor, stream=None) -> torch.Tensor:
     """Test hook: the SiLU's reciprocal 1/d for d >= 1, elementwise."""
     _need(d, torch.float32, "d")
-    y = torch.empty_like(d)
+    y = _empty(d.shape, dtype=d.dtype, device=d.device)
     _check(load_library().qmoe_debug_rcp_ge1(_ptr(d), _ptr(y), d.numel(), _stream(stream)), "debug_rcp_ge1")
     return y
 
@@ -678,7 +684,7 @@ def debug_rcp_ge1(d: torch.Tensor, stream=None) -> torch.Tensor:
 def debug_div_by_scale(x: torch.Tensor, s: float, stream=None) -> torch.Tensor:
     """Test hook: the quantisers' division x / s by a row scale (packed pairs), elementwise."""
     _need(x, torch.float32, "x")
-    q = torch.empty_like(x)
+    q = _empty(x.shape, dtype=x.dtype, device=x.device)
     _check(load_library().qmoe_debug_div_by_scale(_ptr(x), float(s), _ptr(q), x.numel(), _stream(stream)),
            "debug_div_by_scale")
     return q
