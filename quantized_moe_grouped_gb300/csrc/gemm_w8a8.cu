@@ -46,6 +46,12 @@ extern "C" qmoe_status_t qmoe_moe_gemm_w8a8(const qmoe_gemm_args* args, qmoe_str
     return qmoe::run_moe_gemm<false>(args, stream);
 }
 
+extern "C" qmoe_status_t qmoe_debug_moe_gemm_w8a8_tile(const qmoe_gemm_args* args, int32_t tile,
+                                                       qmoe_stream_t stream) {
+    if (tile < qmoe::kTileAuto || tile > qmoe::kTilePair) return QMOE_ERR_INVALID_ARG;
+    return qmoe::run_moe_gemm<false>(args, stream, nullptr, false, static_cast<qmoe::GemmTile>(tile));
+}
+
 extern "C" qmoe_status_t qmoe_moe_gemm_w8a8_silu_mxfp8(const qmoe_gemm_args* args, uint8_t* q, uint8_t* sf,
                                                       int64_t sf_ld, const int32_t* sf_padded_offsets,
                                                       qmoe_stream_t stream) {
