@@ -10,17 +10,27 @@
 namespace qmoe {
 
 // ======================================================================
-// moe_align_block_size: one CTA of 1024 threads.
-//   1. histogram of expert ids in shared memory;
-//   2. exclusive prefix sums (unpadded and padded to BM) by one thread;
-//   3. sentinel fill of sorted_ids and the block -> expert map;
-//   4. stable scatter in chunks of 1024 slots: the rank of a slot among the
-//      slots of its expert in the same warp comes from __match_any_sync, the
-//      offset of the warp from a per-expert scan over the 32 warps, and the
-//      offset of the chunk from a running per-expert cursor.
+// moe_align_block_size: one CTA of 1024 threads; warp w owns the contiguous
+// slot range [w * chunk, (w + 1) * chunk) (chunk a multiple of 32).
+//   1. per-warp expert counts: the warp walks its range 32 slots at a time
+//      (the ids of 8 steps loaded together, kept in registers for step 3 when
+//      the range is at most 256 slots);
+//      __match_any_sync groups equal ids, the group's first lane adds the
+//      group size to the warp's own counter row (no atomics);
+//   2. per expert, an exclusive scan over the 32 warps (the warp's first
+//      position inside the expert's group) and the expert totals; then the
+//      unpadded and padded prefix sums (one thread), sentinel fill and the
+//      block -> expert map;
+//   3. the warp walks its range again: a slot's position is its expert's
+//      padded offset + the warp's running cursor for the expert + its rank
+//      among the equal ids of lower lanes; the group's first lane advances
+//      the cursor.  Ranges, steps and lanes are in ascending slot order, so
+//      the placement is stable.
 // ======================================================================
 constexpr int kAlignThreads = 1024;
 constexpr int kAlignMaxE = 256;
+constexpr int kAlignBatch = 8;  // 32-slot steps whose ids a lane loads at once
+
 
 __global__ void __launch_bounds__(kAlignThreads, 1)
     align_kernel(const int32_t* __restrict__ ids, int64_t T, int E, int BM, int32_t* __restrict__ sorted_ids,
@@ -31,24 +41,52 @@ __global__ void __launch_bounds__(kAlignThreads, 1)
     pdl_wait();  // inputs from, and buffers shared with, the previous kernel
     __shared__ int s_cnt[kAlignMaxE];
     __shared__ int s_poff[kAlignMaxE + 1];
-    __shared__ int s_cursor[kAlignMaxE];
-    __shared__ int s_wcnt[32 * kAlignMaxE];
+    __shared__ int s_wcnt[32 * kAlignMaxE];  // [warp][expert]: counts, then running positions
     __shared__ int s_bad;
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
+    const int64_t chunk = ((T + 31) / 32 + 31) / 32 * 32;
+    const int64_t w_begin = warp * chunk;
+    const int64_t w_end = w_begin + chunk < T ? w_begin + chunk : T;
 
-    for (int e = tid; e < E; e += blockDim.x) {
-        s_cnt[e] = 0;
-        s_cursor[e] = 0;
-    }
     for (int i = tid; i < 32 * E; i += blockDim.x) s_wcnt[i] = 0;
     if (tid == 0) s_bad = 0;
     __syncthreads();
 
-    for (int64_t s = tid; s < T; s += blockDim.x) {
-        const int e = ids[s];
-        if (e >= 0 && e < E) atomicAdd(&s_cnt[e], 1);
-        else s_bad = 1;
+    const unsigned lt_mask = (1u << lane) - 1u;
+    int* wrow = s_wcnt + warp * E;
+    // ids of kAlignBatch 32-slot steps per lane, loaded together (one memory latency per batch)
+    int ev[kAlignBatch];
+    auto load_batch = [&](int64_t base) {
+#pragma unroll
+        for (int i = 0; i < kAlignBatch; ++i) {
+            const int64_t sl = base + i * 32 + lane;
+            ev[i] = (sl < w_end) ? ids[sl] : -1;
+        }
+    };
+    const bool one_batch = chunk <= 32 * kAlignBatch;  // the range's ids stay in registers for pass 3
+    for (int64_t b0 = w_begin; b0 < w_end; b0 += 32 * kAlignBatch) {
+        load_batch(b0);
+#pragma unroll
+        for (int i = 0; i < kAlignBatch; ++i) {
+            const int e = ev[i];
+            const bool valid = e >= 0 && e < E;
+            if (b0 + i * 32 + lane < w_end && !valid) s_bad = 1;
+            const unsigned peers = __match_any_sync(0xFFFFFFFFu, valid ? e : E);
+            if (valid && (peers & lt_mask) == 0) wrow[e] += __popc(peers);
+            __syncwarp();
+        }
+    }
+    __syncthreads();
+
+    for (int e = tid; e < E; e += blockDim.x) {
+        int run = 0;
+        for (int w = 0; w < 32; ++w) {
+            const int c = s_wcnt[w * E + e];
+            s_wcnt[w * E + e] = run;
+            run += c;
+        }
+        s_cnt[e] = run;
     }
     __syncthreads();
 
@@ -87,31 +125,22 @@ __global__ void __launch_bounds__(kAlignThreads, 1)
     }
     __syncthreads();
 
-    const unsigned lt_mask = (1u << lane) - 1u;
-    for (int64_t base = 0; base < T; base += blockDim.x) {
-        const int64_t s = base + tid;
-        int e = (s < T) ? ids[s] : -1;
-        const bool valid = (e >= 0 && e < E);
-        const int key = valid ? e : E;  // invalid slots only match each other
-        const unsigned peers = __match_any_sync(0xFFFFFFFFu, key);
-        const int rank = __popc(peers & lt_mask);
-        const int leader = __ffs(peers) - 1;
-        if (valid && lane == leader) s_wcnt[warp * E + e] = __popc(peers);
-        __syncthreads();
-        for (int ee = tid; ee < E; ee += blockDim.x) {
-            int run = s_cursor[ee];
-            for (int w = 0; w < 32; ++w) {
-                const int c = s_wcnt[w * E + ee];
-                s_wcnt[w * E + ee] = run;
-                run += c;
+    for (int64_t b0 = w_begin; b0 < w_end; b0 += 32 * kAlignBatch) {
+        if (!one_batch) load_batch(b0);
+#pragma unroll
+        for (int i = 0; i < kAlignBatch; ++i) {
+            const int64_t sl = b0 + i * 32 + lane;
+            const int e = ev[i];
+            const bool valid = e >= 0 && e < E;
+            const unsigned peers = __match_any_sync(0xFFFFFFFFu, valid ? e : E);
+            const int cur = valid ? wrow[e] : 0;
+            __syncwarp();
+            if (valid) {
+                sorted_ids[s_poff[e] + cur + __popc(peers & lt_mask)] = static_cast<int32_t>(sl);
+                if ((peers & lt_mask) == 0) wrow[e] = cur + __popc(peers);
             }
-            s_cursor[ee] = run;
+            __syncwarp();
         }
-        __syncthreads();
-        if (valid) sorted_ids[s_poff[e] + s_wcnt[warp * E + e] + rank] = static_cast<int32_t>(s);
-        __syncthreads();
-        for (int i = tid; i < 32 * E; i += blockDim.x) s_wcnt[i] = 0;
-        __syncthreads();
     }
 }
 
@@ -289,6 +318,117 @@ __global__ void __launch_bounds__(kRowThreads)
                     float v[8];
                     unpack8(xv[j], v);
                     *reinterpret_cast<uint2*>(qr + c) = quant8(v, sc, rinv);
+                }
+            }
+        }
+    }
+}
+
+// The same codes and scales, one warp per TOKEN: the token row is read and
+// quantised once and its codes and scale are written to every padded
+// position of the token's top_k slots.  Each CTA (16 warps) first inverts
+// sorted_ids into a slot -> position table in shared memory (T <=
+// kTokMaxSlots, 16-byte loads); pad positions are zero-filled by the same
+// grid.  Rows of up to kWarpVec * 8 * 32 values stay in registers; longer
+// rows take an amax pass and a code pass over batches of kWarpVec vectors
+// (the second read mostly hits L1/L2), which keeps the registers per thread,
+// and so the warps in flight per SM, where the per-position kernel has them.
+constexpr int kTokThreads = 512;
+constexpr int kTokMaxSlots = 8192;
+__global__ void __launch_bounds__(kTokThreads)
+    quant_tokens_fp8_scatter_kernel(const uint16_t* __restrict__ x, int64_t cols, int64_t ldx,
+                                    const int32_t* __restrict__ sorted_ids, const int32_t* __restrict__ npp,
+                                    int64_t M, int top_k, uint8_t* __restrict__ q, float* __restrict__ scale) {
+    __shared__ int32_t s_pos[kTokMaxSlots];
+    pdl_launch_dependents();
+    pdl_wait();  // inputs from, and buffers shared with, the previous kernel
+    const int64_t T = M * top_k;
+    const int64_t n = *npp;
+    for (int64_t i = threadIdx.x; i < T; i += kTokThreads) s_pos[i] = -1;
+    __syncthreads();
+    {
+        // sorted_ids (16-byte aligned, as every tensor the library takes) in 16-byte vectors
+        const int64_t nv = n / 4;
+        const int4* sv = reinterpret_cast<const int4*>(sorted_ids);
+        for (int64_t v0 = threadIdx.x; v0 < nv; v0 += kTokThreads * 4) {
+            int4 w[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int64_t v = v0 + i * kTokThreads;
+                w[i] = v < nv ? sv[v] : make_int4(-1, -1, -1, -1);
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int32_t p = static_cast<int32_t>(4 * (v0 + i * kTokThreads));
+                if (w[i].x >= 0 && w[i].x < T) s_pos[w[i].x] = p;
+                if (w[i].y >= 0 && w[i].y < T) s_pos[w[i].y] = p + 1;
+                if (w[i].z >= 0 && w[i].z < T) s_pos[w[i].z] = p + 2;
+                if (w[i].w >= 0 && w[i].w < T) s_pos[w[i].w] = p + 3;
+            }
+        }
+        for (int64_t p = 4 * nv + threadIdx.x; p < n; p += kTokThreads) {
+            const int sl = sorted_ids[p];
+            if (sl >= 0 && sl < T) s_pos[sl] = static_cast<int32_t>(p);
+        }
+    }
+    __syncthreads();
+    const int lane = threadIdx.x & 31;
+    const int64_t gw = static_cast<int64_t>(blockIdx.x) * (kTokThreads / 32) + (threadIdx.x >> 5);
+    const int64_t nw = static_cast<int64_t>(gridDim.x) * (kTokThreads / 32);
+    for (int64_t p0 = gw * 32; p0 < n; p0 += nw * 32) {  // pad positions, 32 checked per warp step
+        const int64_t p = p0 + lane;
+        const int sl = p < n ? sorted_ids[p] : 0;
+        unsigned pads = __ballot_sync(0xFFFFFFFFu, p < n && (sl < 0 || sl >= T));
+        while (pads) {
+            const int64_t pp = p0 + __ffs(pads) - 1;
+            pads &= pads - 1;
+            uint8_t* qr = q + pp * cols;
+            for (int64_t c = static_cast<int64_t>(lane) * 16; c < cols; c += 32 * 16)
+                *reinterpret_cast<uint4*>(qr + c) = make_uint4(0u, 0u, 0u, 0u);
+            if (lane == 0) scale[pp] = 0.0f;
+        }
+    }
+    const bool in_regs = cols <= static_cast<int64_t>(kWarpVec) * 8 * 32;
+    constexpr int64_t kBatch = static_cast<int64_t>(kWarpVec) * 32 * 8;  // values per batch of loads
+    for (int64_t m = gw; m < M; m += nw) {
+        const uint16_t* xr = x + m * ldx;
+        const int32_t* tpos = s_pos + m * top_k;
+        uint4 xv[kWarpVec];
+        auto load_batch = [&](int64_t c0) {
+#pragma unroll
+            for (int j = 0; j < kWarpVec; ++j) {
+                const int64_t c = c0 + (static_cast<int64_t>(j) * 32 + lane) * 8;
+                xv[j] = (c < cols) ? *reinterpret_cast<const uint4*>(xr + c) : make_uint4(0u, 0u, 0u, 0u);
+            }
+        };
+        float amax = 0.0f;
+        for (int64_t c0 = 0; c0 < cols; c0 += kBatch) {
+            load_batch(c0);
+#pragma unroll
+            for (int j = 0; j < kWarpVec; ++j) {
+                float v[8];
+                unpack8(xv[j], v);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+        const float sc = (amax == 0.0f) ? 1.0f : __fdiv_rn(amax, 448.0f);
+        const float rinv = __frcp_rn(sc);
+        if (lane < top_k && tpos[lane] >= 0) scale[tpos[lane]] = sc;
+        for (int64_t c0 = 0; c0 < cols; c0 += kBatch) {
+            if (!in_regs) load_batch(c0);
+#pragma unroll
+            for (int j = 0; j < kWarpVec; ++j) {
+                const int64_t c = c0 + (static_cast<int64_t>(j) * 32 + lane) * 8;
+                if (c >= cols) break;
+                float v[8];
+                unpack8(xv[j], v);
+                const uint2 code = quant8(v, sc, rinv);
+                for (int t = 0; t < top_k; ++t) {
+                    const int32_t pt = tpos[t];
+                    if (pt >= 0) *reinterpret_cast<uint2*>(q + static_cast<int64_t>(pt) * cols + c) = code;
                 }
             }
         }
@@ -1051,6 +1191,27 @@ qmoe_status_t qmoe_quant_act_fp8_sorted(const uint16_t* x, int64_t M, int64_t co
         cap > 0x7FFFFFFF)
         return QMOE_ERR_INVALID_ARG;
     const int64_t sms = device_sm_count() > 0 ? device_sm_count() : 132;
+    // one warp per token (every row read and quantised once) while the slot -> position
+    // table fits in shared memory and the row in registers
+    const int64_t T = M * top_k;
+    if (T <= kTokMaxSlots && M > 0 && aligned16(sorted_ids)) {
+        static int per_sm_cache[64] = {0};
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return QMOE_ERR_CUDA;
+        if (per_sm_cache[dev] == 0) {
+            int per_sm = 0;
+            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, quant_tokens_fp8_scatter_kernel, kTokThreads,
+                                                              0) != cudaSuccess ||
+                per_sm < 1)
+                per_sm = 1;
+            per_sm_cache[dev] = per_sm;
+        }
+        const int64_t want = (M + kTokThreads / 32 - 1) / (kTokThreads / 32);
+        const int64_t most = sms * per_sm_cache[dev];
+        const int64_t blocks = want < most ? want : most;
+        return launch_pdl(quant_tokens_fp8_scatter_kernel, dim3(static_cast<unsigned>(blocks)), dim3(kTokThreads), 0,
+                          stream, x, cols, ldx, sorted_ids, num_post_padded, M, top_k, q, scale);
+    }
     // rows of 4097..8192 values: bulk copies, at least two in flight per CTA (measured at 6144 values: 37 us
     // against 43 for the warp kernel; at 4096 values the warp kernel is the faster, 31 against 33 us)
     if (cols > 4096 && cols * 2 <= kBulkRowsBytes / 2) {

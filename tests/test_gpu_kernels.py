@@ -220,6 +220,42 @@ def test_fused_align_quant_bitexact(q, orc, M, K, E, top_k, BM):
     assert np.array_equal(ss.cpu().numpy()[valid], rs[srt[valid] // top_k])
 
 
+@pytest.mark.parametrize("M,K,E,top_k,BM,misaligned", [
+    (300, 512, 6, 3, 64, False),     # one warp per token (slot table in shared memory), top_k = 3
+    (300, 512, 6, 3, 64, True),      # sorted_ids only 4-byte aligned: one warp per padded position
+    (5000, 256, 8, 2, 128, False),   # T = 10000 > 8192 slots: one warp per padded position
+    (4200, 6144, 8, 2, 128, False),  # T = 8400 > 8192, rows of 6144 values: bulk row copies
+])
+def test_quant_act_fp8_sorted_bitexact(q, orc, M, K, E, top_k, BM, misaligned):
+    """Every kernel behind quant_act_fp8_sorted: valid padded positions hold the
+    oracle's per-token codes and scale of the slot's token, pad positions zero
+    codes and scale 0; a slot with an invalid expert id is not placed."""
+    x = inputs.activations_bf16(M, K, seed=M + K)
+    ids, _ = inputs.routing(M, E, top_k, seed=M + K)
+    ids[3, 0] = E + 5
+    st = status()
+    al = q.moe_align_block_size(to_dev(ids), E, BM, d_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == q.DEV_INVALID_EXPERT
+    if misaligned:
+        buf = torch.empty(al["sorted_ids"].numel() + 1, dtype=torch.int32, device=dev())
+        buf[1:].copy_(al["sorted_ids"])
+        al = dict(al, sorted_ids=buf[1:])
+    qq, ss = q.quant_act_fp8_sorted(to_dev_bf16(x), al, top_k)
+    torch.cuda.synchronize()
+    ref = orc.moe_align(ids, E, BM)
+    rq, rs = orc.quant_rows_fp8_bf16(x)
+    srt = ref["sorted_ids"][: ref["num_post_padded"]]
+    T = M * top_k
+    valid = np.nonzero(srt < T)[0]
+    pads = np.nonzero(srt >= T)[0]
+    qn, sn = qq.cpu().numpy(), ss.cpu().numpy()
+    assert np.array_equal(qn[valid], rq[srt[valid] // top_k])
+    assert np.array_equal(sn[valid], rs[srt[valid] // top_k])
+    assert not np.any(qn[pads]) and not np.any(sn[pads])
+    assert 3 * top_k not in set(srt[valid].tolist())
+
+
 def test_silu_reciprocal_exhaustive(q):
     """The reciprocal in the SiLU, 1/d with d = 1 + exp(-g) >= 1, equals IEEE
     fp32 division (numpy) bit for bit for every fp32 d in [1, 2^126), and for
