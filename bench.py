@@ -15,7 +15,9 @@ value  = algorithmic bytes of the four GEMMs / device time of the timed steps
 e2e    = the same metric through the public API with pinned host buffers: per
          step the activations and routing go host -> device and the outputs
          device -> host inside the timed region (copies on their own streams,
-         overlapping the kernels of other shapes).
+         overlapping the kernels of other shapes); the calls of up to 100 steps are
+         captured into a CUDA graph that is replayed (the figure with every call
+         enqueued by the host as it runs is reported beside it).
 roofline = the grouped GEMM kernel alone (CUDA events around each launch).
 layers = the compute-bound M=4096 up and down GEMMs of the Mixtral-8x7B- and
          8x22B-shaped layers, each timed alone (median of 20 launches after an
@@ -788,7 +790,6 @@ def main() -> None:
     # end-to-end through the public API with pinned host buffers
     h2d = sum(sh["a_h"].numel() * 2 + sh["ids_h"].numel() * 4 + sh["tw_h"].numel() * 4 for sh in shapes)
     d2h = sum(sh["out_h"].numel() * 2 for sh in shapes)
-    e2e_steps = max(3, min(args.steps, 200))
     # Copies run on their own streams and overlap the kernels: a shape's inputs
     # go host -> device once the previous step's kernels of that shape are done
     # with them, its kernels wait for that copy and for the previous copy-out
@@ -799,38 +800,74 @@ def main() -> None:
     ev_in = [torch.cuda.Event() for _ in shapes]
     ev_gemm = [torch.cuda.Event() for _ in shapes]
     ev_done = [torch.cuda.Event() for _ in shapes]
-    for i in range(n_sh):
-        ev_gemm[i].record(stream)
-        ev_done[i].record(d2h_streams[i % 2])
-    barrier()
-    torch.cuda.synchronize()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    h2d_stream.wait_event(e0)
-    for _ in range(e2e_steps):
-        for i, sh in enumerate(shapes):
-            h2d_stream.wait_event(ev_gemm[i])
-            with torch.cuda.stream(h2d_stream):
-                sh["a"].copy_(sh["a_h"], non_blocking=True)
-                sh["ids"].copy_(sh["ids_h"], non_blocking=True)
-                sh["tw"].copy_(sh["tw_h"], non_blocking=True)
-            ev_in[i].record(h2d_stream)
-            stream.wait_event(ev_in[i])
-            stream.wait_event(ev_done[i])
-            run_path(q, wq, ws, sh, stream)
-            ev_gemm[i].record(stream)
-            out_stream = d2h_streams[i % 2]
-            out_stream.wait_event(ev_gemm[i])
-            with torch.cuda.stream(out_stream):
-                sh["out_h"].copy_(sh["out"], non_blocking=True)
-            ev_done[i].record(out_stream)
-    for ev in ev_done:
-        stream.wait_event(ev)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+
+    def enqueue_e2e(cs, n_steps):
+        """n_steps of the path with their host copies, issued on compute stream cs
+        (the copy streams fork from it and join it again at the end)."""
+        fork = torch.cuda.Event()
+        fork.record(cs)
+        for st_ in (h2d_stream, *d2h_streams):
+            st_.wait_event(fork)
+        for i in range(n_sh):
+            ev_gemm[i].record(cs)
+            ev_done[i].record(d2h_streams[i % 2])
+        for _ in range(n_steps):
+            for i, sh in enumerate(shapes):
+                h2d_stream.wait_event(ev_gemm[i])
+                with torch.cuda.stream(h2d_stream):
+                    sh["a"].copy_(sh["a_h"], non_blocking=True)
+                    sh["ids"].copy_(sh["ids_h"], non_blocking=True)
+                    sh["tw"].copy_(sh["tw_h"], non_blocking=True)
+                ev_in[i].record(h2d_stream)
+                cs.wait_event(ev_in[i])
+                cs.wait_event(ev_done[i])
+                run_path(q, wq, ws, sh, cs)
+                ev_gemm[i].record(cs)
+                out_stream = d2h_streams[i % 2]
+                out_stream.wait_event(ev_gemm[i])
+                with torch.cuda.stream(out_stream):
+                    sh["out_h"].copy_(sh["out"], non_blocking=True)
+                ev_done[i].record(out_stream)
+        for ev in ev_done:
+            cs.wait_event(ev)
+
+    def timed_e2e(run, n_steps):
+        barrier()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        run()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / n_steps
+
+    e2e_steps = max(3, min(args.steps, 200))
+    # (a) every call enqueued by the host as it runs
+    enqueue_e2e(stream, 2)
+    e2e_eager_ms = timed_e2e(lambda: enqueue_e2e(stream, e2e_steps), e2e_steps)
+    # (b) the same calls captured once into a CUDA graph of G steps and replayed:
+    # what a serving loop does to take the host's enqueue time off the GPU's path
+    e2e_mode = "cuda graph"
+    graph_steps = min(e2e_steps, 100)
+    replays = max(1, e2e_steps // graph_steps)
+    try:
+        cap = torch.cuda.Stream(dev)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=cap):
+            enqueue_e2e(cap, graph_steps)
+        graph.replay()
+        torch.cuda.synchronize()
+
+        def replay_all():
+            for _ in range(replays):
+                graph.replay()
+        e2e_ms = timed_e2e(replay_all, replays * graph_steps)
+    except Exception as exc:  # reported in the line, not hidden
+        e2e_mode = f"host-enqueued (graph capture failed: {type(exc).__name__}: {exc})"
+        e2e_ms = e2e_eager_ms
     e2e_ms = max_over_ranks(e2e_ms, world, dev)
+    e2e_eager_ms = max_over_ranks(e2e_eager_ms, world, dev)
 
     # the compute-bound M=4096 layer GEMMs, timed alone with their own clock record
     layers = None
@@ -881,7 +918,8 @@ def main() -> None:
             "vs_baseline_note": f"page aggregate over the same sweep: {page_gbs:.0f} GB/s, {page_tflops:.0f} TFLOPS "
                                 "(ROCm GPU, unnamed)",
             "e2e": {"value": whole_job_rate(step_bytes, e2e_ms * 1e-3, world) / 1e9, "unit": "GB/s",
-                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "how": e2e_mode,
+                    "host_enqueued_value": whole_job_rate(step_bytes, e2e_eager_ms * 1e-3, world) / 1e9},
             "gpu_launches": 2 * n_sh * args.steps,
             "clocks": clk,
             "cpu_baseline": cpu,
