@@ -468,13 +468,17 @@ qmoe_status_t qmoe_debug_div_by_scale(const float* x, float s, float* q, int64_t
 /* y[i] = 1/d[i] with the reciprocal the SiLU uses (correctly rounded, for
  * d >= 1): the exhaustive check of that sequence. */
 qmoe_status_t qmoe_debug_rcp_ge1(const float* d, float* y, int64_t n, qmoe_stream_t stream);
-/* qmoe_moe_gemm_w8a8 with its tile family chosen by the caller, so that tests
- * and timings can run each family on any shape: tile 0 = the library's own
- * choice (exactly qmoe_moe_gemm_w8a8), 1 = one CTA per tile, 2 = CTA pairs
- * (two SMs per 256 x 256 tile through tcgen05 cta_group::2; FP8 per-row
- * activation scales, GROUPED or PADDED activation rows and BM >= 128, else
- * QMOE_ERR_UNSUPPORTED).  Any other value returns QMOE_ERR_INVALID_ARG. */
-qmoe_status_t qmoe_debug_moe_gemm_w8a8_tile(const qmoe_gemm_args* args, int32_t tile, qmoe_stream_t stream);
+/* A grouped GEMM with its tile family chosen by the caller, so that tests and
+ * timings can run each family on any shape.  weights: 0 = qmoe_moe_gemm_w8a8,
+ * 1 = qmoe_moe_gemm_w8a16, 2 = qmoe_moe_gemm_w4a16 (same arguments and
+ * checks).  tile 0 = the library's own choice (exactly that entry point),
+ * 1 = one CTA per tile, 2 = CTA pairs (two SMs per 256 x 256 tile through
+ * tcgen05 cta_group::2; GROUPED or PADDED activation rows, per-token FP8
+ * activation scales with BM >= 128 or bf16 activations, else
+ * QMOE_ERR_UNSUPPORTED).  Any other weights or tile value returns
+ * QMOE_ERR_INVALID_ARG. */
+qmoe_status_t qmoe_debug_moe_gemm_tile(const qmoe_gemm_args* args, int32_t weights, int32_t tile,
+                                       qmoe_stream_t stream);
 
 #ifdef __cplusplus
 }

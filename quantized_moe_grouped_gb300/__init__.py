@@ -35,7 +35,7 @@ EXPORTED = (
     "qmoe_moe_gemm_w8a8_token_sum_noalloc", "qmoe_quant_weight_mxfp8", "qmoe_quant_mxfp8", "qmoe_quant_mxfp8_colwise",
     "qmoe_mx_weight_sf_tiled_bytes", "qmoe_mx_weight_sf_tiled", "qmoe_quant_weight_int4", "qmoe_moe_gemm_w4a16",
     "qmoe_moe_gemm_w8a8_silu_mxfp8", "qmoe_moe_gemm_w8a8_silu_fp8_token", "qmoe_debug_rcp_ge1",
-    "qmoe_debug_moe_gemm_w8a8_tile",
+    "qmoe_debug_moe_gemm_tile",
 )
 TILE_AUTO, TILE_ONE_SM, TILE_PAIR = 0, 1, 2
 NOALLOC_ACCUM_MAX_ELEMS = 4 << 20
@@ -111,7 +111,7 @@ def load_library(path: str | None = None):
             L.qmoe_debug_div_by_scale.argtypes = [vp, ctypes.c_float, vp, i64, vp]
             L.qmoe_debug_rcp_ge1.argtypes = [vp, vp, i64, vp]
             L.qmoe_debug_wait_timeout.argtypes = [vp, i64, vp]
-            L.qmoe_debug_moe_gemm_w8a8_tile.argtypes = [ctypes.POINTER(GemmArgs), i32, vp]
+            L.qmoe_debug_moe_gemm_tile.argtypes = [ctypes.POINTER(GemmArgs), i32, i32, vp]
             for name in EXPORTED:
                 if name not in ("qmoe_status_string", "qmoe_version", "qmoe_align_max_padded"):
                     getattr(L, name).restype = st
@@ -447,7 +447,7 @@ def moe_gemm_w8a8(a_q: torch.Tensor, a_scale: torch.Tensor | None, w_q: torch.Te
     fp32 [M, N] scratch the sum needs, allocated here when not given).  MXFP8 weights:
     w_scale_mode=SCALE_MX_1X32 with w_sf = mx_weight_sf_tiled(factors of quant_weight_mxfp8),
     w_scale then optional; needs MX activations.  tile (tests and timing only): TILE_ONE_SM
-    or TILE_PAIR forces that tile family (qmoe_debug_moe_gemm_w8a8_tile)."""
+    or TILE_PAIR forces that tile family (qmoe_debug_moe_gemm_tile)."""
     _need(a_q, torch.uint8, "a_q")
     _need(w_q, torch.uint8, "w_q")
     if a_scale_mode == SCALE_PER_TOKEN:
@@ -464,11 +464,12 @@ def moe_gemm_w8a8(a_q: torch.Tensor, a_scale: torch.Tensor | None, w_q: torch.Te
     if topk_weights is not None:
         _need(topk_weights, torch.float32, "topk_weights")
     out = _out_for(out, out_layout, M, top_k, w_q.shape[1], a_q.device)
-    return _gemm("qmoe_moe_gemm_w8a8" if tile is None else "qmoe_debug_moe_gemm_w8a8_tile", a=a_q, a_scale=a_scale, w=w_q, w_scale=w_scale, align=align,
-                 topk_weights=topk_weights, out=out, M=M, top_k=top_k, BM=BM, a_layout=a_layout,
-                 out_layout=out_layout, d_status=d_status, accum=accum, a_scale_mode=a_scale_mode, a_sf=a_sf,
-                 a_sf_padded_offsets=a_sf_padded_offsets, stream=stream, w_scale_mode=w_scale_mode, w_sf=w_sf,
-                 extra=() if tile is None else (ctypes.c_int32(tile),))
+    return _gemm("qmoe_moe_gemm_w8a8" if tile is None else "qmoe_debug_moe_gemm_tile", a=a_q, a_scale=a_scale,
+                 w=w_q, w_scale=w_scale, align=align, topk_weights=topk_weights, out=out, M=M, top_k=top_k, BM=BM,
+                 a_layout=a_layout, out_layout=out_layout, d_status=d_status, accum=accum,
+                 a_scale_mode=a_scale_mode, a_sf=a_sf, a_sf_padded_offsets=a_sf_padded_offsets, stream=stream,
+                 w_scale_mode=w_scale_mode, w_sf=w_sf,
+                 extra=() if tile is None else (ctypes.c_int32(0), ctypes.c_int32(tile)))
 
 
 def moe_gemm_w8a8_silu_mxfp8(a_q: torch.Tensor, a_scale: torch.Tensor, w_q: torch.Tensor, w_scale: torch.Tensor,
@@ -570,35 +571,39 @@ def moe_gemm_w8a16(a: torch.Tensor, w_q: torch.Tensor, w_scale: torch.Tensor, al
                    topk_weights: torch.Tensor | None, *, M: int, top_k: int, BM: int,
                    a_layout: int = A_TOKEN_GATHER, out_layout: int = OUT_SLOT, out: torch.Tensor | None = None,
                    d_status: torch.Tensor | None = None, accum: torch.Tensor | None = None,
-                   stream=None) -> torch.Tensor:
-    """INT8 W8A16 grouped GEMM: a bf16 [rows, K], w_q int8 [E, N, K], w_scale fp32 [E, N]."""
+                   stream=None, tile: int | None = None) -> torch.Tensor:
+    """INT8 W8A16 grouped GEMM: a bf16 [rows, K], w_q int8 [E, N, K], w_scale fp32 [E, N].
+    tile (tests and timing only): TILE_ONE_SM or TILE_PAIR forces that tile family."""
     _need(a, torch.bfloat16, "a")
     _need(w_q, torch.int8, "w_q")
     _need(w_scale, torch.float32, "w_scale")
     if topk_weights is not None:
         _need(topk_weights, torch.float32, "topk_weights")
     out = _out_for(out, out_layout, M, top_k, w_q.shape[1], a.device)
-    return _gemm("qmoe_moe_gemm_w8a16", a=a, a_scale=None, w=w_q, w_scale=w_scale, align=align,
-                 topk_weights=topk_weights, out=out, M=M, top_k=top_k, BM=BM, a_layout=a_layout,
-                 out_layout=out_layout, d_status=d_status, accum=accum, stream=stream)
+    return _gemm("qmoe_moe_gemm_w8a16" if tile is None else "qmoe_debug_moe_gemm_tile", a=a, a_scale=None, w=w_q,
+                 w_scale=w_scale, align=align, topk_weights=topk_weights, out=out, M=M, top_k=top_k, BM=BM,
+                 a_layout=a_layout, out_layout=out_layout, d_status=d_status, accum=accum, stream=stream,
+                 extra=() if tile is None else (ctypes.c_int32(1), ctypes.c_int32(tile)))
 
 
 def moe_gemm_w4a16(a: torch.Tensor, w_q: torch.Tensor, w_scale: torch.Tensor, align: dict,
                    topk_weights: torch.Tensor | None, *, M: int, top_k: int, BM: int,
                    a_layout: int = A_TOKEN_GATHER, out_layout: int = OUT_SLOT, out: torch.Tensor | None = None,
                    d_status: torch.Tensor | None = None, accum: torch.Tensor | None = None,
-                   stream=None) -> torch.Tensor:
+                   stream=None, tile: int | None = None) -> torch.Tensor:
     """INT4 W4A16 grouped GEMM: a bf16 [rows, K], w_q packed int4 uint8 [E, N, K/2],
-    w_scale fp32 group scales [E, N, K/128] (quant_weight_int4); BM 128 or 256."""
+    w_scale fp32 group scales [E, N, K/128] (quant_weight_int4); BM 128 or 256.
+    tile (tests and timing only): TILE_ONE_SM or TILE_PAIR forces that tile family."""
     _need(a, torch.bfloat16, "a")
     _need(w_q, torch.uint8, "w_q")
     _need(w_scale, torch.float32, "w_scale")
     if topk_weights is not None:
         _need(topk_weights, torch.float32, "topk_weights")
     out = _out_for(out, out_layout, M, top_k, w_q.shape[1], a.device)
-    return _gemm("qmoe_moe_gemm_w4a16", a=a, a_scale=None, w=w_q, w_scale=w_scale, align=align,
-                 topk_weights=topk_weights, out=out, M=M, top_k=top_k, BM=BM, a_layout=a_layout,
-                 out_layout=out_layout, d_status=d_status, accum=accum, stream=stream, K=2 * w_q.shape[2])
+    return _gemm("qmoe_moe_gemm_w4a16" if tile is None else "qmoe_debug_moe_gemm_tile", a=a, a_scale=None, w=w_q,
+                 w_scale=w_scale, align=align, topk_weights=topk_weights, out=out, M=M, top_k=top_k, BM=BM,
+                 a_layout=a_layout, out_layout=out_layout, d_status=d_status, accum=accum, stream=stream,
+                 K=2 * w_q.shape[2], extra=() if tile is None else (ctypes.c_int32(2), ctypes.c_int32(tile)))
 
 
 # ------------------------------------------------------ SwiGLU + quant ---

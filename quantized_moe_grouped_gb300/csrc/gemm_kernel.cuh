@@ -1077,7 +1077,12 @@ qmoe_status_t launch_token_sum_finalize(const float* accum, uint16_t* out, int64
 qmoe_status_t launch_gemm_pair(const void* w, int64_t E, int64_t N, int64_t K, const GemmParams& p,
                                int64_t max_padded, int64_t a_rows, int64_t lda, cudaStream_t st);
 
-// Tile family of the FP8 GEMM: the library's choice, or one forced by a test.
+// INT8 / INT4 weight-only GEMM on CTA pairs (defined in gemm_pair_a16.cu): bf16
+// activation tiles by TMA (GROUPED / PADDED rows).
+qmoe_status_t launch_gemm_pair_a16(bool int4, const void* w, int64_t E, int64_t N, int64_t K, const GemmParams& p,
+                                   int64_t max_padded, int64_t a_rows, int64_t lda, cudaStream_t st);
+
+// Tile family of the GEMMs: the library's choice, or one forced by a test.
 enum GemmTile { kTileAuto = 0, kTileOneSm = 1, kTilePair = 2 };
 
 // Outputs of the SwiGLU epilogues: MXFP8 codes and factors
@@ -1144,8 +1149,9 @@ inline qmoe_status_t run_moe_gemm(const qmoe_gemm_args* a, cudaStream_t st, cons
                   : (!so->q || !so->sf || !so->sf_poff || !aligned16(so->q) || so->sf_ld < a->N / 64))
             return QMOE_ERR_INVALID_ARG;
     }
-    // CTA-pair tile: FP8 with per-row scales, contiguous activation rows, BM >= 128
-    const bool pair_ok = !kBF16 && !mx && !wmx && !so && a->a_layout != QMOE_A_TOKEN_GATHER && a->BM >= 128;
+    // CTA-pair tile: per-row (FP8, INT8) or per-group (INT4) weight scales, per-token or bf16
+    // activations in contiguous rows; FP8 with BM >= 128
+    const bool pair_ok = !mx && !wmx && !so && a->a_layout != QMOE_A_TOKEN_GATHER && (kBF16 || a->BM >= 128);
     if (tile == kTilePair && !pair_ok) return QMOE_ERR_UNSUPPORTED;
     // The library's choice (measured on the Mixtral-shaped projections, E = 8): the pair
     // tile for long K at 256-512 slots per expert on average (down projections at
@@ -1157,7 +1163,11 @@ inline qmoe_status_t run_moe_gemm(const qmoe_gemm_args* a, cudaStream_t st, cons
     const int64_t slots_per_expert = a->M * a->top_k / a->E;
     const bool pair_auto = (a->K >= 8192 && slots_per_expert >= 256 && slots_per_expert <= 512) ||
                            (a->K < 8192 && slots_per_expert >= 96 && slots_per_expert <= 160);
-    const bool use_pair = pair_ok && (tile == kTilePair || (tile == kTileAuto && pair_auto));
+    // INT8 / INT4 weights: the pair tile from 1024 slots per expert (M = 4096 at N = 14336:
+    // W8A16 870 -> 854 us, W4A16 1016 -> 943 us); at decode its 256 x 32 MMAs issue at
+    // about 170 cycles each and the one-SM wide tile is faster (125 against 184 us at M = 64)
+    const bool pair_auto_a16 = slots_per_expert >= 1024;
+    const bool use_pair = pair_ok && (tile == kTilePair || (tile == kTileAuto && (kBF16 ? pair_auto_a16 : pair_auto)));
     if (check_only) return QMOE_OK;
 
     const bool tsum = a->out_layout == QMOE_OUT_TOKEN_SUM;
@@ -1215,6 +1225,12 @@ inline qmoe_status_t run_moe_gemm(const qmoe_gemm_args* a, cudaStream_t st, cons
     // the kernel numbers its tiles (slot blocks x weight blocks) with 32-bit ints
     if (max_padded / 16 * ((a->N + 127) / 128) >= (int64_t(1) << 31)) return QMOE_ERR_UNSUPPORTED;
     qmoe_status_t r;
+    if (use_pair) {
+        r = kBF16 ? launch_gemm_pair_a16(kI4, a->w, a->E, a->N, a->K, p, max_padded, a_rows, a->lda, st)
+                  : launch_gemm_pair(a->w, a->E, a->N, a->K, p, max_padded, a_rows, a->lda, st);
+        if (r != QMOE_OK || !tsum) return r;
+        return launch_token_sum_finalize(a->accum, a->out, a->M * a->N, st);
+    }
     if constexpr (kI4) {
         r = launch_gemm<true, true, 128, false, true>(a->w, a->E, a->N, a->K, p, max_padded, a_rows, a->lda, st);
         if (r != QMOE_OK || !tsum) return r;
@@ -1233,11 +1249,7 @@ inline qmoe_status_t run_moe_gemm(const qmoe_gemm_args* a, cudaStream_t st, cons
             return launch_token_sum_finalize(a->accum, a->out, a->M * a->N, st);
         }
     }
-    if (use_pair) {
-        r = launch_gemm_pair(a->w, a->E, a->N, a->K, p, max_padded, a_rows, a->lda, st);
-        if (r != QMOE_OK || !tsum) return r;
-        return launch_token_sum_finalize(a->accum, a->out, a->M * a->N, st);
-    }
+
     if constexpr (!kBF16) {
         // long K (e.g. a down projection): one weight pass for two 128-slot
         // blocks, which halves the weight-operand reads per MMA; at short K the

@@ -46,10 +46,16 @@ extern "C" qmoe_status_t qmoe_moe_gemm_w8a8(const qmoe_gemm_args* args, qmoe_str
     return qmoe::run_moe_gemm<false>(args, stream);
 }
 
-extern "C" qmoe_status_t qmoe_debug_moe_gemm_w8a8_tile(const qmoe_gemm_args* args, int32_t tile,
-                                                       qmoe_stream_t stream) {
+extern "C" qmoe_status_t qmoe_debug_moe_gemm_tile(const qmoe_gemm_args* args, int32_t weights, int32_t tile,
+                                                  qmoe_stream_t stream) {
     if (tile < qmoe::kTileAuto || tile > qmoe::kTilePair) return QMOE_ERR_INVALID_ARG;
-    return qmoe::run_moe_gemm<false>(args, stream, nullptr, false, static_cast<qmoe::GemmTile>(tile));
+    const qmoe::GemmTile t = static_cast<qmoe::GemmTile>(tile);
+    switch (weights) {
+        case 0: return qmoe::run_moe_gemm<false>(args, stream, nullptr, false, t);
+        case 1: return qmoe::run_moe_gemm<true>(args, stream, nullptr, false, t);
+        case 2: return qmoe::run_moe_gemm<true, true>(args, stream, nullptr, false, t);
+        default: return QMOE_ERR_INVALID_ARG;
+    }
 }
 
 extern "C" qmoe_status_t qmoe_moe_gemm_w8a8_silu_mxfp8(const qmoe_gemm_args* args, uint8_t* q, uint8_t* sf,

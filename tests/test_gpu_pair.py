@@ -128,3 +128,83 @@ def test_regular_entry_point_takes_the_pair_tile_for_long_k(q, orc):
                        topk_ids=ids, topk_w=tw, E=E, a_layout="grouped", out_layout="token_sum")
     ok, ratio = orc.gemm_tolerance_ok(bf16_to_np_f32(out), ref)
     assert ok, f"worst |err|/bound = {ratio:.3f}"
+
+
+@pytest.mark.parametrize("kind", ["int8", "int4"])
+@pytest.mark.parametrize("a_layout,out_layout", [(1, 0), (2, 1), (2, 2), (1, 2)])
+@pytest.mark.parametrize("M,K,N,E,top_k,BM,zipf", [
+    (64, 256, 512, 8, 2, 128, None),       # decode-like: about 16 slots per expert (32-slot tiles)
+    (520, 384, 272, 8, 2, 128, 1.2),       # N % 256 = 16, skewed experts
+    (90, 512, 528, 5, 3, 64, None),        # top_k = 3, BM = 64
+    (1100, 256, 1024, 8, 2, 128, None),    # more tiles than CTA pairs, full 256-slot tiles
+])
+def test_pair_tile_a16_parity(q, orc, kind, a_layout, out_layout, M, K, N, E, top_k, BM, zipf):
+    """The weight-only GEMMs (INT8 per-row scales, INT4 per-group scales) on the
+    CTA-pair tile against the oracle's fp64 dequantisation."""
+    if kind == "int4":
+        BM = max(BM, 128)  # the W4A16 entry point takes BM 128 or 256
+    a = inputs.activations_bf16(M, K, seed=M + N + a_layout)
+    w = inputs.expert_weights_f32(E, N, K, seed=M + N)
+    ids, tw = inputs.routing(M, E, top_k, seed=M + N, zipf_s=zipf)
+    T = M * top_k
+    al = q.moe_align_block_size(to_dev(ids), E, BM)
+    if a_layout == q.A_GROUPED:
+        pos = orc.compact_row_of_slot(ids, E)
+        order = np.empty(T, dtype=np.int64)
+        order[pos] = np.arange(T)
+        a_in = np.ascontiguousarray(a[order // top_k])
+        a_dev = to_dev_bf16(a_in)
+        ref_layout = "grouped"
+    else:
+        a_dev = q.gather_sorted_bf16(to_dev_bf16(a), al, top_k)
+        a_in, ref_layout = a, "token"
+    if kind == "int8":
+        wq, ws = q.quant_weight_int8(to_dev(w))
+        rwq, rws = orc.quant_rows_int8_f32(w)
+        gemm, w_kind = q.moe_gemm_w8a16, orc.W_INT8
+    else:
+        wq, ws = q.quant_weight_int4(to_dev(w))
+        rwq, rws = orc.quant_rows_int4_f32(w)
+        gemm, w_kind = q.moe_gemm_w4a16, orc.W_INT4
+    assert np.array_equal(wq.cpu().numpy(), rwq)
+    st = status()
+    out = gemm(a_dev, wq, ws, al, to_dev(tw), M=M, top_k=top_k, BM=BM, a_layout=a_layout, out_layout=out_layout,
+               d_status=st, tile=q.TILE_PAIR)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0, f"device status {int(st.item())}"
+    ref = orc.moe_gemm(a_kind=orc.A_BF16, a=a_in, w_kind=w_kind, w=rwq, w_scale=rws, topk_ids=ids, topk_w=tw,
+                       E=E, a_layout=ref_layout, out_layout={0: "slot", 1: "grouped", 2: "token_sum"}[out_layout])
+    gpu = bf16_to_np_f32(out)
+    assert np.all(np.isfinite(gpu))
+    ok, ratio = orc.gemm_tolerance_ok(gpu, ref)
+    assert ok, f"worst |err|/bound = {ratio:.3f}"
+
+
+@pytest.mark.parametrize("kind", ["int8", "int4"])
+def test_regular_a16_entry_points_take_the_pair_tile_at_large_m(q, orc, kind):
+    """qmoe_moe_gemm_w8a16 / _w4a16 themselves at 1024 slots per expert (the
+    library sends these to the pair tile), padded rows, routing weights."""
+    M, K, N, E, top_k, BM = 4096, 256, 512, 8, 2, 128
+    a = inputs.activations_bf16(M, K, 77)
+    w = inputs.expert_weights_f32(E, N, K, 77)
+    ids, tw = inputs.routing(M, E, top_k, 77)
+    al = q.moe_align_block_size(to_dev(ids), E, BM)
+    ap = q.gather_sorted_bf16(to_dev_bf16(a), al, top_k)
+    if kind == "int8":
+        wq, ws = q.quant_weight_int8(to_dev(w))
+        rwq, rws = orc.quant_rows_int8_f32(w)
+        gemm, w_kind = q.moe_gemm_w8a16, orc.W_INT8
+    else:
+        wq, ws = q.quant_weight_int4(to_dev(w))
+        rwq, rws = orc.quant_rows_int4_f32(w)
+        gemm, w_kind = q.moe_gemm_w4a16, orc.W_INT4
+    st = status()
+    out = gemm(ap, wq, ws, al, to_dev(tw), M=M, top_k=top_k, BM=BM, a_layout=q.A_PADDED, d_status=st)
+    one = gemm(ap, wq, ws, al, to_dev(tw), M=M, top_k=top_k, BM=BM, a_layout=q.A_PADDED, d_status=st,
+               tile=q.TILE_ONE_SM)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    assert torch.equal(out, one)   # both families give the same bytes on this shape
+    ref = orc.moe_gemm(a_kind=orc.A_BF16, a=a, w_kind=w_kind, w=rwq, w_scale=rws, topk_ids=ids, topk_w=tw, E=E)
+    ok, ratio = orc.gemm_tolerance_ok(bf16_to_np_f32(out), ref)
+    assert ok, f"worst |err|/bound = {ratio:.3f}"
