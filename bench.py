@@ -26,6 +26,8 @@ layers = the compute-bound M=4096 up and down GEMMs of the Mixtral-8x7B- and
 cpu_baseline / --impl reference = the CPU oracle on a bounded sample of slots.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+       python bench.py --suite [--only TEXT]        (every other kernel, timed alone)
+       python bench.py --tile-sweep [--only TEXT]   (one-SM against CTA-pair GEMM tiles)
 """
 from __future__ import annotations
 
@@ -711,6 +713,82 @@ def run_suite(reps: int = 50, only: str | None = None) -> None:
         del up
 
 
+# ------------------------------------------------------------ tile sweep ---
+def run_tile_sweep(reps: int = 20, only: str | None = None, launches: int = 0) -> None:
+    """One-SM against CTA-pair tiles of the grouped GEMMs (forced through the
+    debug tile entry point) on the Mixtral-shaped projections and the W8A16 /
+    W4A16 sweep: median µs of `reps` launches each after a 512 MB L2 flush, one
+    JSON line per shape.  Weights are random codes with random scales (timing
+    only).  launches > 0: instead of timing, run that many launches of each
+    family per shape (a fixed launch list for a profiler)."""
+    import torch
+
+    import quantized_moe_grouped_gb300 as q
+    from quantized_moe_grouped_gb300 import inputs
+
+    q.load_library()
+    dev = torch.device("cuda", 0)
+    g = torch.Generator(device=dev).manual_seed(3)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    fp8 = [("fp8 up N=28672 K=4096", 28672, 4096, q.OUT_GROUPED, (1024, 2048, 4096), None),
+           ("fp8 down N=4096 K=14336", 4096, 14336, q.OUT_TOKEN_SUM, (1024, 2048, 4096), None),
+           ("fp8 up N=32768 K=6144 zipf1.2", 32768, 6144, q.OUT_GROUPED, (2048, 4096), 1.2),
+           ("fp8 down N=6144 K=16384", 6144, 16384, q.OUT_TOKEN_SUM, (1024, 2048, 4096), None),
+           ("fp8 decode N=14336 K=4096", 14336, 4096, q.OUT_SLOT, (256, 512, 1024), None)]
+    a16 = [("a16 N=14336 K=4096", 14336, 4096, (64, 1024, 4096)), ("a16 N=7168 K=4096", 7168, 4096, (64, 1024, 4096))]
+
+    def measure(fn):
+        if launches > 0:
+            for _ in range(launches):
+                fn()
+            torch.cuda.synchronize()
+            return float("nan")
+        return _timed(fn, reps, flush) * 1e3
+
+    for name, N, K, ol, Ms, zipf in fp8:
+        if only and only not in name:
+            continue
+        wq = torch.randint(0, 120, (E, N, K), device=dev, dtype=torch.uint8, generator=g)
+        ws = torch.rand(E, N, device=dev, generator=g)
+        for M in Ms:
+            ids, tw = inputs.routing(M, E, TOP_K, 7000 + M, zipf)
+            al = q.moe_align_block_size(torch.from_numpy(ids).to(dev), E, 128)
+            twd = torch.from_numpy(tw).to(dev)
+            a = torch.randn(M, K, device=dev, generator=g).to(torch.bfloat16)
+            aq, sa = q.quant_act_fp8_sorted(a, al, TOP_K)
+            out = torch.empty(M if ol == q.OUT_TOKEN_SUM else M * TOP_K, N, dtype=torch.bfloat16, device=dev)
+            acc = torch.empty(M, N, dtype=torch.float32, device=dev)
+            r = {"tile_sweep": name, "M": M}
+            for tile, key in ((q.TILE_ONE_SM, "one_sm_us"), (q.TILE_PAIR, "pair_us")):
+                r[key] = measure(lambda: q.moe_gemm_w8a8(aq, sa, wq, ws, al, twd, M=M, top_k=TOP_K, BM=128,
+                                                         a_layout=q.A_PADDED, out_layout=ol, out=out, accum=acc,
+                                                         tile=tile))
+            print(json.dumps(r), flush=True)
+        del wq, ws
+        torch.cuda.empty_cache()
+    for name, N, K, Ms in a16:
+        if only and only not in name:
+            continue
+        w8 = torch.randint(-127, 128, (E, N, K), device=dev, dtype=torch.int16, generator=g).to(torch.int8)
+        s8 = torch.rand(E, N, device=dev, generator=g) * 1e-2
+        w4 = torch.randint(0, 256, (E, N, K // 2), device=dev, dtype=torch.int16, generator=g).to(torch.uint8)
+        s4 = torch.rand(E, N, K // 128, device=dev, generator=g) * 1e-2
+        for M in Ms:
+            ids, tw = inputs.routing(M, E, TOP_K, 2000 + M)
+            al = q.moe_align_block_size(torch.from_numpy(ids).to(dev), E, 128)
+            twd = torch.from_numpy(tw).to(dev)
+            ap = q.gather_sorted_bf16(torch.randn(M, K, device=dev, generator=g).to(torch.bfloat16), al, TOP_K)
+            out = torch.empty(M * TOP_K, N, dtype=torch.bfloat16, device=dev)
+            r = {"tile_sweep": name, "M": M}
+            for kind, fn, ww, ss in (("w8a16", q.moe_gemm_w8a16, w8, s8), ("w4a16", q.moe_gemm_w4a16, w4, s4)):
+                for tile, key in ((q.TILE_ONE_SM, "one_sm_us"), (q.TILE_PAIR, "pair_us")):
+                    r[f"{kind}_{key}"] = measure(lambda: fn(ap, ww, ss, al, twd, M=M, top_k=TOP_K, BM=128,
+                                                            a_layout=q.A_PADDED, out=out, tile=tile))
+            print(json.dumps(r), flush=True)
+        del w8, w4
+        torch.cuda.empty_cache()
+
+
 # ------------------------------------------------------------------ main ---
 def main() -> None:
     ap = argparse.ArgumentParser()
@@ -723,10 +801,17 @@ def main() -> None:
     ap.add_argument("--only", default=None, help="--suite: workloads whose name contains this text")
     ap.add_argument("--reps", type=int, default=50, help="--suite: timed repetitions per kernel (median)")
     ap.add_argument("--no-layers", action="store_true", help="skip the M=4096 layer GEMM timings")
+    ap.add_argument("--tile-sweep", action="store_true",
+                    help="one-SM against CTA-pair tiles of the grouped GEMMs (--only filters the shapes)")
+    ap.add_argument("--launches", type=int, default=0,
+                    help="--tile-sweep: run this many launches per family and shape instead of timing")
     ap.add_argument("--layer-reps", type=int, default=20, help="timed launches per M=4096 layer GEMM (median)")
     args = ap.parse_args()
     if args.suite:
         run_suite(args.reps, args.only)
+        return
+    if args.tile_sweep:
+        run_tile_sweep(args.reps if args.reps != 50 else 20, args.only, args.launches)
         return
     args.warmup = max(args.warmup, 3)
     if args.impl == "reference":
@@ -910,7 +995,8 @@ def main() -> None:
             "data": "synthetic",
             "config": {"workload": WORKLOAD, "BM": [sh["BM"] for sh in shapes], "l2": "inputs larger than L2 "
                        "(470 MB of e4m3 weights streamed by every GEMM)", "parallelism": f"replicas x{world}"},
-            "roofline": {"bound": "hbm", "kernel": "moe_gemm_kernel<fp8>", "achieved": achieved, "peak": peak,
+            "roofline": {"bound": "hbm", "kernel": "grouped GEMM (moe_gemm_kernel<fp8> at M=64..256, "
+                         "moe_gemm_pair_kernel at M=512)", "achieved": achieved, "peak": peak,
                          "peak_kind": f"{peak_kind} (hbm_gbs, burst)", "unit": "GB/s", "frac": achieved / peak,
                          "traffic": recorded_traffic(), "algorithmic_bytes": step_bytes,
                          "per": "one step = the four GEMM launches of the sweep"},
