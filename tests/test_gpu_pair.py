@@ -1,10 +1,11 @@
-"""GPU parity of the FP8 grouped GEMM's CTA-pair tile (two SMs per 256 x 256
-tile, tcgen05 cta_group::2) against the CPU oracle, forced on every shape
-through qmoe_debug_moe_gemm_w8a8_tile: grouped and padded activation rows,
-every output layout, ragged N and K tails, empty experts, skewed routing,
-top_k = 3, more tiles than CTA pairs, and experts whose last slot pair holds a
-single or a partly filled 128-slot block.  Bound:
-|gpu - oracle| <= 8e-3 |oracle| + 1e-2 rms(oracle)."""
+"""GPU parity of the grouped GEMMs' CTA-pair tiles (two SMs per 256 x 256
+tile, tcgen05 cta_group::2; FP8 W8A8 and the INT8 / INT4 weight-only GEMMs)
+against the CPU oracle, forced on every shape through qmoe_debug_moe_gemm_tile:
+grouped and padded activation rows, every output layout, ragged N and K tails,
+empty experts, skewed routing, top_k = 3, more tiles than CTA pairs, and
+experts whose last slot pair holds a single or a partly filled 128-slot block;
+and the regular entry points on shapes the library sends to the pair tiles.
+Bound: |gpu - oracle| <= 8e-3 |oracle| + 1e-2 rms(oracle)."""
 import numpy as np
 import pytest
 import torch
