@@ -145,6 +145,179 @@ __global__ void __launch_bounds__(kAlignThreads, 1)
 }
 
 // ======================================================================
+// moe_align_block_size for many slots: a cluster of kAlignCtas CTAs (16 warps
+// each).  Global warp g = rank * 16 + warp owns slots [g * chunk, (g+1) *
+// chunk), so ranks, warps, steps and lanes run in ascending slot order.
+//   1. per-warp expert counts, as in align_kernel;
+//   2. per expert, an exclusive scan over the CTA's warps and the CTA's total;
+//      cluster barrier; each CTA reads the other CTAs' totals through
+//      distributed shared memory (its own offset inside every expert's group
+//      and the expert totals); cluster barrier (no CTA leaves while another
+//      may still read its shared memory);
+//   3. every CTA computes the padded offsets; CTA 0 writes them; the CTAs
+//      split the sentinel fill of the pad positions and the block -> expert
+//      map; each warp places its slots.
+// Pad positions and slot positions are disjoint, so the fill and the scatter
+// need no ordering between CTAs.
+// ======================================================================
+constexpr int kAlignCtas = 8;
+constexpr int kAlignCThreads = 512;
+constexpr int64_t kAlignClusterMinSlots = 2048;
+constexpr int kAlignCWarps = kAlignCThreads / 32;
+
+QMOE_DI uint32_t align_cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+// A 32-bit word of CTA `rank`'s shared memory at the offset of `p` in this CTA.
+QMOE_DI int load_cluster_peer(const int* p, uint32_t rank) {
+    uint32_t a;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(smem_u32(p)), "r"(rank));
+    int v;
+    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(a));
+    return v;
+}
+QMOE_DI void align_cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__global__ void __launch_bounds__(kAlignCThreads, 1)
+    align_cluster_kernel(const int32_t* __restrict__ ids, int64_t T, int E, int BM, int32_t* __restrict__ sorted_ids,
+                         int64_t sorted_cap, int32_t* __restrict__ expert_ids, int64_t blocks_cap,
+                         int32_t* __restrict__ num_post_padded, int32_t* __restrict__ expert_offsets,
+                         int32_t* __restrict__ padded_offsets, int32_t* d_status) {
+    pdl_launch_dependents();
+    pdl_wait();  // inputs from, and buffers shared with, the previous kernel
+    __shared__ int s_wcnt[kAlignCWarps * kAlignMaxE];  // [warp][expert]: counts, then running positions
+    __shared__ int s_ccnt[kAlignMaxE];                  // this CTA's count per expert (read by the others)
+    __shared__ int s_coff[kAlignMaxE];                  // this CTA's first position inside each expert's group
+    __shared__ int s_cnt[kAlignMaxE];
+    __shared__ int s_poff[kAlignMaxE + 1];
+    __shared__ int s_bad;
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    const uint32_t rank = align_cluster_rank();
+    const int64_t nwarps = static_cast<int64_t>(kAlignCtas) * kAlignCWarps;
+    const int64_t chunk = ((T + nwarps - 1) / nwarps + 31) / 32 * 32;
+    const int64_t gw = static_cast<int64_t>(rank) * kAlignCWarps + warp;
+    const int64_t w_begin = gw * chunk < T ? gw * chunk : T;
+    const int64_t w_end = w_begin + chunk < T ? w_begin + chunk : T;
+
+    for (int i = tid; i < kAlignCWarps * E; i += blockDim.x) s_wcnt[i] = 0;
+    if (tid == 0) s_bad = 0;
+    __syncthreads();
+
+    const unsigned lt_mask = (1u << lane) - 1u;
+    int* wrow = s_wcnt + warp * E;
+    int ev[kAlignBatch];
+    auto load_batch = [&](int64_t base) {
+#pragma unroll
+        for (int i = 0; i < kAlignBatch; ++i) {
+            const int64_t sl = base + i * 32 + lane;
+            ev[i] = (sl < w_end) ? ids[sl] : -1;
+        }
+    };
+    const bool one_batch = chunk <= 32 * kAlignBatch;
+    for (int64_t b0 = w_begin; b0 < w_end; b0 += 32 * kAlignBatch) {
+        load_batch(b0);
+#pragma unroll
+        for (int i = 0; i < kAlignBatch; ++i) {
+            const int e = ev[i];
+            const bool valid = e >= 0 && e < E;
+            if (b0 + i * 32 + lane < w_end && !valid) s_bad = 1;
+            const unsigned peers = __match_any_sync(0xFFFFFFFFu, valid ? e : E);
+            if (valid && (peers & lt_mask) == 0) wrow[e] += __popc(peers);
+            __syncwarp();
+        }
+    }
+    __syncthreads();
+    for (int e = tid; e < E; e += blockDim.x) {
+        int run = 0;
+        for (int w = 0; w < kAlignCWarps; ++w) {
+            const int c = s_wcnt[w * E + e];
+            s_wcnt[w * E + e] = run;
+            run += c;
+        }
+        s_ccnt[e] = run;
+    }
+    align_cluster_sync();  // every CTA's totals are in its shared memory
+    for (int e = tid; e < E; e += blockDim.x) {
+        int v[kAlignCtas];  // all CTAs' counts, loaded together (one remote latency)
+#pragma unroll
+        for (int c = 0; c < kAlignCtas; ++c) v[c] = load_cluster_peer(&s_ccnt[e], static_cast<uint32_t>(c));
+        int before = 0, total = 0;
+#pragma unroll
+        for (int c = 0; c < kAlignCtas; ++c) {
+            if (c < static_cast<int>(rank)) before += v[c];
+            total += v[c];
+        }
+        s_coff[e] = before;
+        s_cnt[e] = total;
+    }
+    align_cluster_sync();  // no CTA reads another's shared memory after this point
+    if (tid == 0) {
+        int off = 0, poff = 0;
+        for (int e = 0; e < E; ++e) {
+            if (rank == 0) {
+                expert_offsets[e] = off;
+                padded_offsets[e] = poff;
+            }
+            s_poff[e] = poff;
+            off += s_cnt[e];
+            poff += (s_cnt[e] + BM - 1) / BM * BM;
+        }
+        s_poff[E] = poff;
+        if (rank == 0) {
+            expert_offsets[E] = off;
+            padded_offsets[E] = poff;
+            *num_post_padded = poff;
+        }
+        if (s_bad && d_status) atomicOr(reinterpret_cast<int*>(d_status), QMOE_DEV_INVALID_EXPERT);
+    }
+    __syncthreads();
+
+    // the expert owning padded position p (last e with s_poff[e] <= p), or -1 past the groups
+    auto owner_of = [&](int64_t p) {
+        if (p >= s_poff[E]) return -1;
+        int lo = 0, hi = E - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (s_poff[mid] <= p) lo = mid;
+            else hi = mid - 1;
+        }
+        return lo;
+    };
+    const int32_t sentinel = static_cast<int32_t>(T);
+    const int64_t stride = static_cast<int64_t>(kAlignCtas) * kAlignCThreads;
+    for (int64_t p = static_cast<int64_t>(rank) * kAlignCThreads + tid; p < sorted_cap; p += stride) {
+        const int e = owner_of(p);
+        if (e < 0 || p - s_poff[e] >= s_cnt[e]) sorted_ids[p] = sentinel;
+    }
+    for (int64_t b = static_cast<int64_t>(rank) * kAlignCThreads + tid; b < blocks_cap; b += stride)
+        expert_ids[b] = owner_of(b * BM);
+
+    for (int64_t b0 = w_begin; b0 < w_end; b0 += 32 * kAlignBatch) {
+        if (!one_batch) load_batch(b0);
+#pragma unroll
+        for (int i = 0; i < kAlignBatch; ++i) {
+            const int64_t sl = b0 + i * 32 + lane;
+            const int e = ev[i];
+            const bool valid = e >= 0 && e < E;
+            const unsigned peers = __match_any_sync(0xFFFFFFFFu, valid ? e : E);
+            const int cur = valid ? wrow[e] : 0;
+            __syncwarp();
+            if (valid) {
+                sorted_ids[s_poff[e] + s_coff[e] + cur + __popc(peers & lt_mask)] = static_cast<int32_t>(sl);
+                if ((peers & lt_mask) == 0) wrow[e] = cur + __popc(peers);
+            }
+            __syncwarp();
+        }
+    }
+}
+
+// ======================================================================
 // Per-row quantisers: one CTA per row.  Pass 1 takes the row's amax, pass 2
 // re-reads the row (L1/L2) and writes the codes.  The vector path moves 8
 // elements per step (16-byte bf16 or 2x16-byte fp32 loads, 8-byte stores).
@@ -1164,6 +1337,26 @@ qmoe_status_t qmoe_moe_align_block_size(const int32_t* topk_ids, int64_t T, int3
     if ((T > 0 && !topk_ids) || !sorted_ids || !expert_ids || !num_post_padded || !expert_offsets ||
         !padded_offsets)
         return QMOE_ERR_INVALID_ARG;
+    if (T >= kAlignClusterMinSlots) {  // a cluster of CTAs: more SMs on the per-slot work
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[2];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = kAlignCtas;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[1].val.programmaticStreamSerializationAllowed = 1;
+        cfg.gridDim = dim3(kAlignCtas);
+        cfg.blockDim = dim3(kAlignCThreads);
+        cfg.stream = stream;
+        cfg.attrs = attr;
+        cfg.numAttrs = 2;
+        return cudaLaunchKernelEx(&cfg, align_cluster_kernel, topk_ids, T, static_cast<int>(E), static_cast<int>(BM),
+                                  sorted_ids, cap, expert_ids, cap / BM, num_post_padded, expert_offsets,
+                                  padded_offsets, d_status) == cudaSuccess
+                   ? QMOE_OK
+                   : QMOE_ERR_CUDA;
+    }
     return launch_pdl(align_kernel, dim3(1), dim3(kAlignThreads), 0, stream, topk_ids, T, E, BM, sorted_ids, cap,
                       expert_ids, cap / BM, num_post_padded, expert_offsets, padded_offsets, d_status);
 }

@@ -78,8 +78,11 @@ def test_silu_sequence_exhaustive(q, orc):
 
 
 @pytest.mark.parametrize("M,E,BM", [(64, 8, 16), (64, 8, 32), (200, 8, 64), (4096, 8, 128), (4096, 8, 256),
-                                    (17, 3, 16), (1, 1, 16), (3000, 64, 32), (512, 256, 16)])
+                                    (17, 3, 16), (1, 1, 16), (3000, 64, 32), (512, 256, 16),
+                                    (1024, 256, 16), (1023, 8, 64), (20000, 8, 128)])
 def test_align_bitexact(q, orc, M, E, BM):
+    """Single-CTA kernel below 2048 slots, the cluster kernel from 2048 on (one
+    id batch per lane up to 32768 slots, several beyond)."""
     ids, _ = inputs.routing(M, E, 2 if E > 1 else 1, seed=M + E)
     st = status()
     al = q.moe_align_block_size(to_dev(ids), E, BM, d_status=st)
@@ -110,6 +113,16 @@ def test_align_skewed_empty_and_invalid(q, orc):
     refb = orc.moe_align(bad, 3, 16)
     assert int(st.item()) == q.DEV_INVALID_EXPERT and refb["invalid"]
     assert np.array_equal(alb["sorted_ids"].cpu().numpy(), refb["sorted_ids"])
+    # the same on the cluster kernel (several thousand slots, a few invalid ids in two CTAs' ranges)
+    big, _ = inputs.routing(3000, 8, 2, seed=4001)
+    big = big.ravel().copy()
+    big[[5, 4100, 5999]] = [8, -3, 100]
+    st = status()
+    alc = q.moe_align_block_size(to_dev(big), 8, 64, d_status=st)
+    refc = orc.moe_align(big, 8, 64)
+    assert int(st.item()) == q.DEV_INVALID_EXPERT and refc["invalid"]
+    assert np.array_equal(alc["sorted_ids"].cpu().numpy(), refc["sorted_ids"])
+    assert np.array_equal(alc["expert_ids"].cpu().numpy(), refc["expert_ids"][: alc["expert_ids"].numel()])
 
 
 @pytest.mark.parametrize("rows,cols", [(64, 128), (64, 4096), (333, 6144), (5, 100), (7, 24), (1, 8)])
