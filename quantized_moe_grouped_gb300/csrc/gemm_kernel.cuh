@@ -118,7 +118,10 @@ struct GemmCfg {
     static constexpr int kStageBytes = kWBytes + kActBytes;
     static constexpr int kStagesFit = (200 * 1024) / kStageBytes;
     static constexpr int kStages = kBF16 ? (kWide ? 3 : 4) : (kStagesFit > 8 ? 8 : kStagesFit);
-    static constexpr int kRawFit = kBF16 ? (200 * 1024 - kStages * kStageBytes) / (kRawBytes > 0 ? kRawBytes : 1) : 0;
+    // W8A16 / W4A16: the raw ring gets what the main ring leaves of 216 KB (the raw weight
+    // bytes in flight bound the decode stream: 3 -> 4 int8 stages took M = 64 at N = 14336
+    // from 125 to 121 us and M = 1024 from 289 to 278 us)
+    static constexpr int kRawFit = kBF16 ? (216 * 1024 - kStages * kStageBytes) / (kRawBytes > 0 ? kRawBytes : 1) : 0;
     static constexpr int kRawStages = kBF16 ? (kRawFit > 16 ? 16 : kRawFit) : 0;
     // cp.async completion lag (stages): the MMA can run kStages - kLag - 1 stages
     // ahead of the gather warps, so the lag shrinks when the ring is short.
