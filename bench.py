@@ -531,7 +531,10 @@ def run_suite(reps: int = 50, only: str | None = None) -> None:
         wq, ws = weights_int8(E, wl.N, wl.K)
         a = torch.from_numpy(inputs.activations_bf16(wl.M, wl.K, wl.seed).view(np.int16)).to(dev).view(torch.bfloat16)
         ids, tw = inputs.routing(wl.M, E, TOP_K, wl.seed)
-        BM = 128  # the wide tile: more weight bytes per bf16 MMA than the swapped one, also at decode
+        # the wide tile: more weight bytes per bf16 MMA than the swapped one, also at decode; 64 slots
+        # when every expert's slots fit one such tile (the weights are still read once, the bf16
+        # activation tile per stage halves)
+        BM = 64 if np.bincount(ids.ravel(), minlength=E).max() <= 64 else 128
         al = q.moe_align_block_size(torch.from_numpy(ids).to(dev), E, BM)
         twd = torch.from_numpy(tw).to(dev)
         out = torch.empty(wl.M * TOP_K, wl.N, dtype=torch.bfloat16, device=dev)
@@ -558,7 +561,7 @@ def run_suite(reps: int = 50, only: str | None = None) -> None:
             q.quant_weight_int4(w, q=wq[e], scale=ws[e])
         a = torch.from_numpy(inputs.activations_bf16(wl.M, wl.K, wl.seed).view(np.int16)).to(dev).view(torch.bfloat16)
         ids, tw = inputs.routing(wl.M, E, TOP_K, wl.seed)
-        BM = 128
+        BM = 64 if np.bincount(ids.ravel(), minlength=E).max() <= 64 else 128
         al = q.moe_align_block_size(torch.from_numpy(ids).to(dev), E, BM)
         twd = torch.from_numpy(tw).to(dev)
         out = torch.empty(wl.M * TOP_K, wl.N, dtype=torch.bfloat16, device=dev)

@@ -328,7 +328,7 @@ qmoe_status_t qmoe_moe_gemm_w8a8(const qmoe_gemm_args* args, qmoe_stream_t strea
  * exact for the scales qmoe_quant_weight_int4 writes (other scales: the
  * product is rounded to bf16).
  * Activation and output layouts as qmoe_moe_gemm_w8a16.  Limits: K % 128 == 0,
- * BM in {128, 256} (else QMOE_ERR_UNSUPPORTED), w_scale_mode PER_ROW. */
+ * BM in {64, 128, 256} (else QMOE_ERR_UNSUPPORTED), w_scale_mode PER_ROW. */
 qmoe_status_t qmoe_moe_gemm_w4a16(const qmoe_gemm_args* args, qmoe_stream_t stream);
 
 /* FP8 W8A8 grouped GEMM with the TOKEN_SUM layout that allocates nothing.

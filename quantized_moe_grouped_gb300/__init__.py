@@ -592,7 +592,7 @@ def moe_gemm_w4a16(a: torch.Tensor, w_q: torch.Tensor, w_scale: torch.Tensor, al
                    d_status: torch.Tensor | None = None, accum: torch.Tensor | None = None,
                    stream=None, tile: int | None = None) -> torch.Tensor:
     """INT4 W4A16 grouped GEMM: a bf16 [rows, K], w_q packed int4 uint8 [E, N, K/2],
-    w_scale fp32 group scales [E, N, K/128] (quant_weight_int4); BM 128 or 256.
+    w_scale fp32 group scales [E, N, K/128] (quant_weight_int4); BM 64, 128 or 256.
     tile (tests and timing only): TILE_ONE_SM or TILE_PAIR forces that tile family."""
     _need(a, torch.bfloat16, "a")
     _need(w_q, torch.uint8, "w_q")

@@ -154,15 +154,19 @@ struct GemmCfg {
     static constexpr int kSfaCol = kAccCols;
     static constexpr int kSfbCol = (kAccCols + 4 * kStages + 7) / 8 * 8;
     static constexpr int kTmemCols = (kMX || kW2) ? 512 : (2 * kAccCols < 32 ? 32 : 2 * kAccCols);
+    // MMA M: 128 rows, or 64 for the 64-slot wide bf16 tile (D row i then sits in TMEM
+    // lane 32 * (i / 16) + i % 16: each warp's lane quadrant holds 16 rows in lanes 0-15)
+    static constexpr int kMmaM = (kWide && BN == 64) ? 64 : 128;
+    static constexpr int kRowsPerQuad = kMmaM / 4;
     static constexpr uint32_t kIdesc =
-        kMX ? make_idesc_mx(128, kMmaN) : make_idesc(kBF16 ? kFmtBF16 : kFmtE4M3, 128, kMmaN);
+        kMX ? make_idesc_mx(128, kMmaN) : make_idesc(kBF16 ? kFmtBF16 : kFmtE4M3, kMmaM, kMmaN);
     // Tail split (plain FP8 wide tile): quarter tiles of 64 weight rows (MMA N = 64)
     static constexpr bool kTailSplit = kWide && !kBF16 && !kMX && kAct == 0 && !kW2;
     static constexpr int kQRows = 64;
     static constexpr uint32_t kIdescQ = make_idesc(kFmtE4M3, 128, kQRows);
     static_assert(!kMX || (kWide && !kBF16), "MX scales: FP8 wide tile only");
     static_assert(!kI4 || (kBF16 && kWide), "W4A16: wide bf16 tile only");
-    static_assert(!kWide || BN == 128 || BN == 256, "wide tile: 128 or 256 slots");
+    static_assert(!kWide || BN == 128 || BN == 256 || (BN == 64 && kBF16), "wide tile: 128 or 256 slots (64: bf16)");
     static_assert(!kW2 || (!kBF16 && !kMX), "two-half tile: FP8 with per-row scales only");
     static_assert(kAct == 0 || (kWide && BN == 128 && !kBF16 && !kMX), "SwiGLU epilogue: FP8 wide 128-slot tile only");
     static_assert(!kMX || kSfbCol + 8 * kStages <= 512, "TMEM columns");  // per-stage weight scales
@@ -677,8 +681,8 @@ __global__ void __launch_bounds__(GemmCfg<kBF16, kWide, BN, kMX, kI4, kAct>::kTh
                     s_wsc[c] = (n < p.N) ? (p.w_scale ? p.w_scale[static_cast<int64_t>(e) * p.N + n] : 1.0f) : 0.0f;
                 }
                 named_bar_sync(2, C::kEpiThreads);
-                const int pos = sb * SRB + hs * 128 + q * 32 + lane;
-                const bool in_tile = !C::kW2 || hs == 0 || second_half(e, sb);
+                const int pos = sb * SRB + hs * 128 + q * C::kRowsPerQuad + lane;
+                const bool in_tile = (!C::kW2 || hs == 0 || second_half(e, sb)) && lane < C::kRowsPerQuad;
                 const int s = in_tile ? p.sorted_ids[pos] : -1;
                 const bool valid = s >= 0 && s < p.T;
                 float rs = 0.0f;
@@ -1108,7 +1112,7 @@ inline qmoe_status_t run_moe_gemm(const qmoe_gemm_args* a, cudaStream_t st, cons
     static_assert(!kI4 || kBF16, "W4A16 is a bf16-activation GEMM");
     if (kI4 && a && a->struct_size >= sizeof(qmoe_gemm_args)) {
         // packed int4 weights with a scale per 128-wide group of K: wide tile only
-        if (a->BM != 128 && a->BM != 256) return QMOE_ERR_UNSUPPORTED;
+        if (a->BM != 64 && a->BM != 128 && a->BM != 256) return QMOE_ERR_UNSUPPORTED;
         if (a->K % 128 != 0 || a->w_scale_mode != QMOE_SCALE_PER_ROW) return QMOE_ERR_INVALID_ARG;
     }
     if (!a || a->struct_size < sizeof(qmoe_gemm_args)) return QMOE_ERR_INVALID_ARG;
@@ -1235,7 +1239,9 @@ inline qmoe_status_t run_moe_gemm(const qmoe_gemm_args* a, cudaStream_t st, cons
         return launch_token_sum_finalize(a->accum, a->out, a->M * a->N, st);
     }
     if constexpr (kI4) {
-        r = launch_gemm<true, true, 128, false, true>(a->w, a->E, a->N, a->K, p, max_padded, a_rows, a->lda, st);
+        r = a->BM == 64
+                ? launch_gemm<true, true, 64, false, true>(a->w, a->E, a->N, a->K, p, max_padded, a_rows, a->lda, st)
+                : launch_gemm<true, true, 128, false, true>(a->w, a->E, a->N, a->K, p, max_padded, a_rows, a->lda, st);
         if (r != QMOE_OK || !tsum) return r;
         return launch_token_sum_finalize(a->accum, a->out, a->M * a->N, st);
     }
@@ -1266,7 +1272,10 @@ inline qmoe_status_t run_moe_gemm(const qmoe_gemm_args* a, cudaStream_t st, cons
     switch (a->BM) {
         case 16: r = launch_gemm<kBF16, false, 16>(a->w, a->E, a->N, a->K, p, max_padded, a_rows, a->lda, st); break;
         case 32: r = launch_gemm<kBF16, false, 32>(a->w, a->E, a->N, a->K, p, max_padded, a_rows, a->lda, st); break;
-        case 64: r = launch_gemm<kBF16, false, 64>(a->w, a->E, a->N, a->K, p, max_padded, a_rows, a->lda, st); break;
+        case 64:  // bf16 activations: the 64-slot wide tile (M = 64 MMAs, 256 weight rows each)
+            r = kBF16 ? launch_gemm<true, true, 64, false, kI4>(a->w, a->E, a->N, a->K, p, max_padded, a_rows, a->lda, st)
+                      : launch_gemm<false, false, 64>(a->w, a->E, a->N, a->K, p, max_padded, a_rows, a->lda, st);
+            break;
         default: r = launch_gemm<kBF16, true, 128>(a->w, a->E, a->N, a->K, p, max_padded, a_rows, a->lda, st); break;
     }
     if (r != QMOE_OK || !tsum) return r;

@@ -97,7 +97,7 @@ _CASES = {
     "w8a16: lda < K": (1, lambda L, q: L.qmoe_moe_gemm_w8a16(_gemm_args(q, a_scale=None, lda=128), None)),
     "w8a16: activations not 16-byte aligned": (1, lambda L, q: L.qmoe_moe_gemm_w8a16(
         _gemm_args(q, a_scale=None, a=_U), None)),
-    "w4a16: BM below 128": (2, lambda L, q: L.qmoe_moe_gemm_w4a16(_gemm_args(q, a_scale=None, BM=64), None)),
+    "w4a16: BM below 64": (2, lambda L, q: L.qmoe_moe_gemm_w4a16(_gemm_args(q, a_scale=None, BM=32), None)),
     "w4a16: K not a multiple of 128": (1, lambda L, q: L.qmoe_moe_gemm_w4a16(
         _gemm_args(q, a_scale=None, K=192, lda=192), None)),
     "fused per-token SwiGLU: K % 16 != 0": (1, lambda L, q: L.qmoe_moe_gemm_w8a8_silu_fp8_token(

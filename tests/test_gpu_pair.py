@@ -142,8 +142,6 @@ def test_regular_entry_point_takes_the_pair_tile_for_long_k(q, orc):
 def test_pair_tile_a16_parity(q, orc, kind, a_layout, out_layout, M, K, N, E, top_k, BM, zipf):
     """The weight-only GEMMs (INT8 per-row scales, INT4 per-group scales) on the
     CTA-pair tile against the oracle's fp64 dequantisation."""
-    if kind == "int4":
-        BM = max(BM, 128)  # the W4A16 entry point takes BM 128 or 256
     a = inputs.activations_bf16(M, K, seed=M + N + a_layout)
     w = inputs.expert_weights_f32(E, N, K, seed=M + N)
     ids, tw = inputs.routing(M, E, top_k, seed=M + N, zipf_s=zipf)

@@ -97,7 +97,7 @@ def test_w8a16_readout(q, BM):
     assert bad.numel() == 0, (bad[:4].tolist(), got[tuple(bad[0])].item(), exp[tuple(bad[0])].item())
 
 
-@pytest.mark.parametrize("BM", [128, 256])
+@pytest.mark.parametrize("BM", [64, 128, 256])
 def test_w4a16_readout(q, BM):
     """Packed int4 (element 2j in the low nibble of byte j) times its group's
     scale (groups of 128 along K): every code in every nibble position."""

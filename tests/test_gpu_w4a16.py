@@ -40,7 +40,8 @@ def check(gpu, ref):
 
 @pytest.mark.parametrize("a_layout,out_layout", [(0, 0), (1, 2), (2, 1), (0, 2)])
 @pytest.mark.parametrize("M,K,N,E,top_k,BM,zipf", [(64, 256, 272, 8, 2, 128, None), (520, 384, 256, 8, 2, 128, 1.2),
-                                                   (90, 128, 528, 5, 3, 256, None), (1024, 256, 1024, 8, 2, 128, None)])
+                                                   (90, 128, 528, 5, 3, 256, None), (1024, 256, 1024, 8, 2, 128, None),
+                                                   (64, 256, 272, 8, 2, 64, None), (300, 384, 512, 6, 3, 64, 1.2)])
 def test_w4a16_parity(q, orc, a_layout, out_layout, M, K, N, E, top_k, BM, zipf):
     a = inputs.activations_bf16(M, K, seed=M + N)
     w = inputs.expert_weights_f32(E, N, K, seed=M + N)
