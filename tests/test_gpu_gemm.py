@@ -104,6 +104,88 @@ def test_w8a8_token_sum_deterministic(q, orc):
     assert all(torch.equal(outs[0], o) for o in outs[1:])
 
 
+@pytest.mark.parametrize("BM,K", [(128, 256), (256, 8192)])
+def test_w8a8_token_sum_deterministic_wide(q, orc, BM, K):
+    """The wide tiles (one 128-slot block, and two of them sharing each weight
+    stage at K >= 8192) add their slot results into the fp32 accumulator: for
+    top_k = 2 the sum 0 + a + b does not depend on the order, so repeated
+    launches agree bit for bit."""
+    M, N, E, top_k = 300, 272, 8, 2
+    p = fp8_problem(q, orc, M, K, N, E, top_k, seed=6)
+    al = q.moe_align_block_size(to_dev(p["ids"]), E, BM)
+    pos = orc.compact_row_of_slot(p["ids"], E)
+    order = np.empty(M * top_k, dtype=np.int64)
+    order[pos] = np.arange(M * top_k)
+    rows = to_dev(order // top_k)
+    aq_g, sa_g = p["aq"][rows].contiguous(), p["sa"][rows].contiguous()
+    outs = [q.moe_gemm_w8a8(aq_g, sa_g, p["wq"], p["ws"], al, to_dev(p["tw"]), M=M, top_k=top_k, BM=BM,
+                            a_layout=q.A_GROUPED, out_layout=q.OUT_TOKEN_SUM).clone() for _ in range(3)]
+    assert all(torch.equal(outs[0], o) for o in outs[1:])
+    ref = orc.moe_gemm(a_kind=orc.A_FP8_TOKEN, a=p["raq"][order // top_k], a_scale=p["rsa"][order // top_k],
+                       w_kind=orc.W_FP8, w=p["rwq"], w_scale=p["rws"], topk_ids=p["ids"], topk_w=p["tw"], E=E,
+                       a_layout="grouped", out_layout="token_sum")
+    check(bf16_to_np_f32(outs[0]), ref)
+
+
+@pytest.mark.parametrize("M,K,N,E,top_k,BM", [(96, 256, 400, 16, 8, 128), (130, 128, 528, 12, 5, 256),
+                                              (64, 128, 256, 8, 1, 128)])
+def test_w8a8_token_sum_large_top_k(q, orc, M, K, N, E, top_k, BM):
+    """TOKEN_SUM with up to eight contributions per token and output segment."""
+    p = fp8_problem(q, orc, M, K, N, E, top_k, seed=M + top_k)
+    al = q.moe_align_block_size(to_dev(p["ids"]), E, BM)
+    st = status()
+    out = q.moe_gemm_w8a8(p["aq"], p["sa"], p["wq"], p["ws"], al, to_dev(p["tw"]), M=M, top_k=top_k, BM=BM,
+                          out_layout=q.OUT_TOKEN_SUM, d_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    ref = orc.moe_gemm(a_kind=orc.A_FP8_TOKEN, a=p["raq"], a_scale=p["rsa"], w_kind=orc.W_FP8, w=p["rwq"],
+                       w_scale=p["rws"], topk_ids=p["ids"], topk_w=p["tw"], E=E, out_layout="token_sum")
+    check(bf16_to_np_f32(out), ref)
+
+
+@pytest.mark.parametrize("BM,K,a_layout", [(128, 256, 0), (64, 256, 0), (256, 8192, 1)])
+def test_w8a8_token_sum_dropped_slots(q, orc, BM, K, a_layout):
+    """Slots routed outside [0, E) are dropped by the align; their tokens then
+    have fewer than top_k contributions (some none at all): TOKEN_SUM gives
+    every token's sum over its valid slots, 0 for a token without any."""
+    M, N, E, top_k = 160, 272, 8, 2
+    p = fp8_problem(q, orc, M, K, N, E, top_k, seed=21)
+    ids = p["ids"].copy()
+    rng = np.random.default_rng(21)
+    drop = rng.random(ids.shape) < 0.15
+    ids[drop] = np.where(rng.random(ids.shape) < 0.5, -1, E + 3)[drop]
+    ids[:5] = -1                                             # tokens without any valid slot
+    valid = ((ids >= 0) & (ids < E)).ravel()
+    T = M * top_k
+    al = q.moe_align_block_size(to_dev(ids), E, BM)
+    slots = np.nonzero(valid)[0]
+    if a_layout == q.A_GROUPED:
+        pos = orc.compact_row_of_slot(ids, E)
+        order = np.empty(slots.size, dtype=np.int64)
+        order[pos[slots]] = slots
+        a_rows = order // top_k                              # compact row -> token row
+        aq_in, sa_in = p["aq"][to_dev(a_rows)].contiguous(), p["sa"][to_dev(a_rows)].contiguous()
+        ra, rs = p["raq"][a_rows], p["rsa"][a_rows]
+        a_row_of_slot = np.zeros(T, dtype=np.int64)
+        a_row_of_slot[slots] = pos[slots]
+    else:
+        aq_in, sa_in, ra, rs = p["aq"], p["sa"], p["raq"], p["rsa"]
+        a_row_of_slot = np.arange(T, dtype=np.int64) // top_k
+    st = status()
+    out = q.moe_gemm_w8a8(aq_in, sa_in, p["wq"], p["ws"], al, to_dev(p["tw"]), M=M, top_k=top_k, BM=BM,
+                          a_layout=a_layout, out_layout=q.OUT_TOKEN_SUM, d_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    per_slot = orc.moe_gemm_slots(a_kind=orc.A_FP8_TOKEN, a=ra, a_scale=rs, w_kind=orc.W_FP8, w=p["rwq"],
+                                  w_scale=p["rws"], topk_ids=np.where(valid.reshape(ids.shape), ids, 0),
+                                  topk_w=p["tw"], a_row=a_row_of_slot, slots=slots, N=N, K=K)
+    ref = np.zeros((M, N))
+    np.add.at(ref, slots // top_k, per_slot)
+    got = bf16_to_np_f32(out)
+    check(got, ref)
+    assert np.all(got[:5] == 0.0)
+
+
 def test_w8a8_skewed_and_empty_experts(q, orc):
     M, K, N, E, top_k, BM = 512, 256, 128, 8, 2, 64
     ids = np.zeros((M, top_k), dtype=np.int32)
