@@ -1078,6 +1078,7 @@ inline qmoe_status_t launch_gemm(const void* w, int64_t E, int64_t N, int64_t K,
 
 // out[i] = bf16(accum[i]) for the TOKEN_SUM layout (defined in gemm_w8a8.cu).
 qmoe_status_t launch_token_sum_finalize(const float* accum, uint16_t* out, int64_t n, cudaStream_t st);
+qmoe_status_t launch_token_sum_zero(float* accum, int64_t n, cudaStream_t st);
 
 // FP8 GEMM on CTA pairs (tcgen05 cta_group::2, defined in gemm_pair.cu): per-row
 // scales, activation tiles by TMA (GROUPED / PADDED rows), BM >= 128.
@@ -1180,8 +1181,8 @@ inline qmoe_status_t run_moe_gemm(const qmoe_gemm_args* a, cudaStream_t st, cons
     const bool tsum = a->out_layout == QMOE_OUT_TOKEN_SUM;
     if (tsum) {
         if (!a->accum || !aligned16(a->accum)) return QMOE_ERR_INVALID_ARG;
-        if (cudaMemsetAsync(a->accum, 0, static_cast<size_t>(a->M * a->N) * sizeof(float), st) != cudaSuccess)
-            return QMOE_ERR_CUDA;
+        const qmoe_status_t rz = launch_token_sum_zero(a->accum, a->M * a->N, st);
+        if (rz != QMOE_OK) return rz;
     }
     GemmParams p{};  // every field set below; value-initialised so that none can be left undefined
     p.a = static_cast<const uint8_t*>(a->a);

@@ -5,25 +5,49 @@
 namespace qmoe {
 
 // out = bf16(accum), 8 elements per step (n % 8 == 0, 16-byte aligned), else 1.
+// Each thread has four steps' loads in flight before it converts them.
 __global__ void token_sum_finalize_kernel(const float* __restrict__ accum, uint16_t* __restrict__ out, int64_t n) {
     pdl_launch_dependents();
     pdl_wait();  // the GEMM's sums are complete
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     const int64_t i0 = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
     if ((n & 7) == 0) {
-        for (int64_t i = i0; i < n / 8; i += stride) {
-            const float4 a = reinterpret_cast<const float4*>(accum)[2 * i];
-            const float4 b = reinterpret_cast<const float4*>(accum)[2 * i + 1];
-            uint4 o;
-            o.x = pack_bf16x2(a.x, a.y);
-            o.y = pack_bf16x2(a.z, a.w);
-            o.z = pack_bf16x2(b.x, b.y);
-            o.w = pack_bf16x2(b.z, b.w);
-            reinterpret_cast<uint4*>(out)[i] = o;
+        const float4* a4 = reinterpret_cast<const float4*>(accum);
+        uint4* o4 = reinterpret_cast<uint4*>(out);
+        const int64_t n8 = n / 8;
+        int64_t i = i0;
+        for (; i + 3 * stride < n8; i += 4 * stride) {
+            float4 a[4], b[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                a[u] = __ldcs(a4 + 2 * (i + u * stride));
+                b[u] = __ldcs(a4 + 2 * (i + u * stride) + 1);
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                o4[i + u * stride] = make_uint4(pack_bf16x2(a[u].x, a[u].y), pack_bf16x2(a[u].z, a[u].w),
+                                                pack_bf16x2(b[u].x, b[u].y), pack_bf16x2(b[u].z, b[u].w));
+        }
+        for (; i < n8; i += stride) {
+            const float4 a = __ldcs(a4 + 2 * i), b = __ldcs(a4 + 2 * i + 1);
+            o4[i] = make_uint4(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w), pack_bf16x2(b.x, b.y),
+                               pack_bf16x2(b.z, b.w));
         }
     } else {
         for (int64_t i = i0; i < n; i += stride) out[i] = static_cast<uint16_t>(pack_bf16x2(accum[i], 0.0f) & 0xFFFFu);
     }
+}
+
+// accum[0, n) = 0 before a TOKEN_SUM GEMM adds into it (n % 4 == 0, 16-byte
+// aligned); launched like the GEMM so that it can start under the previous
+// kernel's tail.
+__global__ void token_sum_zero_kernel(float* __restrict__ accum, int64_t n) {
+    pdl_launch_dependents();
+    pdl_wait();  // earlier users of accum are complete
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    float4* a4 = reinterpret_cast<float4*>(accum);
+    const float4 z = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n / 4; i += stride) a4[i] = z;
 }
 
 // Per-token quantisation of the fp32 h rows (defined in align_quant.cu).
@@ -38,6 +62,15 @@ qmoe_status_t launch_token_sum_finalize(const float* accum, uint16_t* out, int64
     const int64_t cap = static_cast<int64_t>(sms > 0 ? sms : 132) * 8;
     if (blocks > cap) blocks = cap;
     return launch_pdl(token_sum_finalize_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, st, accum, out, n);
+}
+
+qmoe_status_t launch_token_sum_zero(float* accum, int64_t n, cudaStream_t st) {
+    if (n <= 0) return QMOE_OK;
+    const int sms = device_sm_count();
+    int64_t blocks = (n / 4 + 255) / 256;
+    const int64_t cap = static_cast<int64_t>(sms > 0 ? sms : 132) * 8;
+    if (blocks > cap) blocks = cap;
+    return launch_pdl(token_sum_zero_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, st, accum, n);
 }
 
 }  // namespace qmoe
