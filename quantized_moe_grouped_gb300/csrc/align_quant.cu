@@ -165,11 +165,6 @@ constexpr int kAlignCThreads = 512;
 constexpr int64_t kAlignClusterMinSlots = 2048;
 constexpr int kAlignCWarps = kAlignCThreads / 32;
 
-QMOE_DI uint32_t align_cluster_rank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
 // A 32-bit word of CTA `rank`'s shared memory at the offset of `p` in this CTA.
 QMOE_DI int load_cluster_peer(const int* p, uint32_t rank) {
     uint32_t a;
@@ -177,10 +172,6 @@ QMOE_DI int load_cluster_peer(const int* p, uint32_t rank) {
     int v;
     asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(a));
     return v;
-}
-QMOE_DI void align_cluster_sync() {
-    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
-    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 __global__ void __launch_bounds__(kAlignCThreads, 1)
@@ -198,7 +189,7 @@ __global__ void __launch_bounds__(kAlignCThreads, 1)
     __shared__ int s_bad;
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
-    const uint32_t rank = align_cluster_rank();
+    const uint32_t rank = cluster_ctarank();
     const int64_t nwarps = static_cast<int64_t>(kAlignCtas) * kAlignCWarps;
     const int64_t chunk = ((T + nwarps - 1) / nwarps + 31) / 32 * 32;
     const int64_t gw = static_cast<int64_t>(rank) * kAlignCWarps + warp;
@@ -242,7 +233,7 @@ __global__ void __launch_bounds__(kAlignCThreads, 1)
         }
         s_ccnt[e] = run;
     }
-    align_cluster_sync();  // every CTA's totals are in its shared memory
+    cluster_sync_all();  // every CTA's totals are in its shared memory
     for (int e = tid; e < E; e += blockDim.x) {
         int v[kAlignCtas];  // all CTAs' counts, loaded together (one remote latency)
 #pragma unroll
@@ -256,7 +247,7 @@ __global__ void __launch_bounds__(kAlignCThreads, 1)
         s_coff[e] = before;
         s_cnt[e] = total;
     }
-    align_cluster_sync();  // no CTA reads another's shared memory after this point
+    cluster_sync_all();  // no CTA reads another's shared memory after this point
     if (tid == 0) {
         int off = 0, poff = 0;
         for (int e = 0; e < E; ++e) {

@@ -13,21 +13,8 @@ constexpr int kTileRows = 256;                // weight rows per pair tile (both
 constexpr int kRowsCta = 128;                 // weight rows per CTA (the MMA A operand's half)
 
 // ------------------------------------------------------------ cluster PTX ---
-QMOE_DI uint32_t cluster_ctarank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-QMOE_DI uint32_t cluster_id_x() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
-    return r;
-}
-QMOE_DI uint32_t num_clusters_x() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
-    return r;
-}
+// (cluster_ctarank, cluster_id_x, num_clusters_x and cluster_sync_all are in
+// common.cuh)
 // Address of the same shared-memory location in CTA `rank` of the cluster.
 QMOE_DI uint32_t map_shared_rank(const void* p, uint32_t rank) {
     uint32_t r;
@@ -68,11 +55,6 @@ QMOE_DI void tma_prefetch_l2_3d_box(const CUtensorMap* map, int x, int y, int z)
                      reinterpret_cast<uint64_t>(map)),
                  "r"(x), "r"(y), "r"(z)
                  : "memory");
-}
-
-QMOE_DI void cluster_sync_all() {
-    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
-    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 // -------------------------------------------------- tcgen05, CTA pairs ---
