@@ -462,9 +462,13 @@ qmoe_status_t qmoe_debug_silu_mul(const float* g, const float* u, float* h, int6
  * (at most 1 s) it gives up and ORs QMOE_DEV_TIMEOUT into *d_status.  The
  * kernel returns normally and the context stays usable. */
 qmoe_status_t qmoe_debug_wait_timeout(int32_t* d_status, int64_t limit_ns, qmoe_stream_t stream);
-/* q = x / s through the kernels' division by a row scale (correctly rounded,
- * like IEEE fp32 division), n values. */
+/* q = x / s through the correctly rounded division by a row scale (like IEEE
+ * fp32 division; the int8 weight quantiser's), n values. */
 qmoe_status_t qmoe_debug_div_by_scale(const float* x, float s, float* q, int64_t n, qmoe_stream_t stream);
+/* q[i] = the e4m3 code the quantisers write for x[i] / s (what
+ * qmoe_quant_act_fp8 and the other per-row quantisers compute per value from
+ * the row scale s), n values: the exhaustive check of that code path. */
+qmoe_status_t qmoe_debug_quant_by_scale(const float* x, float s, uint8_t* q, int64_t n, qmoe_stream_t stream);
 /* y[i] = 1/d[i] with the reciprocal the SiLU uses (correctly rounded, for
  * d >= 1): the exhaustive check of that sequence. */
 qmoe_status_t qmoe_debug_rcp_ge1(const float* d, float* y, int64_t n, qmoe_stream_t stream);

@@ -31,7 +31,7 @@ EXPORTED = (
     "qmoe_status_string", "qmoe_version", "qmoe_align_max_padded", "qmoe_moe_align_block_size",
     "qmoe_quant_act_fp8", "qmoe_quant_act_fp8_sorted", "qmoe_moe_align_quant_fp8", "qmoe_moe_router_topk", "qmoe_moe_route_align_quant_fp8", "qmoe_gather_sorted_bf16", "qmoe_quant_weight_fp8", "qmoe_quant_weight_int8", "qmoe_moe_gemm_w8a8",
     "qmoe_moe_gemm_w8a16", "qmoe_silu_mul_quant", "qmoe_srelu_quant", "qmoe_debug_e4m3_encode", "qmoe_debug_int8_to_bf16",
-    "qmoe_debug_silu_mul", "qmoe_debug_div_by_scale", "qmoe_debug_wait_timeout",
+    "qmoe_debug_silu_mul", "qmoe_debug_div_by_scale", "qmoe_debug_quant_by_scale", "qmoe_debug_wait_timeout",
     "qmoe_moe_gemm_w8a8_token_sum_noalloc", "qmoe_quant_weight_mxfp8", "qmoe_quant_mxfp8", "qmoe_quant_mxfp8_colwise",
     "qmoe_mx_weight_sf_tiled_bytes", "qmoe_mx_weight_sf_tiled", "qmoe_quant_weight_int4", "qmoe_moe_gemm_w4a16",
     "qmoe_moe_gemm_w8a8_silu_mxfp8", "qmoe_moe_gemm_w8a8_silu_fp8_token", "qmoe_debug_rcp_ge1",
@@ -109,6 +109,7 @@ def load_library(path: str | None = None):
             L.qmoe_debug_int8_to_bf16.argtypes = [vp, vp, i64, vp]
             L.qmoe_debug_silu_mul.argtypes = [vp, vp, vp, i64, vp]
             L.qmoe_debug_div_by_scale.argtypes = [vp, ctypes.c_float, vp, i64, vp]
+            L.qmoe_debug_quant_by_scale.argtypes = [vp, ctypes.c_float, vp, i64, vp]
             L.qmoe_debug_rcp_ge1.argtypes = [vp, vp, i64, vp]
             L.qmoe_debug_wait_timeout.argtypes = [vp, i64, vp]
             L.qmoe_debug_moe_gemm_tile.argtypes = [ctypes.POINTER(GemmArgs), i32, i32, vp]
@@ -691,8 +692,18 @@ def debug_rcp_ge1(d: torch.Tensor, stream=None) -> torch.Tensor:
     return y
 
 
+def debug_quant_by_scale(x: torch.Tensor, s: float, stream=None) -> torch.Tensor:
+    """Test hook: the e4m3 codes the quantisers write for x / s (row scale s), elementwise."""
+    _need(x, torch.float32, "x")
+    q = _empty(x.shape, dtype=torch.uint8, device=x.device)
+    _check(load_library().qmoe_debug_quant_by_scale(_ptr(x), float(s), _ptr(q), x.numel(), _stream(stream)),
+           "debug_quant_by_scale")
+    return q
+
+
 def debug_div_by_scale(x: torch.Tensor, s: float, stream=None) -> torch.Tensor:
-    """Test hook: the quantisers' division x / s by a row scale (packed pairs), elementwise."""
+    """Test hook: the correctly rounded division x / s by a row scale (packed pairs;
+    the int8 weight quantiser's), elementwise."""
     _need(x, torch.float32, "x")
     q = _empty(x.shape, dtype=x.dtype, device=x.device)
     _check(load_library().qmoe_debug_div_by_scale(_ptr(x), float(s), _ptr(q), x.numel(), _stream(stream)),

@@ -1247,6 +1247,22 @@ __global__ void debug_div_kernel(const float* __restrict__ x, float s, float* __
     }
 }
 
+// The quantisers' e4m3 codes of x[i] / s (quant8), eight values per thread
+// (a short tail padded with zeros, its codes dropped).
+__global__ void debug_quant_kernel(const float* __restrict__ x, float s, uint8_t* __restrict__ q, int64_t n) {
+    const float rinv = __frcp_rn(s);
+    for (int64_t i = 8 * (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x); i < n;
+         i += 8 * static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        float v[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) v[k] = i + k < n ? x[i + k] : 0.0f;
+        const uint2 c = quant8(v, s, rinv);
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+            if (i + k < n) q[i + k] = static_cast<uint8_t>(((k < 4 ? c.x : c.y) >> (8 * (k & 3))) & 0xFFu);
+    }
+}
+
 // One thread waits on an mbarrier that nothing arrives at, through the same
 // bounded wait the GEMM uses, with a short limit: it must give up, record
 // QMOE_DEV_TIMEOUT and return.
@@ -1592,6 +1608,13 @@ qmoe_status_t qmoe_debug_div_by_scale(const float* x, float s, float* q, int64_t
     if (n < 0 || (n > 0 && (!x || !q))) return QMOE_ERR_INVALID_ARG;
     if (n == 0) return QMOE_OK;
     debug_div_kernel<<<grid_for((n + 1) / 2, 256), 256, 0, stream>>>(x, s, q, n);
+    return launch_status();
+}
+
+qmoe_status_t qmoe_debug_quant_by_scale(const float* x, float s, uint8_t* q, int64_t n, qmoe_stream_t stream) {
+    if (n < 0 || (n > 0 && (!x || !q))) return QMOE_ERR_INVALID_ARG;
+    if (n == 0) return QMOE_OK;
+    debug_quant_kernel<<<grid_for((n + 7) / 8, 256), 256, 0, stream>>>(x, s, q, n);
     return launch_status();
 }
 

@@ -315,6 +315,52 @@ def test_division_by_row_scale_exhaustive(q, s):
         assert bad.size == 0, (float(sd), x[bad[:4]], got[bad[:4]], ref[bad[:4]])
 
 
+# Every quantiser's code for x / s (row scale s): the correction of the reciprocal
+# product above its guard (2^-99 max(1, s)), the IEEE division below it.  The whole
+# range |x| <= 512 s for the typical activation scale and the tiny ones; for the
+# others every dividend within a factor 4 of the guard (the switch between the two
+# paths) and every 509th bit pattern elsewhere.
+QUANT_SCALES = [(np.float32(1.0 / 448.0), True), (np.float32(1.0), False), (np.float32(1.37 * 2.0 ** 100), False),
+                (np.float32(3.0), False), (np.float32(0.0123456), False),
+                (np.float32(7.0e-3) / np.float32(448.0), False),
+                # tiny scales: every dividend lies below the guard (the IEEE path), whole range
+                (np.float32(1.5 * 2.0 ** -130), True),     # subnormal: RN(1/s) overflows
+                (np.float32(2.0 ** -127), True), (np.float32(0.75 * 2.0 ** -120), True),
+                (np.nextafter(np.float32(1.0), np.float32(0)), False)]
+
+
+def _dividend_bits(lim, guard, full):
+    """Positive fp32 bit patterns to check, in chunks: all up to lim (full), or
+    all in [guard / 4, 4 guard) and every 509th one elsewhere up to lim."""
+    f32_bits = lambda v: int(np.float32(v).view(np.uint32))
+    top = min(f32_bits(lim) + 1, f32_bits(np.finfo(np.float32).max) + 1)
+    lo, hi = (0, top) if full else (min(top, f32_bits(guard / 4)), min(top, f32_bits(4 * guard)))
+    chunk = 1 << 26
+    for b in range(0, lo, chunk * 509):
+        yield np.arange(b, min(lo, b + chunk * 509), 509, dtype=np.uint32)
+    for b in range(lo, hi, chunk):
+        yield np.arange(b, min(hi, b + chunk), dtype=np.uint32)
+    for b in range(hi, top, chunk * 509):
+        yield np.arange(b, min(top, b + chunk * 509), 509, dtype=np.uint32)
+
+
+@pytest.mark.parametrize("s,full", QUANT_SCALES)
+def test_quant_codes_by_row_scale_exhaustive(q, orc, s, full):
+    """The e4m3 code every quantiser writes for x / s equals the oracle's e4m3
+    conversion of the IEEE fp32 quotient (numpy), for dividends of both signs
+    up to |x| <= 512 s (the quantisers divide values bounded by amax = 448 s)."""
+    sd = np.float32(s)
+    lim = np.float32(512.0) * sd
+    guard = np.float32(2.0 ** -99) * max(np.float32(1.0), sd)
+    for bits in _dividend_bits(lim, guard, full):
+        x = np.concatenate([bits.view(np.float32), (bits | np.uint32(0x80000000)).view(np.float32)])
+        got = q.debug_quant_by_scale(to_dev(x), float(sd)).cpu().numpy()
+        with np.errstate(under="ignore", over="ignore"):
+            ref = orc.e4m3_from_f32_array((x / sd).astype(np.float32))
+        bad = np.nonzero(got != ref)[0]
+        assert bad.size == 0, (float(sd), x[bad[:4]], got[bad[:4]], ref[bad[:4]])
+
+
 def test_bounded_wait_reports_timeout_and_context_survives(q, orc):
     """A wait on an mbarrier that nothing arrives at gives up after its limit,
     records QMOE_DEV_TIMEOUT in d_status and returns; the context keeps
