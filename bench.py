@@ -55,13 +55,11 @@ PAGE_ROWS = ((64, 47.124442, 1480.603863), (128, 93.602312, 1478.376964),
 
 
 def slot_tile(M: int) -> int:
-    """Slot tile (BM) per M: the smallest power of two >= twice the mean slots
-    per expert, in [16, 128] (BM <= 64 runs the swapped tile, 128 the wide one)."""
+    """Slot tile (BM) per M: 64 or 128, the smaller when it holds twice the mean
+    slots per expert (both run the wide tile: 256 weight rows against 64 or 128
+    slots; the swapped tiles of BM 16 and 32 measured slower at decode)."""
     mean = 2 * M * TOP_K // E
-    bm = 16
-    while bm < mean and bm < 128:
-        bm *= 2
-    return bm
+    return 64 if mean <= 64 else 128
 
 
 def algorithmic_bytes(M: int, ids: np.ndarray) -> int:

@@ -154,7 +154,7 @@ struct GemmCfg {
     static constexpr int kSfaCol = kAccCols;
     static constexpr int kSfbCol = (kAccCols + 4 * kStages + 7) / 8 * 8;
     static constexpr int kTmemCols = (kMX || kW2) ? 512 : (2 * kAccCols < 32 ? 32 : 2 * kAccCols);
-    // MMA M: 128 rows, or 64 for the 64-slot wide bf16 tile (D row i then sits in TMEM
+    // MMA M: 128 rows, or 64 for the 64-slot wide tile (D row i then sits in TMEM
     // lane 32 * (i / 16) + i % 16: each warp's lane quadrant holds 16 rows in lanes 0-15)
     static constexpr int kMmaM = (kWide && BN == 64) ? 64 : 128;
     static constexpr int kRowsPerQuad = kMmaM / 4;
@@ -163,10 +163,11 @@ struct GemmCfg {
     // Tail split (plain FP8 wide tile): quarter tiles of 64 weight rows (MMA N = 64)
     static constexpr bool kTailSplit = kWide && !kBF16 && !kMX && kAct == 0 && !kW2;
     static constexpr int kQRows = 64;
-    static constexpr uint32_t kIdescQ = make_idesc(kFmtE4M3, 128, kQRows);
+    static constexpr uint32_t kIdescQ = make_idesc(kFmtE4M3, kMmaM, kQRows);
     static_assert(!kMX || (kWide && !kBF16), "MX scales: FP8 wide tile only");
     static_assert(!kI4 || (kBF16 && kWide), "W4A16: wide bf16 tile only");
-    static_assert(!kWide || BN == 128 || BN == 256 || (BN == 64 && kBF16), "wide tile: 128 or 256 slots (64: bf16)");
+    static_assert(!kWide || BN == 128 || BN == 256 || BN == 64, "wide tile: 64, 128 or 256 slots");
+    static_assert(!(kWide && BN == 64) || (!kMX && kAct == 0), "64-slot wide tile: per-row scales, plain epilogue");
     static_assert(!kW2 || (!kBF16 && !kMX), "two-half tile: FP8 with per-row scales only");
     static_assert(kAct == 0 || (kWide && BN == 128 && !kBF16 && !kMX), "SwiGLU epilogue: FP8 wide 128-slot tile only");
     static_assert(!kMX || kSfbCol + 8 * kStages <= 512, "TMEM columns");  // per-stage weight scales
@@ -1225,7 +1226,7 @@ inline qmoe_status_t run_moe_gemm(const qmoe_gemm_args* a, cudaStream_t st, cons
     // 128 KB 5641, 256 KB 5652, 512 KB 5646 GB/s on the decode sweep)
     {
         const int64_t slot_rows = a->BM >= 128 ? 128 : a->BM;
-        const int64_t w_stage = (a->BM >= 128 ? 256 : 128) * 128;
+        const int64_t w_stage = (a->BM >= 64 ? 256 : 128) * 128;  // weight rows of the tile x 128 bytes
         p.l2_prefetch_kb = (!kBF16 && !mx && !so && T <= slot_rows * a->E) ? static_cast<int32_t>(262144 / w_stage) : 0;
     }
     const int64_t max_padded = (T + static_cast<int64_t>(a->E) * (a->BM - 1) + a->BM - 1) / a->BM * a->BM;
@@ -1273,9 +1274,8 @@ inline qmoe_status_t run_moe_gemm(const qmoe_gemm_args* a, cudaStream_t st, cons
     switch (a->BM) {
         case 16: r = launch_gemm<kBF16, false, 16>(a->w, a->E, a->N, a->K, p, max_padded, a_rows, a->lda, st); break;
         case 32: r = launch_gemm<kBF16, false, 32>(a->w, a->E, a->N, a->K, p, max_padded, a_rows, a->lda, st); break;
-        case 64:  // bf16 activations: the 64-slot wide tile (M = 64 MMAs, 256 weight rows each)
-            r = kBF16 ? launch_gemm<true, true, 64, false, kI4>(a->w, a->E, a->N, a->K, p, max_padded, a_rows, a->lda, st)
-                      : launch_gemm<false, false, 64>(a->w, a->E, a->N, a->K, p, max_padded, a_rows, a->lda, st);
+        case 64:  // the 64-slot wide tile (M = 64 MMAs, 256 weight rows each)
+            r = launch_gemm<kBF16, true, 64, false, kI4>(a->w, a->E, a->N, a->K, p, max_padded, a_rows, a->lda, st);
             break;
         default: r = launch_gemm<kBF16, true, 128>(a->w, a->E, a->N, a->K, p, max_padded, a_rows, a->lda, st); break;
     }

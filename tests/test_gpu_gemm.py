@@ -95,6 +95,40 @@ def test_w8a8_layouts_ragged(q, orc, a_layout, out_layout, M, K, N, E, top_k, BM
     check(bf16_to_np_f32(out), ref)
 
 
+@pytest.mark.parametrize("a_layout,out_layout", [(0, 0), (1, 2), (2, 1), (0, 2)])
+@pytest.mark.parametrize("M,K,N,E,top_k", [(64, 256, 272, 8, 2), (150, 400, 528, 6, 3), (520, 128, 256, 8, 2)])
+def test_w8a8_wide64_tile(q, orc, a_layout, out_layout, M, K, N, E, top_k):
+    """The 64-slot wide FP8 tile (M = 64 MMAs over 256 weight rows, the BM = 64
+    tile): every activation layout, ragged N and K, top_k = 3."""
+    p = fp8_problem(q, orc, M, K, N, E, top_k, seed=M + K + N + 3)
+    T = M * top_k
+    BM = 64
+    ids_d = to_dev(p["ids"])
+    al = q.moe_align_block_size(ids_d, E, BM)
+    if a_layout == q.A_GROUPED:
+        pos = orc.compact_row_of_slot(p["ids"], E)
+        order = np.empty(T, dtype=np.int64)
+        order[pos] = np.arange(T)
+        rows = order // top_k
+        aq_in, sa_in = p["aq"][to_dev(rows)].contiguous(), p["sa"][to_dev(rows)].contiguous()
+        ra, rs, ref_layout = p["raq"][rows], p["rsa"][rows], "grouped"
+    elif a_layout == q.A_PADDED:
+        a_bf = to_dev_bf16(p["a"])
+        aq_in, sa_in = q.quant_act_fp8_sorted(a_bf, al, top_k)
+        ra, rs, ref_layout = p["raq"], p["rsa"], "token"
+    else:
+        aq_in, sa_in, ra, rs, ref_layout = p["aq"], p["sa"], p["raq"], p["rsa"], "token"
+    st = status()
+    out = q.moe_gemm_w8a8(aq_in, sa_in, p["wq"], p["ws"], al, to_dev(p["tw"]), M=M, top_k=top_k, BM=BM,
+                          a_layout=a_layout, out_layout=out_layout, d_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    ref = orc.moe_gemm(a_kind=orc.A_FP8_TOKEN, a=ra, a_scale=rs, w_kind=orc.W_FP8, w=p["rwq"], w_scale=p["rws"],
+                       topk_ids=p["ids"], topk_w=p["tw"], E=E, a_layout=ref_layout,
+                       out_layout={0: "slot", 1: "grouped", 2: "token_sum"}[out_layout])
+    check(bf16_to_np_f32(out), ref)
+
+
 def test_w8a8_token_sum_deterministic(q, orc):
     M, K, N, E, top_k, BM = 256, 256, 256, 8, 2, 32
     p = fp8_problem(q, orc, M, K, N, E, top_k, seed=5)
