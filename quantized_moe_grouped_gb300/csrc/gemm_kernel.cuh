@@ -1162,16 +1162,18 @@ inline qmoe_status_t run_moe_gemm(const qmoe_gemm_args* a, cudaStream_t st, cons
     // activations in contiguous rows; FP8 with BM >= 128
     const bool pair_ok = !mx && !wmx && !so && a->a_layout != QMOE_A_TOKEN_GATHER && (kBF16 || a->BM >= 128);
     if (tile == kTilePair && !pair_ok) return QMOE_ERR_UNSUPPORTED;
-    // The library's choice (measured on the Mixtral-shaped projections, E = 8): the pair
-    // tile for long K at 256-512 slots per expert on average (down projections at
-    // M = 1024-2048: 11-20 % faster, its 256-slot tiles balance the waves better than
-    // the one-SM two-half tile), and at short K for about one 128-slot block per
-    // expert (the decode GEMM at M = 512: 95.7 -> 93.7 us; the MMA width follows the
-    // expert's slot count instead of two padded 128-slot blocks); elsewhere the one-SM
-    // tiles are as fast or faster.
+    // The library's choice (measured on the Mixtral-shaped projections, E = 8, with
+    // two k-blocks per pair stage): the pair tile for long K from 256 slots per
+    // expert on average (down projections, M = 1024-4096: 150 / 212 / 339 us against
+    // 183 / 259 / 349 at N = 4096, K = 14336), and at short K for about one 128-slot
+    // block per expert (the decode GEMM at M = 512: 101 against 106 us) and from 512
+    // slots per expert (up projections at M = 2048-4096: 567 / 1007 against 596 /
+    // 1049 us at N = 32768, K = 6144; even at N = 28672, K = 4096); elsewhere the
+    // one-SM tiles are as fast or faster.
     const int64_t slots_per_expert = a->M * a->top_k / a->E;
-    const bool pair_auto = (a->K >= 8192 && slots_per_expert >= 256 && slots_per_expert <= 512) ||
-                           (a->K < 8192 && slots_per_expert >= 96 && slots_per_expert <= 160);
+    const bool pair_auto =
+        (a->K >= 8192 && slots_per_expert >= 256) ||
+        (a->K < 8192 && ((slots_per_expert >= 96 && slots_per_expert <= 160) || slots_per_expert >= 512));
     // INT8 / INT4 weights: the pair tile from 1024 slots per expert (M = 4096 at N = 14336:
     // W8A16 870 -> 854 us, W4A16 1016 -> 943 us); at decode its 256 x 32 MMAs issue at
     // about 170 cycles each and the one-SM wide tile is faster (125 against 184 us at M = 64)

@@ -39,26 +39,37 @@
 namespace qmoe {
 namespace pairtile {
 
-constexpr int kStages = 6;
-constexpr int kBoxRows = 128;                 // activation rows loaded per CTA per stage (B half <= 128)
-constexpr int kBK = 128;                      // K bytes per stage
-constexpr int kABytes = kRowsCta * kBK;       // 16 KB
-constexpr int kBBytes = kBoxRows * kBK;       // 16 KB
-constexpr int kStageBytes = kABytes + kBBytes;
+constexpr int kBoxRows = 128;                 // activation rows loaded per CTA per k-block (B half <= 128)
+constexpr int kBK = 128;                      // K bytes per k-block (one 128-byte swizzled box per operand)
+constexpr int kABytes = kRowsCta * kBK;       // 16 KB of weight rows per k-block
+constexpr int kBBytes = kBoxRows * kBK;       // 16 KB of activation rows per k-block
 constexpr int kEpiThreads = 128;
 constexpr int kThreads = 64 + kEpiThreads;
 constexpr int kAccCols = 256;
-constexpr int kDynSmem = kStages * kStageBytes + 1024;
-constexpr int kPfStages = kStages;            // weight boxes prefetched into L2 this many stages ahead
 constexpr bool kPfFirstPairOnly = true;       // only the first slot pair of a weight block prefetches it
+// Ring of kKS k-blocks per stage: one barrier round trip per stage moves kKS x 32
+// KB per CTA (the weight halves first, then the activation halves), with the
+// ring's 192 KB in 6 / kKS stages; weight boxes are prefetched into L2 one ring
+// ahead.  Two k-blocks per stage halve the per-stage handshakes, which bound
+// the decode-sized launches (16 KB of weights per stage and CTA).
+template <int kKS>
+struct PairCfg {
+    static constexpr int kStages = 6 / kKS;
+    static constexpr int kStageBytes = kKS * (kABytes + kBBytes);
+    static constexpr int kDynSmem = kStages * kStageBytes + 1024;
+    static constexpr int kPfStages = kStages;  // stages prefetched ahead
+};
 
 // kAccBufs: accumulators in tensor memory (2: the epilogue of one tile
 // overlaps the MMAs of the next; 1: 256 columns, one tile at a time).
-template <int kAccBufs>
+template <int kAccBufs, int kKS>
 __global__ void __launch_bounds__(kThreads, 1)
     moe_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_a,
                          const GemmParams p) {
-    constexpr int S = kStages;
+    using PC = PairCfg<kKS>;
+    constexpr int S = PC::kStages;
+    constexpr int kStageBytes = PC::kStageBytes;
+    constexpr int kPfStages = PC::kPfStages;
     constexpr int kTmemCols = kAccBufs * kAccCols;
     extern __shared__ uint8_t smem_raw[];
     __shared__ uint64_t bar_full[S], bar_empty[S];
@@ -123,8 +134,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int c0 = static_cast<int>(cluster_id_x());
     const int nc = static_cast<int>(num_clusters_x());
     const int nkb = p.num_k_blocks;
-    auto a_tile = [&](int s) { return smem + s * kStageBytes; };            // weight rows (MMA A)
-    auto b_tile = [&](int s) { return smem + s * kStageBytes + kABytes; };  // slot rows (MMA B)
+    const int nks = (nkb + kKS - 1) / kKS;  // stages per tile (a last k-block past K loads zeros)
+    // k-block kk of stage s: weight rows (MMA A), slot rows (MMA B)
+    auto a_tile = [&](int s, int kk) { return smem + s * kStageBytes + kk * kABytes; };
+    auto b_tile = [&](int s, int kk) { return smem + s * kStageBytes + kKS * kABytes + kk * kBBytes; };
 
     if (warp == 0) {
         // ------------------------------------------------ TMA producer ---
@@ -143,24 +156,35 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const bool has_next = t + nc < num_tiles;
                 const Tile xn = has_next ? decode_tile(t + nc, p.E, n_blocks, s_pre, s_poff, p.expert_offsets) : x;
                 const int wrow_n = xn.nb * kTileRows + static_cast<int>(rank) * kRowsCta;
-                for (int kb = 0; kb < nkb; ++kb, ++it) {
+                for (int ks = 0; ks < nks; ++ks, ++it) {
                     const int s = it % S;
                     const uint32_t ph = (it / S) & 1;
                     if (!mbar_wait(&bar_empty[s], ph ^ 1, abort, p.d_status)) { ok = false; break; }
                     if (rank == 0) {  // both CTAs' loads complete on CTA 0's barrier
                         mbar_arrive_expect_tx(&bar_full[s], 2 * kStageBytes);
-                        tma_load_3d(&tmap_w, &bar_full[s], a_tile(s), kb * kBK, wrow, x.e);
-                        tma_load_2d(&tmap_a, &bar_full[s], b_tile(s), kb * kBK, arow);
+#pragma unroll
+                        for (int kk = 0; kk < kKS; ++kk) {
+                            tma_load_3d(&tmap_w, &bar_full[s], a_tile(s, kk), (ks * kKS + kk) * kBK, wrow, x.e);
+                            tma_load_2d(&tmap_a, &bar_full[s], b_tile(s, kk), (ks * kKS + kk) * kBK, arow);
+                        }
                     } else {
                         const uint32_t bar0 = map_shared_rank(&bar_full[s], 0);
-                        tma_load_3d_to_leader(&tmap_w, bar0, a_tile(s), kb * kBK, wrow, x.e);
-                        tma_load_2d_to_leader(&tmap_a, bar0, b_tile(s), kb * kBK, arow);
+#pragma unroll
+                        for (int kk = 0; kk < kKS; ++kk) {
+                            tma_load_3d_to_leader(&tmap_w, bar0, a_tile(s, kk), (ks * kKS + kk) * kBK, wrow, x.e);
+                            tma_load_2d_to_leader(&tmap_a, bar0, b_tile(s, kk), (ks * kKS + kk) * kBK, arow);
+                        }
                     }
-                    const int kp = kb + kPfStages;
-                    if (kp < nkb) {
-                        if (!kPfFirstPairOnly || x.pr == 0) tma_prefetch_l2_3d_box(&tmap_w, kp * kBK, wrow, x.e);
-                    } else if (has_next && kp - nkb < nkb && (!kPfFirstPairOnly || xn.pr == 0)) {
-                        tma_prefetch_l2_3d_box(&tmap_w, (kp - nkb) * kBK, wrow_n, xn.e);
+                    const int kp = ks + kPfStages;  // the stage one ring ahead, in this tile or the next
+#pragma unroll
+                    for (int kk = 0; kk < kKS; ++kk) {
+                        if (kp < nks) {
+                            if ((!kPfFirstPairOnly || x.pr == 0) && kp * kKS + kk < nkb)
+                                tma_prefetch_l2_3d_box(&tmap_w, (kp * kKS + kk) * kBK, wrow, x.e);
+                        } else if (has_next && kp - nks < nks && (!kPfFirstPairOnly || xn.pr == 0) &&
+                                   (kp - nks) * kKS + kk < nkb) {
+                            tma_prefetch_l2_3d_box(&tmap_w, ((kp - nks) * kKS + kk) * kBK, wrow_n, xn.e);
+                        }
                     }
                 }
             }
@@ -182,15 +206,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kAccCols);
                 const uint32_t idesc = make_idesc(kFmtE4M3, 256, x.nt);
-                for (int kb = 0; kb < nkb; ++kb, ++it) {
+                for (int ks = 0; ks < nks; ++ks, ++it) {
                     const int s = it % S;
                     const uint32_t ph = (it / S) & 1;
                     if (!mbar_wait(&bar_full[s], ph, abort, p.d_status)) { ok = false; break; }
                     tc_fence_after();
-                    const uint64_t da = desc_kmajor_sw128(smem_u32(a_tile(s)));
-                    const uint64_t db = desc_kmajor_sw128(smem_u32(b_tile(s)));
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) mma_pair_f8f6f4(d_tmem, da + 2 * k, db + 2 * k, idesc, (kb | k) != 0);
+                    for (int kk = 0; kk < kKS; ++kk) {
+                        const uint64_t da = desc_kmajor_sw128(smem_u32(a_tile(s, kk)));
+                        const uint64_t db = desc_kmajor_sw128(smem_u32(b_tile(s, kk)));
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)
+                            mma_pair_f8f6f4(d_tmem, da + 2 * k, db + 2 * k, idesc, (ks | kk | k) != 0);
+                    }
                     tc_commit_pair(&bar_empty[s], 0x3);
                 }
                 if (!ok) break;
@@ -282,13 +310,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <int kAccBufs>
+template <int kAccBufs, int kKS>
 qmoe_status_t launch_pair(const void* w, int64_t E, int64_t N, int64_t K, const GemmParams& p, int64_t max_padded,
                           int64_t a_rows, int64_t lda, cudaStream_t st) {
+    using PC = PairCfg<kKS>;
+    constexpr int kDynSmem = PC::kDynSmem;
     static std::mutex mu;
     static bool attr_set[64] = {false};
     static int max_clusters[64] = {0};
-    auto kern = moe_gemm_pair_kernel<kAccBufs>;
+    auto kern = moe_gemm_pair_kernel<kAccBufs, kKS>;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return QMOE_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
@@ -340,7 +370,7 @@ qmoe_status_t launch_pair(const void* w, int64_t E, int64_t N, int64_t K, const 
 // tile (GROUPED or PADDED layouts, loaded by TMA), any output layout.
 qmoe_status_t launch_gemm_pair(const void* w, int64_t E, int64_t N, int64_t K, const GemmParams& p,
                                int64_t max_padded, int64_t a_rows, int64_t lda, cudaStream_t st) {
-    return pairtile::launch_pair<2>(w, E, N, K, p, max_padded, a_rows, lda, st);
+    return pairtile::launch_pair<2, 2>(w, E, N, K, p, max_padded, a_rows, lda, st);
 }
 
 }  // namespace qmoe

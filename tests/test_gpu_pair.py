@@ -179,6 +179,32 @@ def test_pair_tile_a16_parity(q, orc, kind, a_layout, out_layout, M, K, N, E, to
     assert ok, f"worst |err|/bound = {ratio:.3f}"
 
 
+def test_regular_entry_point_takes_the_pair_tile_for_large_m_short_k(q, orc):
+    """qmoe_moe_gemm_w8a8 itself at 512 slots per expert and K < 8192 (an up
+    projection the library sends to the pair tile), padded rows, slot output."""
+    M, K, N, E, top_k = 2048, 256, 512, 8, 2
+    a = inputs.activations_bf16(M, K, 41)
+    w = inputs.expert_weights_f32(E, N, K, 41)
+    ids, tw = inputs.routing(M, E, top_k, 41)
+    wq, ws = q.quant_weight_fp8(to_dev(w))
+    al = q.moe_align_block_size(to_dev(ids), E, 128)
+    aq, sa = q.quant_act_fp8_sorted(to_dev_bf16(a), al, top_k)
+    st = status()
+    out = q.moe_gemm_w8a8(aq, sa, wq, ws, al, to_dev(tw), M=M, top_k=top_k, BM=128, a_layout=q.A_PADDED,
+                          d_status=st)
+    forced = q.moe_gemm_w8a8(aq, sa, wq, ws, al, to_dev(tw), M=M, top_k=top_k, BM=128, a_layout=q.A_PADDED,
+                             d_status=st, tile=q.TILE_PAIR)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    assert torch.equal(out, forced)
+    raq, rsa = orc.quant_rows_fp8_bf16(a)
+    rwq, rws = orc.quant_rows_fp8_f32(w)
+    ref = orc.moe_gemm(a_kind=orc.A_FP8_TOKEN, a=raq, a_scale=rsa, w_kind=orc.W_FP8, w=rwq, w_scale=rws,
+                       topk_ids=ids, topk_w=tw, E=E)
+    ok, ratio = orc.gemm_tolerance_ok(bf16_to_np_f32(out), ref)
+    assert ok, f"worst |err|/bound = {ratio:.3f}"
+
+
 @pytest.mark.parametrize("kind", ["int8", "int4"])
 def test_regular_a16_entry_points_take_the_pair_tile_at_large_m(q, orc, kind):
     """qmoe_moe_gemm_w8a16 / _w4a16 themselves at 1024 slots per expert (the
