@@ -2,14 +2,16 @@
 //
 // Two tile shapes share one warp-specialised kernel template:
 //
-//  * swapped (BM <= 64, the decode regime): one tile = 128 output channels n
-//    of one expert x BN sorted slots (one BM block, BN == BM).  The weight rows
-//    are the MMA "A" operand (M = 128) and the slot activations the "B"
-//    operand (N = BN), so a handful of slots per expert still fills the
-//    tensor-core M dimension while the kernel streams W at HBM rate.
-//  * wide (BM >= 128): one tile = 128 sorted slots (MMA M) x 256 output
-//    channels (MMA N).  Per byte of weights it gathers a quarter of the
-//    activation bytes the swapped shape would need at BN = 256.
+//  * swapped (BM 16 or 32): one tile = 128 output channels n of one expert x
+//    BN sorted slots (one BM block, BN == BM).  The weight rows are the MMA
+//    "A" operand (M = 128) and the slot activations the "B" operand (N = BN),
+//    so a handful of slots per expert still fills the tensor-core M dimension
+//    while the kernel streams W at HBM rate.
+//  * wide (BM >= 64): one tile = 128 sorted slots (MMA M) x 256 output
+//    channels (MMA N), or at BM = 64 64 slots (M = 64 MMAs; the decode tile:
+//    32 KB of weights per stage, where a fixed cost per ring stage made the
+//    swapped tile's 16 KB stages the bound).  Per byte of weights it gathers a
+//    quarter of the activation bytes the swapped shape would need at BN = 256.
 //
 // D lives in TMEM (fp32), double-buffered so the epilogue of one tile overlaps
 // the main loop of the next.
